@@ -1,0 +1,318 @@
+"""Float64 CPU oracle for attention-matching compaction of one layer's KV cache.
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the CPU-baseline
+leg of the benchmark may import this package.  The library never calls it and
+shares no code with it; the two meet only in the seeded input generator
+(``synth``), which holds none of the method's arithmetic.
+
+Every function works in float64 on the exact values of its (bf16- or
+fp32-valued) inputs, in query-row chunks of at most ``CHUNK`` rows so that the
+score matrix never has to be held whole.  Chunking only regroups the sums over
+query rows; nothing else is blocked, fused or reordered.
+
+Sources (page title, then section / equation):
+
+* [LC]  "Latent Compaction with Test-Time Training" -- §3 Preliminaries Eq. (1)
+  (attention output and normaliser, scale s = 1/sqrt(d)); §3.1 Eq. (2)-(3)
+  (biased compact attention: logits s*K_cmp q + b, output V_cmp^T softmax);
+  §3.2 Eq. (6) (key score: max over reference queries of the softmax
+  probability); Appendix A.2 "Normalizer Computation and Storage".
+* [KVC] "KV compaction" (bkal01 blog) -- section "Fast KV Compaction via
+  Attention Matching": output- and mass-matching equations, the q = 0 argument
+  for beta, the three steps (top keys by attention, beta by NNLS on the mass
+  equation, C_v by OLS on the output equation), C_k a subset of K.
+
+Readings taken where the pages leave a step open (each is also listed in the
+design notes):
+
+* All reference queries see all T keys (no causal mask).
+* The key score is reduced with max (Eq. 6), in the log domain:
+  u_j = max_i (S_ij - lse_i) = log a_j.
+* Top-t ties go to the lower key index; -0 counts as +0; output ascending.
+* NNLS is solved in per-query max-shifted form: A_ij = exp(S_C,ij - m_i),
+  b_i = exp(lse_i - m_i) with m_i the full-row max of S; w = exp(beta) >= 0 is
+  unbounded above; Lawson-Hanson with tolerance 10*eps*t*max|c|, at most 3t
+  outer steps and t inner steps per outer step.
+* The OLS design matrix is the compact softmax X = softmax_j(s q.C_kj + beta_j)
+  over the keys with w_j > 0; C_v = (X^T X)^-1 X^T O by Cholesky; keys with
+  w_j = 0 keep their original value row.  If the Cholesky factorisation fails
+  a ridge of 1e-8 * mean(diag) is added once and the status says so.
+
+Parity is pinned for every function here by the CPU tests (brute force on tiny
+inputs, closed forms, library cross-checks, invariants); see tests/.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+try:  # scipy is a convenience for triangular solves; numpy alone also works
+    from scipy.linalg import solve_triangular as _solve_tri
+except Exception:  # pragma: no cover
+    _solve_tri = None
+
+CHUNK = 2048
+
+# Status codes, numerically equal to the library's, so that reports compare.
+OK = 0
+NOT_CONVERGED = 5
+SINGULAR = 6
+
+
+def _f64(a):
+    return np.asarray(a, dtype=np.float64)
+
+
+def _chunks(n, size=CHUNK):
+    for a in range(0, n, size):
+        yield a, min(n, a + size)
+
+
+# ---------------------------------------------------------------- step 1 ----
+def full_stats(Q, K, V, scale):
+    """Full-cache statistics of every reference query ([LC] Eq. 1).
+
+    S = scale * Q K^T; m_i = max_j S_ij; lse_i = log sum_j exp(S_ij) (the log
+    attention mass, computed as m_i + log sum_j exp(S_ij - m_i));
+    O_i = sum_j exp(S_ij - lse_i) V_j (the attention output).
+    Q [n_q, d], K [T, d], V [T, d_v] -> m [n_q], lse [n_q], O [n_q, d_v].
+    """
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    n_q = Q.shape[0]
+    m = np.empty(n_q)
+    lse = np.empty(n_q)
+    O = np.empty((n_q, V.shape[1]))
+    for a, b in _chunks(n_q):
+        S = scale * (Q[a:b] @ K.T)
+        mm = S.max(axis=1)
+        ls = mm + np.log(np.exp(S - mm[:, None]).sum(axis=1))
+        P = np.exp(S - ls[:, None])
+        m[a:b] = mm
+        lse[a:b] = ls
+        O[a:b] = P @ V
+    return m, lse, O
+
+
+# ---------------------------------------------------------------- step 2 ----
+def key_scores(Q, K, lse, scale):
+    """Log of each key's maximum attention probability ([LC] Eq. 6).
+
+    u_j = max_i (scale * q_i . k_j - lse_i), so a_j = exp(u_j) is the largest
+    softmax probability any reference query puts on key j.  -> u [T].
+    """
+    Q, K, lse = _f64(Q), _f64(K), _f64(lse)
+    u = np.full(K.shape[0], -np.inf)
+    for a, b in _chunks(Q.shape[0]):
+        S = scale * (Q[a:b] @ K.T) - lse[a:b, None]
+        u = np.maximum(u, S.max(axis=0))
+    return u
+
+
+# ---------------------------------------------------------------- step 3 ----
+def select(u, t):
+    """Indices of the t highest scores ([KVC]: C_k = the keys with the highest
+    attention), ascending.
+
+    tau is the t-th largest value; the result is every j with u_j > tau plus
+    the lowest-index keys with u_j == tau until t are taken.  Works on the
+    array's own dtype (so an fp32 score array is compared in fp32); -0 is
+    treated as +0.
+    """
+    u = np.asarray(u)
+    T = u.shape[0]
+    if not (0 < t <= T):
+        raise ValueError("need 0 < t <= T")
+    u = u + u.dtype.type(0)           # -0 + 0 = +0
+    tau = np.sort(u)[::-1][t - 1]
+    above = np.flatnonzero(u > tau)
+    ties = np.flatnonzero(u == tau)[: t - above.size]
+    return np.sort(np.concatenate([above, ties])).astype(np.int64)
+
+
+# ---------------------------------------------------------------- step 4 ----
+def mass_system(Q, Kc, m, lse, scale):
+    """Normal equations of the mass-matching fit ([KVC] mass equation), in
+    per-query max-shifted form.
+
+    A_ij = exp(scale * q_i . c_j - m_i) (compact unnormalised weights),
+    b_i  = exp(lse_i - m_i) (full mass).  Returns G = A^T A [t, t],
+    c = A^T b [t] and bb = b^T b, so ||A w - b||^2 = w^T G w - 2 c^T w + bb.
+    """
+    Q, Kc, m, lse = _f64(Q), _f64(Kc), _f64(m), _f64(lse)
+    t = Kc.shape[0]
+    G = np.zeros((t, t))
+    c = np.zeros(t)
+    bb = 0.0
+    for a, b in _chunks(Q.shape[0]):
+        A = np.exp(scale * (Q[a:b] @ Kc.T) - m[a:b, None])
+        bv = np.exp(lse[a:b] - m[a:b])
+        G += A.T @ A
+        c += A.T @ bv
+        bb += bv @ bv
+    return G, c, bb
+
+
+def _chol_solve(M, r):
+    """Solve M x = r for symmetric positive definite M by Cholesky; None if the
+    factorisation breaks down."""
+    try:
+        L = np.linalg.cholesky(M)
+    except np.linalg.LinAlgError:
+        return None
+    if _solve_tri is not None:
+        y = _solve_tri(L, r, lower=True)
+        return _solve_tri(L.T, y, lower=False)
+    return np.linalg.solve(L.T, np.linalg.solve(L, r))
+
+
+def nnls_tolerance(c, t, eps=np.finfo(np.float64).eps):
+    return 10.0 * eps * t * float(np.max(np.abs(c))) if c.size else 0.0
+
+
+def nnls_lh(G, c, max_outer=0, max_inner=0, tol=None):
+    """min_{w >= 0} ||A w - b||^2 given G = A^T A and c = A^T b, by the
+    Lawson-Hanson active-set method ([KVC]: beta is fitted by NNLS on the mass
+    equation; w = exp(beta)).
+
+    Steps: start with an empty passive set P and w = 0.  Each outer step
+    computes the descent direction g = c - G w; it stops when P holds every
+    index or no index outside P has g_j > tol; otherwise the index with the
+    largest g_j (lowest index on ties) joins P.  The inner loop solves the
+    unconstrained problem on P (G_PP z = c_P); if every z_j > 0 it becomes w;
+    otherwise w moves toward z by the largest step that keeps w >= 0 and the
+    indices that reach zero leave P.  Should the index that just joined get
+    z_j <= 0 (no progress possible in exact arithmetic, so a rounding effect)
+    it leaves again and is not retried until w changes.
+
+    Returns (w, info) with info = {"outer", "inner", "status"}.
+    """
+    G, c = _f64(G), _f64(c)
+    t = c.shape[0]
+    max_outer = max_outer or 3 * t
+    max_inner = max_inner or t
+    tol = nnls_tolerance(c, t) if tol is None else tol
+    w = np.zeros(t)
+    P = np.zeros(t, dtype=bool)
+    blocked = np.zeros(t, dtype=bool)
+    status = NOT_CONVERGED
+    outer = inner_total = 0
+    while outer < max_outer:
+        g = c - G @ w
+        cand = np.where(~P & ~blocked, g, -np.inf)
+        if P.all() or not (cand.max() > tol):
+            status = OK
+            break
+        j = int(np.argmax(cand))
+        P[j] = True
+        outer += 1
+        first = True
+        for _ in range(max_inner):
+            inner_total += 1
+            idx = np.flatnonzero(P)
+            zP = _chol_solve(G[np.ix_(idx, idx)], c[idx])
+            if zP is None:
+                return w, {"outer": outer, "inner": inner_total, "status": SINGULAR}
+            z = np.zeros(t)
+            z[idx] = zP
+            if np.all(zP > 0):
+                w = z
+                blocked[:] = False
+                break
+            if first and z[j] <= 0:
+                P[j] = False
+                blocked[j] = True
+                break
+            first = False
+            # largest step toward z that keeps w >= 0: the smallest
+            # w_j / (w_j - z_j) over the indices of P with z_j <= 0
+            neg = idx[zP <= 0]
+            den = w[neg] - z[neg]
+            ratio = np.where(den > 0, w[neg] / np.where(den > 0, den, 1.0), 0.0)
+            k = int(np.argmin(ratio))
+            w = w + ratio[k] * (z - w)
+            w[neg[k]] = 0.0
+            P &= w > 0
+            w[~P] = 0.0
+            blocked[:] = False
+        else:
+            return w, {"outer": outer, "inner": inner_total, "status": NOT_CONVERGED}
+    return w, {"outer": outer, "inner": inner_total, "status": status}
+
+
+# ---------------------------------------------------------------- step 5 ----
+def compact_weights(Q, Kc, beta, scale):
+    """Compact attention probabilities ([LC] Eq. 2-3): X = softmax_j(scale *
+    q . c_j + beta_j) over the given keys.  Q [n, d], Kc [p, d] -> X [n, p]."""
+    L = scale * (_f64(Q) @ _f64(Kc).T) + _f64(beta)[None, :]
+    L = L - L.max(axis=1, keepdims=True)
+    E = np.exp(L)
+    return E / E.sum(axis=1, keepdims=True)
+
+
+def output_system(Q, Kc, w, O, scale):
+    """Normal equations of the output-matching fit ([KVC] output equation).
+
+    On the support P = {j : w_j > 0}: X = compact softmax with beta = log w;
+    returns (support indices, H = X^T X, R = X^T O)."""
+    w = _f64(w)
+    sup = np.flatnonzero(w > 0)
+    Q, O = _f64(Q), _f64(O)
+    Kp = _f64(Kc)[sup]
+    bp = np.log(w[sup])
+    p = sup.size
+    H = np.zeros((p, p))
+    R = np.zeros((p, O.shape[1]))
+    for a, b in _chunks(Q.shape[0]):
+        X = compact_weights(Q[a:b], Kp, bp, scale)
+        H += X.T @ X
+        R += X.T @ O[a:b]
+    return sup, H, R
+
+
+def ols(H, R):
+    """C = H^-1 R by Cholesky; on breakdown a ridge of 1e-8 * mean(diag H) is
+    added once.  Returns (C, status)."""
+    H, R = _f64(H), _f64(R)
+    C = _chol_solve(H, R)
+    if C is not None:
+        return C, OK
+    lam = 1e-8 * float(np.mean(np.diag(H)))
+    C = _chol_solve(H + lam * np.eye(H.shape[0]), R)
+    if C is None:
+        C = np.zeros_like(R)
+    return C, SINGULAR
+
+
+# ------------------------------------------------------------ one head ------
+def fit_head(Q, K, V, idx, m, lse, O, scale, max_outer=0, max_inner=0):
+    """Steps 4-5 for one head given the selected keys and the full statistics:
+    returns dict(w, beta, Cv, nnls=info, ols_status)."""
+    idx = np.asarray(idx, np.int64)
+    Kc = _f64(K)[idx]
+    G, c, bb = mass_system(Q, Kc, m, lse, scale)
+    w, info = nnls_lh(G, c, max_outer, max_inner)
+    with np.errstate(divide="ignore"):
+        beta = np.log(w)
+    sup, H, R = output_system(Q, Kc, w, O, scale)
+    Cv = _f64(V)[idx].copy()
+    C, st = ols(H, R)
+    Cv[sup] = C
+    return {"w": w, "beta": beta, "Cv": Cv, "nnls": info, "ols_status": st,
+            "G": G, "c": c, "bb": bb, "H": H, "R": R, "support": sup}
+
+
+def compact_head(Q, K, V, t, scale, max_outer=0, max_inner=0):
+    """All five steps for one KV head.  Q [n_q, d] holds the reference queries
+    of every query head in the group; K, V [T, d]."""
+    m, lse, O = full_stats(Q, K, V, scale)
+    u = key_scores(Q, K, lse, scale)
+    idx = select(u, t)
+    res = fit_head(Q, K, V, idx, m, lse, O, scale, max_outer, max_inner)
+    res.update({"m": m, "lse": lse, "O": O, "u": u, "idx": idx})
+    return res
+
+
+def compact_layer(Q, K, V, t, scale, max_outer=0, max_inner=0):
+    """``compact_head`` for each KV head of a layer: Q [H, n_q, d], K, V
+    [H, T, d] -> list of per-head result dicts."""
+    return [compact_head(Q[h], K[h], V[h], t, scale, max_outer, max_inner)
+            for h in range(Q.shape[0])]

@@ -1,0 +1,320 @@
+"""Pins for the float64 oracle: checks against things other than the oracle
+itself -- brute-force loops on tiny inputs, closed forms, library routines
+(scipy's Lawson-Hanson NNLS, numpy's SVD least squares, a stable sort), and
+invariants of the method.
+
+Each ``check_*`` takes the oracle module as an argument and raises
+AssertionError on a mismatch, so that ``test_oracle_mutants`` can show that a
+plausible mistake planted in a copy of the oracle fails at least one pin.
+
+Sources of the closed forms: "Latent Compaction with Test-Time Training" §3
+Eq. (1)-(3) and (6); "KV compaction" (bkal01 blog), section "Fast KV
+Compaction via Attention Matching" (the mass/output equations; with q = 0 an
+unbiased compact cache has mass t instead of T, which is why beta exists).
+"""
+from __future__ import annotations
+
+import itertools
+import math
+
+import numpy as np
+
+
+def _rng(seed):
+    return np.random.Generator(np.random.PCG64(seed))
+
+
+def _close(a, b, tol, what):
+    a, b = np.asarray(a, float), np.asarray(b, float)
+    err = np.max(np.abs(a - b)) if a.size else 0.0
+    assert a.shape == b.shape and err <= tol, f"{what}: max abs err {err:.3e} > {tol:.1e}"
+
+
+# ----------------------------------------------------------------- step 1 ---
+def check_full_stats_brute(o):
+    """m, lse, O against plain loops over the definition (Eq. 1)."""
+    rng = _rng(11)
+    for n_q, T, d, dv in [(5, 7, 3, 2), (3, 1, 4, 3), (4, 64, 8, 2)]:
+        Q = rng.standard_normal((n_q, d))
+        K = rng.standard_normal((T, d))
+        V = rng.standard_normal((T, dv))
+        s = 0.37
+        m, lse, O = o.full_stats(Q, K, V, s)
+        for i in range(n_q):
+            logit = [s * sum(Q[i, k] * K[j, k] for k in range(d)) for j in range(T)]
+            Z = sum(math.exp(x) for x in logit)
+            _close(m[i], max(logit), 1e-12, "rowmax")
+            _close(lse[i], math.log(Z), 1e-12, "lse")
+            for c in range(dv):
+                _close(O[i, c], sum(math.exp(x) / Z * V[j, c] for j, x in enumerate(logit)),
+                       1e-12, "O")
+
+
+def check_full_stats_closed_forms(o):
+    rng = _rng(12)
+    T, d = 9, 5
+    K = rng.standard_normal((T, d))
+    V = rng.standard_normal((T, 3))
+    # q = 0: every key equally likely
+    m, lse, O = o.full_stats(np.zeros((2, d)), K, V, 0.5)
+    _close(m, [0, 0], 0, "q=0 rowmax")
+    _close(lse, [math.log(T)] * 2, 1e-14, "q=0 lse = log T")
+    _close(O, np.tile(V.mean(0), (2, 1)), 1e-14, "q=0 O = mean V")
+    # a single key: lse is its logit, the output its value
+    q = rng.standard_normal((1, d))
+    m, lse, O = o.full_stats(q, K[:1], V[:1], 0.5)
+    _close(lse, [0.5 * float(q[0] @ K[0])], 1e-14, "T=1 lse")
+    _close(O, V[:1], 1e-14, "T=1 O")
+    # identical huge logits: lse = L + log T without overflow
+    Kb = np.tile(np.array([[1.0, 0, 0, 0, 0]]), (T, 1))
+    qb = np.array([[4000.0, 0, 0, 0, 0]])
+    m, lse, O = o.full_stats(qb, Kb, V, 0.5)
+    _close(lse, [2000.0 + math.log(T)], 1e-10, "huge logits")
+    assert np.all(np.isfinite(O))
+
+
+# ----------------------------------------------------------------- step 2 ---
+def check_key_scores_brute(o):
+    """u_j = log max_i softmax_i,j against loops (Eq. 6)."""
+    rng = _rng(21)
+    n_q, T, d = 6, 10, 4
+    Q = rng.standard_normal((n_q, d)) * 2
+    K = rng.standard_normal((T, d))
+    s = 0.6
+    _, lse, _ = o.full_stats(Q, K, np.zeros((T, 1)), s)
+    u = o.key_scores(Q, K, lse, s)
+    for j in range(T):
+        best = 0.0
+        for i in range(n_q):
+            logit = [s * float(Q[i] @ K[l]) for l in range(T)]
+            p = math.exp(logit[j]) / sum(math.exp(x) for x in logit)
+            best = max(best, p)
+        _close(u[j], math.log(best), 1e-12, "key score")
+    assert np.all(u <= 1e-12), "a probability above 1"
+    # q = 0: every probability is 1/T
+    _, lse0, _ = o.full_stats(np.zeros((3, d)), K, np.zeros((T, 1)), s)
+    _close(o.key_scores(np.zeros((3, d)), K, lse0, s), [-math.log(T)] * T, 1e-14, "q=0 scores")
+    # the log-domain order is the probability order
+    a = np.exp(u)
+    assert list(np.argsort(-u, kind="stable")) == list(np.argsort(-a, kind="stable"))
+
+
+# ----------------------------------------------------------------- step 3 ---
+def _select_by_sort(u, t):
+    u = [0.0 if x == 0 else float(x) for x in u]
+    order = sorted(range(len(u)), key=lambda j: (-u[j], j))
+    return sorted(order[:t])
+
+
+def check_select(o):
+    import synth
+    cases = [synth.continuous_scores(3, 97, 31), synth.tie_heavy_scores(3, 200, 32),
+             synth.tie_heavy_scores(2, 64, 33, levels=(0.0, -0.0))]
+    for arr in cases:
+        for row in arr:
+            for t in (1, 2, 7, len(row) // 2, len(row)):
+                got = list(o.select(row, t))
+                assert got == _select_by_sort(row, t), f"select t={t}"
+    # fp32 input is compared in fp32: two keys equal in fp32 tie
+    u = np.array([-1.0, np.float32(-1.0 + 1e-9), -2.0], dtype=np.float32)
+    assert list(o.select(u, 1)) == [0]
+    try:
+        o.select(np.zeros(4), 5)
+    except ValueError:
+        pass
+    else:
+        raise AssertionError("t > T accepted")
+
+
+# ----------------------------------------------------------------- step 4 ---
+def _nnls_by_supports(A, b):
+    """Exhaustive NNLS for tiny t: the best feasible unconstrained fit over all
+    supports (the minimiser is the unconstrained fit on its own support)."""
+    t = A.shape[1]
+    best_w, best_r = np.zeros(t), float(b @ b)
+    for k in range(1, t + 1):
+        for S in itertools.combinations(range(t), k):
+            S = list(S)
+            x, *_ = np.linalg.lstsq(A[:, S], b, rcond=None)
+            if np.all(x > 0):
+                w = np.zeros(t)
+                w[S] = x
+                r = float(np.sum((A @ w - b) ** 2))
+                if r < best_r - 1e-12:
+                    best_w, best_r = w, r
+    return best_w
+
+
+def _random_problem(rng, n, t):
+    A = np.exp(rng.standard_normal((n, t)))
+    b = A @ np.abs(rng.standard_normal(t)) - 0.8 * A[:, 0] * rng.uniform(0, 2) \
+        + rng.standard_normal(n) * 3
+    return A, b
+
+
+def check_mass_system_brute(o):
+    """G = A^T A, c = A^T b in per-query max-shifted form, against loops:
+    A_ij = exp(s q_i.c_j - m_i), b_i = exp(lse_i - m_i) with m_i the full-row
+    max and lse_i the full log mass."""
+    rng = _rng(45)
+    n_q, T, d, t = 5, 8, 3, 3
+    Q = rng.standard_normal((n_q, d)) * 3
+    K = rng.standard_normal((T, d))
+    s = 0.9
+    m, lse, _ = o.full_stats(Q, K, np.zeros((T, 1)), s)
+    idx = [1, 4, 6]
+    G, c, bb = o.mass_system(Q, K[idx], m, lse, s)
+    for j in range(t):
+        for k in range(t):
+            ref = 0.0
+            for i in range(n_q):
+                logit = [s * float(Q[i] @ K[l]) for l in range(T)]
+                mx = max(logit)
+                ref += math.exp(logit[idx[j]] - mx) * math.exp(logit[idx[k]] - mx)
+            _close(G[j, k], ref, 1e-12, "mass Gram")
+        ref = 0.0
+        for i in range(n_q):
+            logit = [s * float(Q[i] @ K[l]) for l in range(T)]
+            mx = max(logit)
+            ref += math.exp(logit[idx[j]] - mx) * sum(math.exp(x - mx) for x in logit)
+        _close(c[j], ref, 1e-11, "mass right-hand side")
+
+
+def check_nnls_bruteforce(o):
+    rng = _rng(41)
+    for _ in range(12):
+        A, b = _random_problem(rng, 14, 6)
+        w, info = o.nnls_lh(A.T @ A, A.T @ b)
+        assert info["status"] == o.OK
+        _close(w, _nnls_by_supports(A, b), 1e-8, "NNLS vs support enumeration")
+
+
+def check_nnls_scipy(o):
+    from scipy.optimize import nnls as scipy_nnls
+    rng = _rng(42)
+    for t in (5, 12, 30):
+        A, b = _random_problem(rng, 3 * t, t)
+        w, info = o.nnls_lh(A.T @ A, A.T @ b)
+        ws, _ = scipy_nnls(A, b)
+        assert info["status"] == o.OK
+        _close(w, ws, 1e-8 * max(1.0, np.abs(ws).max()), "NNLS vs scipy")
+
+
+def check_nnls_planted_and_kkt(o):
+    rng = _rng(43)
+    t = 10
+    A = np.exp(rng.standard_normal((40, t)))
+    ws = np.abs(rng.standard_normal(t))
+    ws[[1, 4, 7]] = 0.0
+    w, _ = o.nnls_lh(A.T @ A, A.T @ (A @ ws))
+    _close(w, ws, 1e-9, "planted NNLS solution")
+    # KKT on a problem with active bounds
+    A, b = _random_problem(rng, 60, 20)
+    G, c = A.T @ A, A.T @ b
+    w, info = o.nnls_lh(G, c)
+    g = c - G @ w
+    tol = 1e-9 * np.abs(c).max()
+    assert np.all(w >= 0), "negative weight"
+    assert np.all(g[w == 0] <= tol), "a zero weight could still lower the residual"
+    assert np.all(np.abs(g[w > 0]) <= tol), "gradient not zero on the support"
+    assert np.any(w == 0), "problem has no active bound (test is not testing)"
+
+
+def check_nnls_q_zero_and_caps(o):
+    """All queries at q = 0: A = 1, b = T (the pages' argument for beta): an
+    unbiased compact cache (w = 1) has mass t, the fit restores sum w = T."""
+    n, t, T = 7, 4, 50
+    A = np.ones((n, t))
+    b = np.full(n, float(T))
+    w, info = o.nnls_lh(A.T @ A, A.T @ b)
+    _close(w.sum(), T, 1e-9, "q=0: compact mass sum(w) = T")
+    assert abs(np.ones(t).sum() - T) > 1, "unbiased mass equals T (test is not testing)"
+    rng = _rng(44)
+    A, b = _random_problem(rng, 30, 10)
+    _, info = o.nnls_lh(A.T @ A, A.T @ b, max_outer=1)
+    assert info["status"] == o.NOT_CONVERGED, "iteration cap not reported"
+
+
+# ----------------------------------------------------------------- step 5 ---
+def check_compact_weights(o):
+    rng = _rng(51)
+    Q = rng.standard_normal((5, 3))
+    Kc = rng.standard_normal((4, 3))
+    beta = rng.standard_normal(4)
+    s = 0.8
+    X = o.compact_weights(Q, Kc, beta, s)
+    for i in range(5):
+        e = [math.exp(s * float(Q[i] @ Kc[j]) + beta[j]) for j in range(4)]
+        _close(X[i], np.array(e) / sum(e), 1e-14, "compact softmax (Eq. 2-3)")
+    _close(X.sum(1), np.ones(5), 1e-14, "rows sum to 1")
+    _close(o.compact_weights(Q, Kc, beta + 7.0, s), X, 1e-14, "shift invariance")
+
+
+def check_ols(o):
+    rng = _rng(52)
+    n, t, d = 80, 9, 4
+    X = o.compact_weights(rng.standard_normal((n, 3)) * 2, rng.standard_normal((t, 3)),
+                          rng.standard_normal(t), 1.0)
+    Ot = rng.standard_normal((n, d))
+    C, st = o.ols(X.T @ X, X.T @ Ot)
+    Cref, *_ = np.linalg.lstsq(X, Ot, rcond=None)
+    assert st == o.OK
+    _close(C, Cref, 1e-8 * max(1, np.abs(Cref).max()), "OLS vs SVD least squares")
+    H, R = X.T @ X, X.T @ Ot
+    res = np.linalg.norm(H @ C - R) / (np.linalg.norm(H) * np.linalg.norm(C) + np.linalg.norm(R))
+    assert res <= 1e-12, f"normal-equation residual {res:.2e}"
+    Cs = rng.standard_normal((t, d))
+    C2, _ = o.ols(X.T @ X, X.T @ (X @ Cs))
+    _close(C2, Cs, 1e-7, "planted OLS solution")
+    # duplicated column: singular, ridge fallback, finite answer
+    Xd = np.concatenate([X, X[:, :1]], axis=1)
+    C3, st = o.ols(Xd.T @ Xd, Xd.T @ Ot)
+    assert st == o.SINGULAR and np.all(np.isfinite(C3))
+
+
+# ------------------------------------------------------------ end to end ----
+def check_t_equals_T(o):
+    """Keeping every key (t = T) matches the full cache exactly: w = 1,
+    C_v = V, and for every query the compact mass and output equal the full
+    ones."""
+    rng = _rng(61)
+    T, d, n_q = 12, 6, 40
+    K = rng.standard_normal((T, d))
+    Q = 0.5 * K[rng.integers(0, T, n_q)] + rng.standard_normal((n_q, d))
+    V = rng.standard_normal((T, 3))
+    s = 1 / math.sqrt(d)
+    r = o.compact_head(Q, K, V, T, s)
+    assert list(r["idx"]) == list(range(T))
+    _close(r["w"], np.ones(T), 1e-8, "t=T: w = 1")
+    _close(r["Cv"], V, 1e-6, "t=T: C_v = V")
+    logit = s * Q @ K.T + r["beta"][None, :]
+    mass = np.log(np.exp(logit).sum(1))
+    _close(mass, r["lse"], 1e-8, "t=T: compact log mass = full")
+    X = o.compact_weights(Q, K, r["beta"], s)
+    _close(X @ r["Cv"], r["O"], 1e-6, "t=T: compact output = full")
+
+
+def check_fit_reduces_error(o):
+    """With t < T the fitted beta and C_v match mass and output better than
+    keeping the selected keys unchanged (beta = 0, C_v = V[idx])."""
+    import synth
+    w = synth.workload("cfg2", H=1, T=256, t=16)
+    dd = synth.make(w)
+    Q, K, V = dd["Q"][0], dd["K"][0], dd["V"][0]
+    s = w.softmax_scale
+    r = o.compact_head(Q, K, V, w.t, s)
+    Kc = K[r["idx"]].astype(float)
+    base_mass = np.log(np.exp(s * Q.astype(float) @ Kc.T).sum(1))
+    fit_mass = np.log(np.exp(s * Q.astype(float) @ Kc.T + r["beta"]).sum(1))
+    assert np.mean((fit_mass - r["lse"]) ** 2) < np.mean((base_mass - r["lse"]) ** 2)
+    Xb = o.compact_weights(Q, Kc, np.zeros(w.t), s)
+    Xf = o.compact_weights(Q, Kc, r["beta"], s)
+    assert np.sum((Xf @ r["Cv"] - r["O"]) ** 2) < np.sum((Xb @ V[r["idx"]] - r["O"]) ** 2)
+
+
+ALL_CHECKS = [
+    check_full_stats_brute, check_full_stats_closed_forms, check_key_scores_brute,
+    check_select, check_mass_system_brute, check_nnls_bruteforce, check_nnls_scipy, check_nnls_planted_and_kkt,
+    check_nnls_q_zero_and_caps, check_compact_weights, check_ols, check_t_equals_T,
+    check_fit_reduces_error,
+]

@@ -1,0 +1,94 @@
+"""Planted mistakes in a private copy of the oracle (CPU only): each plausible
+slip -- a dropped scale, a flipped sign, a wrong reduction, a tie broken the
+wrong way, a missing normalisation, a skipped step-back in the active set --
+must fail at least one pin.  The real oracle is never modified."""
+import importlib.util
+import os
+
+import numpy as np
+import pytest
+
+from oracle_pins import ALL_CHECKS
+
+ORACLE_FILE = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                           "oracle", "__init__.py")
+
+
+def _fresh_oracle():
+    spec = importlib.util.spec_from_file_location("oracle_mutant", ORACLE_FILE)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def _no_scale(o):
+    orig = o.full_stats
+    o.full_stats = lambda Q, K, V, scale: orig(Q, K, V, 1.0)
+
+
+def _unnormalised_output(o):
+    orig = o.full_stats
+
+    def f(Q, K, V, scale):
+        m, lse, O = orig(Q, K, V, scale)
+        return m, lse, O * np.exp(lse - m)[:, None]
+    o.full_stats = f
+
+
+def _score_plus_lse(o):
+    orig = o.key_scores
+    o.key_scores = lambda Q, K, lse, scale: orig(Q, K, -np.asarray(lse, float), scale)
+
+
+def _score_min(o):
+    def f(Q, K, lse, scale):
+        S = scale * (np.asarray(Q, float) @ np.asarray(K, float).T) - np.asarray(lse)[:, None]
+        return S.min(axis=0)
+    o.key_scores = f
+
+
+def _ties_high(o):
+    def f(u, t):
+        u = np.asarray(u)
+        order = sorted(range(len(u)), key=lambda j: (-float(u[j]), -j))
+        return np.sort(np.array(order[:t]))
+    o.select = f
+
+
+def _no_stepback(o):
+    def f(G, c, max_outer=0, max_inner=0, tol=None):
+        w = np.linalg.solve(np.asarray(G, float), np.asarray(c, float))
+        return w, {"outer": 1, "inner": 1, "status": o.OK}
+    o.nnls_lh = f
+
+
+def _mass_unshifted(o):
+    orig = o.mass_system
+    o.mass_system = lambda Q, Kc, m, lse, scale: orig(Q, Kc, np.zeros_like(m), lse, scale)
+
+
+def _weights_no_bias(o):
+    orig = o.compact_weights
+    o.compact_weights = lambda Q, Kc, beta, scale: orig(Q, Kc, np.zeros_like(beta), scale)
+
+
+def _ols_diag(o):
+    o.ols = lambda H, R: (np.asarray(R) / np.diag(H)[:, None], o.OK)
+
+
+MUTANTS = [_no_scale, _unnormalised_output, _score_plus_lse, _score_min, _ties_high,
+           _no_stepback, _mass_unshifted, _weights_no_bias, _ols_diag]
+
+
+@pytest.mark.parametrize("mutate", MUTANTS, ids=lambda f: f.__name__)
+def test_planted_mistake_is_caught(mutate):
+    o = _fresh_oracle()
+    mutate(o)
+    caught = []
+    for check in ALL_CHECKS:
+        try:
+            with np.errstate(all="ignore"):
+                check(o)
+        except (AssertionError, np.linalg.LinAlgError) as e:
+            caught.append((check.__name__, type(e).__name__))
+    assert caught, f"no pin catches {mutate.__name__}"
