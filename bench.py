@@ -1,0 +1,384 @@
+#!/usr/bin/env python
+"""Benchmark of one-layer attention-matching compaction on GB300.
+
+Workload: one GQA layer with 8 KV heads x 4 query heads per group,
+T = 8192 cached positions, n_q = 4*T = 32768 context-prefill reference
+queries per KV head, d = 128, t = 256 keys kept (32x), bf16 Q/K/V with the
+synthetic "peaked" recipe (outlier key channels, queries drawn near keys).
+A step compacts one layer: all five steps (full statistics, key scores,
+top-t selection, NNLS biases, OLS values) on inputs already in HBM.
+Successive steps cycle through four distinct layers (400 MB of inputs, more
+than the 129 MB L2), so no step finds its inputs in L2.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl lc|reference]
+
+Prints one JSON line.  `value` is ms per compacted layer over the whole job;
+`roofline` is the dominant kernel's algorithmic throughput against the
+measured peak; `e2e` is the same metric through the host-buffer entry point
+with the host<->device copies inside the timed region; `cpu_baseline` is the
+float64 oracle timed on this machine's host cores on a bounded sample.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "ms per layer compaction (8 KV heads, T=8192, t=256); QK^T TFLOP/s vs peak"
+WORKLOAD = "cfg3"
+N_LAYERS = 4
+
+
+def args_():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="lc", choices=["lc", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=20.0,
+                    help="seconds of oracle work for the cpu_baseline sample")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            m = json.load(f)
+        return {"hbm_gbs": m["hbm_gbs"], "bf16_tflops": m["bf16_tflops"],
+                "bf16_tflops_sustained": m.get("bf16_tflops_sustained", m["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def workload():
+    import synth
+    return synth.workload(WORKLOAD)
+
+
+def flops(w):
+    """Algorithmic flops of one layer (per launch of each kernel)."""
+    H, nq, T, d, t = w.H, w.n_q, w.T, w.d, w.t
+    return {
+        "attn_stats": 4.0 * nq * T * d * H,        # S = Q K^T and O = P V
+        "key_scores": 2.0 * nq * T * d * H,        # S recomputed
+        "gram_mass": H * (2.0 * nq * t * d + 2.0 * nq * t * t),
+        "gram_out": H * (2.0 * nq * t * d + 2.0 * nq * t * t + 2.0 * nq * t * d),
+        "layer": H * (6.0 * nq * T * d + 6.0 * nq * t * d + 4.0 * nq * t * t),
+    }
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.f = None
+
+    def start(self):
+        try:
+            self.f = tempfile.TemporaryFile(mode="w+")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.seek(0)
+        rows = [r.split(",") for r in self.f.read().strip().splitlines() if r.strip()]
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx = max(mx, float(r[2]))
+                for n, v in zip(names, r[5:9]):
+                    if v.strip().lower() == "active":
+                        reasons.add(n)
+            except (ValueError, IndexError):
+                continue
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ oracle
+def oracle_sample(budget_s: float):
+    """Time the float64 oracle on one KV head of the workload with a subset of
+    the reference queries sized to about `budget_s` seconds, and scale to ms
+    per layer by the ratio of work (linear in the number of queries) times the
+    number of heads."""
+    import numpy as np
+
+    import oracle
+    import synth
+    w = workload()
+    d = synth.make(w, heads=[0])
+    Q, K, V = d["Q"][0], d["K"][0], d["V"][0]
+    s = w.softmax_scale
+
+    def run(nq):
+        q = Q[:nq].astype(np.float64)
+        t0 = time.perf_counter()
+        oracle.compact_head(q, K, V, w.t, s)
+        return time.perf_counter() - t0
+
+    probe_n = 1024
+    tp = run(probe_n)
+    n = int(min(w.n_q, max(probe_n, probe_n * budget_s / max(tp, 1e-3))))
+    n = max(probe_n, n // 1024 * 1024)
+    t_s = run(n)
+    ms_layer = t_s * 1e3 * (w.n_q / n) * w.H
+    return ms_layer, n, t_s
+
+
+def reference_arm(a):
+    """The float64 oracle as it stands, on the host cores (rank 0 only)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = workload()
+    total_budget = 120.0
+    per_step = max(0.5, min(10.0, total_budget / max(1, a.steps + a.warmup)))
+    times = []
+    n_used = None
+    for i in range(a.warmup + a.steps):
+        ms, n, _ = oracle_sample(per_step)
+        n_used = n
+        if i >= a.warmup:
+            times.append(ms)
+    value = statistics.mean(times)
+    cores = os.cpu_count()
+    sample = (f"1 of {w.H} KV heads of one {WORKLOAD} layer, {n_used} of {w.n_q} reference "
+              f"queries per step; scaled to a full layer by query count x heads")
+    line = {
+        "metric": METRIC, "value": value, "unit": "ms", "impl": "reference",
+        "n_gpus": a.gpus, "steps": a.steps, "warmup": a.warmup, "ms_per_step": value,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_dict(w, a.gpus),
+        "cpu_baseline": {"value": value, "unit": "ms", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_dict(w, n):
+    return {"workload": f"{WORKLOAD}: one GQA layer, {w.H} KV heads x {w.G} query heads, "
+                        f"T={w.T}, n_q={w.n_q} per KV head, d={w.d}, t={w.t}, bf16, "
+                        f"peaked synthetic Q/K/V",
+            "H": w.H, "G": w.G, "T": w.T, "n_q": w.n_q, "d": w.d, "t": w.t,
+            "parallelism": f"independent layers, {n} GPU(s)",
+            "l2": f"steps cycle over {N_LAYERS} distinct layers ({N_LAYERS * 100} MB of inputs > 129 MB L2)"}
+
+
+def traffic_for(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel
+    source has not changed since it was taken."""
+    p = os.path.join(ROOT, "profiles", f"{kernel}_{WORKLOAD}.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f)
+    src = os.path.join(ROOT, "kv_cache_compaction_gb300", "csrc", rec.get("source", ""))
+    if not os.path.exists(src):
+        return None
+    with open(src, "rb") as f:
+        h = hashlib.sha256(f.read()).hexdigest()
+    return rec.get("dram_bytes_per_launch") if h == rec.get("source_sha256") else None
+
+
+# ------------------------------------------------------------------ main arm
+def main():
+    a = args_()
+    if a.impl == "reference":
+        reference_arm(a)
+        return
+    import numpy as np
+    import torch
+
+    import synth
+    from kv_cache_compaction_gb300 import build as lcbuild
+    lcbuild.build()
+    import kv_cache_compaction_gb300 as lc
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = workload()
+    fl = flops(w)
+
+    def up(arr):
+        bits = synth.bf16_bits(arr).view(np.int16)
+        return torch.from_numpy(np.ascontiguousarray(bits)).view(torch.bfloat16)
+
+    layers_host = []
+    layers = []
+    for l in range(N_LAYERS):
+        d = synth.make(w.layer(rank * N_LAYERS + l))
+        hq, hk, hv = up(d["Q"]), up(d["K"]), up(d["V"])
+        layers_host.append((hq, hk, hv))
+        layers.append((hq.to(dev), hk.to(dev), hv.to(dev)))
+    comp = lc.Compactor(local)
+    H, t, dd = w.H, w.t, w.d
+    out = (torch.empty((H, t), dtype=torch.int32, device=dev),
+           torch.empty((H, t), dtype=torch.float32, device=dev),
+           torch.empty((H, t), dtype=torch.float32, device=dev),
+           torch.empty((H, t, dd), dtype=torch.float32, device=dev))
+
+    def step(i):
+        Q, K, V = layers[i % N_LAYERS]
+        comp.compact_layer(Q, K, V, t, out=out)
+
+    for i in range(a.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    rep = comp.report(H)
+    if rep.device_error_bits:
+        raise RuntimeError(f"device error bits {rep.device_error_bits}")
+
+    stream = torch.cuda.current_stream(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    comp.profile_read()
+    comp.profile(True)
+    clk = ClockSampler(local)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clk.start()
+    time.sleep(0.3)  # let the sampler start before the timed work
+    t_wall = time.perf_counter()
+    ev0.record(stream)
+    for i in range(a.steps):
+        step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    wall_s = time.perf_counter() - t_wall
+    if dist:
+        dist.barrier()
+    clocks = clk.stop()
+    comp.profile(False)
+    kern = comp.profile_read()
+    ms_total = ev0.elapsed_time(ev1)
+    ms_step = ms_total / a.steps
+    if dist:
+        tt = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_step = float(tt.item())
+    value = ms_step / world   # whole job: `world` layers per step
+
+    # per-kernel breakdown (per step) and the dominant kernel's roofline
+    pk = peaks()
+    per_kernel = {k: {"ms_per_step": v[0] / a.steps, "launches_per_step": v[1] / a.steps}
+                  for k, v in kern.items()}
+    launches = int(sum(v[1] for v in kern.values()))
+    dom = max(kern, key=lambda k: kern[k][0])
+    dom_ms = kern[dom][0] / max(kern[dom][1], 1)
+    if dom in ("attn_stats", "key_scores", "gram_mass", "gram_out"):
+        ach = fl[dom] / (dom_ms * 1e-3) / 1e12
+        roof = {"kernel": dom, "bound": "tensor", "achieved": ach,
+                "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                "frac": ach / pk["bf16_tflops_sustained"], "traffic": traffic_for(dom),
+                "peak_kind": f"bf16 dense sustained ({pk['source']})",
+                "algorithmic_flops_per_launch": fl[dom], "avg_launch_ms": dom_ms}
+    else:
+        roof = {"kernel": dom, "bound": "alu", "achieved": None, "peak": None, "unit": None,
+                "frac": None, "traffic": None, "avg_launch_ms": dom_ms}
+    qkt = {}
+    for k, f in (("attn_stats", fl["attn_stats"]), ("key_scores", fl["key_scores"])):
+        if k in kern:
+            ms = kern[k][0] / max(kern[k][1], 1)
+            tf = f / (ms * 1e-3) / 1e12
+            qkt[k] = {"tflops": tf, "frac_of_peak": tf / pk["bf16_tflops_sustained"],
+                      "ms": ms}
+
+    # end to end through the host-buffer entry point
+    e2e = None
+    if a.e2e_steps > 0:
+        pinned = [tuple(x.pin_memory() for x in L) for L in layers_host]
+        hout = (torch.empty((H, t), dtype=torch.int32).pin_memory(),
+                torch.empty((H, t)).pin_memory(), torch.empty((H, t)).pin_memory(),
+                torch.empty((H, t, dd)).pin_memory())
+        for i in range(2):
+            Q, K, V = pinned[i % N_LAYERS]
+            comp.compact_layer_host(Q, K, V, t, hout)
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(a.e2e_steps):
+            Q, K, V = pinned[i % N_LAYERS]
+            comp.compact_layer_host(Q, K, V, t, hout)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms_e2e = e0.elapsed_time(e1) / a.e2e_steps
+        if dist:
+            tt = torch.tensor([ms_e2e], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            ms_e2e = float(tt.item())
+        h2d = sum(x.numel() * x.element_size() for x in pinned[0])
+        d2h = sum(x.numel() * x.element_size() for x in hout)
+        e2e = {"value": ms_e2e / world, "unit": "ms", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if rank == 0 and world == 1 and not a.no_cpu_baseline:
+        ms_l, n, t_s = oracle_sample(a.cpu_budget)
+        cpu = {"value": ms_l, "unit": "ms", "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"1 of {w.H} KV heads of one {WORKLOAD} layer with {n} of {w.n_q} "
+                         f"reference queries ({t_s:.1f} s of CPU work); scaled to a full layer "
+                         f"by query count x heads"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "ms", "n_gpus": world, "steps": a.steps,
+            "warmup": a.warmup, "ms_per_step": ms_step, "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": config_dict(w, world), "roofline": roof, "qkt": qkt,
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
+            "per_kernel": per_kernel, "layer_tflops": fl["layer"] / (ms_step * 1e-3) / 1e12,
+            "wall_s_timed": wall_s,
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,154 @@
+/*
+ * lc.h -- attention-matching compaction of one layer's KV cache on one GPU.
+ *
+ * For each KV head the library runs five steps over the reference queries Q
+ * of every query head that shares that KV head (context-prefill queries):
+ *
+ *  1. full statistics: S = scale * Q K^T, row max m, log mass lse and output
+ *     O = softmax(S) V  ("Latent Compaction with Test-Time Training", §3
+ *     Preliminaries, Eq. (1));
+ *  2. key score: u_j = max_i (S_ij - lse_i), the log of the largest attention
+ *     probability key j receives (same paper, §3.2, Eq. (6));
+ *  3. selection: the t keys with the highest score, ties to the lower index,
+ *     returned in ascending order ("KV compaction" blog, section "Fast KV
+ *     Compaction via Attention Matching": C_k is the set of keys with the
+ *     highest attention and is a subset of K);
+ *  4. biases: w = exp(beta) >= 0 minimising
+ *     sum_i (sum_j exp(s q_i.C_kj + beta_j - m_i) - exp(lse_i - m_i))^2,
+ *     the mass-matching equation of the same blog section solved as
+ *     non-negative least squares in per-query max-shifted form;
+ *  5. values: C_v minimising sum_i || softmax_j(s q_i.C_kj + beta_j) C_v - O_i ||^2,
+ *     the output-matching equation solved as ordinary least squares (biased
+ *     compact attention as in "Latent Compaction ...", §3.1 Eq. (2)-(3)).
+ *
+ * Conventions shared by every entry point
+ *  - Tensors are device pointers owned by the caller; the library never
+ *    allocates or frees caller memory.  Scratch memory is a caller-provided
+ *    device workspace of at least lc_workspace_bytes() bytes (256-byte
+ *    aligned).  Host-side state lives in an lc_handle.
+ *  - Layouts are row-major and dense: Q [H][n_q][d], K and V [H][T][d],
+ *    rowmax and lse [H][n_q], O [H][n_q][d], u [H][T], idx [H][t],
+ *    w and beta [H][t], Cv [H][t][d].  Row g*T + p of a head's Q is query
+ *    head g of the group at position p (any order works: queries are a set).
+ *  - Q, K, V are bfloat16 (in_dtype LC_BF16, d = 64 or 128) or float32
+ *    (LC_FP32, d = 64 only).  All other floating-point tensors are float32;
+ *    idx is int32.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and runs asynchronously.  An error found on the host is
+ *    returned at once and nothing is enqueued.  Outcomes found on the device
+ *    (an NNLS or solver iteration cap, a singular system, a timed-out wait)
+ *    are recorded per head and read back with lc_get_report().
+ *  - Outputs are finite except beta_j = -inf where w_j = 0 (key j keeps a
+ *    zero weight, so it never receives attention).
+ *  - A handle may be used by one host thread at a time; calls that share a
+ *    workspace must not overlap on the device.
+ */
+#ifndef LC_H_
+#define LC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  LC_OK = 0,
+  LC_ERR_INVALID_ARG = 1,    /* bad pointer, size or shape */
+  LC_ERR_UNSUPPORTED = 2,    /* valid but not implemented (e.g. d = 96) */
+  LC_ERR_WORKSPACE = 3,      /* workspace too small or misaligned */
+  LC_ERR_CUDA = 4,           /* a CUDA runtime/driver call failed */
+  LC_ERR_NOT_CONVERGED = 5,  /* NNLS hit its iteration cap (outputs finite) */
+  LC_ERR_SINGULAR = 6,       /* a Cholesky factorisation broke down; a ridge
+                                of 1e-6 * mean(diag) was added once */
+  LC_ERR_TIMEOUT = 7         /* a device-side wait gave up (internal error) */
+} lc_status;
+
+typedef enum { LC_BF16 = 0, LC_FP32 = 1 } lc_dtype;
+
+typedef struct {
+  int n_kv_heads;     /* H >= 1 */
+  int n_q;            /* reference queries per KV head (G*T for context prefill), >= 1 */
+  int T;              /* cached keys per head, >= 1 */
+  int d;              /* head dimension: 64 or 128 */
+  int t;              /* keys kept per head, 1 <= t <= min(T, 1024) */
+  int in_dtype;       /* lc_dtype of Q, K and V */
+  float scale;        /* softmax scale; 0 selects 1/sqrt(d) */
+  int nnls_max_iter;  /* NNLS iteration cap; 0 selects 3*t */
+} lc_shape;
+
+typedef struct lc_context* lc_handle;
+
+/* Create a handle bound to CUDA device `device`.  Allocates the handle's own
+ * per-head report buffers (a few KB) on that device. */
+lc_status lc_create(lc_handle* out, int device);
+lc_status lc_destroy(lc_handle h);
+
+/* Workspace bytes that lc_compact_layer / lc_full_attn_stats / lc_key_scores
+ * / lc_fit_only need for `shape` (the largest of the four). */
+lc_status lc_workspace_bytes(const lc_shape* shape, size_t* bytes);
+
+/* Step 1.  rowmax, lse: [H][n_q] (natural-log units, scale applied);
+ * O: [H][n_q][d].  Any of the three outputs may be NULL to skip it. */
+lc_status lc_full_attn_stats(lc_handle h, const lc_shape* shape, const void* Q, const void* K,
+                             const void* V, float* rowmax, float* lse, float* O, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
+/* Step 2 given the log masses: u [H][T] = max_i (scale*q_i.k_j - lse_i). */
+lc_status lc_key_scores(lc_handle h, const lc_shape* shape, const void* Q, const void* K,
+                        const float* lse, float* u, void* workspace, size_t workspace_bytes,
+                        void* stream);
+
+/* Step 3 on given scores: idx [n_heads][t], ascending; the t largest of each
+ * row of u [n_heads][T]; equal scores go to the lower index; -0 == +0.
+ * Scores must not be NaN. */
+lc_status lc_select_topt(lc_handle h, int n_heads, int T, int t, const float* u, int32_t* idx,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+/* Steps 4-5 for given selected keys and full statistics (rowmax, lse, O as
+ * produced by lc_full_attn_stats).  idx entries must be distinct and in
+ * [0, T).  Outputs w, beta [H][t] and Cv [H][t][d]. */
+lc_status lc_fit_only(lc_handle h, const lc_shape* shape, const void* Q, const void* K,
+                      const void* V, const int32_t* idx, const float* rowmax, const float* lse,
+                      const float* O, float* w, float* beta, float* Cv, void* workspace,
+                      size_t workspace_bytes, void* stream);
+
+/* Steps 1-5.  Outputs idx [H][t], w, beta [H][t], Cv [H][t][d]. */
+lc_status lc_compact_layer(lc_handle h, const lc_shape* shape, const void* Q, const void* K,
+                           const void* V, int32_t* idx, float* w, float* beta, float* Cv,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/* lc_compact_layer on HOST buffers: copies Q, K, V to the device workspace,
+ * runs the five steps, copies idx, w, beta, Cv back, and synchronises
+ * `stream`.  Host buffers should be page-locked for full copy bandwidth.
+ * Needs lc_host_workspace_bytes() bytes of device workspace. */
+lc_status lc_host_workspace_bytes(const lc_shape* shape, size_t* bytes);
+lc_status lc_compact_layer_host(lc_handle h, const lc_shape* shape, const void* Q_host,
+                                const void* K_host, const void* V_host, int32_t* idx_host,
+                                float* w_host, float* beta_host, float* Cv_host,
+                                void* workspace, size_t workspace_bytes, void* stream);
+
+/* Per-head outcome of the last lc_fit_only / lc_compact_layer on this handle:
+ * head_status[H] (lc_status values), nnls_iters[H] and device error bits.
+ * Synchronises `stream`.  Any pointer may be NULL. */
+lc_status lc_get_report(lc_handle h, int n_heads, int32_t* head_status, int32_t* nnls_iters,
+                        uint32_t* device_error_bits, void* stream);
+
+/* Per-kernel timing of this handle's own launches: with profiling on, every
+ * launch is bracketed by CUDA events on the call's stream (a few
+ * microseconds each).  lc_profile_read() waits for the recorded events, fills
+ * up to max_kernels entries -- names (32 chars each, NUL-terminated),
+ * total milliseconds and launch counts, grouped by kernel name -- sets
+ * *n_kernels to the number of distinct names, and clears the totals. */
+lc_status lc_profile_enable(lc_handle h, int on);
+lc_status lc_profile_read(lc_handle h, int max_kernels, char* names, double* total_ms,
+                          int32_t* launches, int* n_kernels);
+
+const char* lc_status_string(lc_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LC_H_ */

@@ -1,0 +1,756 @@
+// Host orchestrator behind include/lc.h: argument checks, workspace carving,
+// TMA tensor maps, and the launch sequence of the five compaction steps.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/lc.h"
+#include "lc_common.cuh"
+#include "lc_kernels.cuh"
+
+using namespace lc;
+
+namespace {
+
+constexpr int kMaxHeads = 4096;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool get_encode() {
+  std::call_once(g_encode_once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// [H][rows][inner] 16-bit tensor, 64-element x box_rows boxes, 128B swizzle,
+// zero fill outside the tensor.
+bool make_map(CUtensorMap* m, const void* ptr, bool bf16, int inner, int rows, int H,
+              int box_rows) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(H)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner) * 2,
+                           static_cast<cuuint64_t>(inner) * 2 * rows};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = g_encode(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                        3, const_cast<void*>(ptr), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+struct Plan {
+  OperandMode mode;
+  bool bf16_in;
+  int H, n_q, T, d, t, d_qk, n_q_pad, t_pad, nblk;
+  float scale;
+  int max_iter;
+  int ks_split, ks_tiles;
+  int g5_split, g5_slabs;
+  int g7_split, g7_slabs;
+  // workspace offsets (bytes)
+  size_t qop, kop, vhi, vlo;            // operand copies (16-bit)
+  size_t m_pad, lse_pad, ohi, olo;      // step-1 results
+  size_t ucode, idx;                    // steps 2-3
+  size_t kc, rowsh2, rowb, colb2, lc2;  // fit inputs
+  size_t gpart, cpart, G, c;            // mass system
+  size_t hpart, rpart, Hm, R, vc;       // output system
+  size_t mat, vec;                      // solver scratch
+  size_t w_tmp, beta_tmp;               // steps 4 results when the caller gives none
+  size_t total;
+};
+
+int choose_split(int units, int per_split_min, int max_split) {
+  // enough CTAs for about two waves over 152 SMs
+  int s = (2 * 152 + units - 1) / units;
+  if (s < 1) s = 1;
+  if (s > max_split) s = max_split;
+  (void)per_split_min;
+  return s;
+}
+
+lc_status validate(const lc_shape* s) {
+  if (!s) return LC_ERR_INVALID_ARG;
+  if (s->n_kv_heads < 1 || s->n_kv_heads > kMaxHeads || s->n_q < 1 || s->T < 1 || s->t < 1)
+    return LC_ERR_INVALID_ARG;
+  if (s->t > s->T) return LC_ERR_INVALID_ARG;
+  if (s->t > 1024) return LC_ERR_UNSUPPORTED;
+  if (s->d != 64 && s->d != 128) return LC_ERR_UNSUPPORTED;
+  if (s->in_dtype != LC_BF16 && s->in_dtype != LC_FP32) return LC_ERR_INVALID_ARG;
+  if (s->in_dtype == LC_FP32 && s->d != 64) return LC_ERR_UNSUPPORTED;
+  if (!(s->scale >= 0.f) || !std::isfinite(s->scale)) return LC_ERR_INVALID_ARG;
+  if (s->nnls_max_iter < 0) return LC_ERR_INVALID_ARG;
+  // tensor-map extents are 32-bit
+  if (static_cast<long long>(s->n_q) + 256 > (1ll << 31) || static_cast<long long>(s->T) + 256 > (1ll << 31))
+    return LC_ERR_UNSUPPORTED;
+  return LC_OK;
+}
+
+Plan make_plan(const lc_shape* s) {
+  Plan p{};
+  p.H = s->n_kv_heads;
+  p.n_q = s->n_q;
+  p.T = s->T;
+  p.d = s->d;
+  p.t = s->t;
+  p.bf16_in = s->in_dtype == LC_BF16;
+  p.mode = p.bf16_in ? (s->d == 128 ? kBF16d128 : kBF16d64) : kSplitF16d64;
+  p.d_qk = p.bf16_in ? s->d : 3 * s->d;
+  p.n_q_pad = static_cast<int>(round_up(s->n_q, 128));
+  p.t_pad = static_cast<int>(round_up(s->t, 128));
+  p.nblk = p.t_pad / 128;
+  p.scale = s->scale > 0.f ? s->scale : 1.f / std::sqrt(static_cast<float>(s->d));
+  p.max_iter = s->nnls_max_iter > 0 ? s->nnls_max_iter : 3 * s->t;
+
+  const int nqt = p.n_q_pad / 128;
+  const int ktiles = (p.T + 127) / 128;
+  p.ks_split = choose_split(ktiles * p.H, 1, nqt);
+  p.ks_tiles = (nqt + p.ks_split - 1) / p.ks_split;
+  p.ks_split = (nqt + p.ks_tiles - 1) / p.ks_tiles;
+
+  const int slabs = p.n_q_pad / 64;
+  const int npairs = p.nblk * (p.nblk + 1) / 2;
+  p.g5_split = choose_split(npairs * p.H, 1, slabs);
+  p.g5_slabs = (slabs + p.g5_split - 1) / p.g5_split;
+  p.g5_split = (slabs + p.g5_slabs - 1) / p.g5_slabs;
+  p.g7_split = choose_split((npairs + p.nblk) * p.H, 1, slabs);
+  p.g7_slabs = (slabs + p.g7_split - 1) / p.g7_split;
+  p.g7_split = (slabs + p.g7_slabs - 1) / p.g7_slabs;
+
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = round_up(off + bytes, 256);
+    return o;
+  };
+  const size_t H = p.H;
+  if (p.bf16_in) {
+    p.qop = p.kop = 0;  // caller's Q and K are used directly
+    p.vhi = take(H * p.T * p.d * 2);
+    p.vlo = 0;
+  } else {
+    p.qop = take(H * p.n_q * p.d_qk * 2);
+    p.kop = take(H * p.T * p.d_qk * 2);
+    p.vhi = take(H * p.T * p.d * 2);
+    p.vlo = take(H * p.T * p.d * 2);
+  }
+  p.m_pad = take(H * p.n_q_pad * 4);
+  p.lse_pad = take(H * p.n_q_pad * 4);
+  p.ohi = take(H * p.n_q * p.d * 2);
+  p.olo = take(H * p.n_q * p.d * 2);
+  p.ucode = take(H * p.T * 4);
+  p.idx = take(H * p.t * 4);
+  p.kc = take(H * p.t_pad * p.d_qk * 2);
+  p.rowsh2 = take(H * p.n_q_pad * 4);
+  p.rowb = take(H * p.n_q_pad * 4);
+  p.colb2 = take(H * p.t_pad * 4);
+  p.lc2 = take(H * p.n_q_pad * 4);
+  const size_t tt = static_cast<size_t>(p.t_pad) * p.t_pad;
+  p.gpart = take(static_cast<size_t>(p.g5_split) * H * tt * 4);
+  p.cpart = take(static_cast<size_t>(p.g5_split) * H * p.t_pad * 4);
+  p.G = take(H * tt * 4);
+  p.c = take(H * p.t_pad * 4);
+  p.hpart = take(static_cast<size_t>(p.g7_split) * H * tt * 4);
+  p.rpart = take(static_cast<size_t>(p.g7_split) * H * p.t_pad * p.d * 4);
+  p.Hm = take(H * tt * 4);
+  p.R = take(H * p.t_pad * p.d * 4);
+  p.vc = take(H * p.t_pad * p.d * 4);
+  p.mat = take(H * tt * 4);
+  p.vec = take(H * 8 * p.t_pad * 4);
+  p.w_tmp = take(H * p.t * 4);
+  p.beta_tmp = take(H * p.t * 4);
+  p.total = off;
+  return p;
+}
+
+#define LC_CUDA(call)                                   \
+  do {                                                  \
+    cudaError_t e_ = (call);                            \
+    if (e_ != cudaSuccess) {                            \
+      std::fprintf(stderr, "lc: %s failed: %s\n", #call, cudaGetErrorString(e_)); \
+      return LC_ERR_CUDA;                               \
+    }                                                   \
+  } while (0)
+
+}  // namespace
+
+// Optional per-kernel timing: CUDA events recorded on the call's stream
+// around each of the library's launches, resolved when read.
+struct Profiler {
+  bool on = false;
+  struct Pending {
+    std::string name;
+    int launches;
+    cudaEvent_t a, b;
+  };
+  std::vector<Pending> pending;
+  std::vector<cudaEvent_t> pool;
+  std::map<std::string, std::pair<double, int>> acc;
+
+  cudaEvent_t get() {
+    if (!pool.empty()) {
+      cudaEvent_t e = pool.back();
+      pool.pop_back();
+      return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+  }
+  void resolve() {
+    for (auto& p : pending) {
+      float ms = 0.f;
+      cudaEventSynchronize(p.b);
+      cudaEventElapsedTime(&ms, p.a, p.b);
+      auto& a = acc[p.name];
+      a.first += ms;
+      a.second += p.launches;
+      pool.push_back(p.a);
+      pool.push_back(p.b);
+    }
+    pending.clear();
+  }
+  ~Profiler() {
+    for (auto& p : pending) {
+      cudaEventDestroy(p.a);
+      cudaEventDestroy(p.b);
+    }
+    for (auto e : pool) cudaEventDestroy(e);
+  }
+};
+
+struct lc_context {
+  int device = 0;
+  int32_t* d_status = nullptr;  // [kMaxHeads]
+  int32_t* d_iters = nullptr;   // [kMaxHeads]
+  uint32_t* d_err = nullptr;
+  Profiler prof;
+};
+
+namespace {
+
+struct Ctx {
+  lc_context* h;
+  Plan p;
+  uint8_t* ws;
+  cudaStream_t st;
+  template <class T>
+  T* at(size_t off) const {
+    return reinterpret_cast<T*>(ws + off);
+  }
+};
+
+// Brackets one kernel launch with profiler events when profiling is on.
+struct ProfScope {
+  lc_context* h;
+  cudaStream_t st;
+  cudaEvent_t b = nullptr;
+  ProfScope(lc_context* h_, cudaStream_t st_, const char* name, int launches)
+      : h(h_), st(st_) {
+    if (!h->prof.on) return;
+    if (h->prof.pending.size() > 8192) h->prof.resolve();
+    cudaEvent_t a = h->prof.get();
+    b = h->prof.get();
+    cudaEventRecord(a, st);
+    h->prof.pending.push_back({name, launches, a, b});
+  }
+  ~ProfScope() {
+    if (b) cudaEventRecord(b, st);
+  }
+};
+// `n`: kernel launches inside the scope (0 for a memset).
+#define LC_PROF(c, name, n) ProfScope prof_scope_##__LINE__((c).h, (c).st, name, n)
+
+lc_status check_ws(const Plan& p, void* ws, size_t bytes) {
+  if (!ws) return LC_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(ws) % 256) return LC_ERR_WORKSPACE;
+  if (bytes < p.total) return LC_ERR_WORKSPACE;
+  return LC_OK;
+}
+
+lc_status enter(lc_context* h) {
+  if (!h) return LC_ERR_INVALID_ARG;
+  if (!get_encode()) return LC_ERR_CUDA;
+  LC_CUDA(cudaSetDevice(h->device));
+  return LC_OK;
+}
+
+// Operand copies: fp16 V for bf16 inputs; split fp16 Q/K/V for fp32 inputs.
+lc_status prepare_operands(const Ctx& c, const void* Q, const void* K, const void* V, bool need_v,
+                           const void** qop, const void** kop) {
+  const Plan& p = c.p;
+  const size_t nv = static_cast<size_t>(p.H) * p.T * p.d;
+  if (p.bf16_in) {
+    *qop = Q;
+    *kop = K;
+    if (need_v) {
+      LC_PROF(c, "convert_v", 1);
+      LC_CUDA(launch_convert_bf16_to_f16(static_cast<const __nv_bfloat16*>(V), c.at<__half>(p.vhi),
+                                         nv, c.st));
+    }
+  } else {
+    LC_CUDA(launch_split_rows3(static_cast<const float*>(Q), c.at<__half>(p.qop),
+                               static_cast<size_t>(p.H) * p.n_q, p.d, 0, c.st));
+    LC_CUDA(launch_split_rows3(static_cast<const float*>(K), c.at<__half>(p.kop),
+                               static_cast<size_t>(p.H) * p.T, p.d, 1, c.st));
+    if (need_v)
+      LC_CUDA(launch_split_f32(static_cast<const float*>(V), c.at<__half>(p.vhi), c.at<__half>(p.vlo),
+                               nv, c.st));
+    *qop = c.ws + p.qop;
+    *kop = c.ws + p.kop;
+  }
+  return LC_OK;
+}
+
+lc_status run_pass1(const Ctx& c, const void* qop, const void* kop, float* rowmax, float* lse,
+                    float* O, bool to_ws) {
+  const Plan& p = c.p;
+  const bool qk_bf16 = p.bf16_in;
+  const int bn = p.mode == kSplitF16d64 ? 64 : 128;
+  CUtensorMap mQ, mK, mV, mVlo;
+  if (!make_map(&mQ, qop, qk_bf16, p.d_qk, p.n_q, p.H, 128)) return LC_ERR_CUDA;
+  if (!make_map(&mK, kop, qk_bf16, p.d_qk, p.T, p.H, bn)) return LC_ERR_CUDA;
+  if (!make_map(&mV, c.ws + p.vhi, false, p.d, p.T, p.H, bn)) return LC_ERR_CUDA;
+  if (!make_map(&mVlo, p.bf16_in ? c.ws + p.vhi : c.ws + p.vlo, false, p.d, p.T, p.H, bn))
+    return LC_ERR_CUDA;
+  AttnStatsParams a{};
+  a.n_q = p.n_q;
+  a.T = p.T;
+  a.n_q_pad = p.n_q_pad;
+  a.scale_log2 = p.scale * kLog2e;
+  a.rowmax = rowmax;
+  a.lse = lse;
+  a.O = O;
+  if (to_ws) {
+    a.rowmax_pad = c.at<float>(p.m_pad);
+    a.lse_pad = c.at<float>(p.lse_pad);
+    a.O_hi = c.at<__half>(p.ohi);
+    a.O_lo = c.at<__half>(p.olo);
+  }
+  a.err = c.h->d_err;
+  {
+    LC_PROF(c, "attn_stats", 1);
+    LC_CUDA(launch_attn_stats(p.mode, mQ, mK, mV, mVlo, a, p.H, c.st));
+  }
+  return LC_OK;
+}
+
+lc_status run_pass2(const Ctx& c, const void* qop, const void* kop) {
+  const Plan& p = c.p;
+  CUtensorMap mQ, mK;
+  if (!make_map(&mQ, qop, p.bf16_in, p.d_qk, p.n_q, p.H, 128)) return LC_ERR_CUDA;
+  if (!make_map(&mK, kop, p.bf16_in, p.d_qk, p.T, p.H, 128)) return LC_ERR_CUDA;
+  {
+    LC_PROF(c, "clear_scores", 0);
+    LC_CUDA(cudaMemsetAsync(c.ws + p.ucode, 0, static_cast<size_t>(p.H) * p.T * 4, c.st));
+  }
+  KeyScoreParams k{};
+  k.n_q_pad = p.n_q_pad;
+  k.T = p.T;
+  k.tiles_per_split = p.ks_tiles;
+  k.scale = p.scale;
+  k.lse_pad = c.at<float>(p.lse_pad);
+  k.u_code = c.at<uint32_t>(p.ucode);
+  k.err = c.h->d_err;
+  {
+    LC_PROF(c, "key_scores", 1);
+    LC_CUDA(launch_key_scores(p.mode, mK, mQ, k, p.H, p.ks_split, c.st));
+  }
+  return LC_OK;
+}
+
+// Steps 4-5 from the workspace's m_pad, lse_pad, O hi/lo and the given idx.
+lc_status run_fit(const Ctx& c, const void* qop, const void* kop, const void* V,
+                  const int32_t* idx, float* w, float* beta, float* Cv) {
+  const Plan& p = c.p;
+  const size_t H = p.H;
+  const int row_bytes = p.d_qk * 2;
+  {
+    LC_PROF(c, "gather_keys", 1);
+    LC_CUDA(launch_gather_rows(kop, c.ws + p.kc, idx, p.H, p.T, p.t, p.t_pad, row_bytes, c.st));
+  }
+  CUtensorMap mQ64, mKc, mOhi, mOlo;
+  if (!make_map(&mQ64, qop, p.bf16_in, p.d_qk, p.n_q, p.H, 64)) return LC_ERR_CUDA;
+  if (!make_map(&mKc, c.ws + p.kc, p.bf16_in, p.d_qk, p.t_pad, p.H, 128)) return LC_ERR_CUDA;
+  if (!make_map(&mOhi, c.ws + p.ohi, false, p.d, p.n_q, p.H, 64)) return LC_ERR_CUDA;
+  if (!make_map(&mOlo, c.ws + p.olo, false, p.d, p.n_q, p.H, 64)) return LC_ERR_CUDA;
+
+  // ---- step 4: mass system and NNLS
+  {
+    LC_PROF(c, "mass_rows", 2);
+    LC_CUDA(launch_mass_rows(c.at<float>(p.m_pad), c.at<float>(p.lse_pad), c.at<float>(p.rowsh2),
+                             c.at<float>(p.rowb), p.H, p.n_q, p.n_q_pad, c.st));
+    LC_CUDA(launch_fill_colb2(c.at<float>(p.colb2), p.H, p.t, p.t_pad, c.st));
+  }
+  GramParams g{};
+  g.n_q_pad = p.n_q_pad;
+  g.n_q = p.n_q;
+  g.t_pad = p.t_pad;
+  g.nblk = p.nblk;
+  g.slabs_per_split = p.g5_slabs;
+  g.scale_log2 = p.scale * kLog2e;
+  g.rowsh2 = c.at<float>(p.rowsh2);
+  g.row_b = c.at<float>(p.rowb);
+  g.colb2 = c.at<float>(p.colb2);
+  g.Gpart = c.at<float>(p.gpart);
+  g.cpart = c.at<float>(p.cpart);
+  g.Rpart = nullptr;
+  g.d_v = p.d;
+  g.err = c.h->d_err;
+  {
+    LC_PROF(c, "gram_mass", 1);
+    LC_CUDA(launch_gram(p.mode, false, mKc, mQ64, mOhi, mOlo, g, p.H, p.g5_split, c.st));
+  }
+  const size_t tt = static_cast<size_t>(p.t_pad) * p.t_pad;
+  {
+    LC_PROF(c, "reduce_mass", 3);
+    LC_CUDA(launch_reduce_partials(c.at<float>(p.gpart), c.at<float>(p.G), p.g5_split, H * tt, c.st));
+    LC_CUDA(launch_reduce_partials(c.at<float>(p.cpart), c.at<float>(p.c), p.g5_split, H * p.t_pad,
+                                   c.st));
+    LC_CUDA(launch_symmetrize(c.at<float>(p.G), p.H, p.t_pad, c.st));
+  }
+  SolveParams sp{};
+  sp.H = p.H;
+  sp.t = p.t;
+  sp.t_pad = p.t_pad;
+  sp.d_v = p.d;
+  sp.max_iter = p.max_iter;
+  sp.G = c.at<float>(p.G);
+  sp.c = c.at<float>(p.c);
+  sp.w = w;
+  sp.beta = beta;
+  sp.colb2 = c.at<float>(p.colb2);
+  sp.mat = c.at<float>(p.mat);
+  sp.vec = c.at<float>(p.vec);
+  sp.head_status = c.h->d_status;
+  sp.head_iters = c.h->d_iters;
+  sp.err = c.h->d_err;
+  {
+    LC_PROF(c, "nnls", 1);
+    LC_CUDA(launch_nnls(sp, c.st));
+  }
+
+  // ---- step 5: compact log mass, output system, OLS
+  CUtensorMap mQ128;
+  if (!make_map(&mQ128, qop, p.bf16_in, p.d_qk, p.n_q, p.H, 128)) return LC_ERR_CUDA;
+  CompactLseParams cl{};
+  cl.n_q = p.n_q;
+  cl.n_q_pad = p.n_q_pad;
+  cl.t_pad = p.t_pad;
+  cl.scale_log2 = p.scale * kLog2e;
+  cl.colb2 = c.at<float>(p.colb2);
+  cl.lc2_pad = c.at<float>(p.lc2);
+  cl.err = c.h->d_err;
+  {
+    LC_PROF(c, "compact_lse", 1);
+    LC_CUDA(launch_compact_lse(p.mode, mQ128, mKc, cl, p.H, c.st));
+  }
+  g.slabs_per_split = p.g7_slabs;
+  g.rowsh2 = c.at<float>(p.lc2);
+  g.row_b = nullptr;
+  g.Gpart = c.at<float>(p.hpart);
+  g.cpart = nullptr;
+  g.Rpart = c.at<float>(p.rpart);
+  {
+    LC_PROF(c, "gram_out", 1);
+    LC_CUDA(launch_gram(p.mode, true, mKc, mQ64, mOhi, mOlo, g, p.H, p.g7_split, c.st));
+  }
+  {
+    LC_PROF(c, "reduce_out", 4);
+    LC_CUDA(launch_reduce_partials(c.at<float>(p.hpart), c.at<float>(p.Hm), p.g7_split, H * tt, c.st));
+    LC_CUDA(launch_reduce_partials(c.at<float>(p.rpart), c.at<float>(p.R), p.g7_split,
+                                   H * p.t_pad * p.d, c.st));
+    LC_CUDA(launch_symmetrize(c.at<float>(p.Hm), p.H, p.t_pad, c.st));
+    LC_CUDA(launch_gather_v(V, p.bf16_in ? 0 : 1, idx, c.at<float>(p.vc), p.H, p.T, p.t, p.t_pad,
+                            p.d, c.st));
+  }
+  OlsParams op{};
+  op.H = p.H;
+  op.t = p.t;
+  op.t_pad = p.t_pad;
+  op.d_v = p.d;
+  op.Hm = c.at<float>(p.Hm);
+  op.R = c.at<float>(p.R);
+  op.Vc = c.at<float>(p.vc);
+  op.w = w;
+  op.mat = c.at<float>(p.mat);
+  op.Cv = Cv;
+  op.head_status = c.h->d_status;
+  op.err = c.h->d_err;
+  {
+    LC_PROF(c, "ols", 1);
+    LC_CUDA(launch_ols(op, c.st));
+  }
+  return LC_OK;
+}
+
+lc_status reset_report(const Ctx& c) {
+  LC_CUDA(cudaMemsetAsync(c.h->d_status, 0, sizeof(int32_t) * c.p.H, c.st));
+  LC_CUDA(cudaMemsetAsync(c.h->d_iters, 0, sizeof(int32_t) * c.p.H, c.st));
+  LC_CUDA(cudaMemsetAsync(c.h->d_err, 0, sizeof(uint32_t), c.st));
+  return LC_OK;
+}
+
+#define LC_TRY(x)                \
+  do {                           \
+    lc_status s_ = (x);          \
+    if (s_ != LC_OK) return s_;  \
+  } while (0)
+
+}  // namespace
+
+extern "C" {
+
+lc_status lc_create(lc_handle* out, int device) {
+  if (!out) return LC_ERR_INVALID_ARG;
+  *out = nullptr;
+  int n = 0;
+  if (cudaGetDeviceCount(&n) != cudaSuccess || device < 0 || device >= n) return LC_ERR_INVALID_ARG;
+  if (!get_encode()) return LC_ERR_CUDA;
+  lc_context* h = new lc_context();
+  h->device = device;
+  if (cudaSetDevice(device) != cudaSuccess ||
+      cudaMalloc(&h->d_status, sizeof(int32_t) * kMaxHeads) != cudaSuccess ||
+      cudaMalloc(&h->d_iters, sizeof(int32_t) * kMaxHeads) != cudaSuccess ||
+      cudaMalloc(&h->d_err, sizeof(uint32_t)) != cudaSuccess) {
+    cudaFree(h->d_status);
+    cudaFree(h->d_iters);
+    cudaFree(h->d_err);
+    delete h;
+    return LC_ERR_CUDA;
+  }
+  cudaMemset(h->d_status, 0, sizeof(int32_t) * kMaxHeads);
+  cudaMemset(h->d_iters, 0, sizeof(int32_t) * kMaxHeads);
+  cudaMemset(h->d_err, 0, sizeof(uint32_t));
+  *out = h;
+  return LC_OK;
+}
+
+lc_status lc_destroy(lc_handle h) {
+  if (!h) return LC_ERR_INVALID_ARG;
+  cudaSetDevice(h->device);
+  cudaFree(h->d_status);
+  cudaFree(h->d_iters);
+  cudaFree(h->d_err);
+  delete h;
+  return LC_OK;
+}
+
+lc_status lc_workspace_bytes(const lc_shape* shape, size_t* bytes) {
+  LC_TRY(validate(shape));
+  if (!bytes) return LC_ERR_INVALID_ARG;
+  *bytes = make_plan(shape).total;
+  return LC_OK;
+}
+
+lc_status lc_full_attn_stats(lc_handle h, const lc_shape* shape, const void* Q, const void* K,
+                             const void* V, float* rowmax, float* lse, float* O, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  LC_TRY(validate(shape));
+  if (!Q || !K || !V) return LC_ERR_INVALID_ARG;
+  const Plan p = make_plan(shape);
+  LC_TRY(check_ws(p, workspace, workspace_bytes));
+  LC_TRY(enter(h));
+  Ctx c{h, p, static_cast<uint8_t*>(workspace), static_cast<cudaStream_t>(stream)};
+  const void *qop, *kop;
+  LC_TRY(prepare_operands(c, Q, K, V, true, &qop, &kop));
+  return run_pass1(c, qop, kop, rowmax, lse, O, false);
+}
+
+lc_status lc_key_scores(lc_handle h, const lc_shape* shape, const void* Q, const void* K,
+                        const float* lse, float* u, void* workspace, size_t workspace_bytes,
+                        void* stream) {
+  LC_TRY(validate(shape));
+  if (!Q || !K || !lse || !u) return LC_ERR_INVALID_ARG;
+  const Plan p = make_plan(shape);
+  LC_TRY(check_ws(p, workspace, workspace_bytes));
+  LC_TRY(enter(h));
+  Ctx c{h, p, static_cast<uint8_t*>(workspace), static_cast<cudaStream_t>(stream)};
+  const void *qop, *kop;
+  LC_TRY(prepare_operands(c, Q, K, nullptr, false, &qop, &kop));
+  LC_CUDA(launch_pad_rows(lse, c.at<float>(p.lse_pad), p.H, p.n_q, p.n_q_pad, kInf, c.st));
+  LC_TRY(run_pass2(c, qop, kop));
+  LC_CUDA(launch_decode_scores(c.at<uint32_t>(p.ucode), u, static_cast<size_t>(p.H) * p.T, c.st));
+  return LC_OK;
+}
+
+lc_status lc_select_topt(lc_handle h, int n_heads, int T, int t, const float* u, int32_t* idx,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+  if (n_heads < 1 || T < 1 || t < 1 || t > T || !u || !idx) return LC_ERR_INVALID_ARG;
+  if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 256) return LC_ERR_WORKSPACE;
+  const size_t need = static_cast<size_t>(n_heads) * T * 4;
+  if (workspace_bytes < need) return LC_ERR_WORKSPACE;
+  LC_TRY(enter(h));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t* code = static_cast<uint32_t*>(workspace);
+  LC_CUDA(launch_encode_scores(u, code, static_cast<size_t>(n_heads) * T, st));
+  LC_CUDA(launch_select_topt(code, n_heads, T, t, idx, st));
+  return LC_OK;
+}
+
+lc_status lc_fit_only(lc_handle h, const lc_shape* shape, const void* Q, const void* K,
+                      const void* V, const int32_t* idx, const float* rowmax, const float* lse,
+                      const float* O, float* w, float* beta, float* Cv, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+  LC_TRY(validate(shape));
+  if (!Q || !K || !V || !idx || !rowmax || !lse || !O || !w || !beta || !Cv)
+    return LC_ERR_INVALID_ARG;
+  const Plan p = make_plan(shape);
+  LC_TRY(check_ws(p, workspace, workspace_bytes));
+  LC_TRY(enter(h));
+  Ctx c{h, p, static_cast<uint8_t*>(workspace), static_cast<cudaStream_t>(stream)};
+  LC_TRY(reset_report(c));
+  const void *qop, *kop;
+  LC_TRY(prepare_operands(c, Q, K, V, false, &qop, &kop));
+  LC_CUDA(launch_pad_rows(rowmax, c.at<float>(p.m_pad), p.H, p.n_q, p.n_q_pad, kInf, c.st));
+  LC_CUDA(launch_pad_rows(lse, c.at<float>(p.lse_pad), p.H, p.n_q, p.n_q_pad, kInf, c.st));
+  LC_CUDA(launch_split_f32(O, c.at<__half>(p.ohi), c.at<__half>(p.olo),
+                           static_cast<size_t>(p.H) * p.n_q * p.d, c.st));
+  return run_fit(c, qop, kop, V, idx, w, beta, Cv);
+}
+
+lc_status lc_compact_layer(lc_handle h, const lc_shape* shape, const void* Q, const void* K,
+                           const void* V, int32_t* idx, float* w, float* beta, float* Cv,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+  LC_TRY(validate(shape));
+  if (!Q || !K || !V || !idx || !w || !beta || !Cv) return LC_ERR_INVALID_ARG;
+  const Plan p = make_plan(shape);
+  LC_TRY(check_ws(p, workspace, workspace_bytes));
+  LC_TRY(enter(h));
+  Ctx c{h, p, static_cast<uint8_t*>(workspace), static_cast<cudaStream_t>(stream)};
+  LC_TRY(reset_report(c));
+  const void *qop, *kop;
+  LC_TRY(prepare_operands(c, Q, K, V, true, &qop, &kop));
+  LC_TRY(run_pass1(c, qop, kop, nullptr, nullptr, nullptr, true));
+  LC_TRY(run_pass2(c, qop, kop));
+  {
+    LC_PROF(c, "select_topt", 1);
+    LC_CUDA(launch_select_topt(c.at<uint32_t>(p.ucode), p.H, p.T, p.t, idx, c.st));
+  }
+  return run_fit(c, qop, kop, V, idx, w, beta, Cv);
+}
+
+lc_status lc_host_workspace_bytes(const lc_shape* shape, size_t* bytes) {
+  LC_TRY(validate(shape));
+  if (!bytes) return LC_ERR_INVALID_ARG;
+  const Plan p = make_plan(shape);
+  const size_t el = shape->in_dtype == LC_BF16 ? 2 : 4;
+  const size_t H = p.H;
+  size_t extra = round_up(H * p.n_q * p.d * el, 256) + 2 * round_up(H * p.T * p.d * el, 256) +
+                 3 * round_up(H * p.t * 4, 256) + round_up(H * p.t * p.d * 4, 256);
+  *bytes = p.total + extra;
+  return LC_OK;
+}
+
+lc_status lc_compact_layer_host(lc_handle h, const lc_shape* shape, const void* Q_host,
+                                const void* K_host, const void* V_host, int32_t* idx_host,
+                                float* w_host, float* beta_host, float* Cv_host, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+  LC_TRY(validate(shape));
+  if (!Q_host || !K_host || !V_host || !idx_host || !w_host || !beta_host || !Cv_host)
+    return LC_ERR_INVALID_ARG;
+  size_t need = 0;
+  LC_TRY(lc_host_workspace_bytes(shape, &need));
+  if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 256 || workspace_bytes < need)
+    return LC_ERR_WORKSPACE;
+  LC_TRY(enter(h));
+  const Plan p = make_plan(shape);
+  const size_t el = shape->in_dtype == LC_BF16 ? 2 : 4;
+  const size_t H = p.H;
+  uint8_t* base = static_cast<uint8_t*>(workspace) + p.total;
+  const size_t qb = H * p.n_q * p.d * el, kb = H * p.T * p.d * el;
+  uint8_t* dQ = base;
+  uint8_t* dK = dQ + round_up(qb, 256);
+  uint8_t* dV = dK + round_up(kb, 256);
+  uint8_t* dIdx = dV + round_up(kb, 256);
+  uint8_t* dW = dIdx + round_up(H * p.t * 4, 256);
+  uint8_t* dB = dW + round_up(H * p.t * 4, 256);
+  uint8_t* dC = dB + round_up(H * p.t * 4, 256);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  LC_CUDA(cudaMemcpyAsync(dQ, Q_host, qb, cudaMemcpyHostToDevice, st));
+  LC_CUDA(cudaMemcpyAsync(dK, K_host, kb, cudaMemcpyHostToDevice, st));
+  LC_CUDA(cudaMemcpyAsync(dV, V_host, kb, cudaMemcpyHostToDevice, st));
+  LC_TRY(lc_compact_layer(h, shape, dQ, dK, dV, reinterpret_cast<int32_t*>(dIdx),
+                          reinterpret_cast<float*>(dW), reinterpret_cast<float*>(dB),
+                          reinterpret_cast<float*>(dC), workspace, p.total, stream));
+  LC_CUDA(cudaMemcpyAsync(idx_host, dIdx, H * p.t * 4, cudaMemcpyDeviceToHost, st));
+  LC_CUDA(cudaMemcpyAsync(w_host, dW, H * p.t * 4, cudaMemcpyDeviceToHost, st));
+  LC_CUDA(cudaMemcpyAsync(beta_host, dB, H * p.t * 4, cudaMemcpyDeviceToHost, st));
+  LC_CUDA(cudaMemcpyAsync(Cv_host, dC, H * p.t * p.d * 4, cudaMemcpyDeviceToHost, st));
+  LC_CUDA(cudaStreamSynchronize(st));
+  return LC_OK;
+}
+
+lc_status lc_get_report(lc_handle h, int n_heads, int32_t* head_status, int32_t* nnls_iters,
+                        uint32_t* device_error_bits, void* stream) {
+  if (!h || n_heads < 1 || n_heads > kMaxHeads) return LC_ERR_INVALID_ARG;
+  LC_TRY(enter(h));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  LC_CUDA(cudaStreamSynchronize(st));
+  if (head_status)
+    LC_CUDA(cudaMemcpy(head_status, h->d_status, sizeof(int32_t) * n_heads, cudaMemcpyDeviceToHost));
+  if (nnls_iters)
+    LC_CUDA(cudaMemcpy(nnls_iters, h->d_iters, sizeof(int32_t) * n_heads, cudaMemcpyDeviceToHost));
+  if (device_error_bits)
+    LC_CUDA(cudaMemcpy(device_error_bits, h->d_err, sizeof(uint32_t), cudaMemcpyDeviceToHost));
+  return LC_OK;
+}
+
+lc_status lc_profile_enable(lc_handle h, int on) {
+  if (!h) return LC_ERR_INVALID_ARG;
+  h->prof.on = on != 0;
+  return LC_OK;
+}
+
+lc_status lc_profile_read(lc_handle h, int max_kernels, char* names, double* total_ms,
+                          int32_t* launches, int* n_kernels) {
+  if (!h || max_kernels < 0 || !n_kernels) return LC_ERR_INVALID_ARG;
+  LC_TRY(enter(h));
+  h->prof.resolve();
+  int i = 0;
+  for (auto& kv : h->prof.acc) {
+    if (i < max_kernels) {
+      if (names) {
+        std::strncpy(names + 32 * i, kv.first.c_str(), 31);
+        names[32 * i + 31] = 0;
+      }
+      if (total_ms) total_ms[i] = kv.second.first;
+      if (launches) launches[i] = kv.second.second;
+    }
+    ++i;
+  }
+  *n_kernels = i;
+  h->prof.acc.clear();
+  return LC_OK;
+}
+
+const char* lc_status_string(lc_status s) {
+  switch (s) {
+    case LC_OK: return "ok";
+    case LC_ERR_INVALID_ARG: return "invalid argument";
+    case LC_ERR_UNSUPPORTED: return "unsupported shape or type";
+    case LC_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case LC_ERR_CUDA: return "CUDA call failed";
+    case LC_ERR_NOT_CONVERGED: return "NNLS iteration cap reached";
+    case LC_ERR_SINGULAR: return "singular system (ridge added)";
+    case LC_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

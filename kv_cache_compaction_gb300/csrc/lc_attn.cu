@@ -1,0 +1,501 @@
+// Step 1 of attention-matching compaction: full-cache statistics of every
+// reference query ("Latent Compaction with Test-Time Training", §3
+// Preliminaries, Eq. (1)): row max m, log mass lse and output O.
+//
+// One CTA owns 128 query rows of one KV head and streams the head's keys in
+// tiles of BN.  Warp roles:
+//   warp 0      TMA producer: the Q tile once, then K/V tiles into a 2-stage ring;
+//   warp 1      tensor-core issuer: S_j = Q K_j^T into a double-buffered TMEM
+//               accumulator, then O += P_j V_j (P split into fp16 hi + lo);
+//   warps 2..5  softmax: thread = query row; reads S_j from TMEM, keeps a
+//               running row max and sum, writes P_j to shared memory.
+// The exponent reference of a row moves only when the row max grows by more
+// than 8 (base 2), so the O accumulator in TMEM is rescaled rarely; the final
+// division by the row sum makes the result independent of the reference.
+#include "lc_common.cuh"
+#include "lc_kernels.cuh"
+
+namespace lc {
+namespace {
+
+constexpr int kBM = 128;
+
+template <int D_QK, int D_V, int V_TERMS, int BN>
+struct AttnLayout {
+  static constexpr int NQC = D_QK / 64;
+  static constexpr int NVC = D_V / 64;
+  static constexpr int Q_BYTES = kBM * D_QK * 2;
+  static constexpr int KCHUNK = BN * 128;
+  static constexpr int K_BYTES = NQC * KCHUNK;
+  static constexpr int V_BYTES = NVC * KCHUNK;
+  static constexpr int STAGE = K_BYTES + V_TERMS * V_BYTES;
+  static constexpr int NST = 2;
+  static constexpr int PCHUNK = kBM * 128;
+  static constexpr int P_BYTES = (BN / 64) * PCHUNK;
+  static constexpr int OFF_STAGE = Q_BYTES;
+  static constexpr int OFF_PHI = OFF_STAGE + NST * STAGE;
+  static constexpr int OFF_PLO = OFF_PHI + P_BYTES;
+  static constexpr int OFF_BAR = OFF_PLO + P_BYTES;
+  static constexpr int SMEM = 1024 + OFF_BAR + 256;
+};
+
+template <bool QK_BF16, int D_QK, int D_V, int V_TERMS, int BN>
+__global__ void __launch_bounds__(192, 1)
+    attn_stats_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
+                      const __grid_constant__ CUtensorMap mV,
+                      const __grid_constant__ CUtensorMap mVlo, const AttnStatsParams p) {
+  using L = AttnLayout<D_QK, D_V, V_TERMS, BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = align1024(smem_raw);
+  uint8_t* sQ = base;
+  uint8_t* sStage = base + L::OFF_STAGE;
+  uint8_t* sPhi = base + L::OFF_PHI;
+  uint8_t* sPlo = base + L::OFF_PLO;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + L::OFF_BAR);
+  uint64_t* bar_q = bars + 0;
+  uint64_t* kv_full = bars + 1;             // [NST]
+  uint64_t* kv_empty = bars + 1 + L::NST;   // [NST]
+  uint64_t* s_full = bars + 1 + 2 * L::NST; // [2]
+  uint64_t* s_free = s_full + 2;            // [2]
+  uint64_t* p_full = s_free + 2;
+  uint64_t* pv_done = p_full + 1;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(pv_done + 1);
+  __shared__ volatile int abort_flag;
+
+  const int warp = warp_id(), lane = lane_id();
+  const int q0 = blockIdx.x * kBM;
+  const int h = blockIdx.y;
+  const int nkt = (p.T + BN - 1) / BN;
+
+  if (threadIdx.x == 0) {
+    abort_flag = launch_aborted(p.err) ? 1 : 0;
+    mbar_init(bar_q, 1);
+    for (int s = 0; s < L::NST; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s_full[b], 1);
+      mbar_init(&s_free[b], 128);
+    }
+    mbar_init(p_full, 128);
+    mbar_init(pv_done, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(tslot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tslot;
+  const uint32_t tO = tbase + 2 * BN;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&mQ);
+      tma_prefetch_desc(&mK);
+      tma_prefetch_desc(&mV);
+      mbar_arrive_expect_tx(bar_q, L::Q_BYTES);
+      for (int c = 0; c < L::NQC; ++c) tma_load_3d(sQ + c * kBM * 128, &mQ, bar_q, 64 * c, q0, h);
+      int issued = 0;
+      for (int j = 0; j < nkt; ++j) {
+        const int s = j % L::NST;
+        if (j >= L::NST && !wait_bar(&kv_empty[s], ((j / L::NST) - 1) & 1, &abort_flag, p.err))
+          break;
+        uint8_t* st = sStage + s * L::STAGE;
+        mbar_arrive_expect_tx(&kv_full[s], L::STAGE);
+        for (int c = 0; c < L::NQC; ++c)
+          tma_load_3d(st + c * L::KCHUNK, &mK, &kv_full[s], 64 * c, j * BN, h);
+        for (int c = 0; c < L::NVC; ++c)
+          tma_load_3d(st + L::K_BYTES + c * L::KCHUNK, &mV, &kv_full[s], 64 * c, j * BN, h);
+        if (V_TERMS == 2)
+          for (int c = 0; c < L::NVC; ++c)
+            tma_load_3d(st + L::K_BYTES + L::V_BYTES + c * L::KCHUNK, &mVlo, &kv_full[s], 64 * c,
+                        j * BN, h);
+        issued = j + 1;
+      }
+      // On abort, let the copies already in flight land before the CTA exits.
+      if (abort_flag) {
+        for (int j = (issued > L::NST ? issued - L::NST : 0); j < issued; ++j) {
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(&kv_full[j % L::NST], (j / L::NST) & 1) &&
+                 globaltimer_ns() - t0 < kWaitLimitNs) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_f16(kBM, BN, QK_BF16, false, false);
+      constexpr uint32_t idesc_pv = idesc_f16(kBM, D_V, false, false, true);
+      const uint32_t aQ = smem_u32(sQ);
+      bool ok = wait_bar(bar_q, 0, &abort_flag, p.err);
+      auto issue_s = [&](int j) -> bool {
+        const int s = j % L::NST, b = j & 1;
+        if (!wait_bar(&kv_full[s], (j / L::NST) & 1, &abort_flag, p.err)) return false;
+        if (j >= 2 && !wait_bar(&s_free[b], ((j >> 1) - 1) & 1, &abort_flag, p.err)) return false;
+        tc_fence_after();
+        const uint32_t aK = smem_u32(sStage + s * L::STAGE);
+#pragma unroll
+        for (int k = 0; k < D_QK / 16; ++k) {
+          const uint64_t da = sdesc_sw128(aQ + (k >> 2) * (kBM * 128) + (k & 3) * 32, 16, 1024);
+          const uint64_t db = sdesc_sw128(aK + (k >> 2) * L::KCHUNK + (k & 3) * 32, 16, 1024);
+          umma_f16_ss(tbase + b * BN, da, db, idesc_s, k > 0 ? 1u : 0u);
+        }
+        umma_commit(&s_full[b]);
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int j = 0; ok && j < nkt; ++j) {
+        if (j + 1 < nkt && !issue_s(j + 1)) break;
+        if (!wait_bar(p_full, j & 1, &abort_flag, p.err)) break;
+        tc_fence_after();
+        const int s = j % L::NST;
+        const uint32_t aV = smem_u32(sStage + s * L::STAGE + L::K_BYTES);
+        const uint32_t aPh = smem_u32(sPhi), aPl = smem_u32(sPlo);
+#pragma unroll
+        for (int k = 0; k < BN / 16; ++k) {
+          const uint32_t poff = (k >> 2) * L::PCHUNK + (k & 3) * 32;
+          const uint64_t dph = sdesc_sw128(aPh + poff, 16, 1024);
+          const uint64_t dpl = sdesc_sw128(aPl + poff, 16, 1024);
+          const uint64_t dv = sdesc_sw128(aV + k * 2048, L::KCHUNK, 1024);
+          umma_f16_ss(tO, dph, dv, idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
+          umma_f16_ss(tO, dpl, dv, idesc_pv, 1u);
+          if (V_TERMS == 2) {
+            const uint64_t dvl = sdesc_sw128(aV + L::V_BYTES + k * 2048, L::KCHUNK, 1024);
+            umma_f16_ss(tO, dph, dvl, idesc_pv, 1u);
+          }
+        }
+        umma_commit(&kv_empty[s]);
+        umma_commit(pv_done);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const float sl2 = p.scale_log2;
+    float m_ref = -kInf;   // exponent reference (base 2)
+    float m_true = -kInf;  // exact running row max (base 2)
+    float l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nkt; ++j) {
+      const int b = j & 1;
+      if (!wait_bar(&s_full[b], (j >> 1) & 1, &abort_flag, p.err)) { ok = false; break; }
+      tc_fence_after();
+      float x[BN];
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) {
+        float v[32];
+        tmem_ld32(tbase + lane_off + b * BN + c * 32, v);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) x[c * 32 + e] = v[e];
+      }
+      tc_fence_before();
+      mbar_arrive(&s_free[b]);
+      const int valid = p.T - j * BN;
+      float mx = -kInf;
+#pragma unroll
+      for (int k = 0; k < BN; ++k) {
+        x[k] = (k < valid) ? x[k] * sl2 : -kInf;
+        mx = fmaxf(mx, x[k]);
+      }
+      m_true = fmaxf(m_true, mx);
+      const bool resc = mx > m_ref + 8.f;
+      const float new_ref = resc ? mx : m_ref;
+      const float alpha = resc ? ex2(m_ref - new_ref) : 1.f;
+      // P buffer free and O up to date once the previous P.V has completed.
+      if (j > 0) {
+        if (!wait_bar(pv_done, (j - 1) & 1, &abort_flag, p.err)) { ok = false; break; }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll
+          for (int c = 0; c < D_V / 32; ++c) {
+            float o[32];
+            tmem_ld32(tO + lane_off + c * 32, o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] *= alpha;
+            tmem_st32(tO + lane_off + c * 32, o);
+          }
+        }
+      }
+      l *= alpha;
+      m_ref = new_ref;
+#pragma unroll
+      for (int c8 = 0; c8 < BN / 8; ++c8) {
+        float pv[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          pv[e] = ex2(x[c8 * 8 + e] - m_ref);
+          l += pv[e];
+        }
+        uint4 hi, lo;
+        split8(pv, hi, lo);
+        const uint32_t off = (c8 >> 3) * L::PCHUNK + sw128_offset(row, (c8 & 7) * 8);
+        *reinterpret_cast<uint4*>(sPhi + off) = hi;
+        *reinterpret_cast<uint4*>(sPlo + off) = lo;
+      }
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(p_full);
+    }
+    if (ok && wait_bar(pv_done, (nkt - 1) & 1, &abort_flag, p.err)) {
+      tc_fence_after();
+      const int qr = q0 + row;
+      const size_t hq = static_cast<size_t>(h) * p.n_q;
+      const float inv_l = 1.f / l;
+      if (qr < p.n_q) {
+        const float m_nat = m_true * kLn2;
+        const float lse_nat = (m_ref + log2f(l)) * kLn2;
+        if (p.rowmax) p.rowmax[hq + qr] = m_nat;
+        if (p.lse) p.lse[hq + qr] = lse_nat;
+        if (p.rowmax_pad) p.rowmax_pad[static_cast<size_t>(h) * p.n_q_pad + qr] = m_nat;
+        if (p.lse_pad) p.lse_pad[static_cast<size_t>(h) * p.n_q_pad + qr] = lse_nat;
+      } else if (qr < p.n_q_pad) {
+        if (p.rowmax_pad) p.rowmax_pad[static_cast<size_t>(h) * p.n_q_pad + qr] = kInf;
+        if (p.lse_pad) p.lse_pad[static_cast<size_t>(h) * p.n_q_pad + qr] = kInf;
+      }
+#pragma unroll
+      for (int c = 0; c < D_V / 32; ++c) {
+        float o[32];
+        tmem_ld32(tO + lane_off + c * 32, o);
+        if (qr < p.n_q) {
+          const size_t off = (hq + qr) * D_V + c * 32;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] *= inv_l;
+          if (p.O) {
+            float4* dst = reinterpret_cast<float4*>(p.O + off);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              dst[e] = make_float4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
+          }
+          if (p.O_hi) {
+            uint4* dh = reinterpret_cast<uint4*>(p.O_hi + off);
+            uint4* dl = reinterpret_cast<uint4*>(p.O_lo + off);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              uint4 hi, lo;
+              split8(o + 8 * e, hi, lo);
+              dh[e] = hi;
+              dl[e] = lo;
+            }
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tbase, 512);
+}
+
+// ---------------------------------------------------------------------------
+// Compact log mass of each query under the fitted biases:
+//   lc2_r = log2 sum_j 2^(scale*log2e * S_rj + colb2_j)   (base-2 units)
+// i.e. the log-normaliser of the biased compact attention ("Latent Compaction
+// ...", §3.1 Eq. (2)-(4)).  Thread = query row; key blocks of 128 streamed.
+template <bool QK_BF16, int D_QK>
+struct CLLayout {
+  static constexpr int NQC = D_QK / 64;
+  static constexpr int Q_BYTES = kBM * D_QK * 2;
+  static constexpr int KC_BYTES = 128 * D_QK * 2;
+  static constexpr int OFF_K = Q_BYTES;
+  static constexpr int OFF_BAR = OFF_K + 2 * KC_BYTES;
+  static constexpr int SMEM = 1024 + OFF_BAR + 256;
+};
+
+template <bool QK_BF16, int D_QK>
+__global__ void __launch_bounds__(192, 1)
+    compact_lse_kernel(const __grid_constant__ CUtensorMap mQ,
+                       const __grid_constant__ CUtensorMap mKc, const CompactLseParams p) {
+  using L = CLLayout<QK_BF16, D_QK>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = align1024(smem_raw);
+  uint8_t* sQ = base;
+  uint8_t* sK = base + L::OFF_K;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + L::OFF_BAR);
+  uint64_t* bar_q = bars;
+  uint64_t* k_full = bars + 1;   // [2]
+  uint64_t* k_empty = bars + 3;  // [2]
+  uint64_t* s_full = bars + 5;   // [2]
+  uint64_t* s_free = bars + 7;   // [2]
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 9);
+  __shared__ volatile int abort_flag;
+  const int warp = warp_id(), lane = lane_id();
+  const int q0 = blockIdx.x * kBM, h = blockIdx.y;
+  const int nkb = p.t_pad / 128;
+  if (threadIdx.x == 0) {
+    abort_flag = launch_aborted(p.err) ? 1 : 0;
+    mbar_init(bar_q, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], 128);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(tslot, 256);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tslot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar_q, L::Q_BYTES);
+      for (int c = 0; c < L::NQC; ++c) tma_load_3d(sQ + c * kBM * 128, &mQ, bar_q, 64 * c, q0, h);
+      int issued = 0;
+      for (int j = 0; j < nkb; ++j) {
+        const int s = j & 1;
+        if (j >= 2 && !wait_bar(&k_empty[s], ((j >> 1) - 1) & 1, &abort_flag, p.err)) break;
+        mbar_arrive_expect_tx(&k_full[s], L::KC_BYTES);
+        for (int c = 0; c < L::NQC; ++c)
+          tma_load_3d(sK + s * L::KC_BYTES + c * 128 * 128, &mKc, &k_full[s], 64 * c, j * 128, h);
+        issued = j + 1;
+      }
+      if (abort_flag) {
+        for (int j = (issued > 2 ? issued - 2 : 0); j < issued; ++j) {
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(&k_full[j & 1], (j >> 1) & 1) &&
+                 globaltimer_ns() - t0 < kWaitLimitNs) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_f16(kBM, 128, QK_BF16, false, false);
+      bool ok = wait_bar(bar_q, 0, &abort_flag, p.err);
+      for (int j = 0; ok && j < nkb; ++j) {
+        const int s = j & 1;
+        if (!wait_bar(&k_full[s], (j >> 1) & 1, &abort_flag, p.err)) break;
+        if (j >= 2 && !wait_bar(&s_free[s], ((j >> 1) - 1) & 1, &abort_flag, p.err)) break;
+        tc_fence_after();
+        const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK + s * L::KC_BYTES);
+#pragma unroll
+        for (int k = 0; k < D_QK / 16; ++k) {
+          const uint64_t da = sdesc_sw128(aQ + (k >> 2) * (kBM * 128) + (k & 3) * 32, 16, 1024);
+          const uint64_t db = sdesc_sw128(aK + (k >> 2) * (128 * 128) + (k & 3) * 32, 16, 1024);
+          umma_f16_ss(tbase + s * 128, da, db, idesc, k > 0 ? 1u : 0u);
+        }
+        umma_commit(&s_full[s]);
+        umma_commit(&k_empty[s]);
+      }
+    }
+  } else {
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const float* cb = p.colb2 + static_cast<size_t>(h) * p.t_pad;
+    float mref = -kInf, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nkb; ++j) {
+      const int s = j & 1;
+      if (!wait_bar(&s_full[s], (j >> 1) & 1, &abort_flag, p.err)) { ok = false; break; }
+      tc_fence_after();
+      float x[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float v[32];
+        tmem_ld32(tbase + lane_off + s * 128 + c * 32, v);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) x[c * 32 + e] = v[e];
+      }
+      tc_fence_before();
+      mbar_arrive(&s_free[s]);
+      float mx = -kInf;
+#pragma unroll
+      for (int k = 0; k < 128; ++k) {
+        x[k] = fmaf(x[k], p.scale_log2, __ldg(cb + j * 128 + k));
+        mx = fmaxf(mx, x[k]);
+      }
+      const float nref = fmaxf(mref, mx);
+      if (nref > -kInf) {
+        l *= ex2(mref - nref);
+#pragma unroll
+        for (int k = 0; k < 128; ++k) l += ex2(x[k] - nref);
+        mref = nref;
+      }
+    }
+    if (ok) {
+      const int qr = q0 + row;
+      if (qr < p.n_q_pad)
+        p.lc2_pad[static_cast<size_t>(h) * p.n_q_pad + qr] =
+            (qr < p.n_q) ? mref + log2f(l) : kInf;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tbase, 256);
+}
+
+template <bool QK_BF16, int D_QK, int D_V, int V_TERMS, int BN>
+cudaError_t launch_attn_t(const CUtensorMap& mQ, const CUtensorMap& mK, const CUtensorMap& mV,
+                          const CUtensorMap& mVlo, const AttnStatsParams& p, int H,
+                          cudaStream_t st) {
+  using L = AttnLayout<D_QK, D_V, V_TERMS, BN>;
+  auto kern = attn_stats_kernel<QK_BF16, D_QK, D_V, V_TERMS, BN>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
+  if (e != cudaSuccess) return e;
+  dim3 grid((p.n_q + kBM - 1) / kBM, H);
+  kern<<<grid, 192, L::SMEM, st>>>(mQ, mK, mV, mVlo, p);
+  return cudaGetLastError();
+}
+
+template <bool QK_BF16, int D_QK>
+cudaError_t launch_cl_t(const CUtensorMap& mQ, const CUtensorMap& mKc, const CompactLseParams& p,
+                        int H, cudaStream_t st) {
+  using L = CLLayout<QK_BF16, D_QK>;
+  auto kern = compact_lse_kernel<QK_BF16, D_QK>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
+  if (e != cudaSuccess) return e;
+  dim3 grid((p.n_q + kBM - 1) / kBM, H);
+  kern<<<grid, 192, L::SMEM, st>>>(mQ, mKc, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_stats(OperandMode mode, const CUtensorMap& mQ, const CUtensorMap& mK,
+                              const CUtensorMap& mV, const CUtensorMap& mVlo,
+                              const AttnStatsParams& p, int H, cudaStream_t st) {
+  switch (mode) {
+    case kBF16d128: return launch_attn_t<true, 128, 128, 1, 128>(mQ, mK, mV, mVlo, p, H, st);
+    case kBF16d64: return launch_attn_t<true, 64, 64, 1, 128>(mQ, mK, mV, mVlo, p, H, st);
+    case kSplitF16d64: return launch_attn_t<false, 192, 64, 2, 64>(mQ, mK, mV, mVlo, p, H, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+int attn_stats_smem(OperandMode mode) {
+  switch (mode) {
+    case kBF16d128: return AttnLayout<128, 128, 1, 128>::SMEM;
+    case kBF16d64: return AttnLayout<64, 64, 1, 128>::SMEM;
+    case kSplitF16d64: return AttnLayout<192, 64, 2, 64>::SMEM;
+  }
+  return 0;
+}
+
+cudaError_t launch_compact_lse(OperandMode mode, const CUtensorMap& mQ, const CUtensorMap& mKc,
+                               const CompactLseParams& p, int H, cudaStream_t st) {
+  switch (mode) {
+    case kBF16d128: return launch_cl_t<true, 128>(mQ, mKc, p, H, st);
+    case kBF16d64: return launch_cl_t<true, 64>(mQ, mKc, p, H, st);
+    case kSplitF16d64: return launch_cl_t<false, 192>(mQ, mKc, p, H, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+int compact_lse_smem(OperandMode mode) {
+  switch (mode) {
+    case kBF16d128: return CLLayout<true, 128>::SMEM;
+    case kBF16d64: return CLLayout<true, 64>::SMEM;
+    case kSplitF16d64: return CLLayout<false, 192>::SMEM;
+  }
+  return 0;
+}
+
+}  // namespace lc

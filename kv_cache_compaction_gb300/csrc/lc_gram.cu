@@ -1,0 +1,365 @@
+// Normal equations of the two fits of attention-matching compaction ("KV
+// compaction" blog, section "Fast KV Compaction via Attention Matching"):
+//   mass fit   (step 4):  G = A^T A, c = A^T b with
+//                         A_ri = exp(s q_r.C_ki - m_r), b_r = exp(lse_r - m_r);
+//   output fit (step 5):  H = X^T X, R = X^T O with
+//                         X_ri = softmax_i(s q_r.C_ki + beta_i).
+// Both are the same computation, E_ir = 2^(s2 S_ir + colb2_i - rowsh2_r), with
+// a different per-key bias and per-query shift; A and X are never stored.
+//
+// Layout is key-stationary: the score tile S^T = C_k q^T lands in tensor
+// memory with one selected key per lane, so each thread owns one key and
+// writes its row of E in the K-major layout the Gram products read, and
+// c_i = sum_r E_ir b_r is a per-thread dot product.  E is split into fp16
+// hi + lo and each Gram block is the sum of three tensor-core products
+// (hi.hi + hi.lo + lo.hi), which keeps fp32-level accuracy.
+//
+// CTA kinds (blockIdx.x):
+//   [0, npairs)           key-block pair (bi <= bj): G[bi][bj], and c[bi]
+//                         for diagonal pairs when row_b is given;
+//   [npairs, npairs+nblk) R[bi] = E_bi O (output fit only).
+// blockIdx.z splits the query slabs; partial sums are reduced afterwards in
+// a fixed order.
+#include "lc_common.cuh"
+#include "lc_kernels.cuh"
+
+namespace lc {
+namespace {
+
+constexpr int kSL = 64;  // query rows per slab
+
+template <int D_QK, int D_V, int NST_>
+struct GramLayout {
+  static constexpr int NQC = D_QK / 64;
+  static constexpr int NVC = D_V / 64;
+  static constexpr int KC_BYTES = 128 * D_QK * 2;
+  static constexpr int QCHUNK = kSL * 128;
+  static constexpr int Q_BYTES = NQC * QCHUNK;
+  static constexpr int O_BYTES = 2 * NVC * QCHUNK;  // hi + lo
+  static constexpr int STAGE = Q_BYTES + O_BYTES;    // multiple of 1024
+  static constexpr int NST = NST_;
+  static constexpr int ROW_STAGE = 2 * kSL * 4;      // row shift + row b
+  static constexpr int E_BYTES = 128 * 128;          // 128 keys x 64 queries x 2 B
+  static constexpr int OFF_STAGE = 2 * KC_BYTES;
+  static constexpr int OFF_E = OFF_STAGE + NST * STAGE;
+  static constexpr int OFF_ROWS = OFF_E + 4 * E_BYTES;
+  static constexpr int OFF_BAR = OFF_ROWS + NST * ROW_STAGE;
+  static constexpr int SMEM = 1024 + OFF_BAR + 128;
+};
+
+template <bool QK_BF16, int D_QK, int D_V, int NST>
+__global__ void __launch_bounds__(192, 1)
+    gram_kernel(const __grid_constant__ CUtensorMap mKc, const __grid_constant__ CUtensorMap mQ,
+                const __grid_constant__ CUtensorMap mOhi, const __grid_constant__ CUtensorMap mOlo,
+                const GramParams p) {
+  using L = GramLayout<D_QK, D_V, NST>;
+  // With a single stage the next slab's scores cannot be issued before the
+  // current slab's products have released that stage.
+  constexpr bool kPrefetchS = NST > 1;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = align1024(smem_raw);
+  uint8_t* sRows = base + L::OFF_ROWS;
+  uint8_t* sKi = base;
+  uint8_t* sKj = base + L::KC_BYTES;
+  uint8_t* sStage = base + L::OFF_STAGE;
+  uint8_t* sEih = base + L::OFF_E;
+  uint8_t* sEil = sEih + L::E_BYTES;
+  uint8_t* sEjh = sEil + L::E_BYTES;
+  uint8_t* sEjl = sEjh + L::E_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + L::OFF_BAR);
+  uint64_t* k_full = bars + 0;
+  uint64_t* st_full = bars + 1;   // [2]
+  uint64_t* st_empty = bars + 3;  // [2]
+  uint64_t* s_full = bars + 5;    // [2]
+  uint64_t* s_free = bars + 7;    // [2]
+  uint64_t* e_full = bars + 9;
+  uint64_t* e_free = bars + 10;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 11);
+  __shared__ volatile int abort_flag;
+
+  const int warp = warp_id(), lane = lane_id();
+  const int h = blockIdx.y, z = blockIdx.z;
+  const int npairs = p.nblk * (p.nblk + 1) / 2;
+  const bool is_r = static_cast<int>(blockIdx.x) >= npairs;
+  int bi = 0, bj = 0;
+  if (!is_r) {
+    int rem = blockIdx.x;
+    while (rem >= p.nblk - bi) {
+      rem -= p.nblk - bi;
+      ++bi;
+    }
+    bj = bi + rem;
+  } else {
+    bi = bj = blockIdx.x - npairs;
+  }
+  const bool two = !is_r && bi != bj;
+  const bool with_c = !is_r && bi == bj && p.row_b != nullptr;
+  const int total_slabs = p.n_q_pad / kSL;
+  const int s0 = z * p.slabs_per_split;
+  const int s1 = min(total_slabs, s0 + p.slabs_per_split);
+  const int nsl = max(0, s1 - s0);
+
+  if (threadIdx.x == 0) {
+    abort_flag = launch_aborted(p.err) ? 1 : 0;
+    mbar_init(k_full, 1);
+    for (int s = 0; s < L::NST; ++s) {
+      mbar_init(&st_full[s], 1);
+      mbar_init(&st_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s_full[b], 1);
+      mbar_init(&s_free[b], 128);
+    }
+    mbar_init(e_full, 128);
+    mbar_init(e_free, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(tslot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tslot;
+  const uint32_t tAcc = tbase + 256;  // G block or R block
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- producer
+    if (lane == 0 && nsl > 0) {
+      mbar_arrive_expect_tx(k_full, (two ? 2 : 1) * L::KC_BYTES);
+      for (int c = 0; c < L::NQC; ++c) {
+        tma_load_3d(sKi + c * 128 * 128, &mKc, k_full, 64 * c, bi * 128, h);
+        if (two) tma_load_3d(sKj + c * 128 * 128, &mKc, k_full, 64 * c, bj * 128, h);
+      }
+      const uint32_t bytes = L::Q_BYTES + (is_r ? L::O_BYTES : 0) + kSL * 4 + (with_c ? kSL * 4 : 0);
+      int issued = 0;
+      for (int i = 0; i < nsl; ++i) {
+        const int s = i % L::NST;
+        if (i >= L::NST && !wait_bar(&st_empty[s], ((i / L::NST) - 1) & 1, &abort_flag, p.err))
+          break;
+        uint8_t* st = sStage + s * L::STAGE;
+        const int r0 = (s0 + i) * kSL;
+        mbar_arrive_expect_tx(&st_full[s], bytes);
+        for (int c = 0; c < L::NQC; ++c)
+          tma_load_3d(st + c * L::QCHUNK, &mQ, &st_full[s], 64 * c, r0, h);
+        if (is_r) {
+          for (int c = 0; c < L::NVC; ++c) {
+            tma_load_3d(st + L::Q_BYTES + c * L::QCHUNK, &mOhi, &st_full[s], 64 * c, r0, h);
+            tma_load_3d(st + L::Q_BYTES + (L::NVC + c) * L::QCHUNK, &mOlo, &st_full[s], 64 * c,
+                        r0, h);
+          }
+        }
+        const size_t roff = static_cast<size_t>(h) * p.n_q_pad + r0;
+        uint8_t* rw = sRows + s * L::ROW_STAGE;
+        bulk_g2s(rw, p.rowsh2 + roff, kSL * 4, &st_full[s]);
+        if (with_c) bulk_g2s(rw + kSL * 4, p.row_b + roff, kSL * 4, &st_full[s]);
+        issued = i + 1;
+      }
+      if (abort_flag) {
+        for (int i = (issued > L::NST ? issued - L::NST : 0); i < issued; ++i) {
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(&st_full[i % L::NST], (i / L::NST) & 1) &&
+                 globaltimer_ns() - t0 < kWaitLimitNs) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0 && nsl > 0) {
+      constexpr uint32_t idesc_s = idesc_f16(128, kSL, QK_BF16, false, false);
+      constexpr uint32_t idesc_g = idesc_f16(128, 128, false, false, false);
+      constexpr uint32_t idesc_r = idesc_f16(128, D_V, false, false, true);
+      bool ok = wait_bar(k_full, 0, &abort_flag, p.err);
+      auto issue_s = [&](int i) -> bool {
+        const int s = i % L::NST, b = i & 1;
+        if (!wait_bar(&st_full[s], (i / L::NST) & 1, &abort_flag, p.err)) return false;
+        if (i >= 2 && !wait_bar(&s_free[b], ((i >> 1) - 1) & 1, &abort_flag, p.err)) return false;
+        tc_fence_after();
+        const uint32_t aQ = smem_u32(sStage + s * L::STAGE);
+#pragma unroll
+        for (int k = 0; k < D_QK / 16; ++k) {
+          const uint64_t dq = sdesc_sw128(aQ + (k >> 2) * L::QCHUNK + (k & 3) * 32, 16, 1024);
+          const uint32_t koff = (k >> 2) * (128 * 128) + (k & 3) * 32;
+          umma_f16_ss(tbase + b * 128, sdesc_sw128(smem_u32(sKi) + koff, 16, 1024), dq, idesc_s,
+                      k > 0 ? 1u : 0u);
+          if (two)
+            umma_f16_ss(tbase + b * 128 + 64, sdesc_sw128(smem_u32(sKj) + koff, 16, 1024), dq,
+                        idesc_s, k > 0 ? 1u : 0u);
+        }
+        umma_commit(&s_full[b]);
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int i = 0; ok && i < nsl; ++i) {
+        if (kPrefetchS && i + 1 < nsl && !issue_s(i + 1)) break;
+        if (!wait_bar(e_full, i & 1, &abort_flag, p.err)) break;
+        tc_fence_after();
+        const int s = i % L::NST;
+        const uint32_t eih = smem_u32(sEih), eil = smem_u32(sEil);
+        if (!is_r) {
+          const uint32_t ejh = two ? smem_u32(sEjh) : eih;
+          const uint32_t ejl = two ? smem_u32(sEjl) : eil;
+#pragma unroll
+          for (int k = 0; k < kSL / 16; ++k) {
+            const uint32_t o = k * 32;
+            const uint32_t acc0 = (i > 0 || k > 0) ? 1u : 0u;
+            umma_f16_ss(tAcc, sdesc_sw128(eih + o, 16, 1024), sdesc_sw128(ejh + o, 16, 1024),
+                        idesc_g, acc0);
+            umma_f16_ss(tAcc, sdesc_sw128(eih + o, 16, 1024), sdesc_sw128(ejl + o, 16, 1024),
+                        idesc_g, 1u);
+            umma_f16_ss(tAcc, sdesc_sw128(eil + o, 16, 1024), sdesc_sw128(ejh + o, 16, 1024),
+                        idesc_g, 1u);
+          }
+        } else {
+          const uint32_t aO = smem_u32(sStage + s * L::STAGE + L::Q_BYTES);
+          const uint32_t aOl = aO + L::NVC * L::QCHUNK;
+#pragma unroll
+          for (int k = 0; k < kSL / 16; ++k) {
+            const uint32_t o = k * 32;
+            const uint32_t acc0 = (i > 0 || k > 0) ? 1u : 0u;
+            const uint64_t doh = sdesc_sw128(aO + k * 2048, L::QCHUNK, 1024);
+            const uint64_t dol = sdesc_sw128(aOl + k * 2048, L::QCHUNK, 1024);
+            umma_f16_ss(tAcc, sdesc_sw128(eih + o, 16, 1024), doh, idesc_r, acc0);
+            umma_f16_ss(tAcc, sdesc_sw128(eih + o, 16, 1024), dol, idesc_r, 1u);
+            umma_f16_ss(tAcc, sdesc_sw128(eil + o, 16, 1024), doh, idesc_r, 1u);
+          }
+        }
+        umma_commit(&st_empty[s]);
+        umma_commit(e_free);
+        if (!kPrefetchS && i + 1 < nsl && !issue_s(i + 1)) break;
+      }
+    }
+  } else {
+    // ---------------------------------------------------------- E rows
+    const int wq = warp & 3;
+    const int j = wq * 32 + lane;  // key row within the block
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const size_t cb_off = static_cast<size_t>(h) * p.t_pad;
+    const float cbi = p.colb2[cb_off + bi * 128 + j];
+    const float cbj = two ? p.colb2[cb_off + bj * 128 + j] : 0.f;
+    const float s2 = p.scale_log2;
+    float cacc = 0.f;
+    bool ok = nsl > 0;
+    for (int i = 0; ok && i < nsl; ++i) {
+      const int b = i & 1, s = i % L::NST;
+      if (!wait_bar(&s_full[b], (i >> 1) & 1, &abort_flag, p.err)) { ok = false; break; }
+      tc_fence_after();
+      float xi[kSL], xj[kSL];
+#pragma unroll
+      for (int c = 0; c < kSL / 32; ++c) {
+        float v[32];
+        tmem_ld32(tbase + lane_off + b * 128 + c * 32, v);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) xi[c * 32 + e] = v[e];
+        if (two) {
+          tmem_ld32(tbase + lane_off + b * 128 + 64 + c * 32, v);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) xj[c * 32 + e] = v[e];
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&s_free[b]);
+      if (i > 0 && !wait_bar(e_free, (i - 1) & 1, &abort_flag, p.err)) { ok = false; break; }
+      // the row data arrived with the stage's copies
+      if (!wait_bar(&st_full[s], (i / L::NST) & 1, &abort_flag, p.err)) { ok = false; break; }
+      const float* rs = reinterpret_cast<const float*>(sRows + s * L::ROW_STAGE);
+      const float* rb = rs + kSL;
+#pragma unroll
+      for (int c8 = 0; c8 < kSL / 8; ++c8) {
+        float e8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float sh = rs[c8 * 8 + e];
+          e8[e] = ex2(fmaf(xi[c8 * 8 + e], s2, cbi) - sh);
+          if (with_c) cacc = fmaf(e8[e], rb[c8 * 8 + e], cacc);
+        }
+        uint4 hi, lo;
+        split8(e8, hi, lo);
+        const uint32_t off = sw128_offset(j, c8 * 8);
+        *reinterpret_cast<uint4*>(sEih + off) = hi;
+        *reinterpret_cast<uint4*>(sEil + off) = lo;
+        if (two) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) e8[e] = ex2(fmaf(xj[c8 * 8 + e], s2, cbj) - rs[c8 * 8 + e]);
+          split8(e8, hi, lo);
+          *reinterpret_cast<uint4*>(sEjh + off) = hi;
+          *reinterpret_cast<uint4*>(sEjl + off) = lo;
+        }
+      }
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(e_full);
+    }
+    if (ok && nsl > 0 && wait_bar(e_free, (nsl - 1) & 1, &abort_flag, p.err)) {
+      tc_fence_after();
+      const int H = gridDim.y;
+      const size_t zh = static_cast<size_t>(z) * H + h;
+      const int key = bi * 128 + j;
+      if (!is_r) {
+        float* dst = p.Gpart + (zh * p.t_pad + key) * p.t_pad + bj * 128;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float v[32];
+          tmem_ld32(tAcc + lane_off + c * 32, v);
+          float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) d4[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+        }
+        if (with_c) p.cpart[zh * p.t_pad + key] = cacc;
+      } else {
+        float* dst = p.Rpart + (zh * p.t_pad + key) * p.d_v;
+#pragma unroll
+        for (int c = 0; c < D_V / 32; ++c) {
+          float v[32];
+          tmem_ld32(tAcc + lane_off + c * 32, v);
+          float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) d4[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tbase, 512);
+}
+
+template <bool QK_BF16, int D_QK, int D_V, int NST>
+cudaError_t launch_gram_t(bool with_r, const CUtensorMap& mKc, const CUtensorMap& mQ,
+                          const CUtensorMap& mOhi, const CUtensorMap& mOlo, const GramParams& p,
+                          int H, int nsplit, cudaStream_t st) {
+  using L = GramLayout<D_QK, D_V, NST>;
+  auto kern = gram_kernel<QK_BF16, D_QK, D_V, NST>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
+  if (e != cudaSuccess) return e;
+  const int npairs = p.nblk * (p.nblk + 1) / 2;
+  dim3 grid(npairs + (with_r ? p.nblk : 0), H, nsplit);
+  kern<<<grid, 192, L::SMEM, st>>>(mKc, mQ, mOhi, mOlo, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gram(OperandMode mode, bool with_r, const CUtensorMap& mKc,
+                        const CUtensorMap& mQ, const CUtensorMap& mOhi, const CUtensorMap& mOlo,
+                        const GramParams& p, int H, int nsplit, cudaStream_t st) {
+  switch (mode) {
+    case kBF16d128:
+      return launch_gram_t<true, 128, 128, 2>(with_r, mKc, mQ, mOhi, mOlo, p, H, nsplit, st);
+    case kBF16d64:
+      return launch_gram_t<true, 64, 64, 2>(with_r, mKc, mQ, mOhi, mOlo, p, H, nsplit, st);
+    case kSplitF16d64:
+      return launch_gram_t<false, 192, 64, 1>(with_r, mKc, mQ, mOhi, mOlo, p, H, nsplit, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+int gram_smem(OperandMode mode) {
+  switch (mode) {
+    case kBF16d128: return GramLayout<128, 128, 2>::SMEM;
+    case kBF16d64: return GramLayout<64, 64, 2>::SMEM;
+    case kSplitF16d64: return GramLayout<192, 64, 1>::SMEM;
+  }
+  return 0;
+}
+
+}  // namespace lc

@@ -1,0 +1,144 @@
+// Kernel parameter blocks and host-side launch entry points.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace lc {
+
+// Which operand encoding the tensor-core passes use.
+//  kBF16d128 / kBF16d64: Q, K bf16 with d_qk = d; V converted to fp16 (exact
+//      for bf16 values in the fp16 range), one P.V term pair.
+//  kSplitF16d64: fp32 inputs; Q = [Qhi|Qlo|Qhi], K = [Khi|Khi|Klo] as fp16
+//      (d_qk = 3d = 192) so S keeps fp32 accuracy; V = Vhi + Vlo.
+enum OperandMode { kBF16d128 = 0, kBF16d64 = 1, kSplitF16d64 = 2 };
+
+struct AttnStatsParams {
+  int n_q, T, n_q_pad;
+  float scale_log2;        // softmax scale * log2(e)
+  float* rowmax;           // [H][n_q], natural-log units; may be null
+  float* lse;              // [H][n_q]; may be null
+  float* rowmax_pad;       // [H][n_q_pad], +inf in padded rows; may be null
+  float* lse_pad;          // [H][n_q_pad], +inf in padded rows; may be null
+  float* O;                // [H][n_q][d_v] fp32; may be null
+  __half* O_hi;            // [H][n_q][d_v] fp16 hi/lo pair; may be null
+  __half* O_lo;
+  uint32_t* err;
+};
+
+struct KeyScoreParams {
+  int n_q_pad, T;
+  int tiles_per_split;     // query tiles handled by one CTA (blockIdx.z range)
+  float scale;             // softmax scale (natural-log units)
+  const float* lse_pad;    // [H][n_q_pad], +inf padding
+  uint32_t* u_code;        // [H][T] order codes, atomicMax-merged (pre-zeroed)
+  uint32_t* err;
+};
+
+// Gram builder: for key blocks (bi, bj), bi <= bj, of 128 selected keys, over
+// the query rows r of the CTA's split:
+//   E_jr = 2^(s2 * S_jr + colb2_j - rowsh2_r),  S = Kc q^T (scores)
+//   G[bi,bj] += E_bi E_bj^T   (hi/lo split, three products)
+//   c[bi]    += E_bi b         (diagonal blocks, when row_b != null)
+//   R[bi]    += E_bi O         (diagonal blocks, when O maps given)
+struct GramParams {
+  int n_q_pad, n_q;
+  int t_pad;
+  int nblk;                // t_pad / 128
+  int slabs_per_split;     // 64-row query slabs per CTA
+  float scale_log2;
+  const float* rowsh2;     // [H][n_q_pad]; +inf padding zeroes the row
+  const float* row_b;      // [H][n_q_pad] or null
+  const float* colb2;      // [H][t_pad]; -inf for unused keys
+  float* Gpart;            // [nsplit][H][t_pad][t_pad]
+  float* cpart;            // [nsplit][H][t_pad] or null
+  float* Rpart;            // [nsplit][H][t_pad][d_v] or null
+  int d_v;
+  uint32_t* err;
+};
+
+// Compact log mass per query: lc2_r = log2 sum_j 2^(s2 * S_rj + colb2_j).
+struct CompactLseParams {
+  int n_q, n_q_pad, t_pad;
+  float scale_log2;
+  const float* colb2;      // [H][t_pad]
+  float* lc2_pad;          // [H][n_q_pad], +inf padding
+  uint32_t* err;
+};
+
+// Launchers (return cudaGetLastError()).
+cudaError_t launch_attn_stats(OperandMode mode, const CUtensorMap& mQ, const CUtensorMap& mK,
+                              const CUtensorMap& mV, const CUtensorMap& mVlo,
+                              const AttnStatsParams& p, int H, cudaStream_t st);
+cudaError_t launch_key_scores(OperandMode mode, const CUtensorMap& mK, const CUtensorMap& mQ,
+                              const KeyScoreParams& p, int H, int nsplit, cudaStream_t st);
+cudaError_t launch_gram(OperandMode mode, bool with_r, const CUtensorMap& mKc,
+                        const CUtensorMap& mQ, const CUtensorMap& mOhi, const CUtensorMap& mOlo,
+                        const GramParams& p, int H, int nsplit, cudaStream_t st);
+cudaError_t launch_compact_lse(OperandMode mode, const CUtensorMap& mQ, const CUtensorMap& mKc,
+                               const CompactLseParams& p, int H, cudaStream_t st);
+
+// Kernel shared-memory sizes (for the host's capability check).
+int attn_stats_smem(OperandMode mode);
+int key_scores_smem(OperandMode mode);
+int gram_smem(OperandMode mode);
+int compact_lse_smem(OperandMode mode);
+
+// ----------------------------------------------------------- SIMT kernels
+cudaError_t launch_convert_bf16_to_f16(const __nv_bfloat16* in, __half* out, size_t n,
+                                       cudaStream_t st);
+cudaError_t launch_split_f32(const float* in, __half* hi, __half* lo, size_t n, cudaStream_t st);
+// rows of d floats -> rows of 3d halves: qk_order 0 = [hi|lo|hi] (queries),
+// 1 = [hi|hi|lo] (keys)
+cudaError_t launch_split_rows3(const float* in, __half* out, size_t rows, int d, int qk_order,
+                               cudaStream_t st);
+cudaError_t launch_fill_f32(float* p, size_t n, float v, cudaStream_t st);
+cudaError_t launch_pad_rows(const float* in, float* out, int H, int n, int n_pad, float pad,
+                            cudaStream_t st);
+cudaError_t launch_decode_scores(const uint32_t* code, float* u, size_t n, cudaStream_t st);
+cudaError_t launch_encode_scores(const float* u, uint32_t* code, size_t n, cudaStream_t st);
+cudaError_t launch_select_topt(const uint32_t* code, int H, int T, int t, int32_t* idx,
+                               cudaStream_t st);
+cudaError_t launch_gather_rows(const void* src, void* dst, const int32_t* idx, int H, int T,
+                               int t, int t_pad, int row_bytes, cudaStream_t st);
+cudaError_t launch_gather_v(const void* V, int in_dtype, const int32_t* idx, float* Vc, int H,
+                            int T, int t, int t_pad, int d, cudaStream_t st);
+cudaError_t launch_reduce_partials(const float* part, float* out, int nsplit, size_t n,
+                                   cudaStream_t st);
+cudaError_t launch_symmetrize(float* G, int H, int t_pad, cudaStream_t st);
+cudaError_t launch_mass_rows(const float* rowmax_pad, const float* lse_pad, float* rowsh2,
+                             float* row_b, int H, int n_q, int n_q_pad, cudaStream_t st);
+cudaError_t launch_fill_colb2(float* colb2, int H, int t, int t_pad, cudaStream_t st);
+
+struct SolveParams {
+  int H, t, t_pad, d_v, max_iter;
+  const float* G;          // [H][t_pad][t_pad]
+  const float* c;          // [H][t_pad]
+  float* w;                // [H][t]
+  float* beta;             // [H][t]
+  float* colb2;            // [H][t_pad]: beta * log2(e), -inf for w = 0 and padding
+  float* mat;              // [H][t_pad][t_pad] scratch
+  float* vec;              // [H][8][t_pad] scratch
+  int32_t* head_status;    // [H]
+  int32_t* head_iters;     // [H]
+  uint32_t* err;
+};
+cudaError_t launch_nnls(const SolveParams& p, cudaStream_t st);
+
+struct OlsParams {
+  int H, t, t_pad, d_v;
+  const float* Hm;         // [H][t_pad][t_pad]
+  const float* R;          // [H][t_pad][d_v]
+  const float* Vc;         // [H][t_pad][d_v] original values of the selected keys
+  const float* w;          // [H][t]
+  float* mat;              // [H][t_pad][t_pad] scratch
+  float* Cv;               // [H][t][d_v]
+  int32_t* head_status;
+  uint32_t* err;
+};
+cudaError_t launch_ols(const OlsParams& p, cudaStream_t st);
+
+}  // namespace lc

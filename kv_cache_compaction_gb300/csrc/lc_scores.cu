@@ -1,0 +1,515 @@
+// Steps 2-3 of attention-matching compaction, plus the small data-movement
+// kernels of the pipeline.
+//
+// Step 2 ("Latent Compaction with Test-Time Training", §3.2 Eq. (6)): each
+// key's score is the largest softmax probability any reference query gives
+// it.  Because exp is monotone the reduction runs in the log domain,
+//   u_j = max_i (scale * q_i.k_j - lse_i),
+// so the pass needs no exponential at all.  The layout is key-stationary:
+// the tile S^T = K_tile Q_tile^T lands in tensor memory with one key per lane,
+// so each thread reduces its own key over the query columns with one FMA and
+// one max per score, and partial maxima over query splits merge with an
+// atomic max on order-preserving integer codes (exact and order-free).
+//
+// Step 3 ("KV compaction" blog, section "Fast KV Compaction via Attention
+// Matching": keep the keys with the highest attention): a per-head 4-pass
+// 8-bit radix select finds the t-th largest code exactly; keys above it and
+// the lowest-index keys equal to it are written in ascending index order.
+#include "lc_common.cuh"
+#include "lc_kernels.cuh"
+
+namespace lc {
+namespace {
+
+constexpr int kBK = 128;  // keys per CTA (TMEM lanes)
+constexpr int kBQ = 128;  // queries per tile (TMEM columns per buffer)
+
+template <int D_QK>
+struct KSLayout {
+  static constexpr int NQC = D_QK / 64;
+  static constexpr int K_BYTES = kBK * D_QK * 2;
+  static constexpr int QCHUNK = kBQ * 128;
+  static constexpr int Q_BYTES = NQC * QCHUNK;
+  static constexpr int NST = 2;
+  static constexpr int OFF_Q = K_BYTES;
+  static constexpr int OFF_L = OFF_Q + NST * Q_BYTES;
+  static constexpr int OFF_BAR = OFF_L + NST * kBQ * 4;
+  static constexpr int SMEM = 1024 + OFF_BAR + 128;
+};
+
+template <bool QK_BF16, int D_QK>
+__global__ void __launch_bounds__(192, 1)
+    key_scores_kernel(const __grid_constant__ CUtensorMap mK,
+                      const __grid_constant__ CUtensorMap mQ, const KeyScoreParams p) {
+  using L = KSLayout<D_QK>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = align1024(smem_raw);
+  uint8_t* sK = base;
+  uint8_t* sQ = base + L::OFF_Q;
+  float* sL = reinterpret_cast<float*>(base + L::OFF_L);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + L::OFF_BAR);
+  uint64_t* k_full = bars + 0;
+  uint64_t* q_full = bars + 1;   // [2]
+  uint64_t* q_empty = bars + 3;  // [2]
+  uint64_t* d_full = bars + 5;   // [2]
+  uint64_t* d_free = bars + 7;   // [2]
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 9);
+  __shared__ volatile int abort_flag;
+
+  const int warp = warp_id(), lane = lane_id();
+  const int k0 = blockIdx.x * kBK, h = blockIdx.y;
+  const int nqt = p.n_q_pad / kBQ;
+  const int t0i = blockIdx.z * p.tiles_per_split;
+  const int ntile = max(0, min(nqt, t0i + p.tiles_per_split) - t0i);
+
+  if (threadIdx.x == 0) {
+    abort_flag = launch_aborted(p.err) ? 1 : 0;
+    mbar_init(k_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 1 + 128);  // MMA commit + every epilogue thread
+      mbar_init(&d_full[i], 1);
+      mbar_init(&d_free[i], 128);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(tslot, 256);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tslot;
+
+  if (warp == 0) {
+    if (lane == 0 && ntile > 0) {
+      mbar_arrive_expect_tx(k_full, L::K_BYTES);
+      for (int c = 0; c < L::NQC; ++c) tma_load_3d(sK + c * kBK * 128, &mK, k_full, 64 * c, k0, h);
+      int issued = 0;
+      for (int i = 0; i < ntile; ++i) {
+        const int s = i & 1;
+        if (i >= 2 && !wait_bar(&q_empty[s], ((i >> 1) - 1) & 1, &abort_flag, p.err)) break;
+        const int q0 = (t0i + i) * kBQ;
+        mbar_arrive_expect_tx(&q_full[s], L::Q_BYTES + kBQ * 4);
+        for (int c = 0; c < L::NQC; ++c)
+          tma_load_3d(sQ + s * L::Q_BYTES + c * L::QCHUNK, &mQ, &q_full[s], 64 * c, q0, h);
+        bulk_g2s(sL + s * kBQ, p.lse_pad + static_cast<size_t>(h) * p.n_q_pad + q0, kBQ * 4,
+                 &q_full[s]);
+        issued = i + 1;
+      }
+      if (abort_flag) {
+        for (int i = (issued > 2 ? issued - 2 : 0); i < issued; ++i) {
+          const uint64_t tt = globaltimer_ns();
+          while (!mbar_try_wait(&q_full[i & 1], (i >> 1) & 1) &&
+                 globaltimer_ns() - tt < kWaitLimitNs) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && ntile > 0) {
+      constexpr uint32_t idesc = idesc_f16(kBK, kBQ, QK_BF16, false, false);
+      bool ok = wait_bar(k_full, 0, &abort_flag, p.err);
+      const uint32_t aK = smem_u32(sK);
+      for (int i = 0; ok && i < ntile; ++i) {
+        const int s = i & 1;
+        if (!wait_bar(&q_full[s], (i >> 1) & 1, &abort_flag, p.err)) break;
+        if (i >= 2 && !wait_bar(&d_free[s], ((i >> 1) - 1) & 1, &abort_flag, p.err)) break;
+        tc_fence_after();
+        const uint32_t aQ = smem_u32(sQ + s * L::Q_BYTES);
+#pragma unroll
+        for (int k = 0; k < D_QK / 16; ++k) {
+          const uint64_t da = sdesc_sw128(aK + (k >> 2) * (kBK * 128) + (k & 3) * 32, 16, 1024);
+          const uint64_t db = sdesc_sw128(aQ + (k >> 2) * L::QCHUNK + (k & 3) * 32, 16, 1024);
+          umma_f16_ss(tbase + s * kBQ, da, db, idesc, k > 0 ? 1u : 0u);
+        }
+        umma_commit(&d_full[s]);
+        umma_commit(&q_empty[s]);
+      }
+    }
+  } else {
+    const int wq = warp & 3;
+    const int key = k0 + wq * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    float u = -kInf;
+    bool ok = ntile > 0;
+    for (int i = 0; ok && i < ntile; ++i) {
+      const int s = i & 1;
+      if (!wait_bar(&d_full[s], (i >> 1) & 1, &abort_flag, p.err)) { ok = false; break; }
+      if (!wait_bar(&q_full[s], (i >> 1) & 1, &abort_flag, p.err)) { ok = false; break; }
+      tc_fence_after();
+      const float* lt = sL + s * kBQ;
+#pragma unroll
+      for (int c = 0; c < kBQ / 32; ++c) {
+        float v[32];
+        tmem_ld32(tbase + lane_off + s * kBQ + c * 32, v);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) u = fmaxf(u, fmaf(v[e], p.scale, -lt[c * 32 + e]));
+      }
+      tc_fence_before();
+      mbar_arrive(&d_free[s]);
+      mbar_arrive(&q_empty[s]);
+    }
+    if (ok && key < p.T) atomicMax(p.u_code + static_cast<size_t>(h) * p.T + key, order_code(u));
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tbase, 256);
+}
+
+template <bool QK_BF16, int D_QK>
+cudaError_t launch_ks_t(const CUtensorMap& mK, const CUtensorMap& mQ, const KeyScoreParams& p,
+                        int H, int nsplit, cudaStream_t st) {
+  using L = KSLayout<D_QK>;
+  auto kern = key_scores_kernel<QK_BF16, D_QK>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
+  if (e != cudaSuccess) return e;
+  dim3 grid((p.T + kBK - 1) / kBK, H, nsplit);
+  kern<<<grid, 192, L::SMEM, st>>>(mK, mQ, p);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ select
+constexpr int kSelThreads = 1024;
+
+__device__ __forceinline__ int block_exclusive_scan(int v, int* tmp, int& total) {
+  // tmp: 32 ints of shared memory
+  const int lane = lane_id(), w = warp_id();
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) tmp[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    int s = tmp[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    tmp[lane] = s;  // inclusive over warps
+  }
+  __syncthreads();
+  const int before_warp = w > 0 ? tmp[w - 1] : 0;
+  total = tmp[31];
+  __syncthreads();
+  return before_warp + x - v;
+}
+
+__global__ void __launch_bounds__(kSelThreads)
+    select_topt_kernel(const uint32_t* __restrict__ code, int T, int t, int32_t* __restrict__ idx) {
+  __shared__ int hist[256];
+  __shared__ int tmp[32];
+  __shared__ uint32_t s_prefix;
+  __shared__ int s_need;
+  const int h = blockIdx.x, tid = threadIdx.x;
+  const uint32_t* c = code + static_cast<size_t>(h) * T;
+  uint32_t prefix = 0, mask = 0;
+  int need = t;  // rank (from the top) still to locate inside the current bucket
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int b = tid; b < 256; b += kSelThreads) hist[b] = 0;
+    __syncthreads();
+    for (int j = tid; j < T; j += kSelThreads) {
+      const uint32_t v = c[j];
+      if ((v & mask) == prefix) atomicAdd(&hist[(v >> shift) & 255u], 1);
+    }
+    __syncthreads();
+    if (tid == 0) {
+      int acc = 0, b = 255;
+      for (; b > 0; --b) {
+        if (acc + hist[b] >= need) break;
+        acc += hist[b];
+      }
+      s_prefix = prefix | (static_cast<uint32_t>(b) << shift);
+      s_need = need - acc;
+    }
+    __syncthreads();
+    prefix = s_prefix;
+    need = s_need;
+    mask |= 255u << shift;
+    __syncthreads();
+  }
+  // prefix = code of the t-th largest; take all larger codes and the first
+  // `need` (lowest-index) codes equal to it.
+  const uint32_t tau = prefix;
+  const int chunk = (T + kSelThreads - 1) / kSelThreads;
+  const int j0 = min(T, tid * chunk), j1 = min(T, j0 + chunk);
+  int gt = 0, eq = 0;
+  for (int j = j0; j < j1; ++j) {
+    const uint32_t v = c[j];
+    gt += v > tau;
+    eq += v == tau;
+  }
+  int tot;
+  const int eq_before = block_exclusive_scan(eq, tmp, tot);
+  const int take_eq = max(0, min(eq, need - eq_before));
+  const int out0 = block_exclusive_scan(gt + take_eq, tmp, tot);
+  int o = out0, te = 0;
+  int32_t* dst = idx + static_cast<size_t>(h) * t;
+  for (int j = j0; j < j1; ++j) {
+    const uint32_t v = c[j];
+    if ((v > tau || (v == tau && te++ < take_eq)) && o < t) dst[o++] = j;
+  }
+}
+
+// ------------------------------------------------------------ small kernels
+__global__ void convert_bf16_f16_kernel(const __nv_bfloat16* in, __half* out, size_t n) {
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x)
+    out[i] = __float2half_rn(__bfloat162float(in[i]));
+}
+
+__global__ void split_f32_kernel(const float* in, __half* hi, __half* lo, size_t n) {
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    __half a, b;
+    split_f16(in[i], a, b);
+    hi[i] = a;
+    lo[i] = b;
+  }
+}
+
+__global__ void split_rows3_kernel(const float* in, __half* out, size_t rows, int d, int order) {
+  const size_t n = rows * d;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const size_t r = i / d;
+    const int k = static_cast<int>(i % d);
+    __half a, b;
+    split_f16(in[i], a, b);
+    __half* o = out + r * 3 * d;
+    o[k] = a;
+    o[d + k] = order == 0 ? b : a;
+    o[2 * d + k] = order == 0 ? a : b;
+  }
+}
+
+__global__ void fill_f32_kernel(float* p, size_t n, float v) {
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x)
+    p[i] = v;
+}
+
+__global__ void pad_rows_kernel(const float* in, float* out, int H, int n, int n_pad, float pad) {
+  const size_t tot = static_cast<size_t>(H) * n_pad;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < tot;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const size_t h = i / n_pad;
+    const int r = static_cast<int>(i % n_pad);
+    out[i] = r < n ? in[h * n + r] : pad;
+  }
+}
+
+__global__ void decode_kernel(const uint32_t* code, float* u, size_t n) {
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x)
+    u[i] = order_decode(code[i]);
+}
+
+__global__ void encode_kernel(const float* u, uint32_t* code, size_t n) {
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x)
+    code[i] = order_code(u[i]);
+}
+
+// dst[h][r] = src[h][idx[h][r]] for r < t, zero rows for t <= r < t_pad.
+// One warp per destination row, 16-byte moves.
+__global__ void gather_rows_kernel(const uint8_t* src, uint8_t* dst, const int32_t* idx, int H,
+                                   int T, int t, int t_pad, int row_bytes) {
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = lane_id();
+  if (gw >= H * t_pad) return;
+  const int h = gw / t_pad, r = gw % t_pad;
+  uint4* d = reinterpret_cast<uint4*>(dst + static_cast<size_t>(gw) * row_bytes);
+  const int n16 = row_bytes / 16;
+  const int j = r < t ? idx[static_cast<size_t>(h) * t + r] : -1;
+  if (j >= 0 && j < T) {
+    const uint4* s = reinterpret_cast<const uint4*>(src + (static_cast<size_t>(h) * T + j) * row_bytes);
+    for (int k = lane; k < n16; k += 32) d[k] = s[k];
+  } else {
+    for (int k = lane; k < n16; k += 32) d[k] = make_uint4(0, 0, 0, 0);
+  }
+}
+
+__global__ void gather_v_kernel(const void* V, int in_dtype, const int32_t* idx, float* Vc, int H,
+                                int T, int t, int t_pad, int d) {
+  const size_t n = static_cast<size_t>(H) * t_pad * d;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const int k = static_cast<int>(i % d);
+    const size_t hr = i / d;
+    const int r = static_cast<int>(hr % t_pad), h = static_cast<int>(hr / t_pad);
+    float v = 0.f;
+    const int j = r < t ? idx[static_cast<size_t>(h) * t + r] : -1;
+    if (j >= 0 && j < T) {
+      const size_t src = (static_cast<size_t>(h) * T + j) * d + k;
+      v = in_dtype == 0 ? __bfloat162float(static_cast<const __nv_bfloat16*>(V)[src])
+                        : static_cast<const float*>(V)[src];
+    }
+    Vc[i] = v;
+  }
+}
+
+__global__ void reduce_partials_kernel(const float* part, float* out, int nsplit, size_t n) {
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    float s = 0.f;
+    for (int z = 0; z < nsplit; ++z) s += part[static_cast<size_t>(z) * n + i];
+    out[i] = s;
+  }
+}
+
+// Copy the upper triangle to the lower one (the Gram builder writes the
+// upper block triangle only).
+__global__ void symmetrize_kernel(float* G, int H, int t_pad) {
+  const size_t n = static_cast<size_t>(H) * t_pad * t_pad;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const int c = static_cast<int>(i % t_pad);
+    const size_t hr = i / t_pad;
+    const int r = static_cast<int>(hr % t_pad);
+    if (r > c) {
+      const size_t h = hr / t_pad;
+      G[i] = G[(h * t_pad + c) * t_pad + r];
+    }
+  }
+}
+
+// Per-query shift and right-hand side of the mass fit, base 2:
+// rowsh2 = m * log2(e) (+inf in padded rows), row_b = exp(lse - m) (0 there).
+__global__ void mass_rows_kernel(const float* m_pad, const float* lse_pad, float* rowsh2,
+                                 float* row_b, int H, int n_q, int n_q_pad) {
+  const size_t n = static_cast<size_t>(H) * n_q_pad;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const int r = static_cast<int>(i % n_q_pad);
+    if (r < n_q) {
+      rowsh2[i] = m_pad[i] * kLog2e;
+      row_b[i] = ex2((lse_pad[i] - m_pad[i]) * kLog2e);
+    } else {
+      rowsh2[i] = kInf;
+      row_b[i] = 0.f;
+    }
+  }
+}
+
+__global__ void fill_colb2_kernel(float* colb2, int H, int t, int t_pad) {
+  const size_t n = static_cast<size_t>(H) * t_pad;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x)
+    colb2[i] = static_cast<int>(i % t_pad) < t ? 0.f : -kInf;
+}
+
+inline int grid_for(size_t n, int block = 256) {
+  size_t g = (n + block - 1) / block;
+  if (g > 152 * 16) g = 152 * 16;
+  return static_cast<int>(g < 1 ? 1 : g);
+}
+
+}  // namespace
+
+cudaError_t launch_key_scores(OperandMode mode, const CUtensorMap& mK, const CUtensorMap& mQ,
+                              const KeyScoreParams& p, int H, int nsplit, cudaStream_t st) {
+  switch (mode) {
+    case kBF16d128: return launch_ks_t<true, 128>(mK, mQ, p, H, nsplit, st);
+    case kBF16d64: return launch_ks_t<true, 64>(mK, mQ, p, H, nsplit, st);
+    case kSplitF16d64: return launch_ks_t<false, 192>(mK, mQ, p, H, nsplit, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+int key_scores_smem(OperandMode mode) {
+  switch (mode) {
+    case kBF16d128: return KSLayout<128>::SMEM;
+    case kBF16d64: return KSLayout<64>::SMEM;
+    case kSplitF16d64: return KSLayout<192>::SMEM;
+  }
+  return 0;
+}
+
+cudaError_t launch_select_topt(const uint32_t* code, int H, int T, int t, int32_t* idx,
+                               cudaStream_t st) {
+  select_topt_kernel<<<H, kSelThreads, 0, st>>>(code, T, t, idx);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_convert_bf16_to_f16(const __nv_bfloat16* in, __half* out, size_t n,
+                                       cudaStream_t st) {
+  convert_bf16_f16_kernel<<<grid_for(n), 256, 0, st>>>(in, out, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_split_f32(const float* in, __half* hi, __half* lo, size_t n, cudaStream_t st) {
+  split_f32_kernel<<<grid_for(n), 256, 0, st>>>(in, hi, lo, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_split_rows3(const float* in, __half* out, size_t rows, int d, int qk_order,
+                               cudaStream_t st) {
+  split_rows3_kernel<<<grid_for(rows * d), 256, 0, st>>>(in, out, rows, d, qk_order);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fill_f32(float* p, size_t n, float v, cudaStream_t st) {
+  fill_f32_kernel<<<grid_for(n), 256, 0, st>>>(p, n, v);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pad_rows(const float* in, float* out, int H, int n, int n_pad, float pad,
+                            cudaStream_t st) {
+  pad_rows_kernel<<<grid_for(static_cast<size_t>(H) * n_pad), 256, 0, st>>>(in, out, H, n, n_pad,
+                                                                          pad);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_scores(const uint32_t* code, float* u, size_t n, cudaStream_t st) {
+  decode_kernel<<<grid_for(n), 256, 0, st>>>(code, u, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_encode_scores(const float* u, uint32_t* code, size_t n, cudaStream_t st) {
+  encode_kernel<<<grid_for(n), 256, 0, st>>>(u, code, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows(const void* src, void* dst, const int32_t* idx, int H, int T,
+                               int t, int t_pad, int row_bytes, cudaStream_t st) {
+  const int warps = H * t_pad;
+  gather_rows_kernel<<<(warps * 32 + 255) / 256, 256, 0, st>>>(
+      static_cast<const uint8_t*>(src), static_cast<uint8_t*>(dst), idx, H, T, t, t_pad,
+      row_bytes);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_v(const void* V, int in_dtype, const int32_t* idx, float* Vc, int H,
+                            int T, int t, int t_pad, int d, cudaStream_t st) {
+  gather_v_kernel<<<grid_for(static_cast<size_t>(H) * t_pad * d), 256, 0, st>>>(
+      V, in_dtype, idx, Vc, H, T, t, t_pad, d);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reduce_partials(const float* part, float* out, int nsplit, size_t n,
+                                   cudaStream_t st) {
+  reduce_partials_kernel<<<grid_for(n), 256, 0, st>>>(part, out, nsplit, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_symmetrize(float* G, int H, int t_pad, cudaStream_t st) {
+  symmetrize_kernel<<<grid_for(static_cast<size_t>(H) * t_pad * t_pad), 256, 0, st>>>(G, H, t_pad);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mass_rows(const float* rowmax_pad, const float* lse_pad, float* rowsh2,
+                             float* row_b, int H, int n_q, int n_q_pad, cudaStream_t st) {
+  mass_rows_kernel<<<grid_for(static_cast<size_t>(H) * n_q_pad), 256, 0, st>>>(
+      rowmax_pad, lse_pad, rowsh2, row_b, H, n_q, n_q_pad);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fill_colb2(float* colb2, int H, int t, int t_pad, cudaStream_t st) {
+  fill_colb2_kernel<<<grid_for(static_cast<size_t>(H) * t_pad), 256, 0, st>>>(colb2, H, t, t_pad);
+  return cudaGetLastError();
+}
+
+}  // namespace lc

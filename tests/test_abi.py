@@ -1,0 +1,91 @@
+"""The C ABI without a GPU: the library builds and loads, exports every symbol
+include/lc.h declares, and rejects bad shapes on the host."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from kv_cache_compaction_gb300 import build as b
+    b.build()
+    import kv_cache_compaction_gb300 as lc
+    return lc.load_library()
+
+
+def declared_symbols():
+    with open(os.path.join(ROOT, "include", "lc.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\s*(?:lc_status|const char\*)\s+(lc_\w+)\(", text, re.M)))
+
+
+def test_header_declares_the_entry_points():
+    syms = declared_symbols()
+    for name in ("lc_compact_layer", "lc_full_attn_stats", "lc_fit_only", "lc_key_scores",
+                 "lc_select_topt", "lc_workspace_bytes", "lc_get_report"):
+        assert name in syms
+
+
+def test_every_declared_symbol_is_exported(lib):
+    import kv_cache_compaction_gb300 as lc
+    syms = declared_symbols()
+    missing = [s for s in syms if not hasattr(lib, s)]
+    assert not missing, missing
+    assert sorted(lc.EXPORTS) == syms
+
+
+def _shape(**kw):
+    import kv_cache_compaction_gb300 as lc
+    base = dict(n_kv_heads=8, n_q=32768, T=8192, d=128, t=256, in_dtype=0, scale=0.0,
+                nnls_max_iter=0)
+    base.update(kw)
+    return lc.Shape(**base)
+
+
+@pytest.mark.parametrize("kw,code", [
+    ({}, 0),
+    ({"d": 96}, 2),
+    ({"t": 8193}, 1),
+    ({"t": 2048, "T": 4096}, 2),
+    ({"t": 0}, 1),
+    ({"T": 0}, 1),
+    ({"n_q": 0}, 1),
+    ({"in_dtype": 1}, 2),          # fp32 needs d = 64
+    ({"in_dtype": 1, "d": 64}, 0),
+    ({"in_dtype": 7}, 1),
+    ({"scale": -1.0}, 1),
+    ({"scale": float("nan")}, 1),
+    ({"n_kv_heads": 0}, 1),
+    ({"n_kv_heads": 5000}, 1),
+])
+def test_workspace_query_validates_shape(lib, kw, code):
+    n = ctypes.c_size_t(0)
+    s = _shape(**kw)
+    assert lib.lc_workspace_bytes(ctypes.byref(s), ctypes.byref(n)) == code
+    if code == 0:
+        assert n.value > 0
+
+
+def test_workspace_grows_with_the_problem(lib):
+    a, b = ctypes.c_size_t(), ctypes.c_size_t()
+    s1, s2 = _shape(), _shape(T=16384, n_q=65536)
+    lib.lc_workspace_bytes(ctypes.byref(s1), ctypes.byref(a))
+    lib.lc_workspace_bytes(ctypes.byref(s2), ctypes.byref(b))
+    assert b.value > a.value
+    h = ctypes.c_size_t()
+    lib.lc_host_workspace_bytes(ctypes.byref(s1), ctypes.byref(h))
+    assert h.value > a.value
+
+
+def test_null_handle_and_status_strings(lib):
+    s = _shape()
+    assert lib.lc_compact_layer(None, ctypes.byref(s), None, None, None, None, None, None, None,
+                                None, 0, None) != 0
+    assert lib.lc_status_string(0) == b"ok"
+    for code in range(8):
+        assert lib.lc_status_string(code)
+    assert lib.lc_destroy(None) == 1
