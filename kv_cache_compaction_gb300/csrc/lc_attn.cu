@@ -6,7 +6,8 @@
 // tiles of BN.  Warp roles:
 //   warp 0      TMA producer: the Q tile once, then K/V tiles into a 2-stage ring;
 //   warp 1      tensor-core issuer: S_j = Q K_j^T into a double-buffered TMEM
-//               accumulator, then O += P_j V_j (P split into fp16 hi + lo);
+//               accumulator, then O += P_j V_j with P in fp16 (for fp32
+//               inputs P and V are split into fp16 hi + lo pairs);
 //   warps 2..5  softmax: thread = query row; reads S_j from TMEM, keeps a
 //               running row max and sum, writes P_j to shared memory.
 // The exponent reference of a row moves only when the row max grows by more
@@ -35,7 +36,7 @@ struct AttnLayout {
   static constexpr int OFF_STAGE = Q_BYTES;
   static constexpr int OFF_PHI = OFF_STAGE + NST * STAGE;
   static constexpr int OFF_PLO = OFF_PHI + P_BYTES;
-  static constexpr int OFF_BAR = OFF_PLO + P_BYTES;
+  static constexpr int OFF_BAR = OFF_PLO + (V_TERMS == 2 ? P_BYTES : 0);
   static constexpr int SMEM = 1024 + OFF_BAR + 256;
 };
 
@@ -161,9 +162,9 @@ __global__ void __launch_bounds__(192, 1)
           const uint64_t dpl = sdesc_sw128(aPl + poff, 16, 1024);
           const uint64_t dv = sdesc_sw128(aV + k * 2048, L::KCHUNK, 1024);
           umma_f16_ss(tO, dph, dv, idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
-          umma_f16_ss(tO, dpl, dv, idesc_pv, 1u);
           if (V_TERMS == 2) {
             const uint64_t dvl = sdesc_sw128(aV + L::V_BYTES + k * 2048, L::KCHUNK, 1024);
+            umma_f16_ss(tO, dpl, dv, idesc_pv, 1u);
             umma_f16_ss(tO, dph, dvl, idesc_pv, 1u);
           }
         }
@@ -231,11 +232,15 @@ __global__ void __launch_bounds__(192, 1)
           pv[e] = ex2(x[c8 * 8 + e] - m_ref);
           l += pv[e];
         }
-        uint4 hi, lo;
-        split8(pv, hi, lo);
         const uint32_t off = (c8 >> 3) * L::PCHUNK + sw128_offset(row, (c8 & 7) * 8);
-        *reinterpret_cast<uint4*>(sPhi + off) = hi;
-        *reinterpret_cast<uint4*>(sPlo + off) = lo;
+        if (V_TERMS == 2) {
+          uint4 hi, lo;
+          split8(pv, hi, lo);
+          *reinterpret_cast<uint4*>(sPhi + off) = hi;
+          *reinterpret_cast<uint4*>(sPlo + off) = lo;
+        } else {
+          *reinterpret_cast<uint4*>(sPhi + off) = pack8_f16(pv);
+        }
       }
       fence_async_smem();
       tc_fence_before();

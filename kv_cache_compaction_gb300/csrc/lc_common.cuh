@@ -50,6 +50,13 @@ __device__ __forceinline__ void split8(const float* x, uint4& hi, uint4& lo) {
                   pack_h2(l[6], l[7]));
 }
 
+__device__ __forceinline__ uint4 pack8_f16(const float* x) {
+  return make_uint4(pack_h2(__float2half_rn(x[0]), __float2half_rn(x[1])),
+                    pack_h2(__float2half_rn(x[2]), __float2half_rn(x[3])),
+                    pack_h2(__float2half_rn(x[4]), __float2half_rn(x[5])),
+                    pack_h2(__float2half_rn(x[6]), __float2half_rn(x[7])));
+}
+
 // Order-preserving map of a non-NaN float to uint32 (larger float -> larger
 // code); -0 and +0 map to the same code.
 __device__ __forceinline__ uint32_t order_code(float f) {

@@ -11,7 +11,8 @@ namespace lc {
 
 // Which operand encoding the tensor-core passes use.
 //  kBF16d128 / kBF16d64: Q, K bf16 with d_qk = d; V converted to fp16 (exact
-//      for bf16 values in the fp16 range), one P.V term pair.
+//      for bf16 values in the fp16 range) and P rounded to fp16: one P.V
+//      product (the rounding of P moves C_v by ~1e-5 relative).
 //  kSplitF16d64: fp32 inputs; Q = [Qhi|Qlo|Qhi], K = [Khi|Khi|Klo] as fp16
 //      (d_qk = 3d = 192) so S keeps fp32 accuracy; V = Vhi + Vlo.
 enum OperandMode { kBF16d128 = 0, kBF16d64 = 1, kSplitF16d64 = 2 };
@@ -127,6 +128,7 @@ struct SolveParams {
   uint32_t* err;
 };
 cudaError_t launch_nnls(const SolveParams& p, cudaStream_t st);
+size_t solver_smem(int t);  // dynamic shared memory of the solver kernels
 
 struct OlsParams {
   int H, t, t_pad, d_v;
