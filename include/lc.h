@@ -106,6 +106,21 @@ lc_status lc_key_scores(lc_handle h, const lc_shape* shape, const void* Q, const
 lc_status lc_select_topt(lc_handle h, int n_heads, int T, int t, const float* u, int32_t* idx,
                          void* workspace, size_t workspace_bytes, void* stream);
 
+/* Step 3 for callers that cannot allocate device memory or pass a workspace
+ * (for example code under a memory planner that forbids allocation on the
+ * serving path).  No counterpart on the pages: this is a deployment variant
+ * of lc_select_topt with identical results.  Its scratch is a fixed array of
+ * LC_NOALLOC_MAX_SCORES 32-bit codes (4 MiB) compiled into the library, held
+ * on every GPU that loads it until the process exits.  Works on the current
+ * CUDA device; the first call on a device looks up the array's address and
+ * should come before any stream capture.  n_heads*T above
+ * LC_NOALLOC_MAX_SCORES returns LC_ERR_UNSUPPORTED and enqueues nothing.
+ * Calls that overlap on the GPU share the array and race: serialise them.
+ * No cudaMalloc, cudaFree or allocating library call is made. */
+#define LC_NOALLOC_MAX_SCORES (1 << 20)
+lc_status lc_select_topt_noalloc(int n_heads, int T, int t, const float* u, int32_t* idx,
+                                 void* stream);
+
 /* Steps 4-5 for given selected keys and full statistics (rowmax, lse, O as
  * produced by lc_full_attn_stats).  idx entries must be distinct and in
  * [0, T).  Outputs w, beta [H][t] and Cv [H][t][d]. */

@@ -35,7 +35,7 @@ EXPORTS = [
     "lc_create", "lc_destroy", "lc_workspace_bytes", "lc_full_attn_stats", "lc_key_scores",
     "lc_select_topt", "lc_fit_only", "lc_compact_layer", "lc_host_workspace_bytes",
     "lc_compact_layer_host", "lc_get_report", "lc_profile_enable", "lc_profile_read",
-    "lc_status_string",
+    "lc_select_topt_noalloc", "lc_status_string",
 ]
 
 LC_BF16, LC_FP32 = 0, 1
@@ -74,6 +74,7 @@ def load_library(path: str = LIB_PATH):
         "lc_full_attn_stats": ([vp, sp, vp, vp, vp, f32p, f32p, f32p, vp, sz, vp], i32),
         "lc_key_scores": ([vp, sp, vp, vp, vp, vp, vp, sz, vp], i32),
         "lc_select_topt": ([vp, i32, i32, i32, vp, vp, vp, sz, vp], i32),
+        "lc_select_topt_noalloc": ([i32, i32, i32, vp, vp, vp], i32),
         "lc_fit_only": ([vp, sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
         "lc_compact_layer": ([vp, sp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
         "lc_compact_layer_host": ([vp, sp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
