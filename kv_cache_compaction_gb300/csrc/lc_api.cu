@@ -489,11 +489,12 @@ lc_status run_fit(const Ctx& c, const void* qop, const void* kop, const void* V,
   op.Vc = c.at<float>(p.vc);
   op.w = w;
   op.mat = c.at<float>(p.mat);
+  op.dinv = c.at<float>(p.vec);
   op.Cv = Cv;
   op.head_status = c.h->d_status;
   op.err = c.h->d_err;
   {
-    LC_PROF(c, "ols", 1);
+    LC_PROF(c, "ols", 2);
     LC_CUDA(launch_ols(op, c.st));
   }
   return LC_OK;

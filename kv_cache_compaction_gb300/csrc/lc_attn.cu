@@ -187,22 +187,36 @@ __global__ void __launch_bounds__(192, 1)
       if (!wait_bar(&s_full[b], (j >> 1) & 1, &abort_flag, p.err)) { ok = false; break; }
       tc_fence_after();
       float x[BN];
+      if constexpr (BN == 128) {
+        tmem_ld128(tbase + lane_off + b * BN, x);
+      } else {
 #pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
-        float v[32];
-        tmem_ld32(tbase + lane_off + b * BN + c * 32, v);
+        for (int c = 0; c < BN / 32; ++c) {
+          float v[32];
+          tmem_ld32(tbase + lane_off + b * BN + c * 32, v);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) x[c * 32 + e] = v[e];
+          for (int e = 0; e < 32; ++e) x[c * 32 + e] = v[e];
+        }
       }
       tc_fence_before();
       mbar_arrive(&s_free[b]);
       const int valid = p.T - j * BN;
-      float mx = -kInf;
+      if (valid < BN) {  // ragged last tile: keys past T do not exist
 #pragma unroll
-      for (int k = 0; k < BN; ++k) {
-        x[k] = (k < valid) ? x[k] * sl2 : -kInf;
-        mx = fmaxf(mx, x[k]);
+        for (int k = 0; k < BN; ++k)
+          if (k >= valid) x[k] = -kInf;
       }
+      // row max of the raw scores (scale > 0), eight independent chains
+      float m8[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) m8[e] = x[e];
+#pragma unroll
+      for (int k = 8; k < BN; k += 8)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) m8[e] = fmaxf(m8[e], x[k + e]);
+      const float mx =
+          fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * sl2;
       m_true = fmaxf(m_true, mx);
       const bool resc = mx > m_ref + 8.f;
       const float new_ref = resc ? mx : m_ref;
@@ -222,15 +236,22 @@ __global__ void __launch_bounds__(192, 1)
           }
         }
       }
-      l *= alpha;
       m_ref = new_ref;
+      // p = 2^(S * scale*log2e - m_ref): packed FMA, hardware exp2, eight
+      // partial sums
+      const float2 s2 = make_float2(sl2, sl2);
+      const float2 nm2 = make_float2(-m_ref, -m_ref);
+      float2 l4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                      make_float2(0.f, 0.f)};
 #pragma unroll
       for (int c8 = 0; c8 < BN / 8; ++c8) {
         float pv[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          pv[e] = ex2(x[c8 * 8 + e] - m_ref);
-          l += pv[e];
+        for (int e = 0; e < 4; ++e) {
+          const float2 a = __ffma2_rn(make_float2(x[c8 * 8 + 2 * e], x[c8 * 8 + 2 * e + 1]), s2, nm2);
+          pv[2 * e] = ex2(a.x);
+          pv[2 * e + 1] = ex2(a.y);
+          l4[e] = __fadd2_rn(l4[e], make_float2(pv[2 * e], pv[2 * e + 1]));
         }
         const uint32_t off = (c8 >> 3) * L::PCHUNK + sw128_offset(row, (c8 & 7) * 8);
         if (V_TERMS == 2) {
@@ -242,6 +263,8 @@ __global__ void __launch_bounds__(192, 1)
           *reinterpret_cast<uint4*>(sPhi + off) = pack8_f16(pv);
         }
       }
+      l = fmaf(l, alpha, ((l4[0].x + l4[0].y) + (l4[1].x + l4[1].y)) +
+                             ((l4[2].x + l4[2].y) + (l4[3].x + l4[3].y)));
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(p_full);

@@ -50,11 +50,14 @@ __device__ __forceinline__ void split8(const float* x, uint4& hi, uint4& lo) {
                   pack_h2(l[6], l[7]));
 }
 
+__device__ __forceinline__ uint32_t f2_to_h2(float a, float b) {
+  const __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
 __device__ __forceinline__ uint4 pack8_f16(const float* x) {
-  return make_uint4(pack_h2(__float2half_rn(x[0]), __float2half_rn(x[1])),
-                    pack_h2(__float2half_rn(x[2]), __float2half_rn(x[3])),
-                    pack_h2(__float2half_rn(x[4]), __float2half_rn(x[5])),
-                    pack_h2(__float2half_rn(x[6]), __float2half_rn(x[7])));
+  return make_uint4(f2_to_h2(x[0], x[1]), f2_to_h2(x[2], x[3]), f2_to_h2(x[4], x[5]),
+                    f2_to_h2(x[6], x[7]));
 }
 
 // Order-preserving map of a non-NaN float to uint32 (larger float -> larger

@@ -133,10 +133,11 @@ size_t solver_smem(int t);  // dynamic shared memory of the solver kernels
 struct OlsParams {
   int H, t, t_pad, d_v;
   const float* Hm;         // [H][t_pad][t_pad]
-  const float* R;          // [H][t_pad][d_v]
+  float* R;                // [H][t_pad][d_v]; overwritten (solved in place)
   const float* Vc;         // [H][t_pad][d_v] original values of the selected keys
   const float* w;          // [H][t]
-  float* mat;              // [H][t_pad][t_pad] scratch
+  float* mat;              // [H][t_pad][t_pad] scratch (factor, packed blocks)
+  float* dinv;             // [H][t_pad] scratch (reciprocal diagonal of the factor)
   float* Cv;               // [H][t][d_v]
   int32_t* head_status;
   uint32_t* err;

@@ -38,7 +38,7 @@ struct KSLayout {
 };
 
 template <bool QK_BF16, int D_QK>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(192, 2)
     key_scores_kernel(const __grid_constant__ CUtensorMap mK,
                       const __grid_constant__ CUtensorMap mQ, const KeyScoreParams p) {
   using L = KSLayout<D_QK>;
@@ -129,25 +129,36 @@ __global__ void __launch_bounds__(192, 1)
     const int wq = warp & 3;
     const int key = k0 + wq * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    float u = -kInf;
+    float u8[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) u8[e] = -kInf;
     bool ok = ntile > 0;
     for (int i = 0; ok && i < ntile; ++i) {
       const int s = i & 1;
       if (!wait_bar(&d_full[s], (i >> 1) & 1, &abort_flag, p.err)) { ok = false; break; }
       if (!wait_bar(&q_full[s], (i >> 1) & 1, &abort_flag, p.err)) { ok = false; break; }
       tc_fence_after();
-      const float* lt = sL + s * kBQ;
+      const float2* lt = reinterpret_cast<const float2*>(sL + s * kBQ);
+      const float2 sc2 = make_float2(p.scale, p.scale);
 #pragma unroll
       for (int c = 0; c < kBQ / 32; ++c) {
         float v[32];
         tmem_ld32(tbase + lane_off + s * kBQ + c * 32, v);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) u = fmaxf(u, fmaf(v[e], p.scale, -lt[c * 32 + e]));
+        for (int e = 0; e < 16; ++e) {
+          const float2 l2 = lt[c * 16 + e];
+          const float2 a = __ffma2_rn(make_float2(v[2 * e], v[2 * e + 1]), sc2,
+                                      make_float2(-l2.x, -l2.y));
+          u8[(2 * e) & 7] = fmaxf(u8[(2 * e) & 7], a.x);
+          u8[(2 * e + 1) & 7] = fmaxf(u8[(2 * e + 1) & 7], a.y);
+        }
       }
       tc_fence_before();
       mbar_arrive(&d_free[s]);
       mbar_arrive(&q_empty[s]);
     }
+    const float u = fmaxf(fmaxf(fmaxf(u8[0], u8[1]), fmaxf(u8[2], u8[3])),
+                          fmaxf(fmaxf(u8[4], u8[5]), fmaxf(u8[6], u8[7])));
     if (ok && key < p.T) atomicMax(p.u_code + static_cast<size_t>(h) * p.T + key, order_code(u));
   }
   tc_fence_before();

@@ -39,101 +39,153 @@ constexpr int kBS = 32;            // block size
 constexpr int kLD = 33;            // row stride inside a block
 constexpr int kBlk = kBS * kLD;    // floats per block
 constexpr int kResidentMax = 256;  // unknowns kept in shared memory
-// Right-hand sides per pass: fewer when the factor lives in L2, so that the
-// diagonal-block inverses and the chunk still fit in shared memory.
-__host__ __device__ inline int rhs_chunk(int n_pad) { return n_pad <= 256 ? 16 : 8; }
+constexpr int kMaxRhs = 128;       // right-hand sides solved in one pass
 constexpr unsigned kFull = 0xffffffffu;
 
 __device__ __forceinline__ float* blk(float* base, int I, int J) {
   return base + static_cast<size_t>(I * (I + 1) / 2 + J) * kBlk;
 }
 
+// One elimination step of the register Cholesky below; the step index is a
+// template parameter so that every register index is a compile-time constant.
+template <int K>
+__device__ __forceinline__ void chol32_step(float (&a)[kBS], int lane, bool& ok) {
+  const float piv = __shfl_sync(kFull, a[K], K);
+  const bool good = piv > 0.f;
+  ok = ok && good;
+  // 1/sqrt(pivot) from the hardware approximation (relative error ~2^-22)
+  const float rs = rsqrtf(good ? piv : 1.f);
+  const float l = (lane == K) ? (good ? piv : 1.f) * rs : a[K] * rs;
+  if (lane >= K) a[K] = l;
+#pragma unroll
+  for (int c = K + 1; c < kBS; ++c) {
+    const float lc = __shfl_sync(kFull, l, c);
+    if (lane > K) a[c] = fmaf(-l, lc, a[c]);
+  }
+  if constexpr (K + 1 < kBS) chol32_step<K + 1>(a, lane, ok);
+}
+
 // Cholesky of a 32x32 SPD block held by rows in registers (lane r: row r).
 // On return lane r holds row r of L in a[0..r].  Returns false if a pivot
 // was not positive (the pivot is then replaced by 1).
 __device__ __forceinline__ bool warp_chol32(float (&a)[kBS]) {
-  const int lane = lane_id();
   bool ok = true;
-#pragma unroll
-  for (int k = 0; k < kBS; ++k) {
-    const float piv = __shfl_sync(kFull, a[k], k);
-    const bool good = piv > 0.f;
-    ok = ok && good;
-    const float d = sqrtf(good ? piv : 1.f);
-    const float l = (lane == k) ? d : a[k] / d;
-    if (lane >= k) a[k] = l;
-#pragma unroll
-    for (int c = k + 1; c < kBS; ++c) {
-      const float lc = __shfl_sync(kFull, l, c);
-      if (lane > k) a[c] = fmaf(-l, lc, a[c]);
-    }
-  }
+  chol32_step<0>(a, lane_id(), ok);
   return ok;
 }
 
-// Factor the packed block matrix S (NB x NB blocks) in place; Linv receives
-// the inverses of the diagonal blocks (lower, stride 33).  Every diagonal
-// pivot that is not positive is replaced by 1 and reported.
-__device__ bool cta_cholesky(float* S, float* Linv, int NB, int* bad) {
-  const int tid = threadIdx.x, lane = lane_id(), warp = warp_id();
+// Register-tiled 32x32x32 product for one warp: lane = 4*rg + cg owns rows
+// 4rg..4rg+3 and columns 8cg..8cg+7 of the output tile, and
+//   acc[i][j] += sum_k A(4rg+i, k) * B(k, 8cg+j)
+// with A(r, k) = A[r*lda + k] (or A[k*lda + r] when A_T) and B(k, c) =
+// B[k*ldb + c] (or B[c*ldb + k] when B_T).  With the stride-33 blocks every
+// access pattern is free of bank conflicts (equal addresses broadcast).
+template <bool A_T, bool B_T>
+__device__ __forceinline__ void warp_mm32(const float* A, int lda, const float* B, int ldb,
+                                          float (&acc)[4][8]) {
+  const int lane = lane_id(), rg = lane >> 2, cg = lane & 3;
+#pragma unroll 4
+  for (int k = 0; k < kBS; ++k) {
+    float a[4], b[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) a[i] = A_T ? A[k * lda + 4 * rg + i] : A[(4 * rg + i) * lda + k];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) b[j] = B_T ? B[(8 * cg + j) * ldb + k] : B[k * ldb + 8 * cg + j];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+  }
+}
+
+__device__ __forceinline__ void zero_acc(float (&acc)[4][8]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+}
+
+// Factor diagonal block K (one warp) in place and store the reciprocals of
+// its diagonal in dinv[32K..32K+31].
+__device__ __forceinline__ void diag_factor(float* S, float* dinv, int K, int* bad) {
+  const int lane = lane_id();
+  float* Akk = blk(S, K, K);
+  float a[kBS];
+#pragma unroll
+  for (int c = 0; c < kBS; ++c) a[c] = Akk[lane * kLD + c];
+  if (!warp_chol32(a) && lane == 0) *bad = 1;
+#pragma unroll
+  for (int c = 0; c < kBS; ++c)
+    if (c <= lane) Akk[lane * kLD + c] = a[c];
+  float dl = a[0];
+#pragma unroll
+  for (int c = 1; c < kBS; ++c)
+    if (c == lane) dl = a[c];
+  dinv[K * kBS + lane] = __frcp_rn(dl);
+  __syncwarp();
+}
+
+// A_IJ -= L_IK L_JK^T (one warp).
+__device__ __forceinline__ void tile_update(float* S, int I, int J, int K) {
+  float acc[4][8];
+  zero_acc(acc);
+  warp_mm32<false, true>(blk(S, I, K), kLD, blk(S, J, K), kLD, acc);
+  float* C = blk(S, I, J);
+  const int lane = lane_id(), rg = lane >> 2, cg = lane & 3;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) C[(4 * rg + i) * kLD + 8 * cg + j] -= acc[i][j];
+}
+
+// Factor the packed block matrix S (NB x NB blocks) in place; dinv receives
+// the reciprocal diagonal of L.  Right-looking with one block of look-ahead:
+// warp 0 updates and factors the next diagonal block while the other warps
+// finish the trailing update.  Panels are solved row by row (one thread per
+// row, substitution against the factored diagonal block).  Every pivot that
+// is not positive is replaced by 1 and reported.
+__device__ bool cta_cholesky(float* S, float* dinv, int NB, int* bad) {
+  const int tid = threadIdx.x, warp = warp_id();
   if (tid == 0) *bad = 0;
   __syncthreads();
+  if (warp == 0) diag_factor(S, dinv, 0, bad);
+  __syncthreads();
   for (int K = 0; K < NB; ++K) {
-    float* Akk = blk(S, K, K);
-    float* Li = Linv + static_cast<size_t>(K) * kBlk;
-    if (warp == 0) {
-      float a[kBS];
-#pragma unroll
-      for (int c = 0; c < kBS; ++c) a[c] = Akk[lane * kLD + c];
-      if (!warp_chol32(a) && lane == 0) *bad = 1;
-#pragma unroll
-      for (int c = 0; c < kBS; ++c)
-        if (c <= lane) Akk[lane * kLD + c] = a[c];
-      __syncwarp();
-      // column `lane` of L^-1: forward substitution with L read back
+    // panel: rows of L_IK solve x L_KK^T = a
+    const float* Lkk = blk(S, K, K);
+    const float* di = dinv + K * kBS;
+    for (int g = tid; g < (NB - K - 1) * kBS; g += kThreads) {
+      const int I = K + 1 + g / kBS, r = g % kBS;
+      float* row = blk(S, I, K) + r * kLD;
       float x[kBS];
 #pragma unroll
-      for (int r = 0; r < kBS; ++r) {
-        float s = (r == lane) ? 1.f : 0.f;
+      for (int c = 0; c < kBS; ++c) {
+        float v = row[c];
 #pragma unroll
-        for (int k = 0; k < r; ++k) s = fmaf(-Akk[r * kLD + k], x[k], s);
-        x[r] = s / Akk[r * kLD + r];
+        for (int k = 0; k < c; ++k) v = fmaf(-x[k], Lkk[c * kLD + k], v);
+        x[c] = v * di[c];
       }
 #pragma unroll
-      for (int r = 0; r < kBS; ++r) Li[r * kLD + lane] = x[r];
+      for (int c = 0; c < kBS; ++c) row[c] = x[c];
     }
     __syncthreads();
-    // panel: L_IK = A_IK L_KK^-T, one warp per block row, lane = column
-    for (int task = warp; task < (NB - K - 1) * kBS; task += kWarps) {
-      const int I = K + 1 + task / kBS, r = task % kBS;
-      float* row = blk(S, I, K) + r * kLD;
-      float acc = 0.f;
-#pragma unroll
-      for (int k = 0; k < kBS; ++k) acc = fmaf(row[k], Li[lane * kLD + k], acc);
-      __syncwarp();
-      row[lane] = acc;
-    }
-    __syncthreads();
-    // trailing update: A_IJ -= L_IK L_JK^T for K < J <= I, one warp per block
+    // trailing update; warp 0 takes the next diagonal block and factors it
     const int m = NB - K - 1;
-    for (int task = warp; task < m * (m + 1) / 2; task += kWarps) {
-      int i = 0, rem = task;
-      while (rem > i) {
-        rem -= i + 1;
-        ++i;
-      }
-      const int I = K + 1 + i, J = K + 1 + rem;
-      const float* Lik = blk(S, I, K);
-      const float* Ljk = blk(S, J, K);
-      float* Aij = blk(S, I, J);
-      float lj[kBS];
-#pragma unroll
-      for (int k = 0; k < kBS; ++k) lj[k] = Ljk[lane * kLD + k];
-      for (int r = 0; r < kBS; ++r) {
-        float acc = 0.f;
-#pragma unroll
-        for (int k = 0; k < kBS; ++k) acc = fmaf(Lik[r * kLD + k], lj[k], acc);
-        Aij[r * kLD + lane] -= acc;
+    if (m > 0) {
+      if (warp == 0) {
+        tile_update(S, K + 1, K + 1, K);
+        __syncwarp();
+        diag_factor(S, dinv, K + 1, bad);
+      } else {
+        for (int task = warp - 1; task < m * (m + 1) / 2 - 1; task += kWarps - 1) {
+          // tasks enumerate the lower tiles (i >= j) except (0, 0)
+          int i = 0, rem = task + 1;
+          while (rem > i) {
+            rem -= i + 1;
+            ++i;
+          }
+          tile_update(S, K + 1 + i, K + 1 + rem, K);
+        }
       }
     }
     __syncthreads();
@@ -143,61 +195,91 @@ __device__ bool cta_cholesky(float* S, float* Linv, int NB, int* bad) {
   return ok;
 }
 
-// Solve L L^T X = B for the factor in (S, Linv) and nc columns of B
-// (row-major, stride ldb, NB*32 rows) in place.  T: scratch of 32 * nc floats.
-__device__ void cta_chol_solve(const float* S, const float* Linv, int NB, float* B, int ldb,
-                               int nc, float* T) {
-  const int tid = threadIdx.x;
+// Solve L L^T X = B for the factor (S, dinv) and nc columns of B (row-major,
+// stride ldb, NB*32 rows; shared or global memory) in place.  Each 32-row
+// block of B is staged in shared memory (T), solved against the diagonal
+// block by substitution (one thread per column) into T2, written back, and
+// used for the update of the remaining rows -- through the register-tiled
+// warp product when nc is a multiple of 32, element-wise otherwise.  T and T2
+// hold 32 * max(nc, 32) floats.
+__device__ void cta_chol_solve(const float* S, const float* dinv, int NB, float* B, int ldb,
+                               int nc, float* T, float* T2) {
+  const int tid = threadIdx.x, warp = warp_id(), lane = lane_id();
+  const int rg = lane >> 2, cg = lane & 3;
   const int n_out = kBS * nc;
-  // forward: L Y = B
-  for (int K = 0; K < NB; ++K) {
-    const float* Li = Linv + static_cast<size_t>(K) * kBlk;
-    float* BK = B + static_cast<size_t>(K) * kBS * ldb;
-    for (int e = tid; e < n_out; e += kThreads) {
-      const int r = e / nc, j = e % nc;
-      float acc = 0.f;
-      for (int k = 0; k <= r; ++k) acc = fmaf(Li[r * kLD + k], BK[k * ldb + j], acc);
-      T[e] = acc;
-    }
-    __syncthreads();
-    for (int e = tid; e < n_out; e += kThreads) BK[(e / nc) * ldb + e % nc] = T[e];
-    __syncthreads();
-    const int rows = (NB - K - 1) * kBS;
-    for (int e = tid; e < rows * nc; e += kThreads) {
-      const int gi = e / nc, j = e % nc;
-      const int I = K + 1 + gi / kBS, r = gi % kBS;
-      const float* Lik = blk(const_cast<float*>(S), I, K) + r * kLD;
-      float acc = 0.f;
+  const bool wide = (nc % kBS) == 0;
+  const int ntc = nc / kBS;
+  float* Sm = const_cast<float*>(S);
+  for (int pass = 0; pass < 2; ++pass) {
+    const bool fwd = pass == 0;
+    for (int step = 0; step < NB; ++step) {
+      const int K = fwd ? step : NB - 1 - step;
+      const float* Lkk = blk(Sm, K, K);
+      const float* di = dinv + K * kBS;
+      float* BK = B + static_cast<size_t>(K) * kBS * ldb;
+      for (int e = tid; e < n_out; e += kThreads) T[e] = BK[(e / nc) * ldb + e % nc];
+      __syncthreads();
+      for (int j = tid; j < nc; j += kThreads) {
+        float x[kBS];
+        if (fwd) {
 #pragma unroll
-      for (int k = 0; k < kBS; ++k) acc = fmaf(Lik[k], T[k * nc + j], acc);
-      B[(static_cast<size_t>(I) * kBS + r) * ldb + j] -= acc;
-    }
-    __syncthreads();
-  }
-  // backward: L^T X = Y
-  for (int K = NB - 1; K >= 0; --K) {
-    const float* Li = Linv + static_cast<size_t>(K) * kBlk;
-    float* BK = B + static_cast<size_t>(K) * kBS * ldb;
-    for (int e = tid; e < n_out; e += kThreads) {
-      const int r = e / nc, j = e % nc;
-      float acc = 0.f;
-      for (int k = r; k < kBS; ++k) acc = fmaf(Li[k * kLD + r], BK[k * ldb + j], acc);
-      T[e] = acc;
-    }
-    __syncthreads();
-    for (int e = tid; e < n_out; e += kThreads) BK[(e / nc) * ldb + e % nc] = T[e];
-    __syncthreads();
-    const int rows = K * kBS;
-    for (int e = tid; e < rows * nc; e += kThreads) {
-      const int gi = e / nc, j = e % nc;
-      const int I = gi / kBS, r = gi % kBS;  // I < K: Y_I -= L_KI^T X_K
-      const float* Lki = blk(const_cast<float*>(S), K, I);
-      float acc = 0.f;
+          for (int r = 0; r < kBS; ++r) {
+            float v = T[r * nc + j];
 #pragma unroll
-      for (int k = 0; k < kBS; ++k) acc = fmaf(Lki[k * kLD + r], T[k * nc + j], acc);
-      B[(static_cast<size_t>(I) * kBS + r) * ldb + j] -= acc;
+            for (int k = 0; k < r; ++k) v = fmaf(-Lkk[r * kLD + k], x[k], v);
+            x[r] = v * di[r];
+          }
+        } else {
+#pragma unroll
+          for (int r = kBS - 1; r >= 0; --r) {
+            float v = T[r * nc + j];
+#pragma unroll
+            for (int k = r + 1; k < kBS; ++k) v = fmaf(-Lkk[k * kLD + r], x[k], v);
+            x[r] = v * di[r];
+          }
+        }
+#pragma unroll
+        for (int r = 0; r < kBS; ++r) {
+          T2[r * nc + j] = x[r];
+          BK[r * ldb + j] = x[r];
+        }
+      }
+      __syncthreads();
+      // remaining rows: forward Y_I -= L_IK X_K (I > K); backward Y_I -= L_KI^T X_K (I < K)
+      const int i0 = fwd ? K + 1 : 0, i1 = fwd ? NB : K;
+      if (wide) {
+        for (int task = warp; task < (i1 - i0) * ntc; task += kWarps) {
+          const int I = i0 + task / ntc, ct = task % ntc;
+          float acc[4][8];
+          zero_acc(acc);
+          if (fwd) warp_mm32<false, false>(blk(Sm, I, K), kLD, T2 + ct * kBS, nc, acc);
+          else warp_mm32<true, false>(blk(Sm, K, I), kLD, T2 + ct * kBS, nc, acc);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            float* row = B + (static_cast<size_t>(I) * kBS + 4 * rg + i) * ldb + ct * kBS + 8 * cg;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) row[j] -= acc[i][j];
+          }
+        }
+      } else {
+        for (int e = tid; e < (i1 - i0) * kBS * nc; e += kThreads) {
+          const int gi = e / nc, j = e % nc;
+          const int I = i0 + gi / kBS, r = gi % kBS;
+          float acc = 0.f;
+          if (fwd) {
+            const float* Lik = blk(Sm, I, K) + r * kLD;
+#pragma unroll
+            for (int k = 0; k < kBS; ++k) acc = fmaf(Lik[k], T2[k * nc + j], acc);
+          } else {
+            const float* Lki = blk(Sm, K, I);
+#pragma unroll
+            for (int k = 0; k < kBS; ++k) acc = fmaf(Lki[k * kLD + r], T2[k * nc + j], acc);
+          }
+          B[(static_cast<size_t>(I) * kBS + r) * ldb + j] -= acc;
+        }
+      }
+      __syncthreads();
     }
-    __syncthreads();
   }
 }
 
@@ -280,11 +362,11 @@ __device__ int block_compact(const int* flag, int* pos, int n, int* red) {
 // Shared-memory plan of the solver kernels.
 struct SolverSmem {
   float* S;      // packed blocks (resident) or null
-  float* Linv;   // diagonal-block inverses
+  float* dinv;   // reciprocal diagonal of L
   float* vec;    // 4 * n_pad floats
   int* ivec;     // 3 * n_pad ints
-  float* rhs;    // n_pad * kRhsChunk floats
-  float* T;      // 32 * kRhsChunk floats
+  float* T;      // 32 * kMaxRhs floats
+  float* T2;     // 32 * kMaxRhs floats
 };
 
 __host__ __device__ inline size_t solver_smem_bytes(int n_pad) {
@@ -292,9 +374,9 @@ __host__ __device__ inline size_t solver_smem_bytes(int n_pad) {
   const bool resident = n_pad <= kResidentMax;
   size_t b = 0;
   if (resident) b += static_cast<size_t>(NB * (NB + 1) / 2) * kBlk * 4;
-  b += static_cast<size_t>(NB) * kBlk * 4;
+  b += static_cast<size_t>(n_pad) * 4;
   b += 4ull * n_pad * 4 + 3ull * n_pad * 4;
-  b += static_cast<size_t>(n_pad) * rhs_chunk(n_pad) * 4 + kBS * rhs_chunk(n_pad) * 4;
+  b += 2ull * kBS * kMaxRhs * 4;
   return b;
 }
 
@@ -307,16 +389,33 @@ __device__ SolverSmem carve(float* dyn, int n_pad) {
     s.S = p;
     p += static_cast<size_t>(NB * (NB + 1) / 2) * kBlk;
   }
-  s.Linv = p;
-  p += static_cast<size_t>(NB) * kBlk;
+  s.dinv = p;
+  p += n_pad;
   s.vec = p;
   p += 4 * n_pad;
   s.ivec = reinterpret_cast<int*>(p);
   p += 3 * n_pad;
-  s.rhs = p;
-  p += static_cast<size_t>(n_pad) * rhs_chunk(n_pad);
   s.T = p;
+  s.T2 = p + kBS * kMaxRhs;
   return s;
+}
+
+// Packed lower blocks of M_ab = src(a, b) for a, b < n and the identity
+// beyond n: one warp per matrix row, one lane per column, independent loads.
+template <class F>
+__device__ void gather_packed(float* S, int NB, int n, F src) {
+  const int lane = lane_id();
+  for (int task = warp_id(); task < NB * kBS; task += kWarps) {
+    const int I = task / kBS, r = task % kBS, a = task;
+#pragma unroll 4
+    for (int J = 0; J <= I; ++J) {
+      const int b = J * kBS + lane;
+      float v;
+      if (a < n && b < n) v = src(a, b);
+      else v = (a == b) ? 1.f : 0.f;
+      blk(S, I, J)[r * kLD + lane] = v;
+    }
+  }
 }
 
 __global__ void __launch_bounds__(kThreads, 1) nnls_bpp_kernel(const SolveParams p) {
@@ -330,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1) nnls_bpp_kernel(const SolveParams
   float* S = sm.S ? sm.S : p.mat + static_cast<size_t>(h) * tp * tp;
   float* x = sm.vec;
   float* cv = x + n_pad;
-  float* rhs = sm.rhs;
+  float* rhs = cv + n_pad;
   int* F = sm.ivec;
   int* Fidx = F + n_pad;
   int* flip = Fidx + n_pad;
@@ -348,26 +447,13 @@ __global__ void __launch_bounds__(kThreads, 1) nnls_bpp_kernel(const SolveParams
     const int nF = block_compact(F, Fidx, t, redi);
     const int NB = (nF + kBS - 1) / kBS;
     // gather G_FF into packed blocks; identity beyond nF
-    const int nb_el = NB * (NB + 1) / 2 * kBlk;
-    for (int e = tid; e < nb_el; e += kThreads) {
-      const int b = e / kBlk, o = e % kBlk;
-      const int r = o / kLD, c = o % kLD;
-      if (c >= kBS) continue;
-      int I = 0, rem = b;
-      while (rem > I) {
-        rem -= I + 1;
-        ++I;
-      }
-      const int a = I * kBS + r, bb = rem * kBS + c;
-      float v;
-      if (a < nF && bb < nF) v = G[static_cast<size_t>(Fidx[a]) * tp + Fidx[bb]];
-      else v = (a == bb) ? 1.f : 0.f;
-      S[static_cast<size_t>(b) * kBlk + o] = v;
-    }
+    gather_packed(S, NB, nF, [&](int a, int b) {
+      return G[static_cast<size_t>(Fidx[a]) * tp + Fidx[b]];
+    });
     for (int a = tid; a < NB * kBS; a += kThreads) rhs[a] = a < nF ? cv[Fidx[a]] : 0.f;
     __syncthreads();
-    if (!cta_cholesky(S, sm.Linv, NB, &bad)) status = LC_SINGULAR_STATUS;
-    cta_chol_solve(S, sm.Linv, NB, rhs, 1, 1, sm.T);
+    if (!cta_cholesky(S, sm.dinv, NB, &bad)) status = LC_SINGULAR_STATUS;
+    cta_chol_solve(S, sm.dinv, NB, rhs, 1, 1, sm.T, sm.T2);
     for (int j = tid; j < n_pad; j += kThreads) x[j] = 0.f;
     __syncthreads();
     for (int a = tid; a < nF; a += kThreads) x[Fidx[a]] = rhs[a];
@@ -377,6 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1) nnls_bpp_kernel(const SolveParams
     for (int j = warp; j < t; j += kWarps) {
       const float* g = G + static_cast<size_t>(j) * tp;
       float s = 0.f, sa = 0.f;
+#pragma unroll 8
       for (int k = lane; k < t; k += 32) {
         const float v = g[k] * x[k];
         s += v;
@@ -436,7 +523,10 @@ __global__ void __launch_bounds__(kThreads, 1) nnls_bpp_kernel(const SolveParams
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1) ols_kernel(const OlsParams p) {
+// Step 5, part 1: factor the output system (identity rows for zero-weight
+// keys and padding) into the packed blocks in p.mat, reciprocal diagonal in
+// p.dinv; the right-hand sides of those rows become the original values.
+__global__ void __launch_bounds__(kThreads, 1) ols_factor_kernel(const OlsParams p) {
   extern __shared__ float dyn[];
   __shared__ float redf[33];
   __shared__ int bad;
@@ -445,64 +535,71 @@ __global__ void __launch_bounds__(kThreads, 1) ols_kernel(const OlsParams p) {
   const int n_pad = (t + kBS - 1) / kBS * kBS;
   const int NB = n_pad / kBS;
   SolverSmem sm = carve(dyn, n_pad);
-  float* S = sm.S ? sm.S : p.mat + static_cast<size_t>(h) * tp * tp;
+  float* gS = p.mat + static_cast<size_t>(h) * tp * tp;
+  float* S = sm.S ? sm.S : gS;
   const float* Hm = p.Hm + static_cast<size_t>(h) * tp * tp;
-  const float* R = p.R + static_cast<size_t>(h) * tp * dv;
+  float* B = p.R + static_cast<size_t>(h) * tp * dv;
   const float* w = p.w + static_cast<size_t>(h) * t;
   const float* Vc = p.Vc + static_cast<size_t>(h) * tp * dv;
-  float* Cv = p.Cv + static_cast<size_t>(h) * t * dv;
-
-  // system with identity rows for zero-weight keys and padding
   float ridge = 0.f;
   int status = LC_OK_STATUS;
   for (int attempt = 0; attempt < 2; ++attempt) {
-    const int nb_el = NB * (NB + 1) / 2 * kBlk;
-    for (int e = tid; e < nb_el; e += kThreads) {
-      const int b = e / kBlk, o = e % kBlk;
-      const int r = o / kLD, c = o % kLD;
-      if (c >= kBS) continue;
-      int I = 0, rem = b;
-      while (rem > I) {
-        rem -= I + 1;
-        ++I;
-      }
-      const int a = I * kBS + r, bb = rem * kBS + c;
-      float v;
-      const bool za = a >= t || !(w[a] > 0.f), zb = bb >= t || !(w[bb] > 0.f);
-      if (za || zb) v = (a == bb) ? 1.f : 0.f;
-      else v = Hm[static_cast<size_t>(a) * tp + bb] + (a == bb ? ridge : 0.f);
-      S[static_cast<size_t>(b) * kBlk + o] = v;
-    }
+    gather_packed(S, NB, t, [&](int a, int b) {
+      if (!(w[a] > 0.f) || !(w[b] > 0.f)) return (a == b) ? 1.f : 0.f;
+      return Hm[static_cast<size_t>(a) * tp + b] + (a == b ? ridge : 0.f);
+    });
     __syncthreads();
-    if (cta_cholesky(S, sm.Linv, NB, &bad)) break;
+    if (cta_cholesky(S, sm.dinv, NB, &bad)) break;
     status = LC_SINGULAR_STATUS;
     float dsum = 0.f;
     for (int a = tid; a < t; a += kThreads)
       dsum += (w[a] > 0.f) ? Hm[static_cast<size_t>(a) * tp + a] : 0.f;
     ridge = 1e-6f * block_sum_f(dsum, redf) / t;
   }
-  // right-hand sides in chunks of rc columns
-  const int rc = rhs_chunk(n_pad);
-  for (int c0 = 0; c0 < dv; c0 += rc) {
-    const int nc = min(rc, dv - c0);
-    for (int e = tid; e < n_pad * nc; e += kThreads) {
-      const int a = e / nc, j = e % nc;
-      float v = 0.f;
-      if (a < t)
-        v = (w[a] > 0.f) ? R[static_cast<size_t>(a) * dv + c0 + j]
-                         : Vc[static_cast<size_t>(a) * dv + c0 + j];
-      sm.rhs[a * rc + j] = v;
-    }
-    __syncthreads();
-    cta_chol_solve(S, sm.Linv, NB, sm.rhs, rc, nc, sm.T);
-    for (int e = tid; e < t * nc; e += kThreads) {
-      const int a = e / nc, j = e % nc;
-      Cv[static_cast<size_t>(a) * dv + c0 + j] = sm.rhs[a * rc + j];
-    }
-    __syncthreads();
+  for (int e = tid; e < n_pad * dv; e += kThreads) {
+    const int a = e / dv;
+    if (a >= t) B[e] = 0.f;
+    else if (!(w[a] > 0.f)) B[e] = Vc[e];
   }
+  // publish the factor for the solve kernel
+  if (sm.S) {
+    const size_t nel = static_cast<size_t>(NB * (NB + 1) / 2) * kBlk;
+    for (size_t e = tid; e < nel; e += kThreads) gS[e] = sm.S[e];
+  }
+  float* gd = p.dinv + static_cast<size_t>(h) * tp;
+  for (int a = tid; a < n_pad; a += kThreads) gd[a] = sm.dinv[a];
   if (tid == 0 && status != LC_OK_STATUS && p.head_status[h] == LC_OK_STATUS)
     p.head_status[h] = status;
+}
+
+// Step 5, part 2: C_v columns [32*blockIdx.y, +32) by forward and backward
+// substitution with the published factor.
+__global__ void __launch_bounds__(kThreads, 1) ols_solve_kernel(const OlsParams p) {
+  extern __shared__ float dyn[];
+  const int h = blockIdx.x, tid = threadIdx.x;
+  const int t = p.t, tp = p.t_pad, dv = p.d_v;
+  const int n_pad = (t + kBS - 1) / kBS * kBS;
+  const int NB = n_pad / kBS;
+  SolverSmem sm = carve(dyn, n_pad);
+  const float* gS = p.mat + static_cast<size_t>(h) * tp * tp;
+  const float* S = gS;
+  if (sm.S) {
+    const size_t nel = static_cast<size_t>(NB * (NB + 1) / 2) * kBlk;
+    for (size_t e = tid; e < nel; e += kThreads) sm.S[e] = gS[e];
+    S = sm.S;
+  }
+  const float* gd = p.dinv + static_cast<size_t>(h) * tp;
+  for (int a = tid; a < n_pad; a += kThreads) sm.dinv[a] = gd[a];
+  __syncthreads();
+  const int c0 = blockIdx.y * kBS;
+  const int nc = min(kBS, dv - c0);
+  float* B = p.R + static_cast<size_t>(h) * tp * dv + c0;
+  cta_chol_solve(S, sm.dinv, NB, B, dv, nc, sm.T, sm.T2);
+  float* Cv = p.Cv + static_cast<size_t>(h) * t * dv + c0;
+  for (int e = tid; e < t * nc; e += kThreads) {
+    const int a = e / nc, j = e % nc;
+    Cv[static_cast<size_t>(a) * dv + j] = B[static_cast<size_t>(a) * dv + j];
+  }
 }
 
 }  // namespace
@@ -523,10 +620,15 @@ cudaError_t launch_nnls(const SolveParams& p, cudaStream_t st) {
 
 cudaError_t launch_ols(const OlsParams& p, cudaStream_t st) {
   const size_t smem = solver_smem(p.t);
-  cudaError_t e = cudaFuncSetAttribute(ols_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(ols_factor_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  ols_kernel<<<p.H, kThreads, smem, st>>>(p);
+  e = cudaFuncSetAttribute(ols_solve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  ols_factor_kernel<<<p.H, kThreads, smem, st>>>(p);
+  ols_solve_kernel<<<dim3(p.H, (p.d_v + kBS - 1) / kBS), kThreads, smem, st>>>(p);
   return cudaGetLastError();
 }
 

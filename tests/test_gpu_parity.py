@@ -22,6 +22,8 @@ CASES = {
     "bf16_tiny": synth.workload("cfg2", H=1, G=1, T=5, t=3, seed=9),
     "bf16_t_over_128": synth.workload("cfg2", H=2, T=700, G=2, t=160, seed=10),
     "bf16_iid_d128": synth.workload("cfg2", H=1, T=640, G=2, t=64, kind="iid", seed=11),
+    "bf16_t256": synth.workload("cfg2", H=2, T=1024, G=4, t=256, seed=12),
+    "bf16_t300_ragged": synth.workload("cfg2", H=1, T=1100, G=3, t=300, seed=13),
 }
 
 
@@ -170,17 +172,31 @@ def test_zero_queries(comp):
 
 def test_nnls_iteration_cap_reported(comp):
     """With the cap at one iteration the NNLS reports LC_ERR_NOT_CONVERGED on a
-    head that needs more, and every output stays finite (beta may be -inf)."""
+    head whose unconstrained least-squares solution is infeasible, and every
+    output stays finite (beta may be -inf).  The fit runs on the oracle's
+    selection so that both sides solve the same problem."""
     w = synth.workload("cfg2", H=2, T=2048, G=4, t=256, seed=23)
     d, Q, K, V = inputs(w)
     r = [oracle.compact_head(d["Q"][h], d["K"][h], d["V"][h], w.t, w.softmax_scale) for h in range(w.H)]
-    need_more = [int(np.sum(x["w"] == 0) > 0) for x in r]
-    idx, wg, bg, cg = comp.compact_layer(Q, K, V, w.t, nnls_max_iter=1)
+    infeasible = []
+    for x in r:
+        z = np.linalg.solve(x["G"], x["c"])
+        infeasible.append(bool(np.any(z < -1e-3 * np.abs(z).max())))
+    assert any(infeasible), "test case has no infeasible head"
+    args = (dev_i32(np.stack([x["idx"] for x in r])), dev_f32(np.stack([x["m"] for x in r])),
+            dev_f32(np.stack([x["lse"] for x in r])), dev_f32(np.stack([x["O"] for x in r])))
+    wg, bg, cg = comp.fit_only(Q, K, V, *args, nnls_max_iter=1)
     rep = comp.report(w.H)
     for h in range(w.H):
-        if need_more[h]:
+        if infeasible[h]:
             assert rep.head_status[h] == 5
         assert np.all(np.isfinite(host(cg)[h])) and np.all(np.isfinite(host(wg)[h]))
+    wg, bg, cg = comp.fit_only(Q, K, V, *args)
+    rep = comp.report(w.H)
+    for h in range(w.H):
+        assert rep.head_status[h] == 0
+        assert relf(host(wg)[h], r[h]["w"]) <= FIT_REL
+        assert relf(host(cg)[h], r[h]["Cv"]) <= FIT_REL
 
 
 def test_host_entry_matches_device(comp):
