@@ -60,9 +60,7 @@ struct Plan {
   int H, n_q, T, d, t, d_qk, n_q_pad, t_pad, nblk;
   float scale;
   int max_iter;
-  int ks_split, ks_tiles;
-  int g5_split, g5_slabs;
-  int g7_split, g7_slabs;
+  int ks_max, g5_max, g7_max;  // largest query splits the workspace holds
   // workspace offsets (bytes)
   size_t qop, kop, vhi, vlo;            // operand copies (16-bit)
   size_t m_pad, lse_pad, ohi, olo;      // step-1 results
@@ -75,12 +73,32 @@ struct Plan {
   size_t total;
 };
 
-int choose_split(int units, int per_split_min, int max_split) {
-  // enough CTAs for about two waves over 152 SMs
-  int s = (2 * 152 + units - 1) / units;
+// Query-range split for a launch of `units` independent CTAs (times the
+// split) on `sms` SMs with `occ` CTAs resident per SM: the split in
+// [1, max_split] whose last wave is fullest (ties to the smaller split).
+int best_split(int units, int sms, int occ, int max_split) {
+  const int slots = sms * occ;
+  int best = 1;
+  double best_eff = -1.0;
+  for (int s = 1; s <= max_split; ++s) {
+    const long long ctas = static_cast<long long>(units) * s;
+    const long long waves = (ctas + slots - 1) / slots;
+    const double eff = static_cast<double>(ctas) / static_cast<double>(waves * slots);
+    if (eff > best_eff + 1e-3) {
+      best_eff = eff;
+      best = s;
+    }
+  }
+  return best;
+}
+
+// Upper bound on the split used for `units` CTAs: about four full waves of
+// a 160-SM device, never more than the number of query tiles.
+int max_split(int units, int occ, int tiles) {
+  int s = (4 * 160 * occ + units - 1) / units;
   if (s < 1) s = 1;
-  if (s > max_split) s = max_split;
-  (void)per_split_min;
+  if (s > tiles) s = tiles;
+  if (s > 64) s = 64;
   return s;
 }
 
@@ -118,19 +136,11 @@ Plan make_plan(const lc_shape* s) {
   p.max_iter = s->nnls_max_iter > 0 ? s->nnls_max_iter : 3 * s->t;
 
   const int nqt = p.n_q_pad / 128;
-  const int ktiles = (p.T + 127) / 128;
-  p.ks_split = choose_split(ktiles * p.H, 1, nqt);
-  p.ks_tiles = (nqt + p.ks_split - 1) / p.ks_split;
-  p.ks_split = (nqt + p.ks_tiles - 1) / p.ks_tiles;
-
   const int slabs = p.n_q_pad / 64;
   const int npairs = p.nblk * (p.nblk + 1) / 2;
-  p.g5_split = choose_split(npairs * p.H, 1, slabs);
-  p.g5_slabs = (slabs + p.g5_split - 1) / p.g5_split;
-  p.g5_split = (slabs + p.g5_slabs - 1) / p.g5_slabs;
-  p.g7_split = choose_split((npairs + p.nblk) * p.H, 1, slabs);
-  p.g7_slabs = (slabs + p.g7_split - 1) / p.g7_split;
-  p.g7_split = (slabs + p.g7_slabs - 1) / p.g7_slabs;
+  p.ks_max = max_split(((p.T + 255) / 256) * p.H, 2, nqt);
+  p.g5_max = max_split(npairs * p.H, 1, slabs);
+  p.g7_max = max_split((npairs + p.nblk) * p.H, 1, slabs);
 
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -161,12 +171,12 @@ Plan make_plan(const lc_shape* s) {
   p.colb2 = take(H * p.t_pad * 4);
   p.lc2 = take(H * p.n_q_pad * 4);
   const size_t tt = static_cast<size_t>(p.t_pad) * p.t_pad;
-  p.gpart = take(static_cast<size_t>(p.g5_split) * H * tt * 4);
-  p.cpart = take(static_cast<size_t>(p.g5_split) * H * p.t_pad * 4);
+  p.gpart = take(static_cast<size_t>(p.g5_max) * H * tt * 4);
+  p.cpart = take(static_cast<size_t>(p.g5_max) * H * p.t_pad * 4);
   p.G = take(H * tt * 4);
   p.c = take(H * p.t_pad * 4);
-  p.hpart = take(static_cast<size_t>(p.g7_split) * H * tt * 4);
-  p.rpart = take(static_cast<size_t>(p.g7_split) * H * p.t_pad * p.d * 4);
+  p.hpart = take(static_cast<size_t>(p.g7_max) * H * tt * 4);
+  p.rpart = take(static_cast<size_t>(p.g7_max) * H * p.t_pad * p.d * 4);
   p.Hm = take(H * tt * 4);
   p.R = take(H * p.t_pad * p.d * 4);
   p.vc = take(H * p.t_pad * p.d * 4);
@@ -236,6 +246,7 @@ struct Profiler {
 
 struct lc_context {
   int device = 0;
+  int sm_count = 148;
   int32_t* d_status = nullptr;  // [kMaxHeads]
   int32_t* d_iters = nullptr;   // [kMaxHeads]
   uint32_t* d_err = nullptr;
@@ -359,17 +370,23 @@ lc_status run_pass2(const Ctx& c, const void* qop, const void* kop) {
     LC_PROF(c, "clear_scores", 0);
     LC_CUDA(cudaMemsetAsync(c.ws + p.ucode, 0, static_cast<size_t>(p.H) * p.T * 4, c.st));
   }
+  const int nqt = p.n_q_pad / 128;
+  // bf16 inputs: 256 keys and one CTA per SM; fp32 inputs: 128 keys, two per SM
+  const int kpc = p.bf16_in ? 256 : 128, occ = p.bf16_in ? 1 : 2;
+  int split = best_split(((p.T + kpc - 1) / kpc) * p.H, c.h->sm_count, occ, p.ks_max);
+  const int tiles = (nqt + split - 1) / split;
+  split = (nqt + tiles - 1) / tiles;
   KeyScoreParams k{};
   k.n_q_pad = p.n_q_pad;
   k.T = p.T;
-  k.tiles_per_split = p.ks_tiles;
+  k.tiles_per_split = tiles;
   k.scale = p.scale;
   k.lse_pad = c.at<float>(p.lse_pad);
   k.u_code = c.at<uint32_t>(p.ucode);
   k.err = c.h->d_err;
   {
     LC_PROF(c, "key_scores", 1);
-    LC_CUDA(launch_key_scores(p.mode, mK, mQ, k, p.H, p.ks_split, c.st));
+    LC_CUDA(launch_key_scores(p.mode, mK, mQ, k, p.H, split, c.st));
   }
   return LC_OK;
 }
@@ -397,12 +414,22 @@ lc_status run_fit(const Ctx& c, const void* qop, const void* kop, const void* V,
                              c.at<float>(p.rowb), p.H, p.n_q, p.n_q_pad, c.st));
     LC_CUDA(launch_fill_colb2(c.at<float>(p.colb2), p.H, p.t, p.t_pad, c.st));
   }
+  const int slabs = p.n_q_pad / 64;
+  const int npairs = p.nblk * (p.nblk + 1) / 2;
+  auto split_of = [&](int units, int cap, int* per) {
+    int sp = best_split(units, c.h->sm_count, 1, cap);
+    *per = (slabs + sp - 1) / sp;
+    return (slabs + *per - 1) / *per;
+  };
+  int g5_slabs = 0, g7_slabs = 0;
+  const int g5_split = split_of(npairs * p.H, p.g5_max, &g5_slabs);
+  const int g7_split = split_of((npairs + p.nblk) * p.H, p.g7_max, &g7_slabs);
   GramParams g{};
   g.n_q_pad = p.n_q_pad;
   g.n_q = p.n_q;
   g.t_pad = p.t_pad;
   g.nblk = p.nblk;
-  g.slabs_per_split = p.g5_slabs;
+  g.slabs_per_split = g5_slabs;
   g.scale_log2 = p.scale * kLog2e;
   g.rowsh2 = c.at<float>(p.rowsh2);
   g.row_b = c.at<float>(p.rowb);
@@ -414,13 +441,13 @@ lc_status run_fit(const Ctx& c, const void* qop, const void* kop, const void* V,
   g.err = c.h->d_err;
   {
     LC_PROF(c, "gram_mass", 1);
-    LC_CUDA(launch_gram(p.mode, false, mKc, mQ64, mOhi, mOlo, g, p.H, p.g5_split, c.st));
+    LC_CUDA(launch_gram(p.mode, false, mKc, mQ64, mOhi, mOlo, g, p.H, g5_split, c.st));
   }
   const size_t tt = static_cast<size_t>(p.t_pad) * p.t_pad;
   {
     LC_PROF(c, "reduce_mass", 3);
-    LC_CUDA(launch_reduce_partials(c.at<float>(p.gpart), c.at<float>(p.G), p.g5_split, H * tt, c.st));
-    LC_CUDA(launch_reduce_partials(c.at<float>(p.cpart), c.at<float>(p.c), p.g5_split, H * p.t_pad,
+    LC_CUDA(launch_reduce_partials(c.at<float>(p.gpart), c.at<float>(p.G), g5_split, H * tt, c.st));
+    LC_CUDA(launch_reduce_partials(c.at<float>(p.cpart), c.at<float>(p.c), g5_split, H * p.t_pad,
                                    c.st));
     LC_CUDA(launch_symmetrize(c.at<float>(p.G), p.H, p.t_pad, c.st));
   }
@@ -460,7 +487,7 @@ lc_status run_fit(const Ctx& c, const void* qop, const void* kop, const void* V,
     LC_PROF(c, "compact_lse", 1);
     LC_CUDA(launch_compact_lse(p.mode, mQ128, mKc, cl, p.H, c.st));
   }
-  g.slabs_per_split = p.g7_slabs;
+  g.slabs_per_split = g7_slabs;
   g.rowsh2 = c.at<float>(p.lc2);
   g.row_b = nullptr;
   g.Gpart = c.at<float>(p.hpart);
@@ -468,12 +495,12 @@ lc_status run_fit(const Ctx& c, const void* qop, const void* kop, const void* V,
   g.Rpart = c.at<float>(p.rpart);
   {
     LC_PROF(c, "gram_out", 1);
-    LC_CUDA(launch_gram(p.mode, true, mKc, mQ64, mOhi, mOlo, g, p.H, p.g7_split, c.st));
+    LC_CUDA(launch_gram(p.mode, true, mKc, mQ64, mOhi, mOlo, g, p.H, g7_split, c.st));
   }
   {
     LC_PROF(c, "reduce_out", 4);
-    LC_CUDA(launch_reduce_partials(c.at<float>(p.hpart), c.at<float>(p.Hm), p.g7_split, H * tt, c.st));
-    LC_CUDA(launch_reduce_partials(c.at<float>(p.rpart), c.at<float>(p.R), p.g7_split,
+    LC_CUDA(launch_reduce_partials(c.at<float>(p.hpart), c.at<float>(p.Hm), g7_split, H * tt, c.st));
+    LC_CUDA(launch_reduce_partials(c.at<float>(p.rpart), c.at<float>(p.R), g7_split,
                                    H * p.t_pad * p.d, c.st));
     LC_CUDA(launch_symmetrize(c.at<float>(p.Hm), p.H, p.t_pad, c.st));
     LC_CUDA(launch_gather_v(V, p.bf16_in ? 0 : 1, idx, c.at<float>(p.vc), p.H, p.T, p.t, p.t_pad,
@@ -525,6 +552,8 @@ lc_status lc_create(lc_handle* out, int device) {
   if (!get_encode()) return LC_ERR_CUDA;
   lc_context* h = new lc_context();
   h->device = device;
+  cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, device);
+  if (h->sm_count < 1) h->sm_count = 148;
   if (cudaSetDevice(device) != cudaSuccess ||
       cudaMalloc(&h->d_status, sizeof(int32_t) * kMaxHeads) != cudaSuccess ||
       cudaMalloc(&h->d_iters, sizeof(int32_t) * kMaxHeads) != cudaSuccess ||

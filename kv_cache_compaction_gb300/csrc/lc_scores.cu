@@ -140,18 +140,15 @@ __global__ void __launch_bounds__(192, 2)
       tc_fence_after();
       const float2* lt = reinterpret_cast<const float2*>(sL + s * kBQ);
       const float2 sc2 = make_float2(p.scale, p.scale);
+      float v[kBQ];
+      tmem_ld128(tbase + lane_off + s * kBQ, v);
 #pragma unroll
-      for (int c = 0; c < kBQ / 32; ++c) {
-        float v[32];
-        tmem_ld32(tbase + lane_off + s * kBQ + c * 32, v);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float2 l2 = lt[c * 16 + e];
-          const float2 a = __ffma2_rn(make_float2(v[2 * e], v[2 * e + 1]), sc2,
-                                      make_float2(-l2.x, -l2.y));
-          u8[(2 * e) & 7] = fmaxf(u8[(2 * e) & 7], a.x);
-          u8[(2 * e + 1) & 7] = fmaxf(u8[(2 * e + 1) & 7], a.y);
-        }
+      for (int e = 0; e < kBQ / 2; ++e) {
+        const float2 l2 = lt[e];
+        const float2 a = __ffma2_rn(make_float2(v[2 * e], v[2 * e + 1]), sc2,
+                                    make_float2(-l2.x, -l2.y));
+        u8[(2 * e) & 7] = fmaxf(u8[(2 * e) & 7], a.x);
+        u8[(2 * e + 1) & 7] = fmaxf(u8[(2 * e + 1) & 7], a.y);
       }
       tc_fence_before();
       mbar_arrive(&d_free[s]);
@@ -164,6 +161,171 @@ __global__ void __launch_bounds__(192, 2)
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tbase, 256);
+}
+
+// Two-tile variant for bf16 inputs: one CTA holds 256 keys as key tiles A
+// and B that share every streamed query tile (halving the L2 traffic of
+// re-streamed queries), with one reduction warpgroup per key tile.  Warps:
+// 0 TMA, 1 MMA issue, 2..5 keys of tile A, 6..9 keys of tile B.  Tensor
+// memory: D_A and D_B double-buffered, 128 columns each.
+template <int D>
+struct KS2Layout {
+  static constexpr int NC = D / 64;
+  static constexpr int K_BYTES = kBK * D * 2;    // one key tile
+  static constexpr int QCHUNK = kBQ * 128;
+  static constexpr int Q_BYTES = NC * QCHUNK;
+  static constexpr int NST = 3;
+  static constexpr int OFF_Q = 2 * K_BYTES;
+  static constexpr int OFF_L = OFF_Q + NST * Q_BYTES;
+  static constexpr int OFF_BAR = OFF_L + NST * kBQ * 4;
+  static constexpr int SMEM = 1024 + OFF_BAR + 128;
+};
+
+template <int D>
+__global__ void __launch_bounds__(320, 1)
+    key_scores2_kernel(const __grid_constant__ CUtensorMap mK,
+                       const __grid_constant__ CUtensorMap mQ, const KeyScoreParams p) {
+  using L = KS2Layout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = align1024(smem_raw);
+  uint8_t* sK = base;
+  uint8_t* sQ = base + L::OFF_Q;
+  float* sL = reinterpret_cast<float*>(base + L::OFF_L);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + L::OFF_BAR);
+  uint64_t* k_full = bars + 0;
+  uint64_t* q_full = bars + 1;   // [3]
+  uint64_t* q_empty = bars + 4;  // [3]
+  uint64_t* d_full = bars + 7;   // [2]
+  uint64_t* d_free = bars + 9;   // [2]
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 11);
+  __shared__ volatile int abort_flag;
+
+  const int warp = warp_id(), lane = lane_id();
+  const int k0 = blockIdx.x * (2 * kBK), h = blockIdx.y;
+  const int nqt = p.n_q_pad / kBQ;
+  const int t0i = blockIdx.z * p.tiles_per_split;
+  const int ntile = max(0, min(nqt, t0i + p.tiles_per_split) - t0i);
+
+  if (threadIdx.x == 0) {
+    abort_flag = launch_aborted(p.err) ? 1 : 0;
+    mbar_init(k_full, 1);
+    for (int i = 0; i < L::NST; ++i) {
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 1 + 256);  // MMA commit + every reduction thread
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&d_full[b], 1);
+      mbar_init(&d_free[b], 256);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(tslot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tslot;  // D_A(b) at 128b, D_B(b) at 256 + 128b
+
+  if (warp == 0) {
+    if (lane == 0 && ntile > 0) {
+      mbar_arrive_expect_tx(k_full, 2 * L::K_BYTES);
+      for (int x = 0; x < 2; ++x)
+        for (int c = 0; c < L::NC; ++c)
+          tma_load_3d(sK + x * L::K_BYTES + c * kBK * 128, &mK, k_full, 64 * c, k0 + x * kBK, h);
+      int issued = 0;
+      for (int i = 0; i < ntile; ++i) {
+        const int s = i % L::NST;
+        if (i >= L::NST && !wait_bar(&q_empty[s], ((i / L::NST) - 1) & 1, &abort_flag, p.err))
+          break;
+        const int q0 = (t0i + i) * kBQ;
+        mbar_arrive_expect_tx(&q_full[s], L::Q_BYTES + kBQ * 4);
+        for (int c = 0; c < L::NC; ++c)
+          tma_load_3d(sQ + s * L::Q_BYTES + c * L::QCHUNK, &mQ, &q_full[s], 64 * c, q0, h);
+        bulk_g2s(sL + s * kBQ, p.lse_pad + static_cast<size_t>(h) * p.n_q_pad + q0, kBQ * 4,
+                 &q_full[s]);
+        issued = i + 1;
+      }
+      if (abort_flag) {
+        for (int i = (issued > L::NST ? issued - L::NST : 0); i < issued; ++i) {
+          const uint64_t tt = globaltimer_ns();
+          while (!mbar_try_wait(&q_full[i % L::NST], (i / L::NST) & 1) &&
+                 globaltimer_ns() - tt < kWaitLimitNs) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && ntile > 0) {
+      constexpr uint32_t idesc = idesc_f16(kBK, kBQ, true, false, false);
+      bool ok = wait_bar(k_full, 0, &abort_flag, p.err);
+      for (int i = 0; ok && i < ntile; ++i) {
+        const int s = i % L::NST, b = i & 1;
+        if (!wait_bar(&q_full[s], (i / L::NST) & 1, &abort_flag, p.err)) break;
+        if (i >= 2 && !wait_bar(&d_free[b], ((i >> 1) - 1) & 1, &abort_flag, p.err)) break;
+        tc_fence_after();
+        const uint32_t aQ = smem_u32(sQ + s * L::Q_BYTES);
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          const uint32_t aK = smem_u32(sK + x * L::K_BYTES);
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k) {
+            const uint64_t da = sdesc_sw128(aK + (k >> 2) * (kBK * 128) + (k & 3) * 32, 16, 1024);
+            const uint64_t db = sdesc_sw128(aQ + (k >> 2) * L::QCHUNK + (k & 3) * 32, 16, 1024);
+            umma_f16_ss(tbase + x * 256 + b * kBQ, da, db, idesc, k > 0 ? 1u : 0u);
+          }
+        }
+        umma_commit(&d_full[b]);
+        umma_commit(&q_empty[s]);
+      }
+    }
+  } else {
+    const int x = (warp - 2) >> 2;
+    const int wq = warp & 3;
+    const int key = k0 + x * kBK + wq * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    float u8[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) u8[e] = -kInf;
+    const float2 sc2 = make_float2(p.scale, p.scale);
+    bool ok = ntile > 0;
+    for (int i = 0; ok && i < ntile; ++i) {
+      const int s = i % L::NST, b = i & 1;
+      if (!wait_bar(&d_full[b], (i >> 1) & 1, &abort_flag, p.err)) { ok = false; break; }
+      if (!wait_bar(&q_full[s], (i / L::NST) & 1, &abort_flag, p.err)) { ok = false; break; }
+      tc_fence_after();
+      const float2* lt = reinterpret_cast<const float2*>(sL + s * kBQ);
+      float v[kBQ];
+      tmem_ld128(tbase + x * 256 + b * kBQ + lane_off, v);
+      tc_fence_before();
+      mbar_arrive(&d_free[b]);
+#pragma unroll
+      for (int e = 0; e < kBQ / 2; ++e) {
+        const float2 l2 = lt[e];
+        const float2 a = __ffma2_rn(make_float2(v[2 * e], v[2 * e + 1]), sc2,
+                                    make_float2(-l2.x, -l2.y));
+        u8[(2 * e) & 7] = fmaxf(u8[(2 * e) & 7], a.x);
+        u8[(2 * e + 1) & 7] = fmaxf(u8[(2 * e + 1) & 7], a.y);
+      }
+      mbar_arrive(&q_empty[s]);
+    }
+    const float u = fmaxf(fmaxf(fmaxf(u8[0], u8[1]), fmaxf(u8[2], u8[3])),
+                          fmaxf(fmaxf(u8[4], u8[5]), fmaxf(u8[6], u8[7])));
+    if (ok && key < p.T) atomicMax(p.u_code + static_cast<size_t>(h) * p.T + key, order_code(u));
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tbase, 512);
+}
+
+template <int D>
+cudaError_t launch_ks2_t(const CUtensorMap& mK, const CUtensorMap& mQ, const KeyScoreParams& p,
+                         int H, int nsplit, cudaStream_t st) {
+  using L = KS2Layout<D>;
+  auto kern = key_scores2_kernel<D>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
+  if (e != cudaSuccess) return e;
+  dim3 grid((p.T + 2 * kBK - 1) / (2 * kBK), H, nsplit);
+  kern<<<grid, 320, L::SMEM, st>>>(mK, mQ, p);
+  return cudaGetLastError();
 }
 
 template <bool QK_BF16, int D_QK>
@@ -423,8 +585,8 @@ inline int grid_for(size_t n, int block = 256) {
 cudaError_t launch_key_scores(OperandMode mode, const CUtensorMap& mK, const CUtensorMap& mQ,
                               const KeyScoreParams& p, int H, int nsplit, cudaStream_t st) {
   switch (mode) {
-    case kBF16d128: return launch_ks_t<true, 128>(mK, mQ, p, H, nsplit, st);
-    case kBF16d64: return launch_ks_t<true, 64>(mK, mQ, p, H, nsplit, st);
+    case kBF16d128: return launch_ks2_t<128>(mK, mQ, p, H, nsplit, st);
+    case kBF16d64: return launch_ks2_t<64>(mK, mQ, p, H, nsplit, st);
     case kSplitF16d64: return launch_ks_t<false, 192>(mK, mQ, p, H, nsplit, st);
   }
   return cudaErrorInvalidValue;
@@ -432,8 +594,8 @@ cudaError_t launch_key_scores(OperandMode mode, const CUtensorMap& mK, const CUt
 
 int key_scores_smem(OperandMode mode) {
   switch (mode) {
-    case kBF16d128: return KSLayout<128>::SMEM;
-    case kBF16d64: return KSLayout<64>::SMEM;
+    case kBF16d128: return KS2Layout<128>::SMEM;
+    case kBF16d64: return KS2Layout<64>::SMEM;
     case kSplitF16d64: return KSLayout<192>::SMEM;
   }
   return 0;
