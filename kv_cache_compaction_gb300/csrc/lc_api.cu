@@ -332,7 +332,9 @@ lc_status run_pass1(const Ctx& c, const void* qop, const void* kop, float* rowma
                     float* O, bool to_ws) {
   const Plan& p = c.p;
   const bool qk_bf16 = p.bf16_in;
-  const int bn = p.mode == kSplitF16d64 ? 64 : 128;
+  // below 2x compression the output fit amplifies P's rounding: split P.V
+  const bool split_p = 2 * p.t > p.T;
+  const int bn = (p.mode == kSplitF16d64) ? 64 : 128;
   CUtensorMap mQ, mK, mV, mVlo;
   if (!make_map(&mQ, qop, qk_bf16, p.d_qk, p.n_q, p.H, 128)) return LC_ERR_CUDA;
   if (!make_map(&mK, kop, qk_bf16, p.d_qk, p.T, p.H, bn)) return LC_ERR_CUDA;
@@ -356,7 +358,7 @@ lc_status run_pass1(const Ctx& c, const void* qop, const void* kop, float* rowma
   a.err = c.h->d_err;
   {
     LC_PROF(c, "attn_stats", 1);
-    LC_CUDA(launch_attn_stats(p.mode, mQ, mK, mV, mVlo, a, p.H, c.st));
+    LC_CUDA(launch_attn_stats(p.mode, split_p, mQ, mK, mV, mVlo, a, p.H, c.st));
   }
   return LC_OK;
 }

@@ -21,7 +21,7 @@ namespace {
 
 constexpr int kBM = 128;
 
-template <int D_QK, int D_V, int V_TERMS, int BN>
+template <int D_QK, int D_V, int V_TERMS, int BN, int P_TERMS>
 struct AttnLayout {
   static constexpr int NQC = D_QK / 64;
   static constexpr int NVC = D_V / 64;
@@ -36,16 +36,16 @@ struct AttnLayout {
   static constexpr int OFF_STAGE = Q_BYTES;
   static constexpr int OFF_PHI = OFF_STAGE + NST * STAGE;
   static constexpr int OFF_PLO = OFF_PHI + P_BYTES;
-  static constexpr int OFF_BAR = OFF_PLO + (V_TERMS == 2 ? P_BYTES : 0);
+  static constexpr int OFF_BAR = OFF_PLO + (P_TERMS == 2 ? P_BYTES : 0);
   static constexpr int SMEM = 1024 + OFF_BAR + 256;
 };
 
-template <bool QK_BF16, int D_QK, int D_V, int V_TERMS, int BN>
+template <bool QK_BF16, int D_QK, int D_V, int V_TERMS, int BN, int P_TERMS>
 __global__ void __launch_bounds__(192, 1)
     attn_stats_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                       const __grid_constant__ CUtensorMap mV,
                       const __grid_constant__ CUtensorMap mVlo, const AttnStatsParams p) {
-  using L = AttnLayout<D_QK, D_V, V_TERMS, BN>;
+  using L = AttnLayout<D_QK, D_V, V_TERMS, BN, P_TERMS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = align1024(smem_raw);
   uint8_t* sQ = base;
@@ -162,9 +162,9 @@ __global__ void __launch_bounds__(192, 1)
           const uint64_t dpl = sdesc_sw128(aPl + poff, 16, 1024);
           const uint64_t dv = sdesc_sw128(aV + k * 2048, L::KCHUNK, 1024);
           umma_f16_ss(tO, dph, dv, idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
+          if (P_TERMS == 2) umma_f16_ss(tO, dpl, dv, idesc_pv, 1u);
           if (V_TERMS == 2) {
             const uint64_t dvl = sdesc_sw128(aV + L::V_BYTES + k * 2048, L::KCHUNK, 1024);
-            umma_f16_ss(tO, dpl, dv, idesc_pv, 1u);
             umma_f16_ss(tO, dph, dvl, idesc_pv, 1u);
           }
         }
@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(192, 1)
           l4[e] = __fadd2_rn(l4[e], make_float2(pv[2 * e], pv[2 * e + 1]));
         }
         const uint32_t off = (c8 >> 3) * L::PCHUNK + sw128_offset(row, (c8 & 7) * 8);
-        if (V_TERMS == 2) {
+        if (P_TERMS == 2) {
           uint4 hi, lo;
           split8(pv, hi, lo);
           *reinterpret_cast<uint4*>(sPhi + off) = hi;
@@ -749,12 +749,12 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 1) tmem_dealloc(tbase, 256);
 }
 
-template <bool QK_BF16, int D_QK, int D_V, int V_TERMS, int BN>
+template <bool QK_BF16, int D_QK, int D_V, int V_TERMS, int BN, int P_TERMS>
 cudaError_t launch_attn_t(const CUtensorMap& mQ, const CUtensorMap& mK, const CUtensorMap& mV,
                           const CUtensorMap& mVlo, const AttnStatsParams& p, int H,
                           cudaStream_t st) {
-  using L = AttnLayout<D_QK, D_V, V_TERMS, BN>;
-  auto kern = attn_stats_kernel<QK_BF16, D_QK, D_V, V_TERMS, BN>;
+  using L = AttnLayout<D_QK, D_V, V_TERMS, BN, P_TERMS>;
+  auto kern = attn_stats_kernel<QK_BF16, D_QK, D_V, V_TERMS, BN, P_TERMS>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid((p.n_q + kBM - 1) / kBM, H);
@@ -788,22 +788,27 @@ cudaError_t launch_cl_t(const CUtensorMap& mQ, const CUtensorMap& mKc, const Com
 
 }  // namespace
 
-cudaError_t launch_attn_stats(OperandMode mode, const CUtensorMap& mQ, const CUtensorMap& mK,
-                              const CUtensorMap& mV, const CUtensorMap& mVlo,
-                              const AttnStatsParams& p, int H, cudaStream_t st) {
+cudaError_t launch_attn_stats(OperandMode mode, bool split_p, const CUtensorMap& mQ,
+                              const CUtensorMap& mK, const CUtensorMap& mV,
+                              const CUtensorMap& mVlo, const AttnStatsParams& p, int H,
+                              cudaStream_t st) {
   switch (mode) {
-    case kBF16d128: return launch_attn2_t<128>(mQ, mK, mV, p, H, st);
-    case kBF16d64: return launch_attn2_t<64>(mQ, mK, mV, p, H, st);
-    case kSplitF16d64: return launch_attn_t<false, 192, 64, 2, 64>(mQ, mK, mV, mVlo, p, H, st);
+    case kBF16d128:
+      return split_p ? launch_attn_t<true, 128, 128, 1, 128, 2>(mQ, mK, mV, mVlo, p, H, st)
+                     : launch_attn2_t<128>(mQ, mK, mV, p, H, st);
+    case kBF16d64:
+      return split_p ? launch_attn_t<true, 64, 64, 1, 128, 2>(mQ, mK, mV, mVlo, p, H, st)
+                     : launch_attn2_t<64>(mQ, mK, mV, p, H, st);
+    case kSplitF16d64: return launch_attn_t<false, 192, 64, 2, 64, 2>(mQ, mK, mV, mVlo, p, H, st);
   }
   return cudaErrorInvalidValue;
 }
 
 int attn_stats_smem(OperandMode mode) {
   switch (mode) {
-    case kBF16d128: return Attn2Layout<128>::SMEM;
+    case kBF16d128: return AttnLayout<128, 128, 1, 128, 2>::SMEM;
     case kBF16d64: return Attn2Layout<64>::SMEM;
-    case kSplitF16d64: return AttnLayout<192, 64, 2, 64>::SMEM;
+    case kSplitF16d64: return AttnLayout<192, 64, 2, 64, 2>::SMEM;
   }
   return 0;
 }

@@ -12,7 +12,8 @@ namespace lc {
 // Which operand encoding the tensor-core passes use.
 //  kBF16d128 / kBF16d64: Q, K bf16 with d_qk = d; V converted to fp16 (exact
 //      for bf16 values in the fp16 range) and P rounded to fp16: one P.V
-//      product (the rounding of P moves C_v by ~1e-5 relative).
+//      product (moves C_v by ~1e-5..1e-4 relative at 2x or more compression);
+//      below 2x compression P is split into fp16 hi + lo (two products).
 //  kSplitF16d64: fp32 inputs; Q = [Qhi|Qlo|Qhi], K = [Khi|Khi|Klo] as fp16
 //      (d_qk = 3d = 192) so S keeps fp32 accuracy; V = Vhi + Vlo.
 enum OperandMode { kBF16d128 = 0, kBF16d64 = 1, kSplitF16d64 = 2 };
@@ -71,9 +72,13 @@ struct CompactLseParams {
 };
 
 // Launchers (return cudaGetLastError()).
-cudaError_t launch_attn_stats(OperandMode mode, const CUtensorMap& mQ, const CUtensorMap& mK,
-                              const CUtensorMap& mV, const CUtensorMap& mVlo,
-                              const AttnStatsParams& p, int H, cudaStream_t st);
+// split_p: P.V as fp16 hi + lo products (bf16 inputs; fp32 inputs always
+// split).  Needed when more than half of the keys are kept: the output fit
+// is then close to an interpolation and amplifies P's fp16 rounding.
+cudaError_t launch_attn_stats(OperandMode mode, bool split_p, const CUtensorMap& mQ,
+                              const CUtensorMap& mK, const CUtensorMap& mV,
+                              const CUtensorMap& mVlo, const AttnStatsParams& p, int H,
+                              cudaStream_t st);
 cudaError_t launch_key_scores(OperandMode mode, const CUtensorMap& mK, const CUtensorMap& mQ,
                               const KeyScoreParams& p, int H, int nsplit, cudaStream_t st);
 cudaError_t launch_gram(OperandMode mode, bool with_r, const CUtensorMap& mKc,
