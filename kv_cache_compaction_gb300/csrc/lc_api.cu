@@ -68,7 +68,7 @@ struct Plan {
   size_t kc, rowsh2, rowb, colb2, lc2;  // fit inputs
   size_t gpart, cpart, G, c;            // mass system
   size_t hpart, rpart, Hm, R, vc;       // output system
-  size_t mat, vec;                      // solver scratch
+  size_t mat, vec, wbuf;                // solver scratch
   size_t w_tmp, beta_tmp;               // steps 4 results when the caller gives none
   size_t total;
 };
@@ -182,6 +182,7 @@ Plan make_plan(const lc_shape* s) {
   p.vc = take(H * p.t_pad * p.d * 4);
   p.mat = take(H * tt * 4);
   p.vec = take(H * 8 * p.t_pad * 4);
+  p.wbuf = take(H * p.t_pad * 64 * 4);
   p.w_tmp = take(H * p.t * 4);
   p.beta_tmp = take(H * p.t * 4);
   p.total = off;
@@ -466,6 +467,7 @@ lc_status run_fit(const Ctx& c, const void* qop, const void* kop, const void* V,
   sp.colb2 = c.at<float>(p.colb2);
   sp.mat = c.at<float>(p.mat);
   sp.vec = c.at<float>(p.vec);
+  sp.wbuf = c.at<float>(p.wbuf);
   sp.head_status = c.h->d_status;
   sp.head_iters = c.h->d_iters;
   sp.err = c.h->d_err;

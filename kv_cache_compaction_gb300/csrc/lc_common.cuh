@@ -39,15 +39,28 @@ __device__ __forceinline__ uint32_t pack_h2(__half a, __half b) {
          (static_cast<uint32_t>(__half_as_ushort(b)) << 16);
 }
 
-// Split 8 floats into two uint4 of packed fp16 (hi parts, lo parts).
+__device__ __forceinline__ uint32_t f2_to_h2(float a, float b);
+
+// Split 8 floats into two uint4 of packed fp16 (hi parts, lo parts), for
+// values in the fp16 range.  hi is x rounded to 11 significant bits by
+// Veltkamp's splitting (T. J. Dekker, "A floating-point technique for
+// extending the available precision", Numer. Math. 18, 1971): with
+// t = (2^13 + 1) x, hi = t - (t - x) keeps the leading 11 bits of x, so it is
+// exact in fp16 and lo = x - hi is exact in fp32.  Only the packed fp16
+// conversions remain, one per element.  The explicitly rounded operations
+// keep the compiler from contracting the three steps into fused ones.
 __device__ __forceinline__ void split8(const float* x, uint4& hi, uint4& lo) {
-  __half h[8], l[8];
+  float h[8], l[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) split_f16(x[i], h[i], l[i]);
-  hi = make_uint4(pack_h2(h[0], h[1]), pack_h2(h[2], h[3]), pack_h2(h[4], h[5]),
-                  pack_h2(h[6], h[7]));
-  lo = make_uint4(pack_h2(l[0], l[1]), pack_h2(l[2], l[3]), pack_h2(l[4], l[5]),
-                  pack_h2(l[6], l[7]));
+  for (int i = 0; i < 8; ++i) {
+    const float t = __fmul_rn(x[i], 8193.f);
+    h[i] = __fsub_rn(t, __fsub_rn(t, x[i]));
+    l[i] = __fsub_rn(x[i], h[i]);
+  }
+  hi = make_uint4(f2_to_h2(h[0], h[1]), f2_to_h2(h[2], h[3]), f2_to_h2(h[4], h[5]),
+                  f2_to_h2(h[6], h[7]));
+  lo = make_uint4(f2_to_h2(l[0], l[1]), f2_to_h2(l[2], l[3]), f2_to_h2(l[4], l[5]),
+                  f2_to_h2(l[6], l[7]));
 }
 
 __device__ __forceinline__ uint32_t f2_to_h2(float a, float b) {

@@ -323,6 +323,327 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 1) tmem_dealloc(tbase, 512);
 }
 
+// Two-group variant for bf16 inputs (d = 64 or 128): query slabs alternate
+// between two epilogue warpgroups with their own E buffer and score buffer,
+// so the Gram products of one slab run on the tensor core while the other
+// group forms the next slab's E.  Warps: 0 TMA, 1 MMA issue, 2..5 group 0
+// (even slabs), 6..9 group 1 (odd slabs).  A ring stage is refilled once its
+// row shifts are read and -- for pair CTAs -- its scores are formed, or -- for
+// R CTAs -- the product with its O slab is done.  Tensor memory: S[2] (two blocks of
+// 64 columns each) at 0 and 128, accumulator at 256.  Shared memory (pair /
+// R CTAs): C_k blocks, a 2-stage ring of query (and O) slabs, E[2].
+template <int D>
+struct Gram2Layout {
+  static constexpr int NC = D / 64;
+  static constexpr int KC_BYTES = 128 * D * 2;
+  static constexpr int QCHUNK = kSL * 128;
+  static constexpr int Q_BYTES = NC * QCHUNK;
+  static constexpr int O_BYTES = 2 * NC * QCHUNK;   // hi + lo (R CTAs only)
+  static constexpr int E_BLK = 128 * 128;           // one block's E (hi or lo)
+  // pair CTAs: Kc_i, Kc_j | ring 2 x Q | E[2] = 4 blocks each
+  static constexpr int P_OFF_RING = 2 * KC_BYTES;
+  static constexpr int P_STAGE = Q_BYTES;
+  static constexpr int P_OFF_E = P_OFF_RING + 2 * P_STAGE;
+  static constexpr int P_END = P_OFF_E + 2 * 4 * E_BLK;
+  // R CTAs: Kc_i | ring 2 x (Q + O) | E[2] = 2 blocks each
+  static constexpr int R_OFF_RING = KC_BYTES;
+  static constexpr int R_STAGE = Q_BYTES + O_BYTES;
+  static constexpr int R_OFF_E = R_OFF_RING + 2 * R_STAGE;
+  static constexpr int R_END = R_OFF_E + 2 * 2 * E_BLK;
+  static constexpr int OFF_ROWS = (P_END > R_END ? P_END : R_END);
+  static constexpr int ROW_STAGE = 2 * kSL * 4;
+  static constexpr int OFF_BAR = OFF_ROWS + 2 * ROW_STAGE;
+  static constexpr int OFF_CX = OFF_BAR + 256;      // group-1 partial c
+  static constexpr int SMEM = 1024 + OFF_CX + 128 * 4;
+};
+
+template <int D>
+__global__ void __launch_bounds__(320, 1)
+    gram2_kernel(const __grid_constant__ CUtensorMap mKc, const __grid_constant__ CUtensorMap mQ,
+                 const __grid_constant__ CUtensorMap mOhi, const __grid_constant__ CUtensorMap mOlo,
+                 const GramParams p) {
+  using L = Gram2Layout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = align1024(smem_raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + L::OFF_BAR);
+  uint64_t* k_full = bars + 0;
+  uint64_t* st_full = bars + 1;   // [2]
+  uint64_t* st_empty = bars + 3;  // [2]
+  uint64_t* s_full = bars + 5;    // [2] per group
+  uint64_t* s_free = bars + 7;    // [2]
+  uint64_t* e_full = bars + 9;    // [2]
+  uint64_t* e_free = bars + 11;   // [2]
+  uint64_t* done = bars + 13;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 14);
+  float* cx = reinterpret_cast<float*>(base + L::OFF_CX);
+  __shared__ volatile int abort_flag;
+
+  const int warp = warp_id(), lane = lane_id();
+  const int h = blockIdx.y, z = blockIdx.z;
+  const int npairs = p.nblk * (p.nblk + 1) / 2;
+  const bool is_r = static_cast<int>(blockIdx.x) >= npairs;
+  int bi = 0, bj = 0;
+  if (!is_r) {
+    int rem = blockIdx.x;
+    while (rem >= p.nblk - bi) {
+      rem -= p.nblk - bi;
+      ++bi;
+    }
+    bj = bi + rem;
+  } else {
+    bi = bj = blockIdx.x - npairs;
+  }
+  const bool two = !is_r && bi != bj;
+  const bool with_c = !is_r && bi == bj && p.row_b != nullptr;
+  const int total_slabs = p.n_q_pad / kSL;
+  const int s0 = z * p.slabs_per_split;
+  const int nsl = max(0, min(total_slabs, s0 + p.slabs_per_split) - s0);
+
+  uint8_t* sKi = base;
+  uint8_t* sKj = base + L::KC_BYTES;
+  uint8_t* sRing = base + (is_r ? L::R_OFF_RING : L::P_OFF_RING);
+  const int stage_bytes = is_r ? L::R_STAGE : L::P_STAGE;
+  uint8_t* sE = base + (is_r ? L::R_OFF_E : L::P_OFF_E);
+  const int e_buf = (is_r ? 2 : 4) * L::E_BLK;  // one group's E buffer
+  uint8_t* sRows = base + L::OFF_ROWS;
+
+  if (threadIdx.x == 0) {
+    abort_flag = launch_aborted(p.err) ? 1 : 0;
+    mbar_init(k_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&st_full[i], 1);
+      mbar_init(&st_empty[i], 1 + 128);
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], 128);
+      mbar_init(&e_full[i], 128);
+      mbar_init(&e_free[i], 1);
+    }
+    mbar_init(done, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(tslot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tslot;
+  const uint32_t tAcc = tbase + 256;
+
+  if (warp == 0) {
+    if (lane == 0 && nsl > 0) {
+      mbar_arrive_expect_tx(k_full, (two ? 2 : 1) * L::KC_BYTES);
+      for (int c = 0; c < L::NC; ++c) {
+        tma_load_3d(sKi + c * 128 * 128, &mKc, k_full, 64 * c, bi * 128, h);
+        if (two) tma_load_3d(sKj + c * 128 * 128, &mKc, k_full, 64 * c, bj * 128, h);
+      }
+      const uint32_t bytes = L::Q_BYTES + (is_r ? L::O_BYTES : 0) + kSL * 4 + (with_c ? kSL * 4 : 0);
+      int issued = 0;
+      for (int i = 0; i < nsl; ++i) {
+        const int s = i & 1;
+        if (i >= 2 && !wait_bar(&st_empty[s], ((i >> 1) - 1) & 1, &abort_flag, p.err)) break;
+        uint8_t* st = sRing + s * stage_bytes;
+        const int r0 = (s0 + i) * kSL;
+        mbar_arrive_expect_tx(&st_full[s], bytes);
+        for (int c = 0; c < L::NC; ++c)
+          tma_load_3d(st + c * L::QCHUNK, &mQ, &st_full[s], 64 * c, r0, h);
+        if (is_r) {
+          for (int c = 0; c < L::NC; ++c) {
+            tma_load_3d(st + L::Q_BYTES + c * L::QCHUNK, &mOhi, &st_full[s], 64 * c, r0, h);
+            tma_load_3d(st + L::Q_BYTES + (L::NC + c) * L::QCHUNK, &mOlo, &st_full[s], 64 * c,
+                        r0, h);
+          }
+        }
+        const size_t roff = static_cast<size_t>(h) * p.n_q_pad + r0;
+        uint8_t* rw = sRows + s * L::ROW_STAGE;
+        bulk_g2s(rw, p.rowsh2 + roff, kSL * 4, &st_full[s]);
+        if (with_c) bulk_g2s(rw + kSL * 4, p.row_b + roff, kSL * 4, &st_full[s]);
+        issued = i + 1;
+      }
+      if (abort_flag) {
+        for (int i = (issued > 2 ? issued - 2 : 0); i < issued; ++i) {
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(&st_full[i & 1], (i >> 1) & 1) &&
+                 globaltimer_ns() - t0 < kWaitLimitNs) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && nsl > 0) {
+      constexpr uint32_t idesc_s = idesc_f16(128, kSL, true, false, false);
+      constexpr uint32_t idesc_g = idesc_f16(128, 128, false, false, false);
+      constexpr uint32_t idesc_r = idesc_f16(128, D, false, false, true);
+      bool ok = wait_bar(k_full, 0, &abort_flag, p.err);
+      auto issue_s = [&](int i) -> bool {  // scores of slab i into S[i & 1]
+        const int s = i & 1;
+        if (!wait_bar(&st_full[s], (i >> 1) & 1, &abort_flag, p.err)) return false;
+        if (i >= 2 && !wait_bar(&s_free[s], ((i >> 1) - 1) & 1, &abort_flag, p.err)) return false;
+        tc_fence_after();
+        const uint32_t aQ = smem_u32(sRing + s * stage_bytes);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint64_t dq = sdesc_sw128(aQ + (k >> 2) * L::QCHUNK + (k & 3) * 32, 16, 1024);
+          const uint32_t koff = (k >> 2) * (128 * 128) + (k & 3) * 32;
+          umma_f16_ss(tbase + s * 128, sdesc_sw128(smem_u32(sKi) + koff, 16, 1024), dq, idesc_s,
+                      k > 0 ? 1u : 0u);
+          if (two)
+            umma_f16_ss(tbase + s * 128 + 64, sdesc_sw128(smem_u32(sKj) + koff, 16, 1024), dq,
+                        idesc_s, k > 0 ? 1u : 0u);
+        }
+        // a pair CTA is done with the query slab once its scores are formed
+        if (!is_r) umma_commit(&st_empty[s]);
+        umma_commit(&s_full[s]);
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      if (ok && nsl > 1) ok = issue_s(1);
+      for (int i = 0; ok && i < nsl; ++i) {
+        const int g = i & 1;
+        if (!wait_bar(&e_full[g], (i >> 1) & 1, &abort_flag, p.err)) break;
+        tc_fence_after();
+        const uint32_t eb = smem_u32(sE + g * e_buf);
+        const uint32_t eih = eb, eil = eb + L::E_BLK;
+        if (!is_r) {
+          const uint32_t ejh = two ? eb + 2 * L::E_BLK : eih;
+          const uint32_t ejl = two ? eb + 3 * L::E_BLK : eil;
+#pragma unroll
+          for (int k = 0; k < kSL / 16; ++k) {
+            const uint32_t o = k * 32;
+            const uint32_t acc0 = (i > 0 || k > 0) ? 1u : 0u;
+            umma_f16_ss(tAcc, sdesc_sw128(eih + o, 16, 1024), sdesc_sw128(ejh + o, 16, 1024),
+                        idesc_g, acc0);
+            umma_f16_ss(tAcc, sdesc_sw128(eih + o, 16, 1024), sdesc_sw128(ejl + o, 16, 1024),
+                        idesc_g, 1u);
+            umma_f16_ss(tAcc, sdesc_sw128(eil + o, 16, 1024), sdesc_sw128(ejh + o, 16, 1024),
+                        idesc_g, 1u);
+          }
+        } else {
+          const uint32_t aO = smem_u32(sRing + g * stage_bytes + L::Q_BYTES);
+          const uint32_t aOl = aO + L::NC * L::QCHUNK;
+#pragma unroll
+          for (int k = 0; k < kSL / 16; ++k) {
+            const uint32_t o = k * 32;
+            const uint32_t acc0 = (i > 0 || k > 0) ? 1u : 0u;
+            const uint64_t doh = sdesc_sw128(aO + k * 2048, L::QCHUNK, 1024);
+            const uint64_t dol = sdesc_sw128(aOl + k * 2048, L::QCHUNK, 1024);
+            umma_f16_ss(tAcc, sdesc_sw128(eih + o, 16, 1024), doh, idesc_r, acc0);
+            umma_f16_ss(tAcc, sdesc_sw128(eih + o, 16, 1024), dol, idesc_r, 1u);
+            umma_f16_ss(tAcc, sdesc_sw128(eil + o, 16, 1024), doh, idesc_r, 1u);
+          }
+        }
+        if (is_r) umma_commit(&st_empty[g]);  // the O slab feeds the product above
+        umma_commit(&e_free[g]);
+        if (i + 2 < nsl && !issue_s(i + 2)) break;
+      }
+      umma_commit(done);
+    }
+  } else {
+    // ---------------------------------------------------------- E rows
+    const int g = (warp - 2) >> 2;
+    const int wq = warp & 3;
+    const int j = wq * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const size_t cb_off = static_cast<size_t>(h) * p.t_pad;
+    const float cbi = p.colb2[cb_off + bi * 128 + j];
+    const float cbj = two ? p.colb2[cb_off + bj * 128 + j] : 0.f;
+    const float s2 = p.scale_log2;
+    uint8_t* eb = sE + g * e_buf;
+    uint8_t* sEih = eb;
+    uint8_t* sEil = eb + L::E_BLK;
+    uint8_t* sEjh = eb + 2 * L::E_BLK;
+    uint8_t* sEjl = eb + 3 * L::E_BLK;
+    float cacc = 0.f;
+    bool ok = nsl > 0;
+    for (int i = g; ok && i < nsl; i += 2) {
+      const int n = i >> 1;  // this group's n-th slab
+      if (!wait_bar(&s_full[g], n & 1, &abort_flag, p.err)) { ok = false; break; }
+      tc_fence_after();
+      float xi[kSL], xj[kSL];
+      tmem_ld64(tbase + g * 128 + lane_off, xi);
+      if (two) tmem_ld64(tbase + g * 128 + 64 + lane_off, xj);
+      tc_fence_before();
+      mbar_arrive(&s_free[g]);
+      if (n > 0 && !wait_bar(&e_free[g], (n - 1) & 1, &abort_flag, p.err)) { ok = false; break; }
+      if (!wait_bar(&st_full[g], n & 1, &abort_flag, p.err)) { ok = false; break; }
+      const float* rs = reinterpret_cast<const float*>(sRows + g * L::ROW_STAGE);
+      const float* rb = rs + kSL;
+#pragma unroll
+      for (int c8 = 0; c8 < kSL / 8; ++c8) {
+        float e8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float sh = rs[c8 * 8 + e];
+          e8[e] = ex2(fmaf(xi[c8 * 8 + e], s2, cbi) - sh);
+          if (with_c) cacc = fmaf(e8[e], rb[c8 * 8 + e], cacc);
+        }
+        uint4 hi, lo;
+        split8(e8, hi, lo);
+        const uint32_t off = sw128_offset(j, c8 * 8);
+        *reinterpret_cast<uint4*>(sEih + off) = hi;
+        *reinterpret_cast<uint4*>(sEil + off) = lo;
+        if (two) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) e8[e] = ex2(fmaf(xj[c8 * 8 + e], s2, cbj) - rs[c8 * 8 + e]);
+          split8(e8, hi, lo);
+          *reinterpret_cast<uint4*>(sEjh + off) = hi;
+          *reinterpret_cast<uint4*>(sEjl + off) = lo;
+        }
+      }
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(&e_full[g]);
+      mbar_arrive(&st_empty[g]);  // row shifts of this stage read
+    }
+    // combine the groups' partial c and publish the block accumulator
+    if (with_c && g == 1) cx[j] = cacc;
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    if (ok && g == 0 && nsl > 0 && wait_bar(done, 0, &abort_flag, p.err)) {
+      tc_fence_after();
+      const int H = gridDim.y;
+      const size_t zh = static_cast<size_t>(z) * H + h;
+      const int key = bi * 128 + j;
+      if (!is_r) {
+        float* dst = p.Gpart + (zh * p.t_pad + key) * p.t_pad + bj * 128;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float v[32];
+          tmem_ld32(tAcc + lane_off + c * 32, v);
+          float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) d4[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+        }
+        if (with_c) p.cpart[zh * p.t_pad + key] = cacc + (nsl > 1 ? cx[j] : 0.f);
+      } else {
+        float* dst = p.Rpart + (zh * p.t_pad + key) * p.d_v;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          float v[32];
+          tmem_ld32(tAcc + lane_off + c * 32, v);
+          float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) d4[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tbase, 512);
+}
+
+template <int D>
+cudaError_t launch_gram2_t(bool with_r, const CUtensorMap& mKc, const CUtensorMap& mQ,
+                           const CUtensorMap& mOhi, const CUtensorMap& mOlo, const GramParams& p,
+                           int H, int nsplit, cudaStream_t st) {
+  using L = Gram2Layout<D>;
+  auto kern = gram2_kernel<D>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
+  if (e != cudaSuccess) return e;
+  const int npairs = p.nblk * (p.nblk + 1) / 2;
+  dim3 grid(npairs + (with_r ? p.nblk : 0), H, nsplit);
+  kern<<<grid, 320, L::SMEM, st>>>(mKc, mQ, mOhi, mOlo, p);
+  return cudaGetLastError();
+}
+
 template <bool QK_BF16, int D_QK, int D_V, int NST>
 cudaError_t launch_gram_t(bool with_r, const CUtensorMap& mKc, const CUtensorMap& mQ,
                           const CUtensorMap& mOhi, const CUtensorMap& mOlo, const GramParams& p,
@@ -343,10 +664,8 @@ cudaError_t launch_gram(OperandMode mode, bool with_r, const CUtensorMap& mKc,
                         const CUtensorMap& mQ, const CUtensorMap& mOhi, const CUtensorMap& mOlo,
                         const GramParams& p, int H, int nsplit, cudaStream_t st) {
   switch (mode) {
-    case kBF16d128:
-      return launch_gram_t<true, 128, 128, 2>(with_r, mKc, mQ, mOhi, mOlo, p, H, nsplit, st);
-    case kBF16d64:
-      return launch_gram_t<true, 64, 64, 2>(with_r, mKc, mQ, mOhi, mOlo, p, H, nsplit, st);
+    case kBF16d128: return launch_gram2_t<128>(with_r, mKc, mQ, mOhi, mOlo, p, H, nsplit, st);
+    case kBF16d64: return launch_gram2_t<64>(with_r, mKc, mQ, mOhi, mOlo, p, H, nsplit, st);
     case kSplitF16d64:
       return launch_gram_t<false, 192, 64, 1>(with_r, mKc, mQ, mOhi, mOlo, p, H, nsplit, st);
   }
@@ -355,8 +674,8 @@ cudaError_t launch_gram(OperandMode mode, bool with_r, const CUtensorMap& mKc,
 
 int gram_smem(OperandMode mode) {
   switch (mode) {
-    case kBF16d128: return GramLayout<128, 128, 2>::SMEM;
-    case kBF16d64: return GramLayout<64, 64, 2>::SMEM;
+    case kBF16d128: return Gram2Layout<128>::SMEM;
+    case kBF16d64: return Gram2Layout<64>::SMEM;
     case kSplitF16d64: return GramLayout<192, 64, 1>::SMEM;
   }
   return 0;

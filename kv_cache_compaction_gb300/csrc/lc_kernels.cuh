@@ -128,6 +128,7 @@ struct SolveParams {
   float* colb2;            // [H][t_pad]: beta * log2(e), -inf for w = 0 and padding
   float* mat;              // [H][t_pad][t_pad] scratch
   float* vec;              // [H][8][t_pad] scratch
+  float* wbuf;             // [H][t_pad][64] scratch (L^-1 E_D of the active set D)
   int32_t* head_status;    // [H]
   int32_t* head_iters;     // [H]
   uint32_t* err;

@@ -12,7 +12,10 @@
 // sets y = G x - c, and flips the indices with x_j < 0 (passive) or y_j < -tol
 // (active); if the number of infeasible indices stops falling for three steps
 // only the largest such index flips (Murty's rule), which guarantees
-// termination.  A fixed iteration cap bounds the loop.
+// termination.  A fixed iteration cap bounds the loop.  G is factored once;
+// each step's passive solve then goes through the capacitance (Schur
+// complement) form of the active set D (at most 64 indices), see
+// nnls_bpp_kernel.
 //
 // Step 5 (C_v from the output equation by OLS): C = H^-1 R by Cholesky, with
 // the rows of keys whose weight is zero replaced by identity rows and their
@@ -30,6 +33,12 @@
 #include "lc_common.cuh"
 #include "lc_kernels.cuh"
 
+// Phase marks for instrumented builds (clock reads between phases); empty in
+// the library.
+#ifndef LC_SOLVER_MARK
+#define LC_SOLVER_MARK(id) ((void)0)
+#endif
+
 namespace lc {
 namespace {
 
@@ -40,6 +49,8 @@ constexpr int kLD = 33;            // row stride inside a block
 constexpr int kBlk = kBS * kLD;    // floats per block
 constexpr int kResidentMax = 256;  // unknowns kept in shared memory
 constexpr int kMaxRhs = 128;       // right-hand sides solved in one pass
+constexpr int kMaxD = 64;          // active indices handled in capacitance form
+constexpr int kPL = 64;            // row stride of the tile staging buffers
 constexpr unsigned kFull = 0xffffffffu;
 
 __device__ __forceinline__ float* blk(float* base, int I, int J) {
@@ -144,7 +155,7 @@ __device__ __forceinline__ void tile_update(float* S, int I, int J, int K) {
 // finish the trailing update.  Panels are solved row by row (one thread per
 // row, substitution against the factored diagonal block).  Every pivot that
 // is not positive is replaced by 1 and reported.
-__device__ bool cta_cholesky(float* S, float* dinv, int NB, int* bad) {
+__device__ __noinline__ bool cta_cholesky(float* S, float* dinv, int NB, int* bad) {
   const int tid = threadIdx.x, warp = warp_id();
   if (tid == 0) *bad = 0;
   __syncthreads();
@@ -169,15 +180,21 @@ __device__ bool cta_cholesky(float* S, float* dinv, int NB, int* bad) {
       for (int c = 0; c < kBS; ++c) row[c] = x[c];
     }
     __syncthreads();
+    LC_SOLVER_MARK(40);
     // trailing update; warp 0 takes the next diagonal block and factors it
     const int m = NB - K - 1;
     if (m > 0) {
       if (warp == 0) {
         tile_update(S, K + 1, K + 1, K);
         __syncwarp();
+        LC_SOLVER_MARK(41);
         diag_factor(S, dinv, K + 1, bad);
-      } else {
-        for (int task = warp - 1; task < m * (m + 1) / 2 - 1; task += kWarps - 1) {
+        LC_SOLVER_MARK(42);
+      } else if (warp % 4 != 0) {
+        // warps 4, 8, 12 share a scheduler with warp 0 and stay idle, so
+        // the diagonal factorisation -- the critical path -- issues alone
+        const int wi = warp - warp / 4 - 1;
+        for (int task = wi; task < m * (m + 1) / 2 - 1; task += kWarps - kWarps / 4) {
           // tasks enumerate the lower tiles (i >= j) except (0, 0)
           int i = 0, rem = task + 1;
           while (rem > i) {
@@ -189,6 +206,7 @@ __device__ bool cta_cholesky(float* S, float* dinv, int NB, int* bad) {
       }
     }
     __syncthreads();
+    LC_SOLVER_MARK(43);
   }
   const bool ok = *bad == 0;
   __syncthreads();
@@ -201,9 +219,10 @@ __device__ bool cta_cholesky(float* S, float* dinv, int NB, int* bad) {
 // block by substitution (one thread per column) into T2, written back, and
 // used for the update of the remaining rows -- through the register-tiled
 // warp product when nc is a multiple of 32, element-wise otherwise.  T and T2
-// hold 32 * max(nc, 32) floats.
-__device__ void cta_chol_solve(const float* S, const float* dinv, int NB, float* B, int ldb,
-                               int nc, float* T, float* T2) {
+// hold 32 * max(nc, 32) floats.  passes: 1 = forward only (L Y = B),
+// 2 = backward only (L^T X = B), 3 = both.
+__device__ __noinline__ void cta_chol_solve(const float* S, const float* dinv, int NB, float* B, int ldb,
+                               int nc, float* T, float* T2, int passes = 3) {
   const int tid = threadIdx.x, warp = warp_id(), lane = lane_id();
   const int rg = lane >> 2, cg = lane & 3;
   const int n_out = kBS * nc;
@@ -211,6 +230,7 @@ __device__ void cta_chol_solve(const float* S, const float* dinv, int NB, float*
   const int ntc = nc / kBS;
   float* Sm = const_cast<float*>(S);
   for (int pass = 0; pass < 2; ++pass) {
+    if (!(passes & (1 << pass))) continue;
     const bool fwd = pass == 0;
     for (int step = 0; step < NB; ++step) {
       const int K = fwd ? step : NB - 1 - step;
@@ -281,6 +301,148 @@ __device__ void cta_chol_solve(const float* S, const float* dinv, int NB, float*
       __syncthreads();
     }
   }
+}
+
+
+// Solve L L^T x = v (passes as in cta_chol_solve) for one right-hand side v
+// in shared memory (NB*32 entries).  Step K: warp 0 solves block K with one
+// lane per row (x_k broadcast by shuffle, the row updates run in parallel),
+// then one warp per remaining block applies its 32 x 32 product.
+__device__ __noinline__ void cta_solve1(const float* S, const float* dinv, int NB, float* v,
+                                        int passes = 3) {
+  const int warp = warp_id(), lane = lane_id();
+  float* Sm = const_cast<float*>(S);
+  __syncthreads();
+  for (int pass = 0; pass < 2; ++pass) {
+    if (!(passes & (1 << pass))) continue;
+    const bool fwd = pass == 0;
+    for (int step = 0; step < NB; ++step) {
+      const int K = fwd ? step : NB - 1 - step;
+      if (warp == 0) {
+        const float* Lkk = blk(Sm, K, K);
+        const float* di = dinv + K * kBS;
+        float y = v[K * kBS + lane], xr = 0.f;
+        if (fwd) {
+#pragma unroll
+          for (int k = 0; k < kBS; ++k) {
+            const float xk = __shfl_sync(kFull, y, k) * di[k];
+            if (lane == k) xr = xk;
+            if (lane > k) y = fmaf(-Lkk[lane * kLD + k], xk, y);
+          }
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < kBS; ++kk) {
+            const int k = kBS - 1 - kk;
+            const float xk = __shfl_sync(kFull, y, k) * di[k];
+            if (lane == k) xr = xk;
+            if (lane < k) y = fmaf(-Lkk[k * kLD + lane], xk, y);
+          }
+        }
+        v[K * kBS + lane] = xr;
+      }
+      __syncthreads();
+      const int i0 = fwd ? K + 1 : 0, i1 = fwd ? NB : K;
+      for (int I = i0 + warp; I < i1; I += kWarps) {
+        const float* xK = v + K * kBS;
+        float a0 = 0.f, a1 = 0.f;
+        if (fwd) {
+          const float* Lr = blk(Sm, I, K) + lane * kLD;
+#pragma unroll
+          for (int k = 0; k < kBS; k += 2) {
+            a0 = fmaf(Lr[k], xK[k], a0);
+            a1 = fmaf(Lr[k + 1], xK[k + 1], a1);
+          }
+        } else {
+          const float* Lc = blk(Sm, K, I) + lane;
+#pragma unroll
+          for (int k = 0; k < kBS; k += 2) {
+            a0 = fmaf(Lc[k * kLD], xK[k], a0);
+            a1 = fmaf(Lc[(k + 1) * kLD], xK[k + 1], a1);
+          }
+        }
+        v[I * kBS + lane] -= a0 + a1;
+      }
+      __syncthreads();
+    }
+  }
+}
+
+// Blocked substitution with the resident factor (NB <= 8 blocks) for up to
+// two 32-column tiles of right-hand sides that stay in registers: warp w owns
+// row block I = w / nct, column tile ct = w % nct (when I < NB), in the
+// fragment layout of warp_mm32, holding the NEGATED right-hand side on entry
+// and the negated solution on exit (so the block updates accumulate in place).
+// Step K: the owners of block K stage their tile in P, solve it against the
+// diagonal block by substitution (one lane per column) and reload it; after one
+// CTA barrier every warp below (forward) or above (backward) subtracts its
+// product with the solved block.  P holds two 32 x kPL buffers, used in turn.
+template <bool FWD>
+__device__ void reg_tri_solve(const float* S, const float* dinv, int NB, int nct,
+                              float (&nb)[4][8], float* P) {
+  constexpr bool fwd = FWD;
+  const int warp = warp_id(), lane = lane_id(), rg = lane >> 2, cg = lane & 3;
+  const int I = warp / nct, ct = warp % nct;
+  const bool owns = I < NB;
+  float* Sm = const_cast<float*>(S);
+  for (int step = 0; step < NB; ++step) {
+    const int K = fwd ? step : NB - 1 - step;
+    float* Pk = P + (step & 1) * kBS * kPL;
+    if (owns && I == K) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float4* row = reinterpret_cast<float4*>(Pk + (4 * rg + i) * kPL + ct * kBS + 8 * cg);
+        row[0] = make_float4(-nb[i][0], -nb[i][1], -nb[i][2], -nb[i][3]);
+        row[1] = make_float4(-nb[i][4], -nb[i][5], -nb[i][6], -nb[i][7]);
+      }
+      __syncwarp();
+      const float* Lkk = blk(Sm, K, K);
+      const float* di = dinv + K * kBS;
+      float* col = Pk + ct * kBS + lane;
+      float x[kBS];
+      if constexpr (FWD) {
+#pragma unroll
+        for (int r = 0; r < kBS; ++r) {
+          float v0 = col[r * kPL], v1 = 0.f;
+#pragma unroll
+          for (int k = 0; k < r; ++k) {
+            if (k & 1) v1 = fmaf(-Lkk[r * kLD + k], x[k], v1);
+            else v0 = fmaf(-Lkk[r * kLD + k], x[k], v0);
+          }
+          x[r] = (v0 + v1) * di[r];
+        }
+      } else {
+#pragma unroll
+        for (int rr = 0; rr < kBS; ++rr) {
+          const int r = kBS - 1 - rr;
+          float v0 = col[r * kPL], v1 = 0.f;
+#pragma unroll
+          for (int kk = 0; kk < rr; ++kk) {
+            const int k = kBS - 1 - kk;
+            if (kk & 1) v1 = fmaf(-Lkk[k * kLD + r], x[k], v1);
+            else v0 = fmaf(-Lkk[k * kLD + r], x[k], v0);
+          }
+          x[r] = (v0 + v1) * di[r];
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < kBS; ++r) col[r * kPL] = x[r];
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float4* row =
+            reinterpret_cast<const float4*>(Pk + (4 * rg + i) * kPL + ct * kBS + 8 * cg);
+        const float4 u0 = row[0], u1 = row[1];
+        nb[i][0] = -u0.x; nb[i][1] = -u0.y; nb[i][2] = -u0.z; nb[i][3] = -u0.w;
+        nb[i][4] = -u1.x; nb[i][5] = -u1.y; nb[i][6] = -u1.z; nb[i][7] = -u1.w;
+      }
+    }
+    __syncthreads();
+    if (owns && (fwd ? I > K : I < K)) {
+      if constexpr (FWD) warp_mm32<false, false>(blk(Sm, I, K), kLD, Pk + ct * kBS, kPL, nb);
+      else warp_mm32<true, false>(blk(Sm, K, I), kLD, Pk + ct * kBS, kPL, nb);
+    }
+  }
+  __syncthreads();
 }
 
 __device__ int block_sum_int(int v, int* red) {
@@ -418,21 +580,42 @@ __device__ void gather_packed(float* S, int NB, int n, F src) {
   }
 }
 
+// Step 4 for one head (one CTA).
+//
+// G is factored once (L L^T = G) and z0 = G^-1 c.  For an active set D
+// (w_D = 0, |D| <= 64) the passive solution is
+//   x = z0 + G^-1 E_D mu,   (G^-1)_DD mu = -z0_D,
+// which gives x_D = 0 and (G x - c) = E_D mu, i.e. (G x - c)_F = 0.  With
+// Y = L^-1 E_D (one forward substitution with |D| unit right-hand sides, kept
+// in registers), (G^-1)_DD = Y^T Y and G^-1 E_D mu = L^-T (Y mu), so a step
+// costs one forward solve with |D| columns, a |D| x |D| Cholesky and one
+// backward solve with a single column -- no refactorisation.  Systems with
+// more than 256 unknowns, a G that is not positive definite in fp32, or an
+// active set larger than 64 factor G_FF directly at every step instead.
 __global__ void __launch_bounds__(kThreads, 1) nnls_bpp_kernel(const SolveParams p) {
   extern __shared__ float dyn[];
   __shared__ int redi[33];
   __shared__ int bad;
-  const int h = blockIdx.x, tid = threadIdx.x;
+  const int h = blockIdx.x, tid = threadIdx.x, warp = warp_id(), lane = lane_id();
+  const int rg = lane >> 2, cg = lane & 3;
   const int t = p.t, tp = p.t_pad;
   const int n_pad = (t + kBS - 1) / kBS * kBS;
+  const int NB = n_pad / kBS;
   SolverSmem sm = carve(dyn, n_pad);
   float* S = sm.S ? sm.S : p.mat + static_cast<size_t>(h) * tp * tp;
   float* x = sm.vec;
   float* cv = x + n_pad;
-  float* rhs = cv + n_pad;
+  float* z0 = cv + n_pad;
+  float* aux = z0 + n_pad;
   int* F = sm.ivec;
-  int* Fidx = F + n_pad;
-  int* flip = Fidx + n_pad;
+  int* Didx = F + n_pad;
+  int* flip = Didx + n_pad;
+  float* Yg = p.wbuf + static_cast<size_t>(h) * tp * kMaxD;  // Y spilled for Y^T Y
+  // small system in the first staging buffer, tiles staged in the second
+  float* Ms = sm.T;
+  float* ds = Ms + 3 * kBlk;
+  float* mu = ds + 2 * kBS;
+  float* P = sm.T2;
   const float* G = p.G + static_cast<size_t>(h) * tp * tp;
 
   for (int j = tid; j < n_pad; j += kThreads) {
@@ -441,42 +624,144 @@ __global__ void __launch_bounds__(kThreads, 1) nnls_bpp_kernel(const SolveParams
     x[j] = 0.f;
   }
   __syncthreads();
-  int ninf_best = t + 1, backup = 3, status = LC_OK_STATUS, it = 0;
+  int status = LC_OK_STATUS;
+  bool direct = sm.S == nullptr;
+  if (!direct) {
+    gather_packed(S, NB, t, [&](int a, int b) { return G[static_cast<size_t>(a) * tp + b]; });
+    __syncthreads();
+    LC_SOLVER_MARK(0);
+    direct = !cta_cholesky(S, sm.dinv, NB, &bad);
+    LC_SOLVER_MARK(1);
+  }
+  if (!direct) {
+    for (int j = tid; j < n_pad; j += kThreads) z0[j] = cv[j];
+    __syncthreads();
+    cta_solve1(S, sm.dinv, NB, z0);
+    LC_SOLVER_MARK(3);
+  }
+  int ninf_best = t + 1, backup = 3, it = 0;
   bool converged = false;
   for (it = 0; it < p.max_iter; ++it) {
-    const int nF = block_compact(F, Fidx, t, redi);
-    const int NB = (nF + kBS - 1) / kBS;
-    // gather G_FF into packed blocks; identity beyond nF
-    gather_packed(S, NB, nF, [&](int a, int b) {
-      return G[static_cast<size_t>(Fidx[a]) * tp + Fidx[b]];
-    });
-    for (int a = tid; a < NB * kBS; a += kThreads) rhs[a] = a < nF ? cv[Fidx[a]] : 0.f;
+    for (int j = tid; j < n_pad; j += kThreads) flip[j] = (j < t) && !F[j];
     __syncthreads();
-    if (!cta_cholesky(S, sm.dinv, NB, &bad)) status = LC_SINGULAR_STATUS;
-    cta_chol_solve(S, sm.dinv, NB, rhs, 1, 1, sm.T, sm.T2);
-    for (int j = tid; j < n_pad; j += kThreads) x[j] = 0.f;
+    const int nD = block_compact(flip, Didx, t, redi);
+    if (!direct && nD > kMaxD) direct = true;
+    if (!direct) {
+      if (nD == 0) {
+        for (int j = tid; j < n_pad; j += kThreads) x[j] = z0[j];
+        __syncthreads();
+      } else {
+        const int nct = nD > kBS ? 2 : 1;
+        const int NBs = nct;
+        const int I = warp / nct, ct = warp % nct;
+        // -E_D as register tiles, then Y = L^-1 E_D (negated)
+        float nb[4][8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int a = I * kBS + 4 * rg + i, q = ct * kBS + 8 * cg + j;
+            nb[i][j] = (I < NB && q < nD && Didx[q] == a) ? -1.f : 0.f;
+          }
+        for (int e = tid; e < 3 * kBlk; e += kThreads) Ms[e] = 0.f;
+        LC_SOLVER_MARK(10);
+        reg_tri_solve<true>(S, sm.dinv, NB, nct, nb, P);
+        LC_SOLVER_MARK(11);
+        if (I < NB) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            float4* row = reinterpret_cast<float4*>(
+                Yg + static_cast<size_t>(I * kBS + 4 * rg + i) * kMaxD + ct * kBS + 8 * cg);
+            row[0] = make_float4(-nb[i][0], -nb[i][1], -nb[i][2], -nb[i][3]);
+            row[1] = make_float4(-nb[i][4], -nb[i][5], -nb[i][6], -nb[i][7]);
+          }
+        }
+        __syncthreads();
+        // (G^-1)_DD = Y^T Y: tile pairs (0,0), (1,0), (1,1) summed over row blocks
+        const int npair = nct == 2 ? 3 : 1;
+        for (int task = warp; task < npair * NB; task += kWarps) {
+          const int pr = task / NB, Ib = task % NB;
+          const int ta = pr == 0 ? 0 : 1, tb = pr == 2 ? 1 : 0;
+          float acc[4][8];
+          zero_acc(acc);
+          const float* Yb = Yg + static_cast<size_t>(Ib) * kBS * kMaxD;
+          warp_mm32<true, false>(Yb + ta * kBS, kMaxD, Yb + tb * kBS, kMaxD, acc);
+          float* Mt = blk(Ms, ta, tb);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) atomicAdd(&Mt[(4 * rg + i) * kLD + 8 * cg + j], acc[i][j]);
+        }
+        __syncthreads();
+        for (int q = nD + tid; q < NBs * kBS; q += kThreads)
+          blk(Ms, q / kBS, q / kBS)[(q % kBS) * kLD + q % kBS] = 1.f;
+        for (int q = tid; q < NBs * kBS; q += kThreads) mu[q] = q < nD ? -z0[Didx[q]] : 0.f;
+        __syncthreads();
+        if (!cta_cholesky(Ms, ds, NBs, &bad)) status = LC_SINGULAR_STATUS;
+        cta_solve1(Ms, ds, NBs, mu);
+        LC_SOLVER_MARK(12);
+        // v = Y mu, then x = z0 + L^-T v
+        for (int a = tid; a < n_pad; a += kThreads) {
+          const float4* yr = reinterpret_cast<const float4*>(Yg + static_cast<size_t>(a) * kMaxD);
+          float s0 = 0.f, s1 = 0.f;
+          for (int q4 = 0; q4 < NBs * kBS / 4; ++q4) {
+            const float4 y4 = yr[q4];
+            s0 = fmaf(y4.x, mu[4 * q4], s0);
+            s1 = fmaf(y4.y, mu[4 * q4 + 1], s1);
+            s0 = fmaf(y4.z, mu[4 * q4 + 2], s0);
+            s1 = fmaf(y4.w, mu[4 * q4 + 3], s1);
+          }
+          aux[a] = s0 + s1;
+        }
+        __syncthreads();
+        cta_solve1(S, sm.dinv, NB, aux, 2);
+        for (int a = tid; a < n_pad; a += kThreads)
+          x[a] = (a < t && F[a]) ? z0[a] + aux[a] : 0.f;
+        __syncthreads();
+      }
+    } else {
+      // direct: factor G_FF
+      const int nF = block_compact(F, Didx, t, redi);
+      const int NBf = (nF + kBS - 1) / kBS;
+      gather_packed(S, NBf, nF, [&](int a, int b) {
+        return G[static_cast<size_t>(Didx[a]) * tp + Didx[b]];
+      });
+      for (int a = tid; a < NBf * kBS; a += kThreads) aux[a] = a < nF ? cv[Didx[a]] : 0.f;
+      __syncthreads();
+      if (!cta_cholesky(S, sm.dinv, NBf, &bad)) status = LC_SINGULAR_STATUS;
+      cta_solve1(S, sm.dinv, NBf, aux);
+      for (int j = tid; j < n_pad; j += kThreads) x[j] = 0.f;
+      __syncthreads();
+      for (int a = tid; a < nF; a += kThreads) x[Didx[a]] = aux[a];
+      __syncthreads();
+      // the active rows for the dual check below
+      for (int j = tid; j < n_pad; j += kThreads) flip[j] = (j < t) && !F[j];
+      __syncthreads();
+      block_compact(flip, Didx, t, redi);
+    }
+    LC_SOLVER_MARK(13);
+    // infeasible set: x_j < 0 on F; on D, y_j = (G x - c)_j < -tol with tol a
+    // few ulps of the terms of y_j
+    for (int j = tid; j < n_pad; j += kThreads) flip[j] = (j < t) && F[j] && x[j] < 0.f;
     __syncthreads();
-    for (int a = tid; a < nF; a += kThreads) x[Fidx[a]] = rhs[a];
-    __syncthreads();
-    // y = G x - c and the infeasible set; tolerance a few ulps of the terms
-    const int warp = warp_id(), lane = lane_id();
-    for (int j = warp; j < t; j += kWarps) {
+    for (int q = warp; q < nD; q += kWarps) {
+      const int j = Didx[q];
       const float* g = G + static_cast<size_t>(j) * tp;
-      float s = 0.f, sa = 0.f;
+      float sacc = 0.f, sa = 0.f;
 #pragma unroll 8
       for (int k = lane; k < t; k += 32) {
         const float v = g[k] * x[k];
-        s += v;
+        sacc += v;
         sa += fabsf(v);
       }
       for (int o = 16; o > 0; o >>= 1) {
-        s += __shfl_xor_sync(kFull, s, o);
+        sacc += __shfl_xor_sync(kFull, sacc, o);
         sa += __shfl_xor_sync(kFull, sa, o);
       }
       if (lane == 0) {
-        const float yj = s - cv[j];
+        const float yj = sacc - cv[j];
         const float tol = 8.f * 1.1920929e-7f * (sa + fabsf(cv[j]));
-        flip[j] = F[j] ? (x[j] < 0.f) : (yj < -tol);
+        flip[j] = yj < -tol;
       }
     }
     __syncthreads();
@@ -487,6 +772,7 @@ __global__ void __launch_bounds__(kThreads, 1) nnls_bpp_kernel(const SolveParams
         maxj = j;
       }
     cnt = block_sum_int(cnt, redi);
+    LC_SOLVER_MARK(14);
     if (cnt == 0) {
       converged = true;
       break;
@@ -523,6 +809,7 @@ __global__ void __launch_bounds__(kThreads, 1) nnls_bpp_kernel(const SolveParams
   }
 }
 
+
 // Step 5, part 1: factor the output system (identity rows for zero-weight
 // keys and padding) into the packed blocks in p.mat, reciprocal diagonal in
 // p.dinv; the right-hand sides of those rows become the original values.
@@ -549,6 +836,7 @@ __global__ void __launch_bounds__(kThreads, 1) ols_factor_kernel(const OlsParams
       return Hm[static_cast<size_t>(a) * tp + b] + (a == b ? ridge : 0.f);
     });
     __syncthreads();
+    LC_SOLVER_MARK(20);
     if (cta_cholesky(S, sm.dinv, NB, &bad)) break;
     status = LC_SINGULAR_STATUS;
     float dsum = 0.f;
@@ -556,6 +844,7 @@ __global__ void __launch_bounds__(kThreads, 1) ols_factor_kernel(const OlsParams
       dsum += (w[a] > 0.f) ? Hm[static_cast<size_t>(a) * tp + a] : 0.f;
     ridge = 1e-6f * block_sum_f(dsum, redf) / t;
   }
+  LC_SOLVER_MARK(21);
   for (int e = tid; e < n_pad * dv; e += kThreads) {
     const int a = e / dv;
     if (a >= t) B[e] = 0.f;
@@ -573,7 +862,10 @@ __global__ void __launch_bounds__(kThreads, 1) ols_factor_kernel(const OlsParams
 }
 
 // Step 5, part 2: C_v columns [32*blockIdx.y, +32) by forward and backward
-// substitution with the published factor.
+
+// Step 5, part 2: C_v columns [32*blockIdx.y, +32) by forward and backward
+// substitution with the published factor -- held in registers when the system
+// has at most 256 unknowns (reg_tri_solve), else staged through the workspace.
 __global__ void __launch_bounds__(kThreads, 1) ols_solve_kernel(const OlsParams p) {
   extern __shared__ float dyn[];
   const int h = blockIdx.x, tid = threadIdx.x;
@@ -585,20 +877,52 @@ __global__ void __launch_bounds__(kThreads, 1) ols_solve_kernel(const OlsParams 
   const float* S = gS;
   if (sm.S) {
     const size_t nel = static_cast<size_t>(NB * (NB + 1) / 2) * kBlk;
-    for (size_t e = tid; e < nel; e += kThreads) sm.S[e] = gS[e];
+    const float4* src = reinterpret_cast<const float4*>(gS);
+    float4* dst = reinterpret_cast<float4*>(sm.S);
+    for (size_t e = tid; e < nel / 4; e += kThreads) dst[e] = src[e];
     S = sm.S;
   }
   const float* gd = p.dinv + static_cast<size_t>(h) * tp;
   for (int a = tid; a < n_pad; a += kThreads) sm.dinv[a] = gd[a];
+  float* B = p.R + static_cast<size_t>(h) * tp * dv;
+  float* Cv = p.Cv + static_cast<size_t>(h) * t * dv;
+  if (sm.S) {
+    const int warp = warp_id(), lane = lane_id(), rg = lane >> 2, cg = lane & 3;
+    const int c0 = blockIdx.y * kBS;
+    const int nc = min(kBS, dv - c0);
+    const int nct = 1;
+    const int I = warp / nct, ct = warp % nct;
+    float nb[4][8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int a = I * kBS + 4 * rg + i, q = ct * kBS + 8 * cg + j;
+        nb[i][j] = (I < NB && q < nc) ? -B[static_cast<size_t>(a) * dv + c0 + q] : 0.f;
+      }
+    __syncthreads();
+    LC_SOLVER_MARK(30);
+    reg_tri_solve<true>(S, sm.dinv, NB, nct, nb, sm.T2);
+    reg_tri_solve<false>(S, sm.dinv, NB, nct, nb, sm.T2);
+    LC_SOLVER_MARK(31);
+    if (I < NB) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int a = I * kBS + 4 * rg + i, q = ct * kBS + 8 * cg + j;
+          if (a < t && q < nc) Cv[static_cast<size_t>(a) * dv + c0 + q] = -nb[i][j];
+        }
+    }
+    return;
+  }
   __syncthreads();
   const int c0 = blockIdx.y * kBS;
   const int nc = min(kBS, dv - c0);
-  float* B = p.R + static_cast<size_t>(h) * tp * dv + c0;
-  cta_chol_solve(S, sm.dinv, NB, B, dv, nc, sm.T, sm.T2);
-  float* Cv = p.Cv + static_cast<size_t>(h) * t * dv + c0;
+  cta_chol_solve(S, sm.dinv, NB, B + c0, dv, nc, sm.T, sm.T2);
   for (int e = tid; e < t * nc; e += kThreads) {
     const int a = e / nc, j = e % nc;
-    Cv[static_cast<size_t>(a) * dv + j] = B[static_cast<size_t>(a) * dv + j];
+    Cv[static_cast<size_t>(a) * dv + c0 + j] = B[static_cast<size_t>(a) * dv + c0 + j];
   }
 }
 
