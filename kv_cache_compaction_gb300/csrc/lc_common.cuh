@@ -42,20 +42,17 @@ __device__ __forceinline__ uint32_t pack_h2(__half a, __half b) {
 __device__ __forceinline__ uint32_t f2_to_h2(float a, float b);
 
 // Split 8 floats into two uint4 of packed fp16 (hi parts, lo parts), for
-// values in the fp16 range.  hi is x rounded to 11 significant bits by
-// Veltkamp's splitting (T. J. Dekker, "A floating-point technique for
-// extending the available precision", Numer. Math. 18, 1971): with
-// t = (2^13 + 1) x, hi = t - (t - x) keeps the leading 11 bits of x, so it is
-// exact in fp16 and lo = x - hi is exact in fp32.  Only the packed fp16
-// conversions remain, one per element.  The explicitly rounded operations
-// keep the compiler from contracting the three steps into fused ones.
+// values in the fp16 range.  hi is x with its mantissa cut to the 10 bits fp16
+// stores (a bit mask), so it converts to fp16 exactly and lo = x - hi is exact
+// in fp32 with |lo| < 2^-10 |x|; lo rounded to fp16 leaves a relative error
+// below 2^-21 in hi + lo.  One mask, one subtraction and one packed
+// conversion per element.
 __device__ __forceinline__ void split8(const float* x, uint4& hi, uint4& lo) {
   float h[8], l[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const float t = __fmul_rn(x[i], 8193.f);
-    h[i] = __fsub_rn(t, __fsub_rn(t, x[i]));
-    l[i] = __fsub_rn(x[i], h[i]);
+    h[i] = __uint_as_float(__float_as_uint(x[i]) & 0xFFFFE000u);
+    l[i] = x[i] - h[i];
   }
   hi = make_uint4(f2_to_h2(h[0], h[1]), f2_to_h2(h[2], h[3]), f2_to_h2(h[4], h[5]),
                   f2_to_h2(h[6], h[7]));

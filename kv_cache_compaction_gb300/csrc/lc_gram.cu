@@ -23,6 +23,12 @@
 #include "lc_common.cuh"
 #include "lc_kernels.cuh"
 
+// Phase marks for instrumented builds (clock reads at pipeline events); empty
+// in the library.
+#ifndef LC_GRAM_MARK
+#define LC_GRAM_MARK(id, slab) ((void)0)
+#endif
+
 namespace lc {
 namespace {
 
@@ -327,9 +333,9 @@ __global__ void __launch_bounds__(192, 1)
 // between two epilogue warpgroups with their own E buffer and score buffer,
 // so the Gram products of one slab run on the tensor core while the other
 // group forms the next slab's E.  Warps: 0 TMA, 1 MMA issue, 2..5 group 0
-// (even slabs), 6..9 group 1 (odd slabs).  A ring stage is refilled once its
-// row shifts are read and -- for pair CTAs -- its scores are formed, or -- for
-// R CTAs -- the product with its O slab is done.  Tensor memory: S[2] (two blocks of
+// (even slabs), 6..9 group 1 (odd slabs).  A ring stage is refilled as soon
+// as its scores are formed (pair CTAs) or its O slab's product is done (R
+// CTAs); the per-query row data are read through L1.  Tensor memory: S[2] (two blocks of
 // 64 columns each) at 0 and 128, accumulator at 256.  Shared memory (pair /
 // R CTAs): C_k blocks, a 2-stage ring of query (and O) slabs, E[2].
 template <int D>
@@ -350,9 +356,7 @@ struct Gram2Layout {
   static constexpr int R_STAGE = Q_BYTES + O_BYTES;
   static constexpr int R_OFF_E = R_OFF_RING + 2 * R_STAGE;
   static constexpr int R_END = R_OFF_E + 2 * 2 * E_BLK;
-  static constexpr int OFF_ROWS = (P_END > R_END ? P_END : R_END);
-  static constexpr int ROW_STAGE = 2 * kSL * 4;
-  static constexpr int OFF_BAR = OFF_ROWS + 2 * ROW_STAGE;
+  static constexpr int OFF_BAR = (P_END > R_END ? P_END : R_END);
   static constexpr int OFF_CX = OFF_BAR + 256;      // group-1 partial c
   static constexpr int SMEM = 1024 + OFF_CX + 128 * 4;
 };
@@ -405,14 +409,13 @@ __global__ void __launch_bounds__(320, 1)
   const int stage_bytes = is_r ? L::R_STAGE : L::P_STAGE;
   uint8_t* sE = base + (is_r ? L::R_OFF_E : L::P_OFF_E);
   const int e_buf = (is_r ? 2 : 4) * L::E_BLK;  // one group's E buffer
-  uint8_t* sRows = base + L::OFF_ROWS;
 
   if (threadIdx.x == 0) {
     abort_flag = launch_aborted(p.err) ? 1 : 0;
     mbar_init(k_full, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&st_full[i], 1);
-      mbar_init(&st_empty[i], 1 + 128);
+      mbar_init(&st_empty[i], 1);
       mbar_init(&s_full[i], 1);
       mbar_init(&s_free[i], 128);
       mbar_init(&e_full[i], 128);
@@ -435,11 +438,12 @@ __global__ void __launch_bounds__(320, 1)
         tma_load_3d(sKi + c * 128 * 128, &mKc, k_full, 64 * c, bi * 128, h);
         if (two) tma_load_3d(sKj + c * 128 * 128, &mKc, k_full, 64 * c, bj * 128, h);
       }
-      const uint32_t bytes = L::Q_BYTES + (is_r ? L::O_BYTES : 0) + kSL * 4 + (with_c ? kSL * 4 : 0);
+      const uint32_t bytes = L::Q_BYTES + (is_r ? L::O_BYTES : 0);
       int issued = 0;
       for (int i = 0; i < nsl; ++i) {
         const int s = i & 1;
         if (i >= 2 && !wait_bar(&st_empty[s], ((i >> 1) - 1) & 1, &abort_flag, p.err)) break;
+        LC_GRAM_MARK(10, i);
         uint8_t* st = sRing + s * stage_bytes;
         const int r0 = (s0 + i) * kSL;
         mbar_arrive_expect_tx(&st_full[s], bytes);
@@ -452,10 +456,6 @@ __global__ void __launch_bounds__(320, 1)
                         r0, h);
           }
         }
-        const size_t roff = static_cast<size_t>(h) * p.n_q_pad + r0;
-        uint8_t* rw = sRows + s * L::ROW_STAGE;
-        bulk_g2s(rw, p.rowsh2 + roff, kSL * 4, &st_full[s]);
-        if (with_c) bulk_g2s(rw + kSL * 4, p.row_b + roff, kSL * 4, &st_full[s]);
         issued = i + 1;
       }
       if (abort_flag) {
@@ -473,10 +473,8 @@ __global__ void __launch_bounds__(320, 1)
       constexpr uint32_t idesc_g = idesc_f16(128, 128, false, false, false);
       constexpr uint32_t idesc_r = idesc_f16(128, D, false, false, true);
       bool ok = wait_bar(k_full, 0, &abort_flag, p.err);
-      auto issue_s = [&](int i) -> bool {  // scores of slab i into S[i & 1]
+      auto issue_s = [&](int i) {  // scores of slab i into S[i & 1]
         const int s = i & 1;
-        if (!wait_bar(&st_full[s], (i >> 1) & 1, &abort_flag, p.err)) return false;
-        if (i >= 2 && !wait_bar(&s_free[s], ((i >> 1) - 1) & 1, &abort_flag, p.err)) return false;
         tc_fence_after();
         const uint32_t aQ = smem_u32(sRing + s * stage_bytes);
 #pragma unroll
@@ -492,13 +490,9 @@ __global__ void __launch_bounds__(320, 1)
         // a pair CTA is done with the query slab once its scores are formed
         if (!is_r) umma_commit(&st_empty[s]);
         umma_commit(&s_full[s]);
-        return true;
       };
-      if (ok) ok = issue_s(0);
-      if (ok && nsl > 1) ok = issue_s(1);
-      for (int i = 0; ok && i < nsl; ++i) {
+      auto issue_g = [&](int i) {  // Gram (or R) products of slab i
         const int g = i & 1;
-        if (!wait_bar(&e_full[g], (i >> 1) & 1, &abort_flag, p.err)) break;
         tc_fence_after();
         const uint32_t eb = smem_u32(sE + g * e_buf);
         const uint32_t eih = eb, eil = eb + L::E_BLK;
@@ -529,10 +523,39 @@ __global__ void __launch_bounds__(320, 1)
             umma_f16_ss(tAcc, sdesc_sw128(eih + o, 16, 1024), dol, idesc_r, 1u);
             umma_f16_ss(tAcc, sdesc_sw128(eil + o, 16, 1024), doh, idesc_r, 1u);
           }
+          umma_commit(&st_empty[g]);  // the O slab feeds the products above
         }
-        if (is_r) umma_commit(&st_empty[g]);  // the O slab feeds the product above
         umma_commit(&e_free[g]);
-        if (i + 2 < nsl && !issue_s(i + 2)) break;
+      };
+      // Event loop: the scores of a slab are issued as soon as its query slab
+      // is loaded and its S buffer has been read (up to two slabs ahead of
+      // the Gram products), the Gram products as soon as its E is formed.
+      int ns = 0, ng = 0;
+      uint64_t t_last = globaltimer_ns();
+      uint32_t spins = 0;
+      while (ok && ng < nsl) {
+        if (ns < nsl && mbar_test_wait(&st_full[ns & 1], (ns >> 1) & 1) &&
+            (ns < 2 || mbar_test_wait(&s_free[ns & 1], ((ns >> 1) - 1) & 1))) {
+          LC_GRAM_MARK(3, ns);
+          issue_s(ns++);
+          t_last = globaltimer_ns();
+        } else if (ng < ns && mbar_test_wait(&e_full[ng & 1], (ng >> 1) & 1)) {
+          LC_GRAM_MARK(1, ng);
+          issue_g(ng++);
+          LC_GRAM_MARK(2, ng - 1);
+          t_last = globaltimer_ns();
+        } else if ((++spins & 63u) == 0) {
+          if (abort_flag) break;
+          if (*reinterpret_cast<volatile uint32_t*>(p.err) & kErrWaitTimeout) {
+            abort_flag = 1;
+            break;
+          }
+          if (globaltimer_ns() - t_last > kWaitLimitNs) {
+            atomicOr(p.err, kErrWaitTimeout);
+            abort_flag = 1;
+            break;
+          }
+        }
       }
       umma_commit(done);
     }
@@ -555,43 +578,76 @@ __global__ void __launch_bounds__(320, 1)
     bool ok = nsl > 0;
     for (int i = g; ok && i < nsl; i += 2) {
       const int n = i >> 1;  // this group's n-th slab
+      // per-query shifts (and mass) of this slab, read through L1: every
+      // thread of the group reads the same 64 values
+      const size_t roff = static_cast<size_t>(h) * p.n_q_pad + static_cast<size_t>(s0 + i) * kSL;
+      const float* rs = p.rowsh2 + roff;
+      const float* rb = with_c ? p.row_b + roff : rs;
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(rs));
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(rs + 32));
+      if (with_c) {
+        asm volatile("prefetch.global.L1 [%0];" ::"l"(rb));
+        asm volatile("prefetch.global.L1 [%0];" ::"l"(rb + 32));
+      }
       if (!wait_bar(&s_full[g], n & 1, &abort_flag, p.err)) { ok = false; break; }
+      LC_GRAM_MARK(20, i);
       tc_fence_after();
-      float xi[kSL], xj[kSL];
-      tmem_ld64(tbase + g * 128 + lane_off, xi);
-      if (two) tmem_ld64(tbase + g * 128 + 64 + lane_off, xj);
-      tc_fence_before();
-      mbar_arrive(&s_free[g]);
-      if (n > 0 && !wait_bar(&e_free[g], (n - 1) & 1, &abort_flag, p.err)) { ok = false; break; }
-      if (!wait_bar(&st_full[g], n & 1, &abort_flag, p.err)) { ok = false; break; }
-      const float* rs = reinterpret_cast<const float*>(sRows + g * L::ROW_STAGE);
-      const float* rb = rs + kSL;
 #pragma unroll
-      for (int c8 = 0; c8 < kSL / 8; ++c8) {
-        float e8[8];
+      for (int hf = 0; hf < 2; ++hf) {  // 32 query columns at a time
+        // row data of these columns first: their latency overlaps the TMEM load
+        float4 sh4[8], b4[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float sh = rs[c8 * 8 + e];
-          e8[e] = ex2(fmaf(xi[c8 * 8 + e], s2, cbi) - sh);
-          if (with_c) cacc = fmaf(e8[e], rb[c8 * 8 + e], cacc);
+        for (int q = 0; q < 8; ++q) sh4[q] = __ldg(reinterpret_cast<const float4*>(rs + hf * 32) + q);
+        if (with_c) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) b4[q] = __ldg(reinterpret_cast<const float4*>(rb + hf * 32) + q);
         }
-        uint4 hi, lo;
-        split8(e8, hi, lo);
-        const uint32_t off = sw128_offset(j, c8 * 8);
-        *reinterpret_cast<uint4*>(sEih + off) = hi;
-        *reinterpret_cast<uint4*>(sEil + off) = lo;
-        if (two) {
+        float xi[32], xj[32];
+        const uint32_t ts = tbase + g * 128 + hf * 32 + lane_off;
+        if (two) tmem_ld32x2(ts, ts + 64, xi, xj);
+        else tmem_ld32(ts, xi);
+        if (hf == 1) {
+          tc_fence_before();
+          mbar_arrive(&s_free[g]);
+        } else {
+          if (n > 0 && !wait_bar(&e_free[g], (n - 1) & 1, &abort_flag, p.err)) { ok = false; break; }
+          LC_GRAM_MARK(21, i);
+        }
 #pragma unroll
-          for (int e = 0; e < 8; ++e) e8[e] = ex2(fmaf(xj[c8 * 8 + e], s2, cbj) - rs[c8 * 8 + e]);
+        for (int q8 = 0; q8 < 4; ++q8) {
+          const int c8 = hf * 4 + q8;
+          const float sh8[8] = {sh4[2 * q8].x, sh4[2 * q8].y, sh4[2 * q8].z, sh4[2 * q8].w,
+                                sh4[2 * q8 + 1].x, sh4[2 * q8 + 1].y, sh4[2 * q8 + 1].z,
+                                sh4[2 * q8 + 1].w};
+          float e8[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) e8[e] = ex2(fmaf(xi[q8 * 8 + e], s2, cbi) - sh8[e]);
+          if (with_c) {
+            const float b8[8] = {b4[2 * q8].x, b4[2 * q8].y, b4[2 * q8].z, b4[2 * q8].w,
+                                 b4[2 * q8 + 1].x, b4[2 * q8 + 1].y, b4[2 * q8 + 1].z,
+                                 b4[2 * q8 + 1].w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) cacc = fmaf(e8[e], b8[e], cacc);
+          }
+          uint4 hi, lo;
           split8(e8, hi, lo);
-          *reinterpret_cast<uint4*>(sEjh + off) = hi;
-          *reinterpret_cast<uint4*>(sEjl + off) = lo;
+          const uint32_t off = sw128_offset(j, c8 * 8);
+          *reinterpret_cast<uint4*>(sEih + off) = hi;
+          *reinterpret_cast<uint4*>(sEil + off) = lo;
+          if (two) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) e8[e] = ex2(fmaf(xj[q8 * 8 + e], s2, cbj) - sh8[e]);
+            split8(e8, hi, lo);
+            *reinterpret_cast<uint4*>(sEjh + off) = hi;
+            *reinterpret_cast<uint4*>(sEjl + off) = lo;
+          }
         }
       }
+      if (!ok) break;
+      LC_GRAM_MARK(23, i);
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(&e_full[g]);
-      mbar_arrive(&st_empty[g]);  // row shifts of this stage read
     }
     // combine the groups' partial c and publish the block accumulator
     if (with_c && g == 1) cx[j] = cacc;
