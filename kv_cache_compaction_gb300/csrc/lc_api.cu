@@ -2,6 +2,7 @@
 // TMA tensor maps, and the launch sequence of the five compaction steps.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -60,7 +61,8 @@ struct Plan {
   int H, n_q, T, d, t, d_qk, n_q_pad, t_pad, nblk;
   float scale;
   int max_iter;
-  int ks_max, g5_max, g7_max;  // largest query splits the workspace holds
+  bool all_pairs;              // one CTA forms all three Gram blocks (bf16, nblk == 2)
+  int ks_max, g5_max, g7_max, r_max;  // largest query splits the workspace holds
   // workspace offsets (bytes)
   size_t qop, kop, vhi, vlo;            // operand copies (16-bit)
   size_t m_pad, lse_pad, ohi, olo;      // step-1 results
@@ -139,8 +141,16 @@ Plan make_plan(const lc_shape* s) {
   const int slabs = p.n_q_pad / 64;
   const int npairs = p.nblk * (p.nblk + 1) / 2;
   p.ks_max = max_split(((p.T + 255) / 256) * p.H, 2, nqt);
-  p.g5_max = max_split(npairs * p.H, 1, slabs);
-  p.g7_max = max_split((npairs + p.nblk) * p.H, 1, slabs);
+  p.all_pairs = p.bf16_in && p.nblk == 2;
+  if (p.all_pairs) {
+    // long CTAs: at most two waves of a 160-SM device
+    const int cap = std::max(1, std::min(max_split(p.H, 1, slabs), 320 / p.H));
+    p.g5_max = p.g7_max = cap;
+    p.r_max = max_split(p.nblk * p.H, 1, slabs);
+  } else {
+    p.g5_max = max_split(npairs * p.H, 1, slabs);
+    p.g7_max = p.r_max = max_split((npairs + p.nblk) * p.H, 1, slabs);
+  }
 
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -176,7 +186,7 @@ Plan make_plan(const lc_shape* s) {
   p.G = take(H * tt * 4);
   p.c = take(H * p.t_pad * 4);
   p.hpart = take(static_cast<size_t>(p.g7_max) * H * tt * 4);
-  p.rpart = take(static_cast<size_t>(p.g7_max) * H * p.t_pad * p.d * 4);
+  p.rpart = take(static_cast<size_t>(p.r_max) * H * p.t_pad * p.d * 4);
   p.Hm = take(H * tt * 4);
   p.R = take(H * p.t_pad * p.d * 4);
   p.vc = take(H * p.t_pad * p.d * 4);
@@ -424,9 +434,11 @@ lc_status run_fit(const Ctx& c, const void* qop, const void* kop, const void* V,
     *per = (slabs + sp - 1) / sp;
     return (slabs + *per - 1) / *per;
   };
-  int g5_slabs = 0, g7_slabs = 0;
-  const int g5_split = split_of(npairs * p.H, p.g5_max, &g5_slabs);
-  const int g7_split = split_of((npairs + p.nblk) * p.H, p.g7_max, &g7_slabs);
+  int g5_slabs = 0, g7_slabs = 0, r_slabs = 0;
+  const int g5_split = split_of((p.all_pairs ? 1 : npairs) * p.H, p.g5_max, &g5_slabs);
+  const int g7_split =
+      split_of((p.all_pairs ? 1 : npairs + p.nblk) * p.H, p.g7_max, &g7_slabs);
+  const int r_split = p.all_pairs ? split_of(p.nblk * p.H, p.r_max, &r_slabs) : g7_split;
   GramParams g{};
   g.n_q_pad = p.n_q_pad;
   g.n_q = p.n_q;
@@ -444,7 +456,10 @@ lc_status run_fit(const Ctx& c, const void* qop, const void* kop, const void* V,
   g.err = c.h->d_err;
   {
     LC_PROF(c, "gram_mass", 1);
-    LC_CUDA(launch_gram(p.mode, false, mKc, mQ64, mOhi, mOlo, g, p.H, g5_split, c.st));
+    if (p.all_pairs)
+      LC_CUDA(launch_gram_all_pairs(p.mode, mKc, mQ64, g, p.H, g5_split, c.st));
+    else
+      LC_CUDA(launch_gram(p.mode, false, mKc, mQ64, mOhi, mOlo, g, p.H, g5_split, c.st));
   }
   const size_t tt = static_cast<size_t>(p.t_pad) * p.t_pad;
   {
@@ -497,14 +512,24 @@ lc_status run_fit(const Ctx& c, const void* qop, const void* kop, const void* V,
   g.Gpart = c.at<float>(p.hpart);
   g.cpart = nullptr;
   g.Rpart = c.at<float>(p.rpart);
-  {
+  if (p.all_pairs) {
+    {
+      LC_PROF(c, "gram_out", 1);
+      LC_CUDA(launch_gram_all_pairs(p.mode, mKc, mQ64, g, p.H, g7_split, c.st));
+    }
+    GramParams gr = g;
+    gr.r_only = 1;
+    gr.slabs_per_split = r_slabs;
+    LC_PROF(c, "gram_r", 1);
+    LC_CUDA(launch_gram_r(p.mode, mKc, mQ64, mOhi, mOlo, gr, p.H, r_split, c.st));
+  } else {
     LC_PROF(c, "gram_out", 1);
     LC_CUDA(launch_gram(p.mode, true, mKc, mQ64, mOhi, mOlo, g, p.H, g7_split, c.st));
   }
   {
     LC_PROF(c, "reduce_out", 4);
     LC_CUDA(launch_reduce_partials(c.at<float>(p.hpart), c.at<float>(p.Hm), g7_split, H * tt, c.st));
-    LC_CUDA(launch_reduce_partials(c.at<float>(p.rpart), c.at<float>(p.R), g7_split,
+    LC_CUDA(launch_reduce_partials(c.at<float>(p.rpart), c.at<float>(p.R), r_split,
                                    H * p.t_pad * p.d, c.st));
     LC_CUDA(launch_symmetrize(c.at<float>(p.Hm), p.H, p.t_pad, c.st));
     LC_CUDA(launch_gather_v(V, p.bf16_in ? 0 : 1, idx, c.at<float>(p.vc), p.H, p.T, p.t, p.t_pad,

@@ -385,7 +385,7 @@ __global__ void __launch_bounds__(320, 1)
   const int warp = warp_id(), lane = lane_id();
   const int h = blockIdx.y, z = blockIdx.z;
   const int npairs = p.nblk * (p.nblk + 1) / 2;
-  const bool is_r = static_cast<int>(blockIdx.x) >= npairs;
+  const bool is_r = p.r_only || static_cast<int>(blockIdx.x) >= npairs;
   int bi = 0, bj = 0;
   if (!is_r) {
     int rem = blockIdx.x;
@@ -395,7 +395,7 @@ __global__ void __launch_bounds__(320, 1)
     }
     bj = bi + rem;
   } else {
-    bi = bj = blockIdx.x - npairs;
+    bi = bj = p.r_only ? static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x) - npairs;
   }
   const bool two = !is_r && bi != bj;
   const bool with_c = !is_r && bi == bj && p.row_b != nullptr;
@@ -686,6 +686,281 @@ __global__ void __launch_bounds__(320, 1)
   if (warp == 1) tmem_dealloc(tbase, 512);
 }
 
+// All pairs of a two-block (256-key) system in one CTA: the scores of a query
+// slab are formed once for both key blocks (S at TMEM columns 0 and 64), E
+// once per block by eight epilogue warps (one per key row of each block), and
+// the three Gram blocks G00, G01, G11 accumulate at TMEM columns 128, 256 and
+// 384.  Compared with one CTA per pair, each slab's scores and E are computed
+// once instead of twice.  Warps: 0 TMA, 1 MMA issue, 2..9 E rows (warp w holds
+// key rows 32 (w % 4) .. +31 of block (w - 2) / 4, the TMEM lanes it may
+// access).  Shared memory: C_k of both blocks, a 2-stage ring of query slabs,
+// E[2] (hi and lo of both blocks).
+template <int D>
+struct Gram3Layout {
+  static constexpr int NC = D / 64;
+  static constexpr int KC_BYTES = 128 * D * 2;
+  static constexpr int QCHUNK = kSL * 128;
+  static constexpr int Q_BYTES = NC * QCHUNK;
+  static constexpr int E_BLK = 128 * 128;  // 128 keys x 64 queries, fp16
+  static constexpr int OFF_RING = 2 * KC_BYTES;
+  static constexpr int OFF_E = OFF_RING + 2 * Q_BYTES;
+  static constexpr int OFF_BAR = OFF_E + 2 * 4 * E_BLK;
+  static constexpr int SMEM = 1024 + OFF_BAR + 256;
+};
+
+template <int D>
+__global__ void __launch_bounds__(320, 1)
+    gram3_kernel(const __grid_constant__ CUtensorMap mKc, const __grid_constant__ CUtensorMap mQ,
+                 const GramParams p) {
+  using L = Gram3Layout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = align1024(smem_raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + L::OFF_BAR);
+  uint64_t* k_full = bars + 0;
+  uint64_t* st_full = bars + 1;   // [2]
+  uint64_t* st_empty = bars + 3;  // [2]
+  uint64_t* s_full = bars + 5;
+  uint64_t* s_free = bars + 6;
+  uint64_t* e_full = bars + 7;    // [2]
+  uint64_t* e_free = bars + 9;    // [2]
+  uint64_t* done = bars + 11;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 12);
+  __shared__ volatile int abort_flag;
+
+  const int warp = warp_id(), lane = lane_id();
+  const int h = blockIdx.y, z = blockIdx.z;
+  const bool with_c = p.row_b != nullptr;
+  const int total_slabs = p.n_q_pad / kSL;
+  const int s0 = z * p.slabs_per_split;
+  const int nsl = max(0, min(total_slabs, s0 + p.slabs_per_split) - s0);
+  uint8_t* sK0 = base;
+  uint8_t* sK1 = base + L::KC_BYTES;
+  uint8_t* sRing = base + L::OFF_RING;
+  uint8_t* sE = base + L::OFF_E;
+
+  if (threadIdx.x == 0) {
+    abort_flag = launch_aborted(p.err) ? 1 : 0;
+    mbar_init(k_full, 1);
+    mbar_init(s_full, 1);
+    mbar_init(s_free, 256);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&st_full[i], 1);
+      mbar_init(&st_empty[i], 1);
+      mbar_init(&e_full[i], 256);
+      mbar_init(&e_free[i], 1);
+    }
+    mbar_init(done, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(tslot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tslot;
+
+  if (warp == 0) {
+    if (lane == 0 && nsl > 0) {
+      mbar_arrive_expect_tx(k_full, 2 * L::KC_BYTES);
+      for (int c = 0; c < L::NC; ++c) {
+        tma_load_3d(sK0 + c * 128 * 128, &mKc, k_full, 64 * c, 0, h);
+        tma_load_3d(sK1 + c * 128 * 128, &mKc, k_full, 64 * c, 128, h);
+      }
+      int issued = 0;
+      for (int i = 0; i < nsl; ++i) {
+        const int s = i & 1;
+        if (i >= 2 && !wait_bar(&st_empty[s], ((i >> 1) - 1) & 1, &abort_flag, p.err)) break;
+        uint8_t* st = sRing + s * L::Q_BYTES;
+        const int r0 = (s0 + i) * kSL;
+        mbar_arrive_expect_tx(&st_full[s], L::Q_BYTES);
+        for (int c = 0; c < L::NC; ++c)
+          tma_load_3d(st + c * L::QCHUNK, &mQ, &st_full[s], 64 * c, r0, h);
+        issued = i + 1;
+      }
+      if (abort_flag) {
+        for (int i = (issued > 2 ? issued - 2 : 0); i < issued; ++i) {
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(&st_full[i & 1], (i >> 1) & 1) &&
+                 globaltimer_ns() - t0 < kWaitLimitNs) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && nsl > 0) {
+      constexpr uint32_t idesc_s = idesc_f16(128, kSL, true, false, false);
+      constexpr uint32_t idesc_g = idesc_f16(128, 128, false, false, false);
+      bool ok = wait_bar(k_full, 0, &abort_flag, p.err);
+      auto issue_s = [&](int i) {  // scores of slab i for both key blocks
+        const int s = i & 1;
+        tc_fence_after();
+        const uint32_t aQ = smem_u32(sRing + s * L::Q_BYTES);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint64_t dq = sdesc_sw128(aQ + (k >> 2) * L::QCHUNK + (k & 3) * 32, 16, 1024);
+          const uint32_t koff = (k >> 2) * (128 * 128) + (k & 3) * 32;
+          umma_f16_ss(tbase, sdesc_sw128(smem_u32(sK0) + koff, 16, 1024), dq, idesc_s,
+                      k > 0 ? 1u : 0u);
+          umma_f16_ss(tbase + 64, sdesc_sw128(smem_u32(sK1) + koff, 16, 1024), dq, idesc_s,
+                      k > 0 ? 1u : 0u);
+        }
+        umma_commit(&st_empty[s]);
+        umma_commit(s_full);
+      };
+      auto issue_g = [&](int i) {  // G00, G01, G11 products of slab i
+        const int b = i & 1;
+        tc_fence_after();
+        const uint32_t eb = smem_u32(sE + b * 4 * L::E_BLK);
+        const uint32_t e0h = eb, e0l = eb + L::E_BLK;
+        const uint32_t e1h = eb + 2 * L::E_BLK, e1l = eb + 3 * L::E_BLK;
+#pragma unroll
+        for (int k = 0; k < kSL / 16; ++k) {
+          const uint32_t o = k * 32;
+          const uint32_t acc0 = (i > 0 || k > 0) ? 1u : 0u;
+          const uint64_t a0h = sdesc_sw128(e0h + o, 16, 1024), a0l = sdesc_sw128(e0l + o, 16, 1024);
+          const uint64_t a1h = sdesc_sw128(e1h + o, 16, 1024), a1l = sdesc_sw128(e1l + o, 16, 1024);
+          umma_f16_ss(tbase + 128, a0h, a0h, idesc_g, acc0);
+          umma_f16_ss(tbase + 128, a0h, a0l, idesc_g, 1u);
+          umma_f16_ss(tbase + 128, a0l, a0h, idesc_g, 1u);
+          umma_f16_ss(tbase + 256, a0h, a1h, idesc_g, acc0);
+          umma_f16_ss(tbase + 256, a0h, a1l, idesc_g, 1u);
+          umma_f16_ss(tbase + 256, a0l, a1h, idesc_g, 1u);
+          umma_f16_ss(tbase + 384, a1h, a1h, idesc_g, acc0);
+          umma_f16_ss(tbase + 384, a1h, a1l, idesc_g, 1u);
+          umma_f16_ss(tbase + 384, a1l, a1h, idesc_g, 1u);
+        }
+        umma_commit(&e_free[b]);
+      };
+      // Event loop: a slab's scores are issued once its query slab is loaded
+      // and the previous scores have been read; its Gram products once its E
+      // is formed.
+      int ns = 0, ng = 0;
+      uint64_t t_last = globaltimer_ns();
+      uint32_t spins = 0;
+      while (ok && ng < nsl) {
+        if (ns < nsl && mbar_test_wait(&st_full[ns & 1], (ns >> 1) & 1) &&
+            (ns == 0 || mbar_test_wait(s_free, (ns - 1) & 1))) {
+          issue_s(ns++);
+          t_last = globaltimer_ns();
+        } else if (ng < ns && mbar_test_wait(&e_full[ng & 1], (ng >> 1) & 1)) {
+          issue_g(ng++);
+          t_last = globaltimer_ns();
+        } else if ((++spins & 63u) == 0) {
+          if (abort_flag) break;
+          if (*reinterpret_cast<volatile uint32_t*>(p.err) & kErrWaitTimeout) {
+            abort_flag = 1;
+            break;
+          }
+          if (globaltimer_ns() - t_last > kWaitLimitNs) {
+            atomicOr(p.err, kErrWaitTimeout);
+            abort_flag = 1;
+            break;
+          }
+        }
+      }
+      umma_commit(done);
+    }
+  } else {
+    // ---------------------------------------------------------- E rows
+    const int b = (warp - 2) >> 2;
+    const int q = warp & 3;
+    const int j = q * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    const float cb = p.colb2[static_cast<size_t>(h) * p.t_pad + b * 128 + j];
+    const float s2 = p.scale_log2;
+    float cacc = 0.f;
+    bool ok = nsl > 0;
+    for (int i = 0; ok && i < nsl; ++i) {
+      const size_t roff = static_cast<size_t>(h) * p.n_q_pad + static_cast<size_t>(s0 + i) * kSL;
+      const float* rs = p.rowsh2 + roff;
+      const float* rb = with_c ? p.row_b + roff : rs;
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(rs));
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(rs + 32));
+      if (with_c) {
+        asm volatile("prefetch.global.L1 [%0];" ::"l"(rb));
+        asm volatile("prefetch.global.L1 [%0];" ::"l"(rb + 32));
+      }
+      if (!wait_bar(s_full, i & 1, &abort_flag, p.err)) { ok = false; break; }
+      tc_fence_after();
+      uint8_t* sEh = sE + (i & 1) * 4 * L::E_BLK + b * 2 * L::E_BLK;
+      uint8_t* sEl = sEh + L::E_BLK;
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {  // 32 query columns at a time
+        float4 sh4[8], b4[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) sh4[u] = __ldg(reinterpret_cast<const float4*>(rs + hf * 32) + u);
+        if (with_c) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u) b4[u] = __ldg(reinterpret_cast<const float4*>(rb + hf * 32) + u);
+        }
+        float x[32];
+        tmem_ld32(tbase + b * 64 + hf * 32 + lane_off, x);
+        if (hf == 1) {
+          tc_fence_before();
+          mbar_arrive(s_free);
+        } else if (i >= 2 && !wait_bar(&e_free[i & 1], ((i >> 1) - 1) & 1, &abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
+#pragma unroll
+        for (int q8 = 0; q8 < 4; ++q8) {
+          const int c8 = hf * 4 + q8;
+          const float sh8[8] = {sh4[2 * q8].x, sh4[2 * q8].y, sh4[2 * q8].z, sh4[2 * q8].w,
+                                sh4[2 * q8 + 1].x, sh4[2 * q8 + 1].y, sh4[2 * q8 + 1].z,
+                                sh4[2 * q8 + 1].w};
+          float e8[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) e8[e] = ex2(fmaf(x[q8 * 8 + e], s2, cb) - sh8[e]);
+          if (with_c) {
+            const float b8[8] = {b4[2 * q8].x, b4[2 * q8].y, b4[2 * q8].z, b4[2 * q8].w,
+                                 b4[2 * q8 + 1].x, b4[2 * q8 + 1].y, b4[2 * q8 + 1].z,
+                                 b4[2 * q8 + 1].w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) cacc = fmaf(e8[e], b8[e], cacc);
+          }
+          uint4 hi, lo;
+          split8(e8, hi, lo);
+          const uint32_t off = sw128_offset(j, c8 * 8);
+          *reinterpret_cast<uint4*>(sEh + off) = hi;
+          *reinterpret_cast<uint4*>(sEl + off) = lo;
+        }
+      }
+      if (!ok) break;
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(&e_full[i & 1]);
+    }
+    // publish G00 / G11 (own block), half of G01 (block-0 rows), and c
+    if (ok && nsl > 0 && wait_bar(done, 0, &abort_flag, p.err)) {
+      tc_fence_after();
+      const int H = gridDim.y;
+      const size_t zh = static_cast<size_t>(z) * H + h;
+      const int key = b * 128 + j;
+      float* dst = p.Gpart + (zh * p.t_pad + key) * p.t_pad + b * 128;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float v[32];
+        tmem_ld32(tbase + 128 + b * 256 + c * 32 + lane_off, v);
+        float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) d4[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+      }
+      float* dst01 = p.Gpart + (zh * p.t_pad + j) * p.t_pad + 128 + b * 64;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        float v[32];
+        tmem_ld32(tbase + 256 + b * 64 + c * 32 + lane_off, v);
+        float4* d4 = reinterpret_cast<float4*>(dst01 + c * 32);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) d4[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+      }
+      if (with_c) p.cpart[zh * p.t_pad + key] = cacc;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tbase, 512);
+}
+
 template <int D>
 cudaError_t launch_gram2_t(bool with_r, const CUtensorMap& mKc, const CUtensorMap& mQ,
                            const CUtensorMap& mOhi, const CUtensorMap& mOlo, const GramParams& p,
@@ -728,10 +1003,47 @@ cudaError_t launch_gram(OperandMode mode, bool with_r, const CUtensorMap& mKc,
   return cudaErrorInvalidValue;
 }
 
+cudaError_t launch_gram_all_pairs(OperandMode mode, const CUtensorMap& mKc, const CUtensorMap& mQ,
+                                  const GramParams& p, int H, int nsplit, cudaStream_t st) {
+  if (p.nblk != 2 || p.r_only) return cudaErrorInvalidValue;
+  auto go = [&](auto kern, int smem) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    kern<<<dim3(1, H, nsplit), 320, smem, st>>>(mKc, mQ, p);
+    return cudaGetLastError();
+  };
+  switch (mode) {
+    case kBF16d128: return go(gram3_kernel<128>, Gram3Layout<128>::SMEM);
+    case kBF16d64: return go(gram3_kernel<64>, Gram3Layout<64>::SMEM);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_gram_r(OperandMode mode, const CUtensorMap& mKc, const CUtensorMap& mQ,
+                          const CUtensorMap& mOhi, const CUtensorMap& mOlo, const GramParams& p,
+                          int H, int nsplit, cudaStream_t st) {
+  if (!p.r_only || !p.Rpart) return cudaErrorInvalidValue;
+  auto go = [&](auto kern, int smem) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    kern<<<dim3(p.nblk, H, nsplit), 320, smem, st>>>(mKc, mQ, mOhi, mOlo, p);
+    return cudaGetLastError();
+  };
+  switch (mode) {
+    case kBF16d128: return go(gram2_kernel<128>, Gram2Layout<128>::SMEM);
+    case kBF16d64: return go(gram2_kernel<64>, Gram2Layout<64>::SMEM);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 int gram_smem(OperandMode mode) {
   switch (mode) {
-    case kBF16d128: return Gram2Layout<128>::SMEM;
-    case kBF16d64: return Gram2Layout<64>::SMEM;
+    case kBF16d128:
+      return Gram2Layout<128>::SMEM > Gram3Layout<128>::SMEM ? Gram2Layout<128>::SMEM
+                                                              : Gram3Layout<128>::SMEM;
+    case kBF16d64:
+      return Gram2Layout<64>::SMEM > Gram3Layout<64>::SMEM ? Gram2Layout<64>::SMEM
+                                                            : Gram3Layout<64>::SMEM;
     case kSplitF16d64: return GramLayout<192, 64, 1>::SMEM;
   }
   return 0;

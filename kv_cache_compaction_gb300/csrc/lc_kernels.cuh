@@ -59,6 +59,7 @@ struct GramParams {
   float* cpart;            // [nsplit][H][t_pad] or null
   float* Rpart;            // [nsplit][H][t_pad][d_v] or null
   int d_v;
+  int r_only;              // launch holds only the R CTAs (blockIdx.x = key block)
   uint32_t* err;
 };
 
@@ -84,6 +85,14 @@ cudaError_t launch_key_scores(OperandMode mode, const CUtensorMap& mK, const CUt
 cudaError_t launch_gram(OperandMode mode, bool with_r, const CUtensorMap& mKc,
                         const CUtensorMap& mQ, const CUtensorMap& mOhi, const CUtensorMap& mOlo,
                         const GramParams& p, int H, int nsplit, cudaStream_t st);
+// All three key-block pairs of a 256-key system in one CTA per (head, split)
+// (bf16 operand modes, nblk == 2): G and c only.
+cudaError_t launch_gram_all_pairs(OperandMode mode, const CUtensorMap& mKc, const CUtensorMap& mQ,
+                                  const GramParams& p, int H, int nsplit, cudaStream_t st);
+// R CTAs only (bf16 operand modes).
+cudaError_t launch_gram_r(OperandMode mode, const CUtensorMap& mKc, const CUtensorMap& mQ,
+                          const CUtensorMap& mOhi, const CUtensorMap& mOlo, const GramParams& p,
+                          int H, int nsplit, cudaStream_t st);
 cudaError_t launch_compact_lse(OperandMode mode, const CUtensorMap& mQ, const CUtensorMap& mKc,
                                const CompactLseParams& p, int H, cudaStream_t st);
 
