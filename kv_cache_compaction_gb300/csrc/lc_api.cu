@@ -146,7 +146,7 @@ Plan make_plan(const lc_shape* s) {
     // long CTAs: at most two waves of a 160-SM device
     const int cap = std::max(1, std::min(max_split(p.H, 1, slabs), 320 / p.H));
     p.g5_max = p.g7_max = cap;
-    p.r_max = max_split(p.nblk * p.H, 1, slabs);
+    p.r_max = cap;
   } else {
     p.g5_max = max_split(npairs * p.H, 1, slabs);
     p.g7_max = p.r_max = max_split((npairs + p.nblk) * p.H, 1, slabs);
@@ -438,7 +438,7 @@ lc_status run_fit(const Ctx& c, const void* qop, const void* kop, const void* V,
   const int g5_split = split_of((p.all_pairs ? 1 : npairs) * p.H, p.g5_max, &g5_slabs);
   const int g7_split =
       split_of((p.all_pairs ? 1 : npairs + p.nblk) * p.H, p.g7_max, &g7_slabs);
-  const int r_split = p.all_pairs ? split_of(p.nblk * p.H, p.r_max, &r_slabs) : g7_split;
+  const int r_split = p.all_pairs ? split_of(p.H, p.r_max, &r_slabs) : g7_split;
   GramParams g{};
   g.n_q_pad = p.n_q_pad;
   g.n_q = p.n_q;
@@ -457,7 +457,7 @@ lc_status run_fit(const Ctx& c, const void* qop, const void* kop, const void* V,
   {
     LC_PROF(c, "gram_mass", 1);
     if (p.all_pairs)
-      LC_CUDA(launch_gram_all_pairs(p.mode, mKc, mQ64, g, p.H, g5_split, c.st));
+      LC_CUDA(launch_gram_all_pairs(p.mode, mKc, mQ64, mOhi, mOlo, g, p.H, g5_split, c.st));
     else
       LC_CUDA(launch_gram(p.mode, false, mKc, mQ64, mOhi, mOlo, g, p.H, g5_split, c.st));
   }
@@ -515,7 +515,7 @@ lc_status run_fit(const Ctx& c, const void* qop, const void* kop, const void* V,
   if (p.all_pairs) {
     {
       LC_PROF(c, "gram_out", 1);
-      LC_CUDA(launch_gram_all_pairs(p.mode, mKc, mQ64, g, p.H, g7_split, c.st));
+      LC_CUDA(launch_gram_all_pairs(p.mode, mKc, mQ64, mOhi, mOlo, g, p.H, g7_split, c.st));
     }
     GramParams gr = g;
     gr.r_only = 1;

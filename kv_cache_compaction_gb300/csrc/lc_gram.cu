@@ -20,6 +20,8 @@
 //   [npairs, npairs+nblk) R[bi] = E_bi O (output fit only).
 // blockIdx.z splits the query slabs; partial sums are reduced afterwards in
 // a fixed order.
+#include <algorithm>
+
 #include "lc_common.cuh"
 #include "lc_kernels.cuh"
 
@@ -686,57 +688,74 @@ __global__ void __launch_bounds__(320, 1)
   if (warp == 1) tmem_dealloc(tbase, 512);
 }
 
-// All pairs of a two-block (256-key) system in one CTA: the scores of a query
-// slab are formed once for both key blocks (S at TMEM columns 0 and 64), E
-// once per block by eight epilogue warps (one per key row of each block), and
-// the three Gram blocks G00, G01, G11 accumulate at TMEM columns 128, 256 and
-// 384.  Compared with one CTA per pair, each slab's scores and E are computed
-// once instead of twice.  Warps: 0 TMA, 1 MMA issue, 2..9 E rows (warp w holds
-// key rows 32 (w % 4) .. +31 of block (w - 2) / 4, the TMEM lanes it may
-// access).  Shared memory: C_k of both blocks, a 2-stage ring of query slabs,
-// E[2] (hi and lo of both blocks).
-template <int D>
+// Both key blocks of a 256-key system in one CTA per (head, query range): the
+// scores of a query slab are formed once for both blocks (S at TMEM columns 0
+// and 64) and E once per block by eight epilogue warps (warp w holds key rows
+// 32 (w % 4) .. +31 of block (w - 2) / 4, the TMEM lanes it may access).
+// Gram mode accumulates G00, G01 and G11 at TMEM columns 128, 256 and 384
+// (and c for the mass system); R mode accumulates R_b = E_b O at columns
+// 128 + 128 b.  Compared with one CTA per block pair each slab's scores and E
+// are formed once instead of twice.  Warps: 0 TMA, 1 MMA issue, 2..9 E rows.
+// Shared memory: C_k of both blocks, 2-stage rings of query slabs, of O slabs
+// (R mode) and of per-query row data, and E (two buffers in Gram mode, one in
+// R mode).
+template <int D, bool RM>
 struct Gram3Layout {
   static constexpr int NC = D / 64;
   static constexpr int KC_BYTES = 128 * D * 2;
   static constexpr int QCHUNK = kSL * 128;
   static constexpr int Q_BYTES = NC * QCHUNK;
+  static constexpr int O_BYTES = RM ? 2 * NC * QCHUNK : 0;  // hi + lo
   static constexpr int E_BLK = 128 * 128;  // 128 keys x 64 queries, fp16
+  static constexpr int NE = RM ? 1 : 2;    // E buffers
   static constexpr int OFF_RING = 2 * KC_BYTES;
-  static constexpr int OFF_E = OFF_RING + 2 * Q_BYTES;
-  static constexpr int OFF_BAR = OFF_E + 2 * 4 * E_BLK;
+  static constexpr int OFF_O = OFF_RING + 2 * Q_BYTES;
+  static constexpr int OFF_E = OFF_O + 2 * O_BYTES;
+  static constexpr int OFF_ROWS = OFF_E + NE * 4 * E_BLK;
+  static constexpr int ROW_STAGE = 2 * kSL * 4;  // row shift + row mass
+  static constexpr int OFF_BAR = OFF_ROWS + 2 * ROW_STAGE;
   static constexpr int SMEM = 1024 + OFF_BAR + 256;
 };
 
-template <int D>
+template <int D, bool RM>
 __global__ void __launch_bounds__(320, 1)
     gram3_kernel(const __grid_constant__ CUtensorMap mKc, const __grid_constant__ CUtensorMap mQ,
-                 const GramParams p) {
-  using L = Gram3Layout<D>;
+                 const __grid_constant__ CUtensorMap mOhi,
+                 const __grid_constant__ CUtensorMap mOlo, const GramParams p) {
+  using L = Gram3Layout<D, RM>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = align1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + L::OFF_BAR);
   uint64_t* k_full = bars + 0;
-  uint64_t* st_full = bars + 1;   // [2]
+  uint64_t* st_full = bars + 1;   // [2] query slab
   uint64_t* st_empty = bars + 3;  // [2]
-  uint64_t* s_full = bars + 5;
-  uint64_t* s_free = bars + 6;
-  uint64_t* e_full = bars + 7;    // [2]
-  uint64_t* e_free = bars + 9;    // [2]
-  uint64_t* done = bars + 11;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 12);
+  uint64_t* o_full = bars + 5;    // [2] O slab (R mode)
+  uint64_t* o_empty = bars + 7;   // [2]
+  uint64_t* r_full = bars + 9;    // [2] row data
+  uint64_t* r_empty = bars + 11;  // [2]
+  uint64_t* s_full = bars + 13;
+  uint64_t* s_free = bars + 14;
+  uint64_t* e_full = bars + 15;   // [2]
+  uint64_t* e_free = bars + 17;   // [2]
+  uint64_t* done = bars + 19;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 20);
   __shared__ volatile int abort_flag;
 
   const int warp = warp_id(), lane = lane_id();
   const int h = blockIdx.y, z = blockIdx.z;
-  const bool with_c = p.row_b != nullptr;
+  const bool with_c = !RM && p.row_b != nullptr;
   const int total_slabs = p.n_q_pad / kSL;
   const int s0 = z * p.slabs_per_split;
   const int nsl = max(0, min(total_slabs, s0 + p.slabs_per_split) - s0);
   uint8_t* sK0 = base;
   uint8_t* sK1 = base + L::KC_BYTES;
   uint8_t* sRing = base + L::OFF_RING;
+  uint8_t* sO = base + L::OFF_O;
   uint8_t* sE = base + L::OFF_E;
+  float* sRows = reinterpret_cast<float*>(base + L::OFF_ROWS);
+  // E buffer of slab i and the phase of its barriers
+  auto ebuf = [](int i) { return RM ? 0 : (i & 1); };
+  auto ephase = [](int i) { return static_cast<uint32_t>(RM ? (i & 1) : ((i >> 1) & 1)); };
 
   if (threadIdx.x == 0) {
     abort_flag = launch_aborted(p.err) ? 1 : 0;
@@ -746,6 +765,10 @@ __global__ void __launch_bounds__(320, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&st_full[i], 1);
       mbar_init(&st_empty[i], 1);
+      mbar_init(&o_full[i], 1);
+      mbar_init(&o_empty[i], 1);
+      mbar_init(&r_full[i], 1);
+      mbar_init(&r_empty[i], 256);
       mbar_init(&e_full[i], 256);
       mbar_init(&e_free[i], 1);
     }
@@ -765,30 +788,57 @@ __global__ void __launch_bounds__(320, 1)
         tma_load_3d(sK0 + c * 128 * 128, &mKc, k_full, 64 * c, 0, h);
         tma_load_3d(sK1 + c * 128 * 128, &mKc, k_full, 64 * c, 128, h);
       }
-      int issued = 0;
+      // per slab: query slab, row data, O slab -- each stage refilled once
+      // its consumers (scores / E / R products of slab i - 2) are done
+      int nq = 0, nr = 0, no = 0;  // slabs whose copies are issued, per kind
       for (int i = 0; i < nsl; ++i) {
         const int s = i & 1;
-        if (i >= 2 && !wait_bar(&st_empty[s], ((i >> 1) - 1) & 1, &abort_flag, p.err)) break;
-        uint8_t* st = sRing + s * L::Q_BYTES;
+        const uint32_t ph = ((i >> 1) - 1) & 1;
         const int r0 = (s0 + i) * kSL;
+        if (i >= 2 && !wait_bar(&st_empty[s], ph, &abort_flag, p.err)) break;
+        uint8_t* st = sRing + s * L::Q_BYTES;
         mbar_arrive_expect_tx(&st_full[s], L::Q_BYTES);
         for (int c = 0; c < L::NC; ++c)
           tma_load_3d(st + c * L::QCHUNK, &mQ, &st_full[s], 64 * c, r0, h);
-        issued = i + 1;
-      }
-      if (abort_flag) {
-        for (int i = (issued > 2 ? issued - 2 : 0); i < issued; ++i) {
-          const uint64_t t0 = globaltimer_ns();
-          while (!mbar_try_wait(&st_full[i & 1], (i >> 1) & 1) &&
-                 globaltimer_ns() - t0 < kWaitLimitNs) {
+        nq = i + 1;
+        if (i >= 2 && !wait_bar(&r_empty[s], ph, &abort_flag, p.err)) break;
+        const size_t roff = static_cast<size_t>(h) * p.n_q_pad + r0;
+        float* rw = sRows + s * (L::ROW_STAGE / 4);
+        mbar_arrive_expect_tx(&r_full[s], (with_c ? 2 : 1) * kSL * 4);
+        bulk_g2s(rw, p.rowsh2 + roff, kSL * 4, &r_full[s]);
+        if (with_c) bulk_g2s(rw + kSL, p.row_b + roff, kSL * 4, &r_full[s]);
+        nr = i + 1;
+        if (RM) {
+          if (i >= 2 && !wait_bar(&o_empty[s], ph, &abort_flag, p.err)) break;
+          uint8_t* so = sO + s * L::O_BYTES;
+          mbar_arrive_expect_tx(&o_full[s], L::O_BYTES);
+          for (int c = 0; c < L::NC; ++c) {
+            tma_load_3d(so + c * L::QCHUNK, &mOhi, &o_full[s], 64 * c, r0, h);
+            tma_load_3d(so + (L::NC + c) * L::QCHUNK, &mOlo, &o_full[s], 64 * c, r0, h);
           }
         }
+        no = RM ? i + 1 : 0;
+      }
+      if (abort_flag) {
+        // let the copies in flight land before the CTA exits
+        auto drain = [&](uint64_t* full, int n) {
+          for (int i = (n > 2 ? n - 2 : 0); i < n; ++i) {
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(&full[i & 1], (i >> 1) & 1) &&
+                   globaltimer_ns() - t0 < kWaitLimitNs) {
+            }
+          }
+        };
+        drain(st_full, nq);
+        drain(r_full, nr);
+        drain(o_full, no);
       }
     }
   } else if (warp == 1) {
     if (lane == 0 && nsl > 0) {
       constexpr uint32_t idesc_s = idesc_f16(128, kSL, true, false, false);
       constexpr uint32_t idesc_g = idesc_f16(128, 128, false, false, false);
+      constexpr uint32_t idesc_r = idesc_f16(128, D, false, false, true);
       bool ok = wait_bar(k_full, 0, &abort_flag, p.err);
       auto issue_s = [&](int i) {  // scores of slab i for both key blocks
         const int s = i & 1;
@@ -806,33 +856,57 @@ __global__ void __launch_bounds__(320, 1)
         umma_commit(&st_empty[s]);
         umma_commit(s_full);
       };
-      auto issue_g = [&](int i) {  // G00, G01, G11 products of slab i
-        const int b = i & 1;
+      auto issue_g = [&](int i) {  // Gram blocks (or R) of slab i
         tc_fence_after();
-        const uint32_t eb = smem_u32(sE + b * 4 * L::E_BLK);
+        const uint32_t eb = smem_u32(sE + ebuf(i) * 4 * L::E_BLK);
         const uint32_t e0h = eb, e0l = eb + L::E_BLK;
         const uint32_t e1h = eb + 2 * L::E_BLK, e1l = eb + 3 * L::E_BLK;
+        if constexpr (!RM) {
 #pragma unroll
-        for (int k = 0; k < kSL / 16; ++k) {
-          const uint32_t o = k * 32;
-          const uint32_t acc0 = (i > 0 || k > 0) ? 1u : 0u;
-          const uint64_t a0h = sdesc_sw128(e0h + o, 16, 1024), a0l = sdesc_sw128(e0l + o, 16, 1024);
-          const uint64_t a1h = sdesc_sw128(e1h + o, 16, 1024), a1l = sdesc_sw128(e1l + o, 16, 1024);
-          umma_f16_ss(tbase + 128, a0h, a0h, idesc_g, acc0);
-          umma_f16_ss(tbase + 128, a0h, a0l, idesc_g, 1u);
-          umma_f16_ss(tbase + 128, a0l, a0h, idesc_g, 1u);
-          umma_f16_ss(tbase + 256, a0h, a1h, idesc_g, acc0);
-          umma_f16_ss(tbase + 256, a0h, a1l, idesc_g, 1u);
-          umma_f16_ss(tbase + 256, a0l, a1h, idesc_g, 1u);
-          umma_f16_ss(tbase + 384, a1h, a1h, idesc_g, acc0);
-          umma_f16_ss(tbase + 384, a1h, a1l, idesc_g, 1u);
-          umma_f16_ss(tbase + 384, a1l, a1h, idesc_g, 1u);
+          for (int k = 0; k < kSL / 16; ++k) {
+            const uint32_t o = k * 32;
+            const uint32_t acc0 = (i > 0 || k > 0) ? 1u : 0u;
+            const uint64_t a0h = sdesc_sw128(e0h + o, 16, 1024);
+            const uint64_t a0l = sdesc_sw128(e0l + o, 16, 1024);
+            const uint64_t a1h = sdesc_sw128(e1h + o, 16, 1024);
+            const uint64_t a1l = sdesc_sw128(e1l + o, 16, 1024);
+            umma_f16_ss(tbase + 128, a0h, a0h, idesc_g, acc0);
+            umma_f16_ss(tbase + 128, a0h, a0l, idesc_g, 1u);
+            umma_f16_ss(tbase + 128, a0l, a0h, idesc_g, 1u);
+            umma_f16_ss(tbase + 256, a0h, a1h, idesc_g, acc0);
+            umma_f16_ss(tbase + 256, a0h, a1l, idesc_g, 1u);
+            umma_f16_ss(tbase + 256, a0l, a1h, idesc_g, 1u);
+            umma_f16_ss(tbase + 384, a1h, a1h, idesc_g, acc0);
+            umma_f16_ss(tbase + 384, a1h, a1l, idesc_g, 1u);
+            umma_f16_ss(tbase + 384, a1l, a1h, idesc_g, 1u);
+          }
+        } else {
+          const uint32_t aO = smem_u32(sO + (i & 1) * L::O_BYTES);
+          const uint32_t aOl = aO + L::NC * L::QCHUNK;
+#pragma unroll
+          for (int k = 0; k < kSL / 16; ++k) {
+            const uint32_t o = k * 32;
+            const uint32_t acc0 = (i > 0 || k > 0) ? 1u : 0u;
+            const uint64_t doh = sdesc_sw128(aO + k * 2048, L::QCHUNK, 1024);
+            const uint64_t dol = sdesc_sw128(aOl + k * 2048, L::QCHUNK, 1024);
+            const uint64_t a0h = sdesc_sw128(e0h + o, 16, 1024);
+            const uint64_t a0l = sdesc_sw128(e0l + o, 16, 1024);
+            const uint64_t a1h = sdesc_sw128(e1h + o, 16, 1024);
+            const uint64_t a1l = sdesc_sw128(e1l + o, 16, 1024);
+            umma_f16_ss(tbase + 128, a0h, doh, idesc_r, acc0);
+            umma_f16_ss(tbase + 128, a0h, dol, idesc_r, 1u);
+            umma_f16_ss(tbase + 128, a0l, doh, idesc_r, 1u);
+            umma_f16_ss(tbase + 256, a1h, doh, idesc_r, acc0);
+            umma_f16_ss(tbase + 256, a1h, dol, idesc_r, 1u);
+            umma_f16_ss(tbase + 256, a1l, doh, idesc_r, 1u);
+          }
+          umma_commit(&o_empty[i & 1]);
         }
-        umma_commit(&e_free[b]);
+        umma_commit(&e_free[ebuf(i)]);
       };
       // Event loop: a slab's scores are issued once its query slab is loaded
-      // and the previous scores have been read; its Gram products once its E
-      // is formed.
+      // and the previous scores have been read; its products once its E (and
+      // in R mode its O slab) is ready.
       int ns = 0, ng = 0;
       uint64_t t_last = globaltimer_ns();
       uint32_t spins = 0;
@@ -841,7 +915,8 @@ __global__ void __launch_bounds__(320, 1)
             (ns == 0 || mbar_test_wait(s_free, (ns - 1) & 1))) {
           issue_s(ns++);
           t_last = globaltimer_ns();
-        } else if (ng < ns && mbar_test_wait(&e_full[ng & 1], (ng >> 1) & 1)) {
+        } else if (ng < ns && mbar_test_wait(&e_full[ebuf(ng)], ephase(ng)) &&
+                   (!RM || mbar_test_wait(&o_full[ng & 1], (ng >> 1) & 1))) {
           issue_g(ng++);
           t_last = globaltimer_ns();
         } else if ((++spins & 63u) == 0) {
@@ -870,50 +945,38 @@ __global__ void __launch_bounds__(320, 1)
     float cacc = 0.f;
     bool ok = nsl > 0;
     for (int i = 0; ok && i < nsl; ++i) {
-      const size_t roff = static_cast<size_t>(h) * p.n_q_pad + static_cast<size_t>(s0 + i) * kSL;
-      const float* rs = p.rowsh2 + roff;
-      const float* rb = with_c ? p.row_b + roff : rs;
-      asm volatile("prefetch.global.L1 [%0];" ::"l"(rs));
-      asm volatile("prefetch.global.L1 [%0];" ::"l"(rs + 32));
-      if (with_c) {
-        asm volatile("prefetch.global.L1 [%0];" ::"l"(rb));
-        asm volatile("prefetch.global.L1 [%0];" ::"l"(rb + 32));
-      }
+      if (!wait_bar(&r_full[i & 1], (i >> 1) & 1, &abort_flag, p.err)) { ok = false; break; }
       if (!wait_bar(s_full, i & 1, &abort_flag, p.err)) { ok = false; break; }
       tc_fence_after();
-      uint8_t* sEh = sE + (i & 1) * 4 * L::E_BLK + b * 2 * L::E_BLK;
+      const float* rs = sRows + (i & 1) * (L::ROW_STAGE / 4);
+      const float* rb = rs + kSL;
+      uint8_t* sEh = sE + ebuf(i) * 4 * L::E_BLK + b * 2 * L::E_BLK;
       uint8_t* sEl = sEh + L::E_BLK;
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {  // 32 query columns at a time
-        float4 sh4[8], b4[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) sh4[u] = __ldg(reinterpret_cast<const float4*>(rs + hf * 32) + u);
-        if (with_c) {
-#pragma unroll
-          for (int u = 0; u < 8; ++u) b4[u] = __ldg(reinterpret_cast<const float4*>(rb + hf * 32) + u);
-        }
         float x[32];
         tmem_ld32(tbase + b * 64 + hf * 32 + lane_off, x);
         if (hf == 1) {
           tc_fence_before();
           mbar_arrive(s_free);
-        } else if (i >= 2 && !wait_bar(&e_free[i & 1], ((i >> 1) - 1) & 1, &abort_flag, p.err)) {
+        } else if (i >= (RM ? 1 : 2) &&
+                   !wait_bar(&e_free[ebuf(i)], ephase(i) ^ 1u, &abort_flag, p.err)) {
           ok = false;
           break;
         }
 #pragma unroll
         for (int q8 = 0; q8 < 4; ++q8) {
           const int c8 = hf * 4 + q8;
-          const float sh8[8] = {sh4[2 * q8].x, sh4[2 * q8].y, sh4[2 * q8].z, sh4[2 * q8].w,
-                                sh4[2 * q8 + 1].x, sh4[2 * q8 + 1].y, sh4[2 * q8 + 1].z,
-                                sh4[2 * q8 + 1].w};
+          const float4 sa = *reinterpret_cast<const float4*>(rs + c8 * 8);
+          const float4 sb = *reinterpret_cast<const float4*>(rs + c8 * 8 + 4);
+          const float sh8[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
           float e8[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) e8[e] = ex2(fmaf(x[q8 * 8 + e], s2, cb) - sh8[e]);
           if (with_c) {
-            const float b8[8] = {b4[2 * q8].x, b4[2 * q8].y, b4[2 * q8].z, b4[2 * q8].w,
-                                 b4[2 * q8 + 1].x, b4[2 * q8 + 1].y, b4[2 * q8 + 1].z,
-                                 b4[2 * q8 + 1].w};
+            const float4 ba = *reinterpret_cast<const float4*>(rb + c8 * 8);
+            const float4 bb = *reinterpret_cast<const float4*>(rb + c8 * 8 + 4);
+            const float b8[8] = {ba.x, ba.y, ba.z, ba.w, bb.x, bb.y, bb.z, bb.w};
 #pragma unroll
             for (int e = 0; e < 8; ++e) cacc = fmaf(e8[e], b8[e], cacc);
           }
@@ -925,35 +988,38 @@ __global__ void __launch_bounds__(320, 1)
         }
       }
       if (!ok) break;
+      mbar_arrive(&r_empty[i & 1]);
       fence_async_smem();
       tc_fence_before();
-      mbar_arrive(&e_full[i & 1]);
+      mbar_arrive(&e_full[ebuf(i)]);
     }
-    // publish G00 / G11 (own block), half of G01 (block-0 rows), and c
+    // publish: Gram mode G00 / G11 (own block), half of G01 (block-0 rows)
+    // and c; R mode the block's R rows
     if (ok && nsl > 0 && wait_bar(done, 0, &abort_flag, p.err)) {
       tc_fence_after();
       const int H = gridDim.y;
       const size_t zh = static_cast<size_t>(z) * H + h;
       const int key = b * 128 + j;
-      float* dst = p.Gpart + (zh * p.t_pad + key) * p.t_pad + b * 128;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      auto put32 = [&](uint32_t tcol, float* dst) {
         float v[32];
-        tmem_ld32(tbase + 128 + b * 256 + c * 32 + lane_off, v);
-        float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+        tmem_ld32(tbase + tcol + lane_off, v);
+        float4* d4 = reinterpret_cast<float4*>(dst);
 #pragma unroll
         for (int e = 0; e < 8; ++e) d4[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
-      }
-      float* dst01 = p.Gpart + (zh * p.t_pad + j) * p.t_pad + 128 + b * 64;
+      };
+      if constexpr (!RM) {
+        float* dst = p.Gpart + (zh * p.t_pad + key) * p.t_pad + b * 128;
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        float v[32];
-        tmem_ld32(tbase + 256 + b * 64 + c * 32 + lane_off, v);
-        float4* d4 = reinterpret_cast<float4*>(dst01 + c * 32);
+        for (int c = 0; c < 4; ++c) put32(128 + b * 256 + c * 32, dst + c * 32);
+        float* dst01 = p.Gpart + (zh * p.t_pad + j) * p.t_pad + 128 + b * 64;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) d4[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+        for (int c = 0; c < 2; ++c) put32(256 + b * 64 + c * 32, dst01 + c * 32);
+        if (with_c) p.cpart[zh * p.t_pad + key] = cacc;
+      } else {
+        float* dst = p.Rpart + (zh * p.t_pad + key) * D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) put32(128 + b * 128 + c * 32, dst + c * 32);
       }
-      if (with_c) p.cpart[zh * p.t_pad + key] = cacc;
     }
   }
   tc_fence_before();
@@ -1004,17 +1070,18 @@ cudaError_t launch_gram(OperandMode mode, bool with_r, const CUtensorMap& mKc,
 }
 
 cudaError_t launch_gram_all_pairs(OperandMode mode, const CUtensorMap& mKc, const CUtensorMap& mQ,
+                                  const CUtensorMap& mOhi, const CUtensorMap& mOlo,
                                   const GramParams& p, int H, int nsplit, cudaStream_t st) {
-  if (p.nblk != 2 || p.r_only) return cudaErrorInvalidValue;
+  if (p.nblk != 2) return cudaErrorInvalidValue;
   auto go = [&](auto kern, int smem) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    kern<<<dim3(1, H, nsplit), 320, smem, st>>>(mKc, mQ, p);
+    kern<<<dim3(1, H, nsplit), 320, smem, st>>>(mKc, mQ, mOhi, mOlo, p);
     return cudaGetLastError();
   };
   switch (mode) {
-    case kBF16d128: return go(gram3_kernel<128>, Gram3Layout<128>::SMEM);
-    case kBF16d64: return go(gram3_kernel<64>, Gram3Layout<64>::SMEM);
+    case kBF16d128: return go(gram3_kernel<128, false>, Gram3Layout<128, false>::SMEM);
+    case kBF16d64: return go(gram3_kernel<64, false>, Gram3Layout<64, false>::SMEM);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -1022,16 +1089,16 @@ cudaError_t launch_gram_all_pairs(OperandMode mode, const CUtensorMap& mKc, cons
 cudaError_t launch_gram_r(OperandMode mode, const CUtensorMap& mKc, const CUtensorMap& mQ,
                           const CUtensorMap& mOhi, const CUtensorMap& mOlo, const GramParams& p,
                           int H, int nsplit, cudaStream_t st) {
-  if (!p.r_only || !p.Rpart) return cudaErrorInvalidValue;
+  if (p.nblk != 2 || !p.Rpart) return cudaErrorInvalidValue;
   auto go = [&](auto kern, int smem) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    kern<<<dim3(p.nblk, H, nsplit), 320, smem, st>>>(mKc, mQ, mOhi, mOlo, p);
+    kern<<<dim3(1, H, nsplit), 320, smem, st>>>(mKc, mQ, mOhi, mOlo, p);
     return cudaGetLastError();
   };
   switch (mode) {
-    case kBF16d128: return go(gram2_kernel<128>, Gram2Layout<128>::SMEM);
-    case kBF16d64: return go(gram2_kernel<64>, Gram2Layout<64>::SMEM);
+    case kBF16d128: return go(gram3_kernel<128, true>, Gram3Layout<128, true>::SMEM);
+    case kBF16d64: return go(gram3_kernel<64, true>, Gram3Layout<64, true>::SMEM);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -1039,11 +1106,11 @@ cudaError_t launch_gram_r(OperandMode mode, const CUtensorMap& mKc, const CUtens
 int gram_smem(OperandMode mode) {
   switch (mode) {
     case kBF16d128:
-      return Gram2Layout<128>::SMEM > Gram3Layout<128>::SMEM ? Gram2Layout<128>::SMEM
-                                                              : Gram3Layout<128>::SMEM;
+      return std::max({Gram2Layout<128>::SMEM, Gram3Layout<128, false>::SMEM,
+                       Gram3Layout<128, true>::SMEM});
     case kBF16d64:
-      return Gram2Layout<64>::SMEM > Gram3Layout<64>::SMEM ? Gram2Layout<64>::SMEM
-                                                            : Gram3Layout<64>::SMEM;
+      return std::max({Gram2Layout<64>::SMEM, Gram3Layout<64, false>::SMEM,
+                       Gram3Layout<64, true>::SMEM});
     case kSplitF16d64: return GramLayout<192, 64, 1>::SMEM;
   }
   return 0;

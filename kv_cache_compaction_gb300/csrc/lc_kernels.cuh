@@ -85,11 +85,12 @@ cudaError_t launch_key_scores(OperandMode mode, const CUtensorMap& mK, const CUt
 cudaError_t launch_gram(OperandMode mode, bool with_r, const CUtensorMap& mKc,
                         const CUtensorMap& mQ, const CUtensorMap& mOhi, const CUtensorMap& mOlo,
                         const GramParams& p, int H, int nsplit, cudaStream_t st);
-// All three key-block pairs of a 256-key system in one CTA per (head, split)
-// (bf16 operand modes, nblk == 2): G and c only.
+// Both key blocks of a 256-key system in one CTA per (head, split) (bf16
+// operand modes, nblk == 2): all three Gram blocks (and c) ...
 cudaError_t launch_gram_all_pairs(OperandMode mode, const CUtensorMap& mKc, const CUtensorMap& mQ,
+                                  const CUtensorMap& mOhi, const CUtensorMap& mOlo,
                                   const GramParams& p, int H, int nsplit, cudaStream_t st);
-// R CTAs only (bf16 operand modes).
+// ... or R for both blocks.
 cudaError_t launch_gram_r(OperandMode mode, const CUtensorMap& mKc, const CUtensorMap& mQ,
                           const CUtensorMap& mOhi, const CUtensorMap& mOlo, const GramParams& p,
                           int H, int nsplit, cudaStream_t st);
