@@ -504,7 +504,13 @@ lc_status run_fit(const Ctx& c, const void* qop, const void* kop, const void* V,
   cl.err = c.h->d_err;
   {
     LC_PROF(c, "compact_lse", 1);
-    LC_CUDA(launch_compact_lse(p.mode, mQ128, mKc, cl, p.H, c.st));
+    if (p.bf16_in && p.nblk <= 2) {
+      const int ntiles = p.n_q_pad / 128;
+      const int sp = best_split(p.H, c.h->sm_count, 1, ntiles);
+      LC_CUDA(launch_compact_lse_resident(p.mode, mQ128, mKc, cl, p.H, sp, c.st));
+    } else {
+      LC_CUDA(launch_compact_lse(p.mode, mQ128, mKc, cl, p.H, c.st));
+    }
   }
   g.slabs_per_split = g7_slabs;
   g.rowsh2 = c.at<float>(p.lc2);

@@ -96,6 +96,11 @@ cudaError_t launch_gram_r(OperandMode mode, const CUtensorMap& mKc, const CUtens
                           int H, int nsplit, cudaStream_t st);
 cudaError_t launch_compact_lse(OperandMode mode, const CUtensorMap& mQ, const CUtensorMap& mKc,
                                const CompactLseParams& p, int H, cudaStream_t st);
+// bf16 operand modes with t_pad <= 256: C_k resident, persistent over query
+// tiles (grid nsplit x H).
+cudaError_t launch_compact_lse_resident(OperandMode mode, const CUtensorMap& mQ,
+                                        const CUtensorMap& mKc, const CompactLseParams& p, int H,
+                                        int nsplit, cudaStream_t st);
 
 // Kernel shared-memory sizes (for the host's capability check).
 int attn_stats_smem(OperandMode mode);
