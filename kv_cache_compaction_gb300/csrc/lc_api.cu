@@ -461,13 +461,11 @@ lc_status run_fit(const Ctx& c, const void* qop, const void* kop, const void* V,
     else
       LC_CUDA(launch_gram(p.mode, false, mKc, mQ64, mOhi, mOlo, g, p.H, g5_split, c.st));
   }
-  const size_t tt = static_cast<size_t>(p.t_pad) * p.t_pad;
   {
-    LC_PROF(c, "reduce_mass", 3);
-    LC_CUDA(launch_reduce_partials(c.at<float>(p.gpart), c.at<float>(p.G), g5_split, H * tt, c.st));
+    LC_PROF(c, "reduce_mass", 2);
+    LC_CUDA(launch_reduce_gram(c.at<float>(p.gpart), c.at<float>(p.G), g5_split, p.H, p.t_pad, c.st));
     LC_CUDA(launch_reduce_partials(c.at<float>(p.cpart), c.at<float>(p.c), g5_split, H * p.t_pad,
                                    c.st));
-    LC_CUDA(launch_symmetrize(c.at<float>(p.G), p.H, p.t_pad, c.st));
   }
   SolveParams sp{};
   sp.H = p.H;
@@ -533,11 +531,10 @@ lc_status run_fit(const Ctx& c, const void* qop, const void* kop, const void* V,
     LC_CUDA(launch_gram(p.mode, true, mKc, mQ64, mOhi, mOlo, g, p.H, g7_split, c.st));
   }
   {
-    LC_PROF(c, "reduce_out", 4);
-    LC_CUDA(launch_reduce_partials(c.at<float>(p.hpart), c.at<float>(p.Hm), g7_split, H * tt, c.st));
+    LC_PROF(c, "reduce_out", 3);
+    LC_CUDA(launch_reduce_gram(c.at<float>(p.hpart), c.at<float>(p.Hm), g7_split, p.H, p.t_pad, c.st));
     LC_CUDA(launch_reduce_partials(c.at<float>(p.rpart), c.at<float>(p.R), r_split,
                                    H * p.t_pad * p.d, c.st));
-    LC_CUDA(launch_symmetrize(c.at<float>(p.Hm), p.H, p.t_pad, c.st));
     LC_CUDA(launch_gather_v(V, p.bf16_in ? 0 : 1, idx, c.at<float>(p.vc), p.H, p.T, p.t, p.t_pad,
                             p.d, c.st));
   }

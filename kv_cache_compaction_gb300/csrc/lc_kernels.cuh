@@ -130,6 +130,10 @@ cudaError_t launch_gather_v(const void* V, int in_dtype, const int32_t* idx, flo
 cudaError_t launch_reduce_partials(const float* part, float* out, int nsplit, size_t n,
                                    cudaStream_t st);
 cudaError_t launch_symmetrize(float* G, int H, int t_pad, cudaStream_t st);
+// Split-partial sum of a symmetric system built as its upper block triangle,
+// written symmetric (fused sum and transpose).
+cudaError_t launch_reduce_gram(const float* part, float* out, int nsplit, int H, int t_pad,
+                               cudaStream_t st);
 cudaError_t launch_mass_rows(const float* rowmax_pad, const float* lse_pad, float* rowsh2,
                              float* row_b, int H, int n_q, int n_q_pad, cudaStream_t st);
 cudaError_t launch_fill_colb2(float* colb2, int H, int t, int t_pad, cudaStream_t st);

@@ -370,32 +370,115 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* tmp, int& total)
   return before_warp + x - v;
 }
 
+// One CTA per head.  CPT > 0: thread i holds codes [CPT i, CPT i + CPT) in
+// registers (T <= 1024 CPT); CPT == 0: codes are re-read from global memory
+// in each pass.  Four 8-bit radix passes find the code of the t-th largest;
+// equal bins within a thread's run are counted before the shared atomic.
+template <int CPT>
 __global__ void __launch_bounds__(kSelThreads)
     select_topt_kernel(const uint32_t* __restrict__ code, int T, int t, int32_t* __restrict__ idx) {
   __shared__ int hist[256];
   __shared__ int tmp[32];
   __shared__ uint32_t s_prefix;
   __shared__ int s_need;
-  const int h = blockIdx.x, tid = threadIdx.x;
+  const int h = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
   const uint32_t* c = code + static_cast<size_t>(h) * T;
+  constexpr int R = CPT > 0 ? CPT : 1;
+  uint32_t v[R];
+  const int chunk = CPT > 0 ? CPT : (T + kSelThreads - 1) / kSelThreads;
+  const int j0 = min(T, tid * chunk), j1 = min(T, j0 + chunk);
+  if constexpr (CPT > 0) {
+    if (j0 + CPT <= T && CPT % 4 == 0 && (reinterpret_cast<uintptr_t>(c + j0) & 15) == 0) {
+#pragma unroll
+      for (int q = 0; q < CPT / 4; ++q) {
+        const uint4 u = reinterpret_cast<const uint4*>(c + j0)[q];
+        v[4 * q] = u.x;
+        v[4 * q + 1] = u.y;
+        v[4 * q + 2] = u.z;
+        v[4 * q + 3] = u.w;
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < CPT; ++k) v[k] = j0 + k < j1 ? c[j0 + k] : 0u;
+    }
+  }
+  auto get = [&](int k) -> uint32_t {
+    if constexpr (CPT > 0) return v[k];
+    else return c[j0 + k];
+  };
   uint32_t prefix = 0, mask = 0;
   int need = t;  // rank (from the top) still to locate inside the current bucket
   for (int shift = 24; shift >= 0; shift -= 8) {
     for (int b = tid; b < 256; b += kSelThreads) hist[b] = 0;
     __syncthreads();
-    for (int j = tid; j < T; j += kSelThreads) {
-      const uint32_t v = c[j];
-      if ((v & mask) == prefix) atomicAdd(&hist[(v >> shift) & 255u], 1);
-    }
-    __syncthreads();
-    if (tid == 0) {
-      int acc = 0, b = 255;
-      for (; b > 0; --b) {
-        if (acc + hist[b] >= need) break;
-        acc += hist[b];
+    int run_bin = -1, run_cnt = 0;
+    const int n = j1 - j0;
+#pragma unroll
+    for (int k = 0; k < (CPT > 0 ? CPT : 1); ++k) {
+      if constexpr (CPT > 0) {
+        if (k < n) {
+          const uint32_t x = get(k);
+          if ((x & mask) == prefix) {
+            const int bin = static_cast<int>((x >> shift) & 255u);
+            if (bin == run_bin) {
+              ++run_cnt;
+            } else {
+              if (run_cnt) atomicAdd(&hist[run_bin], run_cnt);
+              run_bin = bin;
+              run_cnt = 1;
+            }
+          }
+        }
       }
-      s_prefix = prefix | (static_cast<uint32_t>(b) << shift);
-      s_need = need - acc;
+    }
+    if constexpr (CPT == 0) {
+      for (int k = 0; k < n; ++k) {
+        const uint32_t x = get(k);
+        if ((x & mask) == prefix) {
+          const int bin = static_cast<int>((x >> shift) & 255u);
+          if (bin == run_bin) {
+            ++run_cnt;
+          } else {
+            if (run_cnt) atomicAdd(&hist[run_bin], run_cnt);
+            run_bin = bin;
+            run_cnt = 1;
+          }
+        }
+      }
+    }
+    if (run_cnt) atomicAdd(&hist[run_bin], run_cnt);
+    __syncthreads();
+    if (tid < 32) {
+      // lane l owns bins 255-8l .. 248-8l; locate the bin holding rank `need`
+      // counted from the top
+      int cnt[8], own = 0;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        cnt[k] = hist[255 - 8 * lane - k];
+        own += cnt[k];
+      }
+      int incl = own;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const int excl = incl - own;
+      const uint32_t hit = __ballot_sync(0xffffffffu, incl >= need);
+      const int src = hit ? __ffs(hit) - 1 : 31;
+      if (lane == src) {
+        int acc = excl, b = 255 - 8 * lane - 7;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          if (acc + cnt[k] >= need) {
+            b = 255 - 8 * lane - k;
+            break;
+          }
+          acc += cnt[k];
+        }
+        s_prefix = prefix | (static_cast<uint32_t>(b) << shift);
+        s_need = need - acc;
+      }
     }
     __syncthreads();
     prefix = s_prefix;
@@ -406,13 +489,21 @@ __global__ void __launch_bounds__(kSelThreads)
   // prefix = code of the t-th largest; take all larger codes and the first
   // `need` (lowest-index) codes equal to it.
   const uint32_t tau = prefix;
-  const int chunk = (T + kSelThreads - 1) / kSelThreads;
-  const int j0 = min(T, tid * chunk), j1 = min(T, j0 + chunk);
+  const int n = j1 - j0;
   int gt = 0, eq = 0;
-  for (int j = j0; j < j1; ++j) {
-    const uint32_t v = c[j];
-    gt += v > tau;
-    eq += v == tau;
+  if constexpr (CPT > 0) {
+#pragma unroll
+    for (int k = 0; k < CPT; ++k)
+      if (k < n) {
+        gt += v[k] > tau;
+        eq += v[k] == tau;
+      }
+  } else {
+    for (int k = 0; k < n; ++k) {
+      const uint32_t x = get(k);
+      gt += x > tau;
+      eq += x == tau;
+    }
   }
   int tot;
   const int eq_before = block_exclusive_scan(eq, tmp, tot);
@@ -420,16 +511,37 @@ __global__ void __launch_bounds__(kSelThreads)
   const int out0 = block_exclusive_scan(gt + take_eq, tmp, tot);
   int o = out0, te = 0;
   int32_t* dst = idx + static_cast<size_t>(h) * t;
-  for (int j = j0; j < j1; ++j) {
-    const uint32_t v = c[j];
-    if ((v > tau || (v == tau && te++ < take_eq)) && o < t) dst[o++] = j;
+  if constexpr (CPT > 0) {
+#pragma unroll
+    for (int k = 0; k < CPT; ++k)
+      if (k < n && (v[k] > tau || (v[k] == tau && te++ < take_eq)) && o < t) dst[o++] = j0 + k;
+  } else {
+    for (int k = 0; k < n; ++k) {
+      const uint32_t x = get(k);
+      if ((x > tau || (x == tau && te++ < take_eq)) && o < t) dst[o++] = j0 + k;
+    }
   }
 }
 
 // ------------------------------------------------------------ small kernels
 __global__ void convert_bf16_f16_kernel(const __nv_bfloat16* in, __half* out, size_t n) {
-  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
-       i += static_cast<size_t>(gridDim.x) * blockDim.x)
+  // eight elements per step when both arrays are 16-byte aligned
+  const bool vec = ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(out)) & 15) == 0;
+  const size_t n8 = vec ? n / 8 : 0;
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n8; i += stride) {
+    const uint4 a = reinterpret_cast<const uint4*>(in)[i];
+    const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+    uint32_t r[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float lo = __uint_as_float(w[k] << 16), hi = __uint_as_float(w[k] & 0xffff0000u);
+      r[k] = f2_to_h2(lo, hi);
+    }
+    reinterpret_cast<uint4*>(out)[i] = make_uint4(r[0], r[1], r[2], r[3]);
+  }
+  for (size_t i = n8 * 8 + blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += stride)
     out[i] = __float2half_rn(__bfloat162float(in[i]));
 }
 
@@ -524,13 +636,72 @@ __global__ void gather_v_kernel(const void* V, int in_dtype, const int32_t* idx,
   }
 }
 
-__global__ void reduce_partials_kernel(const float* part, float* out, int nsplit, size_t n) {
-  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
-       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    float s = 0.f;
-    for (int z = 0; z < nsplit; ++z) s += part[static_cast<size_t>(z) * n + i];
-    out[i] = s;
+// Sum over the split partials p[z * stride], z < nsplit, four loads in flight,
+// in a fixed order for every element (independent of the launch).
+__device__ __forceinline__ float4 sum_splits(const float4* p, size_t stride, int nsplit) {
+  float4 acc[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  int z = 0;
+  for (; z + 3 < nsplit; z += 4) {
+    float4 u[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) u[k] = p[static_cast<size_t>(z + k) * stride];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      acc[k].x += u[k].x; acc[k].y += u[k].y; acc[k].z += u[k].z; acc[k].w += u[k].w;
+    }
   }
+  for (int k = 0; z < nsplit; ++z, ++k) {
+    const float4 u = p[static_cast<size_t>(z) * stride];
+    acc[k].x += u.x; acc[k].y += u.y; acc[k].z += u.z; acc[k].w += u.w;
+  }
+  return make_float4((acc[0].x + acc[1].x) + (acc[2].x + acc[3].x),
+                     (acc[0].y + acc[1].y) + (acc[2].y + acc[3].y),
+                     (acc[0].z + acc[1].z) + (acc[2].z + acc[3].z),
+                     (acc[0].w + acc[1].w) + (acc[2].w + acc[3].w));
+}
+
+__global__ void reduce_partials_kernel(const float4* part, float4* out, int nsplit, size_t n4) {
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n4;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    out[i] = sum_splits(part + i, n4, nsplit);
+  }
+}
+
+// Sum of the split partials of a symmetric [H][t_pad][t_pad] system whose
+// builder wrote the upper block triangle: one CTA per 32 x 32 tile (ti <= tj)
+// of one head sums the tile and writes it and, through shared memory, its
+// transpose.
+__global__ void __launch_bounds__(256) reduce_gram_kernel(const float* part, float* out,
+                                                         int nsplit, int t_pad) {
+  __shared__ float tile[32][33];
+  const int h = blockIdx.y;
+  int ti = 0, rem = blockIdx.x;
+  const int nt = t_pad / 32;
+  while (rem >= nt - ti) {
+    rem -= nt - ti;
+    ++ti;
+  }
+  const int tj = ti + rem;
+  const int ty = threadIdx.x >> 3, tx = threadIdx.x & 7;
+  const size_t tt = static_cast<size_t>(t_pad) * t_pad;
+  const size_t off = static_cast<size_t>(h) * tt + static_cast<size_t>(ti * 32 + ty) * t_pad +
+                     tj * 32 + tx * 4;
+  const size_t stride4 = static_cast<size_t>(gridDim.y) * tt / 4;
+  const float4 r = sum_splits(reinterpret_cast<const float4*>(part + off), stride4, nsplit);
+  *reinterpret_cast<float4*>(out + off) = r;
+  if (ti == tj) return;  // diagonal tiles hold both triangles already
+  tile[ty][tx * 4 + 0] = r.x;
+  tile[ty][tx * 4 + 1] = r.y;
+  tile[ty][tx * 4 + 2] = r.z;
+  tile[ty][tx * 4 + 3] = r.w;
+  __syncthreads();
+  const size_t toff = static_cast<size_t>(h) * tt + static_cast<size_t>(tj * 32 + ty) * t_pad +
+                      ti * 32 + tx * 4;
+  *reinterpret_cast<float4*>(out + toff) =
+      make_float4(tile[tx * 4 + 0][ty], tile[tx * 4 + 1][ty], tile[tx * 4 + 2][ty],
+                  tile[tx * 4 + 3][ty]);
 }
 
 // Copy the upper triangle to the lower one (the Gram builder writes the
@@ -603,13 +774,20 @@ int key_scores_smem(OperandMode mode) {
 
 cudaError_t launch_select_topt(const uint32_t* code, int H, int T, int t, int32_t* idx,
                                cudaStream_t st) {
-  select_topt_kernel<<<H, kSelThreads, 0, st>>>(code, T, t, idx);
+  if (T <= 4 * kSelThreads)
+    select_topt_kernel<4><<<H, kSelThreads, 0, st>>>(code, T, t, idx);
+  else if (T <= 8 * kSelThreads)
+    select_topt_kernel<8><<<H, kSelThreads, 0, st>>>(code, T, t, idx);
+  else if (T <= 32 * kSelThreads)
+    select_topt_kernel<32><<<H, kSelThreads, 0, st>>>(code, T, t, idx);
+  else
+    select_topt_kernel<0><<<H, kSelThreads, 0, st>>>(code, T, t, idx);
   return cudaGetLastError();
 }
 
 cudaError_t launch_convert_bf16_to_f16(const __nv_bfloat16* in, __half* out, size_t n,
                                        cudaStream_t st) {
-  convert_bf16_f16_kernel<<<grid_for(n), 256, 0, st>>>(in, out, n);
+  convert_bf16_f16_kernel<<<grid_for(n / 8 + 1), 256, 0, st>>>(in, out, n);
   return cudaGetLastError();
 }
 
@@ -664,7 +842,18 @@ cudaError_t launch_gather_v(const void* V, int in_dtype, const int32_t* idx, flo
 
 cudaError_t launch_reduce_partials(const float* part, float* out, int nsplit, size_t n,
                                    cudaStream_t st) {
-  reduce_partials_kernel<<<grid_for(n), 256, 0, st>>>(part, out, nsplit, n);
+  if (n % 4) return cudaErrorInvalidValue;
+  reduce_partials_kernel<<<grid_for(n / 4), 256, 0, st>>>(reinterpret_cast<const float4*>(part),
+                                                          reinterpret_cast<float4*>(out), nsplit,
+                                                          n / 4);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reduce_gram(const float* part, float* out, int nsplit, int H, int t_pad,
+                               cudaStream_t st) {
+  if (t_pad % 32) return cudaErrorInvalidValue;
+  const int nt = t_pad / 32;
+  reduce_gram_kernel<<<dim3(nt * (nt + 1) / 2, H), 256, 0, st>>>(part, out, nsplit, t_pad);
   return cudaGetLastError();
 }
 
