@@ -611,11 +611,10 @@ __global__ void __launch_bounds__(kThreads, 1) nnls_bpp_kernel(const SolveParams
   int* Didx = F + n_pad;
   int* flip = Didx + n_pad;
   float* Yg = p.wbuf + static_cast<size_t>(h) * tp * kMaxD;  // Y spilled for Y^T Y
-  // small system in the first staging buffer, tiles staged in the second
+  // small system in the first staging buffer
   float* Ms = sm.T;
   float* ds = Ms + 3 * kBlk;
   float* mu = ds + 2 * kBS;
-  float* P = sm.T2;
   const float* G = p.G + static_cast<size_t>(h) * tp * tp;
 
   for (int j = tid; j < n_pad; j += kThreads) {
@@ -653,29 +652,49 @@ __global__ void __launch_bounds__(kThreads, 1) nnls_bpp_kernel(const SolveParams
       } else {
         const int nct = nD > kBS ? 2 : 1;
         const int NBs = nct;
-        const int I = warp / nct, ct = warp % nct;
-        // -E_D as register tiles, then Y = L^-1 E_D (negated)
-        float nb[4][8];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int a = I * kBS + 4 * rg + i, q = ct * kBS + 8 * cg + j;
-            nb[i][j] = (I < NB && q < nD && Didx[q] == a) ? -1.f : 0.f;
-          }
         for (int e = tid; e < 3 * kBlk; e += kThreads) Ms[e] = 0.f;
         LC_SOLVER_MARK(10);
-        reg_tri_solve<true>(S, sm.dinv, NB, nct, nb, P);
-        LC_SOLVER_MARK(11);
-        if (I < NB) {
+        // Y = L^-1 E_D, one warp per column: lane r keeps the running
+        // right-hand side of row r of every block; block K is solved
+        // lane-parallel (x_k broadcast by shuffle) and its product with the
+        // blocks below applied at once.  Rows above the unit entry stay 0.
+        for (int q = warp; q < nct * kBS; q += kWarps) {
+          if (q >= nD) {  // padding columns of Y are zero
+            for (int r = lane; r < n_pad; r += 32) Yg[static_cast<size_t>(r) * kMaxD + q] = 0.f;
+            continue;
+          }
+          const int a = Didx[q], Ka = a / kBS;
+          float acc[8];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            float4* row = reinterpret_cast<float4*>(
-                Yg + static_cast<size_t>(I * kBS + 4 * rg + i) * kMaxD + ct * kBS + 8 * cg);
-            row[0] = make_float4(-nb[i][0], -nb[i][1], -nb[i][2], -nb[i][3]);
-            row[1] = make_float4(-nb[i][4], -nb[i][5], -nb[i][6], -nb[i][7]);
+          for (int I = 0; I < 8; ++I) acc[I] = (I == Ka && lane == a % kBS) ? 1.f : 0.f;
+#pragma unroll
+          for (int K = 0; K < 8; ++K) {
+            if (K >= NB) break;
+            float* ycol = Yg + static_cast<size_t>(K * kBS + lane) * kMaxD + q;
+            if (K < Ka) {
+              *ycol = 0.f;
+              continue;
+            }
+            const float* Lkk = blk(S, K, K);
+            const float* di = sm.dinv + K * kBS;
+            float y = acc[K], xr = 0.f;
+#pragma unroll
+            for (int k = 0; k < kBS; ++k) {
+              const float xk = __shfl_sync(kFull, y, k) * di[k];
+              if (lane == k) xr = xk;
+              if (lane > k) y = fmaf(-Lkk[lane * kLD + k], xk, y);
+            }
+            *ycol = xr;
+#pragma unroll
+            for (int k = 0; k < kBS; ++k) {
+              const float xk = __shfl_sync(kFull, xr, k);
+#pragma unroll
+              for (int I = K + 1; I < 8; ++I)
+                if (I < NB) acc[I] = fmaf(-blk(S, I, K)[lane * kLD + k], xk, acc[I]);
+            }
           }
         }
+        LC_SOLVER_MARK(11);
         __syncthreads();
         // (G^-1)_DD = Y^T Y: tile pairs (0,0), (1,0), (1,1) summed over row blocks
         const int npair = nct == 2 ? 3 : 1;
