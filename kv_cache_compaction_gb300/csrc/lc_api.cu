@@ -262,6 +262,9 @@ struct lc_context {
   int32_t* d_iters = nullptr;   // [kMaxHeads]
   uint32_t* d_err = nullptr;
   Profiler prof;
+  // host entry point: copy stream and events of the pipelined upload
+  cudaStream_t copy_st = nullptr;
+  cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
 };
 
 namespace {
@@ -339,37 +342,46 @@ lc_status prepare_operands(const Ctx& c, const void* Q, const void* K, const voi
   return LC_OK;
 }
 
+// Step 1 for heads [h0, h0 + nh) (all heads by default).
 lc_status run_pass1(const Ctx& c, const void* qop, const void* kop, float* rowmax, float* lse,
-                    float* O, bool to_ws) {
+                    float* O, bool to_ws, int h0 = 0, int nh = -1) {
   const Plan& p = c.p;
+  if (nh < 0) nh = p.H;
   const bool qk_bf16 = p.bf16_in;
   // below 2x compression the output fit amplifies P's rounding: split P.V
   const bool split_p = 2 * p.t > p.T;
   const int bn = (p.mode == kSplitF16d64) ? 64 : 128;
+  // operands are 16-bit (bf16 inputs, or the split fp16 copies of fp32 ones)
+  const size_t q_off = static_cast<size_t>(h0) * p.n_q * p.d_qk * 2;
+  const size_t k_off = static_cast<size_t>(h0) * p.T * p.d_qk * 2;
+  const size_t v_off = static_cast<size_t>(h0) * p.T * p.d * 2;
   CUtensorMap mQ, mK, mV, mVlo;
-  if (!make_map(&mQ, qop, qk_bf16, p.d_qk, p.n_q, p.H, 128)) return LC_ERR_CUDA;
-  if (!make_map(&mK, kop, qk_bf16, p.d_qk, p.T, p.H, bn)) return LC_ERR_CUDA;
-  if (!make_map(&mV, c.ws + p.vhi, false, p.d, p.T, p.H, bn)) return LC_ERR_CUDA;
-  if (!make_map(&mVlo, p.bf16_in ? c.ws + p.vhi : c.ws + p.vlo, false, p.d, p.T, p.H, bn))
+  if (!make_map(&mQ, static_cast<const uint8_t*>(qop) + q_off, qk_bf16, p.d_qk, p.n_q, nh, 128))
     return LC_ERR_CUDA;
+  if (!make_map(&mK, static_cast<const uint8_t*>(kop) + k_off, qk_bf16, p.d_qk, p.T, nh, bn))
+    return LC_ERR_CUDA;
+  if (!make_map(&mV, c.ws + p.vhi + v_off, false, p.d, p.T, nh, bn)) return LC_ERR_CUDA;
+  if (!make_map(&mVlo, (p.bf16_in ? c.ws + p.vhi : c.ws + p.vlo) + v_off, false, p.d, p.T, nh, bn))
+    return LC_ERR_CUDA;
+  const size_t rq = static_cast<size_t>(h0) * p.n_q, rqp = static_cast<size_t>(h0) * p.n_q_pad;
   AttnStatsParams a{};
   a.n_q = p.n_q;
   a.T = p.T;
   a.n_q_pad = p.n_q_pad;
   a.scale_log2 = p.scale * kLog2e;
-  a.rowmax = rowmax;
-  a.lse = lse;
-  a.O = O;
+  a.rowmax = rowmax ? rowmax + rq : nullptr;
+  a.lse = lse ? lse + rq : nullptr;
+  a.O = O ? O + rq * p.d : nullptr;
   if (to_ws) {
-    a.rowmax_pad = c.at<float>(p.m_pad);
-    a.lse_pad = c.at<float>(p.lse_pad);
-    a.O_hi = c.at<__half>(p.ohi);
-    a.O_lo = c.at<__half>(p.olo);
+    a.rowmax_pad = c.at<float>(p.m_pad) + rqp;
+    a.lse_pad = c.at<float>(p.lse_pad) + rqp;
+    a.O_hi = c.at<__half>(p.ohi) + rq * p.d;
+    a.O_lo = c.at<__half>(p.olo) + rq * p.d;
   }
   a.err = c.h->d_err;
   {
     LC_PROF(c, "attn_stats", 1);
-    LC_CUDA(launch_attn_stats(p.mode, split_p, mQ, mK, mV, mVlo, a, p.H, c.st));
+    LC_CUDA(launch_attn_stats(p.mode, split_p, mQ, mK, mV, mVlo, a, nh, c.st));
   }
   return LC_OK;
 }
@@ -609,6 +621,9 @@ lc_status lc_destroy(lc_handle h) {
   cudaFree(h->d_status);
   cudaFree(h->d_iters);
   cudaFree(h->d_err);
+  for (cudaEvent_t e : h->ev)
+    if (e) cudaEventDestroy(e);
+  if (h->copy_st) cudaStreamDestroy(h->copy_st);
   delete h;
   return LC_OK;
 }
@@ -744,12 +759,58 @@ lc_status lc_compact_layer_host(lc_handle h, const lc_shape* shape, const void* 
   uint8_t* dB = dW + round_up(H * p.t * 4, 256);
   uint8_t* dC = dB + round_up(H * p.t * 4, 256);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  LC_CUDA(cudaMemcpyAsync(dQ, Q_host, qb, cudaMemcpyHostToDevice, st));
-  LC_CUDA(cudaMemcpyAsync(dK, K_host, kb, cudaMemcpyHostToDevice, st));
-  LC_CUDA(cudaMemcpyAsync(dV, V_host, kb, cudaMemcpyHostToDevice, st));
-  LC_TRY(lc_compact_layer(h, shape, dQ, dK, dV, reinterpret_cast<int32_t*>(dIdx),
-                          reinterpret_cast<float*>(dW), reinterpret_cast<float*>(dB),
-                          reinterpret_cast<float*>(dC), workspace, p.total, stream));
+  if (!p.bf16_in || H < 2) {
+    LC_CUDA(cudaMemcpyAsync(dQ, Q_host, qb, cudaMemcpyHostToDevice, st));
+    LC_CUDA(cudaMemcpyAsync(dK, K_host, kb, cudaMemcpyHostToDevice, st));
+    LC_CUDA(cudaMemcpyAsync(dV, V_host, kb, cudaMemcpyHostToDevice, st));
+    LC_TRY(lc_compact_layer(h, shape, dQ, dK, dV, reinterpret_cast<int32_t*>(dIdx),
+                            reinterpret_cast<float*>(dW), reinterpret_cast<float*>(dB),
+                            reinterpret_cast<float*>(dC), workspace, p.total, stream));
+  } else {
+    // Pipelined upload: the heads go up in two groups on a copy stream, and
+    // step 1 of the first group runs while the second group is copied.
+    if (!h->copy_st) LC_CUDA(cudaStreamCreateWithFlags(&h->copy_st, cudaStreamNonBlocking));
+    for (cudaEvent_t& e : h->ev)
+      if (!e) LC_CUDA(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+    const int hg[2] = {static_cast<int>((H + 1) / 2), static_cast<int>(H - (H + 1) / 2)};
+    const int h0s[2] = {0, hg[0]};
+    // the previous call on this stream may still read the staging buffers
+    LC_CUDA(cudaEventRecord(h->ev[2], st));
+    LC_CUDA(cudaStreamWaitEvent(h->copy_st, h->ev[2], 0));
+    const size_t qh = static_cast<size_t>(p.n_q) * p.d * el, kh = static_cast<size_t>(p.T) * p.d * el;
+    for (int g = 0; g < 2; ++g) {
+      const size_t o = static_cast<size_t>(h0s[g]);
+      const size_t n = static_cast<size_t>(hg[g]);
+      LC_CUDA(cudaMemcpyAsync(dQ + o * qh, static_cast<const uint8_t*>(Q_host) + o * qh, n * qh,
+                              cudaMemcpyHostToDevice, h->copy_st));
+      LC_CUDA(cudaMemcpyAsync(dK + o * kh, static_cast<const uint8_t*>(K_host) + o * kh, n * kh,
+                              cudaMemcpyHostToDevice, h->copy_st));
+      LC_CUDA(cudaMemcpyAsync(dV + o * kh, static_cast<const uint8_t*>(V_host) + o * kh, n * kh,
+                              cudaMemcpyHostToDevice, h->copy_st));
+      LC_CUDA(cudaEventRecord(h->ev[g], h->copy_st));
+    }
+    Ctx c{h, p, static_cast<uint8_t*>(workspace), st};
+    LC_TRY(reset_report(c));
+    int32_t* idx = reinterpret_cast<int32_t*>(dIdx);
+    for (int g = 0; g < 2; ++g) {
+      LC_CUDA(cudaStreamWaitEvent(st, h->ev[g], 0));
+      const size_t nv = static_cast<size_t>(hg[g]) * p.T * p.d;
+      const size_t ov = static_cast<size_t>(h0s[g]) * p.T * p.d;
+      {
+        LC_PROF(c, "convert_v", 1);
+        LC_CUDA(launch_convert_bf16_to_f16(reinterpret_cast<const __nv_bfloat16*>(dV) + ov,
+                                           c.at<__half>(p.vhi) + ov, nv, st));
+      }
+      LC_TRY(run_pass1(c, dQ, dK, nullptr, nullptr, nullptr, true, h0s[g], hg[g]));
+    }
+    LC_TRY(run_pass2(c, dQ, dK));
+    {
+      LC_PROF(c, "select_topt", 1);
+      LC_CUDA(launch_select_topt(c.at<uint32_t>(p.ucode), p.H, p.T, p.t, idx, st));
+    }
+    LC_TRY(run_fit(c, dQ, dK, dV, idx, reinterpret_cast<float*>(dW), reinterpret_cast<float*>(dB),
+                   reinterpret_cast<float*>(dC)));
+  }
   LC_CUDA(cudaMemcpyAsync(idx_host, dIdx, H * p.t * 4, cudaMemcpyDeviceToHost, st));
   LC_CUDA(cudaMemcpyAsync(w_host, dW, H * p.t * 4, cudaMemcpyDeviceToHost, st));
   LC_CUDA(cudaMemcpyAsync(beta_host, dB, H * p.t * 4, cudaMemcpyDeviceToHost, st));
