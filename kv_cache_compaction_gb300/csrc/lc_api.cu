@@ -262,9 +262,14 @@ struct lc_context {
   int32_t* d_iters = nullptr;   // [kMaxHeads]
   uint32_t* d_err = nullptr;
   Profiler prof;
-  // host entry point: copy stream and events of the pipelined upload
+  // host entry point: copy stream, per-group step-1 streams and events of
+  // the pipelined upload
+  static constexpr int kGroups = 8;
   cudaStream_t copy_st = nullptr;
-  cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
+  cudaStream_t grp_st[kGroups] = {};
+  cudaEvent_t ev_start = nullptr;
+  cudaEvent_t ev_copy[kGroups] = {};
+  cudaEvent_t ev_p1[kGroups] = {};
 };
 
 namespace {
@@ -621,8 +626,12 @@ lc_status lc_destroy(lc_handle h) {
   cudaFree(h->d_status);
   cudaFree(h->d_iters);
   cudaFree(h->d_err);
-  for (cudaEvent_t e : h->ev)
-    if (e) cudaEventDestroy(e);
+  for (int g = 0; g < lc_context::kGroups; ++g) {
+    if (h->ev_copy[g]) cudaEventDestroy(h->ev_copy[g]);
+    if (h->ev_p1[g]) cudaEventDestroy(h->ev_p1[g]);
+    if (h->grp_st[g]) cudaStreamDestroy(h->grp_st[g]);
+  }
+  if (h->ev_start) cudaEventDestroy(h->ev_start);
   if (h->copy_st) cudaStreamDestroy(h->copy_st);
   delete h;
   return LC_OK;
@@ -767,42 +776,51 @@ lc_status lc_compact_layer_host(lc_handle h, const lc_shape* shape, const void* 
                             reinterpret_cast<float*>(dW), reinterpret_cast<float*>(dB),
                             reinterpret_cast<float*>(dC), workspace, p.total, stream));
   } else {
-    // Pipelined upload: the heads go up in two groups on a copy stream, and
-    // step 1 of the first group runs while the second group is copied.
+    // Pipelined upload: the heads go up in groups (one head per group for up
+    // to eight heads) on a copy stream; each group's step 1 runs on its own
+    // stream as soon as its copy lands, so all but the first group's upload
+    // hides under step-1 work, and the groups' CTAs fill the GPU together.
+    constexpr int kG = lc_context::kGroups;
     if (!h->copy_st) LC_CUDA(cudaStreamCreateWithFlags(&h->copy_st, cudaStreamNonBlocking));
-    for (cudaEvent_t& e : h->ev)
-      if (!e) LC_CUDA(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
-    const int hg[2] = {static_cast<int>((H + 1) / 2), static_cast<int>(H - (H + 1) / 2)};
-    const int h0s[2] = {0, hg[0]};
-    // the previous call on this stream may still read the staging buffers
-    LC_CUDA(cudaEventRecord(h->ev[2], st));
-    LC_CUDA(cudaStreamWaitEvent(h->copy_st, h->ev[2], 0));
+    if (!h->ev_start) LC_CUDA(cudaEventCreateWithFlags(&h->ev_start, cudaEventDisableTiming));
+    for (int g = 0; g < kG; ++g) {
+      if (!h->grp_st[g]) LC_CUDA(cudaStreamCreateWithFlags(&h->grp_st[g], cudaStreamNonBlocking));
+      if (!h->ev_copy[g]) LC_CUDA(cudaEventCreateWithFlags(&h->ev_copy[g], cudaEventDisableTiming));
+      if (!h->ev_p1[g]) LC_CUDA(cudaEventCreateWithFlags(&h->ev_p1[g], cudaEventDisableTiming));
+    }
+    const int ng = static_cast<int>(std::min<size_t>(H, kG));
+    const int per = static_cast<int>((H + ng - 1) / ng);
+    Ctx c{h, p, static_cast<uint8_t*>(workspace), st};
+    LC_TRY(reset_report(c));
+    // everything below is ordered after earlier work on the caller's stream
+    // (which may still read the staging buffers) and after the report reset
+    LC_CUDA(cudaEventRecord(h->ev_start, st));
+    LC_CUDA(cudaStreamWaitEvent(h->copy_st, h->ev_start, 0));
     const size_t qh = static_cast<size_t>(p.n_q) * p.d * el, kh = static_cast<size_t>(p.T) * p.d * el;
-    for (int g = 0; g < 2; ++g) {
-      const size_t o = static_cast<size_t>(h0s[g]);
-      const size_t n = static_cast<size_t>(hg[g]);
-      LC_CUDA(cudaMemcpyAsync(dQ + o * qh, static_cast<const uint8_t*>(Q_host) + o * qh, n * qh,
-                              cudaMemcpyHostToDevice, h->copy_st));
+    for (int g = 0; g < ng; ++g) {
+      const int h0 = g * per, nh = std::min(per, static_cast<int>(H) - h0);
+      if (nh <= 0) break;
+      const size_t o = static_cast<size_t>(h0), n = static_cast<size_t>(nh);
       LC_CUDA(cudaMemcpyAsync(dK + o * kh, static_cast<const uint8_t*>(K_host) + o * kh, n * kh,
                               cudaMemcpyHostToDevice, h->copy_st));
       LC_CUDA(cudaMemcpyAsync(dV + o * kh, static_cast<const uint8_t*>(V_host) + o * kh, n * kh,
                               cudaMemcpyHostToDevice, h->copy_st));
-      LC_CUDA(cudaEventRecord(h->ev[g], h->copy_st));
-    }
-    Ctx c{h, p, static_cast<uint8_t*>(workspace), st};
-    LC_TRY(reset_report(c));
-    int32_t* idx = reinterpret_cast<int32_t*>(dIdx);
-    for (int g = 0; g < 2; ++g) {
-      LC_CUDA(cudaStreamWaitEvent(st, h->ev[g], 0));
-      const size_t nv = static_cast<size_t>(hg[g]) * p.T * p.d;
-      const size_t ov = static_cast<size_t>(h0s[g]) * p.T * p.d;
+      LC_CUDA(cudaMemcpyAsync(dQ + o * qh, static_cast<const uint8_t*>(Q_host) + o * qh, n * qh,
+                              cudaMemcpyHostToDevice, h->copy_st));
+      LC_CUDA(cudaEventRecord(h->ev_copy[g], h->copy_st));
+      Ctx cg{h, p, static_cast<uint8_t*>(workspace), h->grp_st[g]};
+      LC_CUDA(cudaStreamWaitEvent(cg.st, h->ev_copy[g], 0));
+      const size_t nv = n * p.T * p.d, ov = o * p.T * p.d;
       {
-        LC_PROF(c, "convert_v", 1);
+        LC_PROF(cg, "convert_v", 1);
         LC_CUDA(launch_convert_bf16_to_f16(reinterpret_cast<const __nv_bfloat16*>(dV) + ov,
-                                           c.at<__half>(p.vhi) + ov, nv, st));
+                                           cg.at<__half>(p.vhi) + ov, nv, cg.st));
       }
-      LC_TRY(run_pass1(c, dQ, dK, nullptr, nullptr, nullptr, true, h0s[g], hg[g]));
+      LC_TRY(run_pass1(cg, dQ, dK, nullptr, nullptr, nullptr, true, h0, nh));
+      LC_CUDA(cudaEventRecord(h->ev_p1[g], cg.st));
+      LC_CUDA(cudaStreamWaitEvent(st, h->ev_p1[g], 0));
     }
+    int32_t* idx = reinterpret_cast<int32_t*>(dIdx);
     LC_TRY(run_pass2(c, dQ, dK));
     {
       LC_PROF(c, "select_topt", 1);
