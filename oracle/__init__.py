@@ -316,3 +316,85 @@ def compact_layer(Q, K, V, t, scale, max_outer=0, max_inner=0):
     [H, T, d] -> list of per-head result dicts."""
     return [compact_head(Q[h], K[h], V[h], t, scale, max_outer, max_inner)
             for h in range(Q.shape[0])]
+
+
+# ------------------------------------------------------------ fast path -----
+# [KVC] "Attempt #3: Two-Pass", "Choosing beta" (uniform redistribution) and
+# "Choosing C_v" (direct selection): a compaction that never forms the full
+# n_q x T score matrix.  Readings (also in the design notes): the query subset
+# Q' is given as row indices (the random draw is an input); first-pass scores
+# are the key scores of Q' under full attention over all T keys (Q' is small,
+# so its exact lse is cheap); the second pass normalises each full query over
+# the k*t shortlist keys only, which is all QK'^T provides; the redistribution
+# takes n = all reference queries and the shortlist as the total mass; the
+# softmax scale s is applied as in [LC] Eq. (1).
+
+def lse_over(Q, K, scale):
+    """log sum_j exp(scale * q_i . k_j) for every row of Q over the rows of K
+    (the log attention mass of each query over those keys)."""
+    Q, K = _f64(Q), _f64(K)
+    out = np.empty(Q.shape[0])
+    for a, b in _chunks(Q.shape[0]):
+        S = scale * (Q[a:b] @ K.T)
+        mm = S.max(axis=1)
+        out[a:b] = mm + np.log(np.exp(S - mm[:, None]).sum(axis=1))
+    return out
+
+
+def two_pass_select(Q, K, qsel, t, k, scale):
+    """Two-pass key selection ([KVC] "Attempt #3: Two-Pass").
+
+    Pass 1: the query subset Q' = Q[qsel] scores every key,
+    u'_j = max_{i in Q'} (s q_i.k_j - lse_i) with lse_i over all T keys; the
+    k*t best keys (capped at T) form the shortlist K'.  Pass 2: every query
+    scores the shortlist normalised over the shortlist,
+    u_j = max_i (s q_i.k'_j - lse'_i), lse'_i = log sum_{l in K'} exp(s q_i.k'_l);
+    the t best shortlist keys are C_k.  Ties go to the lower key index.
+    Returns dict(short, u1, u2, idx) with idx ascending original key indices.
+    """
+    Q, K = _f64(Q), _f64(K)
+    Qs = Q[np.asarray(qsel, np.int64)]
+    u1 = key_scores(Qs, K, lse_over(Qs, K, scale), scale)
+    kt = min(k * t, K.shape[0])
+    short = select(u1, kt)
+    Ks = K[short]
+    u2 = key_scores(Q, Ks, lse_over(Q, Ks, scale), scale)
+    pos = select(u2, t)
+    return {"short": short, "u1": u1, "u2": u2, "idx": short[pos]}
+
+
+def redistribute_beta(Q, K, short, idx, scale):
+    """Uniform redistribution of the missing mass ([KVC] "Choosing beta").
+
+    Over the n reference queries: m_j = (1/n) sum_i exp(s q_i.c_j) for each
+    selected key, Delta = (1/n) sum_i [sum_{l in K'} exp(s q_i.k'_l) -
+    sum_{j in C_k} exp(s q_i.c_j)], and beta_j = log((m_j + Delta/t) / m_j).
+    Computed with one common shift of every exponent (beta is invariant under
+    it).  -> beta [t]."""
+    Q, K = _f64(Q), _f64(K)
+    short = np.asarray(short, np.int64)
+    idx = np.asarray(idx, np.int64)
+    t = idx.size
+    n = Q.shape[0]
+    M = lse_over(Q, K[short], scale).max()  # >= every exponent below
+    tot = 0.0
+    m = np.zeros(t)
+    for a, b in _chunks(n):
+        tot += np.exp(scale * (Q[a:b] @ K[short].T) - M).sum()
+        m += np.exp(scale * (Q[a:b] @ K[idx].T) - M).sum(axis=0)
+    m /= n
+    delta = tot / n - m.sum()
+    return np.log((m + delta / t) / m)
+
+
+def direct_values(V, idx):
+    """C_v = V[idx] ([KVC] "Choosing C_v", direct selection)."""
+    return _f64(V)[np.asarray(idx, np.int64)].copy()
+
+
+def compact_head_fast(Q, K, V, qsel, t, k, scale):
+    """Two-pass selection, redistributed beta, direct C_v for one KV head."""
+    r = two_pass_select(Q, K, qsel, t, k, scale)
+    r["beta"] = redistribute_beta(Q, K, r["short"], r["idx"], scale)
+    r["Cv"] = direct_values(V, r["idx"])
+    return r

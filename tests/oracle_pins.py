@@ -312,9 +312,79 @@ def check_fit_reduces_error(o):
     assert np.sum((Xf @ r["Cv"] - r["O"]) ** 2) < np.sum((Xb @ V[r["idx"]] - r["O"]) ** 2)
 
 
+# ------------------------------------------------------------ fast path -----
+def check_two_pass_brute(o):
+    """Two-pass selection on a tiny head against plain loops: per-row log
+    masses, first-pass key scores of the query subset, shortlist by a stable
+    sort, second-pass scores normalised over the shortlist, final top-t."""
+    rng = _rng(41)
+    n_q, T, d, t, k = 9, 13, 4, 3, 2
+    Q = rng.normal(size=(n_q, d))
+    K = rng.normal(size=(T, d))
+    qsel = np.array([1, 4, 7])
+    s = 0.6
+
+    def lse_row(q, keys):
+        return math.log(sum(math.exp(s * float(q @ kk)) for kk in keys))
+
+    u1 = np.array([max(s * float(Q[i] @ K[j]) - lse_row(Q[i], K) for i in qsel) for j in range(T)])
+    short = np.array(_select_by_sort(u1, k * t))
+    Ks = K[short]
+    u2 = np.array([max(s * float(Q[i] @ Ks[j]) - lse_row(Q[i], Ks) for i in range(n_q))
+                   for j in range(len(short))])
+    idx = short[np.array(_select_by_sort(u2, t))]
+    r = o.two_pass_select(Q, K, qsel, t, k, s)
+    _close(r["u1"], u1, 1e-12, "first-pass scores")
+    assert np.array_equal(r["short"], short), "shortlist"
+    _close(r["u2"], u2, 1e-12, "second-pass scores")
+    assert np.array_equal(r["idx"], np.sort(idx)), "selection"
+
+
+def check_two_pass_full_shortlist(o):
+    """With k*t >= T the shortlist is every key and the second pass is the
+    full method's key scoring: same scores, same selection."""
+    rng = _rng(42)
+    Q = rng.normal(size=(40, 8))
+    K = rng.normal(size=(24, 8))
+    s = 1 / math.sqrt(8)
+    r = o.two_pass_select(Q, K, np.arange(0, 40, 5), 6, 4, s)
+    _, lse, _ = o.full_stats(Q, K, np.zeros((24, 1)), s)
+    u = o.key_scores(Q, K, lse, s)
+    assert np.array_equal(r["short"], np.arange(24))
+    _close(r["u2"], u, 1e-12, "second pass = full key scores")
+    assert np.array_equal(r["idx"], o.select(u, 6))
+
+
+def check_redistribute(o):
+    """Uniform redistribution: against loops on a tiny head; the compact mass
+    with beta reproduces the shortlist mass on average over the queries (the
+    missing mass is redistributed, not lost); no missing mass gives beta = 0;
+    queries at q = 0 give beta_j = log(k t / t)."""
+    rng = _rng(43)
+    n, T, d = 7, 10, 3
+    Q = rng.normal(size=(n, d))
+    K = rng.normal(size=(T, d))
+    s = 0.8
+    short = np.array([0, 2, 3, 5, 8, 9])
+    idx = np.array([2, 5, 9])
+    t = idx.size
+    m = np.array([sum(math.exp(s * float(Q[i] @ K[j])) for i in range(n)) / n for j in idx])
+    tot = sum(math.exp(s * float(Q[i] @ K[j])) for i in range(n) for j in short) / n
+    delta = tot - m.sum()
+    beta = o.redistribute_beta(Q, K, short, idx, s)
+    _close(beta, np.log((m + delta / t) / m), 1e-12, "beta vs loops")
+    _close(np.sum(m * np.exp(beta)), tot, 1e-12, "mass conserved")
+    _close(o.redistribute_beta(Q, K, idx, idx, s), np.zeros(t), 1e-12, "no missing mass")
+    Z = np.zeros((5, d))
+    _close(o.redistribute_beta(Z, K, short, idx, s), np.full(t, math.log(short.size / t)),
+           1e-12, "q = 0")
+    assert np.array_equal(o.direct_values(K, idx), K[idx])
+
+
 ALL_CHECKS = [
     check_full_stats_brute, check_full_stats_closed_forms, check_key_scores_brute,
     check_select, check_mass_system_brute, check_nnls_bruteforce, check_nnls_scipy, check_nnls_planted_and_kkt,
     check_nnls_q_zero_and_caps, check_compact_weights, check_ols, check_t_equals_T,
-    check_fit_reduces_error,
+    check_fit_reduces_error, check_two_pass_brute, check_two_pass_full_shortlist,
+    check_redistribute,
 ]

@@ -76,8 +76,32 @@ def _ols_diag(o):
     o.ols = lambda H, R: (np.asarray(R) / np.diag(H)[:, None], o.OK)
 
 
+def _second_pass_full_lse(o):
+    # the second pass normalised over every key instead of the shortlist
+    def f(Q, K, qsel, t, k, scale):
+        Q, K = np.asarray(Q, float), np.asarray(K, float)
+        Qs = Q[np.asarray(qsel)]
+        u1 = o.key_scores(Qs, K, o.lse_over(Qs, K, scale), scale)
+        short = o.select(u1, min(k * t, K.shape[0]))
+        u2 = o.key_scores(Q, K[short], o.lse_over(Q, K, scale), scale)
+        return {"short": short, "u1": u1, "u2": u2, "idx": short[o.select(u2, t)]}
+    o.two_pass_select = f
+
+
+def _delta_not_shared(o):
+    # the whole missing mass given to every key instead of Delta / t
+    orig = o.redistribute_beta
+
+    def f(Q, K, short, idx, scale):
+        b = orig(Q, K, short, idx, scale)
+        t = len(idx)
+        return np.log(1 + t * np.expm1(b))
+    o.redistribute_beta = f
+
+
 MUTANTS = [_no_scale, _unnormalised_output, _score_plus_lse, _score_min, _ties_high,
-           _no_stepback, _mass_unshifted, _weights_no_bias, _ols_diag]
+           _no_stepback, _mass_unshifted, _weights_no_bias, _ols_diag, _second_pass_full_lse,
+           _delta_not_shared]
 
 
 @pytest.mark.parametrize("mutate", MUTANTS, ids=lambda f: f.__name__)
