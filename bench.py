@@ -46,6 +46,10 @@ def args_():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="lc", choices=["lc", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--fast-steps", type=int, default=100,
+                    help="steps of the two-pass / redistribution path (0: skip)")
+    ap.add_argument("--fast-n-sub", type=int, default=256)
+    ap.add_argument("--fast-k", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0,
                     help="seconds of oracle work for the cpu_baseline sample")
@@ -326,6 +330,45 @@ def main():
             qkt[k] = {"tflops": tf, "frac_of_peak": tf / pk["bf16_tflops_sustained"],
                       "ms": ms}
 
+    # the fast path (two-pass selection, redistributed beta, direct values)
+    # on the same layers, 256-query subsets drawn per layer
+    fast = None
+    if a.fast_steps > 0:
+        qsels = [torch.from_numpy(np.stack([
+            np.random.default_rng(1000 + rank * N_LAYERS + l + 7919 * h).choice(
+                w.n_q, a.fast_n_sub, replace=False) for h in range(H)]).astype(np.int32)).to(dev)
+            for l in range(N_LAYERS)]
+        fout = (out[0], out[2], out[3])
+
+        def fstep(i):
+            Q, K, V = layers[i % N_LAYERS]
+            comp.compact_layer_fast(Q, K, V, qsels[i % N_LAYERS], t, a.fast_k, out=fout)
+
+        for i in range(max(a.warmup, 3)):
+            fstep(i)
+        torch.cuda.synchronize()
+        f0 = torch.cuda.Event(enable_timing=True)
+        f1 = torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for i in range(a.fast_steps):
+            fstep(i)
+        f1.record(stream)
+        torch.cuda.synchronize()
+        ms_fast = f0.elapsed_time(f1) / a.fast_steps
+        comp.profile_read()
+        comp.profile(True)
+        for i in range(20):
+            fstep(i)
+        torch.cuda.synchronize()
+        comp.profile(False)
+        fk = comp.profile_read()
+        if comp.report(H).device_error_bits:
+            raise RuntimeError("device error in the fast path")
+        fast = {"ms_per_layer": ms_fast, "n_sub": a.fast_n_sub, "k": a.fast_k,
+                "steps": a.fast_steps, "vs_full_path": ms_step / ms_fast,
+                "launches_per_step": sum(v[1] for v in fk.values()) / 20,
+                "per_kernel_ms": {k: v[0] / 20 for k, v in fk.items()}}
+
     # end to end through the host-buffer entry point
     e2e = None
     if a.e2e_steps > 0:
@@ -372,7 +415,7 @@ def main():
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": config_dict(w, world), "roofline": roof, "qkt": qkt,
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
-            "per_kernel": per_kernel, "layer_tflops": fl["layer"] / (ms_step * 1e-3) / 1e12,
+            "per_kernel": per_kernel, "fast_path": fast, "layer_tflops": fl["layer"] / (ms_step * 1e-3) / 1e12,
             "wall_s_timed": wall_s,
         }
         print(json.dumps(line), flush=True)

@@ -144,6 +144,30 @@ lc_status lc_compact_layer_host(lc_handle h, const lc_shape* shape, const void* 
                                 float* w_host, float* beta_host, float* Cv_host,
                                 void* workspace, size_t workspace_bytes, void* stream);
 
+/* Fast compaction of one layer without the full score matrix ("KV
+ * compaction" blog: "Attempt #3: Two-Pass", "Choosing beta" -- uniform
+ * redistribution -- and "Choosing C_v" -- direct selection).
+ *   1. the query subset Q' (qsel[h][0..n_sub), row indices 0 <= r < n_q of
+ *      head h; the random draw is the caller's) scores every key under full
+ *      attention, u'_j = max_{i in Q'} (s q_i.k_j - lse_i);
+ *   2. the min(k t, T) best keys form the shortlist K';
+ *   3. every query scores the shortlist normalised over the shortlist,
+ *      u_j = max_i (s q_i.k'_j - lse'_i), lse'_i = log sum_{l in K'} e^{s q_i.k'_l};
+ *      the t best are C_k (idx, ascending; ties to the lower index);
+ *   4. beta_j = log((m_j + Delta/t) / m_j) with m_j = mean_i e^{s q_i.c_j} and
+ *      Delta = mean_i (sum_{K'} e^{s q_i.k'} - sum_{C_k} e^{s q_i.c}) over all
+ *      n_q queries (no fit);
+ *   5. Cv = V[idx] (fp32).
+ * bf16 inputs only (LC_ERR_UNSUPPORTED otherwise); 1 <= n_sub <= n_q, k >= 1.
+ * short_out [H][min(k t, T)] receives the shortlist if not NULL.  All
+ * pointers are device pointers; the workspace has
+ * lc_fast_workspace_bytes(shape, n_sub, k) bytes, 256-byte aligned. */
+lc_status lc_fast_workspace_bytes(const lc_shape* shape, int n_sub, int k, size_t* bytes);
+lc_status lc_compact_layer_fast(lc_handle h, const lc_shape* shape, const void* Q, const void* K,
+                                const void* V, const int32_t* qsel, int n_sub, int k,
+                                int32_t* idx, float* beta, float* Cv, int32_t* short_out,
+                                void* workspace, size_t workspace_bytes, void* stream);
+
 /* Per-head outcome of the last lc_fit_only / lc_compact_layer on this handle:
  * head_status[H] (lc_status values), nnls_iters[H] and device error bits.
  * Synchronises `stream`.  Any pointer may be NULL. */

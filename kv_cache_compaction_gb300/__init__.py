@@ -35,7 +35,8 @@ EXPORTS = [
     "lc_create", "lc_destroy", "lc_workspace_bytes", "lc_full_attn_stats", "lc_key_scores",
     "lc_select_topt", "lc_fit_only", "lc_compact_layer", "lc_host_workspace_bytes",
     "lc_compact_layer_host", "lc_get_report", "lc_profile_enable", "lc_profile_read",
-    "lc_select_topt_noalloc", "lc_status_string",
+    "lc_select_topt_noalloc", "lc_status_string", "lc_fast_workspace_bytes",
+    "lc_compact_layer_fast",
 ]
 
 LC_BF16, LC_FP32 = 0, 1
@@ -78,6 +79,9 @@ def load_library(path: str = LIB_PATH):
         "lc_fit_only": ([vp, sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
         "lc_compact_layer": ([vp, sp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
         "lc_compact_layer_host": ([vp, sp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
+        "lc_fast_workspace_bytes": ([sp, i32, i32, ctypes.POINTER(sz)], i32),
+        "lc_compact_layer_fast": ([vp, sp, vp, vp, vp, vp, i32, i32, vp, vp, vp, vp, vp, sz, vp],
+                                  i32),
         "lc_get_report": ([vp, i32, vp, vp, vp, vp], i32),
         "lc_profile_enable": ([vp, i32], i32),
         "lc_profile_read": ([vp, i32, vp, vp, vp, vp], i32),
@@ -259,6 +263,35 @@ class Compactor:
                                               _ptr(ws), ws.numel(), self._stream()),
                "lc_compact_layer_host")
         return idx, w, beta, Cv
+
+    def compact_layer_fast(self, Q, K, V, qsel, t: int, k: int = 4, scale: float = 0.0,
+                           out=None, with_shortlist: bool = False):
+        """Two-pass selection, redistributed beta and direct values:
+        (idx, beta, Cv[, shortlist]).  ``qsel`` [H, n_sub] int32 holds the rows
+        of Q that form the query subset of the first pass (the random draw is
+        the caller's); the shortlist keeps min(k t, T) keys."""
+        torch = self._torch
+        self._check_inputs(Q, K, V, qsel)
+        if qsel.dtype != torch.int32 or qsel.dim() != 2 or qsel.shape[0] != Q.shape[0]:
+            raise ValueError("qsel must be an [H, n_sub] int32 tensor")
+        s = self.shape(Q, K, t, scale)
+        n_sub = int(qsel.shape[1])
+        n = ctypes.c_size_t()
+        _check(self.lib.lc_fast_workspace_bytes(ctypes.byref(s), n_sub, k, ctypes.byref(n)),
+               "lc_fast_workspace_bytes")
+        ws = self.workspace(n.value)
+        H, _, d = Q.shape
+        if out is None:
+            out = (self._empty((H, t), torch.int32), self._empty((H, t), torch.float32),
+                   self._empty((H, t, d), torch.float32))
+        idx, beta, Cv = out
+        short = self._empty((H, min(k * t, K.shape[1])), torch.int32) if with_shortlist else None
+        _check(self.lib.lc_compact_layer_fast(self.handle, ctypes.byref(s), _ptr(Q), _ptr(K),
+                                              _ptr(V), _ptr(qsel), n_sub, k, _ptr(idx),
+                                              _ptr(beta), _ptr(Cv), _ptr(short), _ptr(ws),
+                                              ws.numel(), self._stream()),
+               "lc_compact_layer_fast")
+        return (idx, beta, Cv, short) if with_shortlist else (idx, beta, Cv)
 
     def profile(self, on: bool):
         """Turn per-kernel CUDA-event timing of the library's launches on/off."""

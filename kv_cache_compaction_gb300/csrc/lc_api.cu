@@ -589,6 +589,195 @@ lc_status reset_report(const Ctx& c) {
     if (s_ != LC_OK) return s_;  \
   } while (0)
 
+// ---------------------------------------------------------------- fast path
+// Two-pass selection, uniform redistribution of the missing mass, direct
+// values ("KV compaction" blog, "Attempt #3: Two-Pass", "Choosing beta",
+// "Choosing C_v").  bf16 operands only.
+struct FastPlan {
+  OperandMode mode;
+  int H, n_q, T, d, t, n_sub, kt;
+  int n_sub_pad, T_pad, kt_pad, n_q_pad, t_pad;
+  float scale;
+  int mass_units, mass_max;  // pass 2 scores: CTAs per query split, largest split
+  // workspace offsets (bytes)
+  size_t qs, colb_all, lc2_sub, lse_sub;  // pass 1 over the query subset
+  size_t ucode, shrt, kp, colb_short;     // scores, shortlist, its keys
+  size_t lc2_q, lse_q, pos;               // pass 2 over all queries
+  size_t part, L2, chosen;                // column masses of the shortlist keys
+  size_t total;
+};
+
+lc_status fast_plan(const lc_shape* s, int n_sub, int k, FastPlan* out) {
+  LC_TRY(validate(s));
+  if (s->in_dtype != LC_BF16) return LC_ERR_UNSUPPORTED;
+  if (n_sub < 1 || n_sub > s->n_q || k < 1) return LC_ERR_INVALID_ARG;
+  FastPlan p{};
+  p.mode = s->d == 128 ? kBF16d128 : kBF16d64;
+  p.H = s->n_kv_heads;
+  p.n_q = s->n_q;
+  p.T = s->T;
+  p.d = s->d;
+  p.t = s->t;
+  p.n_sub = n_sub;
+  p.kt = static_cast<int>(std::min<long long>(static_cast<long long>(k) * s->t, s->T));
+  p.n_sub_pad = static_cast<int>(round_up(n_sub, 128));
+  p.T_pad = static_cast<int>(round_up(s->T, 128));
+  p.kt_pad = static_cast<int>(round_up(p.kt, 128));
+  p.n_q_pad = static_cast<int>(round_up(s->n_q, 128));
+  p.t_pad = static_cast<int>(round_up(s->t, 128));
+  p.scale = s->scale > 0.f ? s->scale : 1.f / std::sqrt(static_cast<float>(s->d));
+  p.mass_units = ((p.kt + 255) / 256) * p.H;
+  p.mass_max = max_split(p.mass_units, 2, p.n_q_pad / 128);
+
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = round_up(off + bytes, 256);
+    return o;
+  };
+  const size_t H = p.H;
+  p.qs = take(H * p.n_sub_pad * p.d * 2);
+  p.colb_all = take(H * p.T_pad * 4);
+  p.lc2_sub = take(H * p.n_sub_pad * 4);
+  p.lse_sub = take(H * p.n_sub_pad * 4);
+  p.ucode = take(H * p.T * 4);
+  p.shrt = take(H * p.kt * 4);
+  p.kp = take(H * p.kt_pad * p.d * 2);
+  p.colb_short = take(H * p.kt_pad * 4);
+  p.lc2_q = take(H * p.n_q_pad * 4);
+  p.lse_q = take(H * p.n_q_pad * 4);
+  p.pos = take(H * p.t * 4);
+  p.part = take(static_cast<size_t>(p.mass_max) * H * p.kt * 8);
+  p.L2 = take(H * p.kt * 4);
+  p.chosen = take(H * p.kt);
+  p.total = off;
+  *out = p;
+  return LC_OK;
+}
+
+// Query split of a key-column pass over `units` CTAs and `tiles` query tiles.
+int column_split(const lc_context* h, int units, int occ, int tiles, int cap, int* per) {
+  int split = best_split(units, h->sm_count, occ, std::min(cap, tiles));
+  *per = (tiles + split - 1) / split;
+  return (tiles + *per - 1) / *per;
+}
+
+struct FastCtx {
+  lc_context* h;
+  cudaStream_t st;
+};
+
+lc_status run_fast(const FastCtx& c, const FastPlan& p, uint8_t* ws, const void* Q, const void* K,
+                   const void* V, const int32_t* qsel, int32_t* idx, float* beta, float* Cv,
+                   int32_t* short_out) {
+  auto F = [&](size_t o) { return reinterpret_cast<float*>(ws + o); };
+  auto I = [&](size_t o) { return reinterpret_cast<int32_t*>(ws + o); };
+  auto U = [&](size_t o) { return reinterpret_cast<uint32_t*>(ws + o); };
+  const size_t H = p.H;
+  const int row_bytes = p.d * 2;
+  const float s2 = p.scale * kLog2e;
+  LC_CUDA(cudaMemsetAsync(c.h->d_status, 0, sizeof(int32_t) * p.H, c.st));
+  LC_CUDA(cudaMemsetAsync(c.h->d_iters, 0, sizeof(int32_t) * p.H, c.st));
+  LC_CUDA(cudaMemsetAsync(c.h->d_err, 0, sizeof(uint32_t), c.st));
+
+  CUtensorMap mQ, mK, mQs, mKp;
+  if (!make_map(&mQ, Q, true, p.d, p.n_q, p.H, 128)) return LC_ERR_CUDA;
+  if (!make_map(&mK, K, true, p.d, p.T, p.H, 128)) return LC_ERR_CUDA;
+  if (!make_map(&mQs, ws + p.qs, true, p.d, p.n_sub_pad, p.H, 128)) return LC_ERR_CUDA;
+  if (!make_map(&mKp, ws + p.kp, true, p.d, p.kt_pad, p.H, 128)) return LC_ERR_CUDA;
+
+  // ---- pass 1: the query subset Q' scores every key under full attention
+  {
+    LC_PROF(c, "fast_prepare", 3);
+    LC_CUDA(launch_gather_rows(Q, ws + p.qs, qsel, p.H, p.n_q, p.n_sub, p.n_sub_pad, row_bytes,
+                               c.st));
+    LC_CUDA(launch_fill_colb2(F(p.colb_all), p.H, p.T, p.T_pad, c.st));
+    LC_CUDA(launch_fill_colb2(F(p.colb_short), p.H, p.kt, p.kt_pad, c.st));
+  }
+  CompactLseParams cl{};
+  cl.n_q = p.n_sub;
+  cl.n_q_pad = p.n_sub_pad;
+  cl.t_pad = p.T_pad;
+  cl.scale_log2 = s2;
+  cl.colb2 = F(p.colb_all);
+  cl.lc2_pad = F(p.lc2_sub);
+  cl.err = c.h->d_err;
+  {
+    LC_PROF(c, "subset_lse", 2);
+    LC_CUDA(launch_compact_lse(p.mode, mQs, mK, cl, p.H, c.st));
+    LC_CUDA(launch_scale_f32(F(p.lc2_sub), F(p.lse_sub), H * p.n_sub_pad, kLn2, c.st));
+  }
+  KeyScoreParams ks{};
+  ks.scale = p.scale;
+  ks.err = c.h->d_err;
+  {
+    LC_PROF(c, "subset_scores", 1);
+    LC_CUDA(cudaMemsetAsync(ws + p.ucode, 0, H * p.T * 4, c.st));
+    const int units = ((p.T + 255) / 256) * p.H, tiles = p.n_sub_pad / 128;
+    ks.n_q_pad = p.n_sub_pad;
+    ks.T = p.T;
+    const int split = column_split(c.h, units, 1, tiles, max_split(units, 2, tiles),
+                                   &ks.tiles_per_split);
+    ks.lse_pad = F(p.lse_sub);
+    ks.u_code = U(p.ucode);
+    LC_CUDA(launch_key_scores(p.mode, mK, mQs, ks, p.H, split, c.st));
+  }
+  {
+    LC_PROF(c, "shortlist", 2);
+    LC_CUDA(launch_select_topt(U(p.ucode), p.H, p.T, p.kt, I(p.shrt), c.st));
+    LC_CUDA(launch_gather_rows(K, ws + p.kp, I(p.shrt), p.H, p.T, p.kt, p.kt_pad, row_bytes,
+                               c.st));
+  }
+
+  // ---- pass 2: every query scores the shortlist, normalised over it
+  cl.n_q = p.n_q;
+  cl.n_q_pad = p.n_q_pad;
+  cl.t_pad = p.kt_pad;
+  cl.colb2 = F(p.colb_short);
+  cl.lc2_pad = F(p.lc2_q);
+  {
+    LC_PROF(c, "shortlist_lse", 2);
+    if (p.kt_pad <= 256) {
+      const int sp = best_split(p.H, c.h->sm_count, 1, p.n_q_pad / 128);
+      LC_CUDA(launch_compact_lse_resident(p.mode, mQ, mKp, cl, p.H, sp, c.st));
+    } else {
+      LC_CUDA(launch_compact_lse(p.mode, mQ, mKp, cl, p.H, c.st));
+    }
+    LC_CUDA(launch_scale_f32(F(p.lc2_q), F(p.lse_q), H * p.n_q_pad, kLn2, c.st));
+  }
+  {
+    // scores and column masses of the shortlist in one pass
+    LC_PROF(c, "shortlist_scores", 2);
+    LC_CUDA(cudaMemsetAsync(ws + p.ucode, 0, H * p.kt * 4, c.st));
+    const int tiles = p.n_q_pad / 128;
+    ks.n_q_pad = p.n_q_pad;
+    ks.T = p.kt;
+    ks.n_rows = p.n_q;
+    const int split = column_split(c.h, p.mass_units, 1, tiles, p.mass_max, &ks.tiles_per_split);
+    ks.lse_pad = F(p.lse_q);
+    ks.part = reinterpret_cast<float2*>(ws + p.part);
+    LC_CUDA(launch_key_scores_mass(p.mode, mKp, mQ, ks, p.H, split, c.st));
+    LC_CUDA(launch_merge_key_lse(ks.part, F(p.L2), split, p.H, p.kt, c.st));
+  }
+  {
+    LC_PROF(c, "select_compose", 3);
+    LC_CUDA(cudaMemsetAsync(ws + p.chosen, 0, H * p.kt, c.st));
+    LC_CUDA(launch_select_topt(U(p.ucode), p.H, p.kt, p.t, I(p.pos), c.st));
+    LC_CUDA(launch_compose_idx(I(p.shrt), I(p.pos), idx, ws + p.chosen, p.H, p.kt, p.t, c.st));
+  }
+  {
+    // beta from the column masses: missing mass = the shortlist keys not chosen
+    LC_PROF(c, "redistribute_values", 2);
+    LC_CUDA(launch_redistribute_beta(F(p.L2), ws + p.chosen, I(p.pos), beta, p.H, p.kt, p.t,
+                                     c.st));
+    LC_CUDA(launch_gather_v(V, 0, idx, Cv, p.H, p.T, p.t, p.t, p.d, c.st));
+  }
+  if (short_out)
+    LC_CUDA(cudaMemcpyAsync(short_out, ws + p.shrt, H * p.kt * 4, cudaMemcpyDeviceToDevice,
+                            c.st));
+  return LC_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -835,6 +1024,29 @@ lc_status lc_compact_layer_host(lc_handle h, const lc_shape* shape, const void* 
   LC_CUDA(cudaMemcpyAsync(Cv_host, dC, H * p.t * p.d * 4, cudaMemcpyDeviceToHost, st));
   LC_CUDA(cudaStreamSynchronize(st));
   return LC_OK;
+}
+
+lc_status lc_fast_workspace_bytes(const lc_shape* shape, int n_sub, int k, size_t* bytes) {
+  FastPlan p;
+  LC_TRY(fast_plan(shape, n_sub, k, &p));
+  if (!bytes) return LC_ERR_INVALID_ARG;
+  *bytes = p.total;
+  return LC_OK;
+}
+
+lc_status lc_compact_layer_fast(lc_handle h, const lc_shape* shape, const void* Q, const void* K,
+                                const void* V, const int32_t* qsel, int n_sub, int k,
+                                int32_t* idx, float* beta, float* Cv, int32_t* short_out,
+                                void* workspace, size_t workspace_bytes, void* stream) {
+  FastPlan p;
+  LC_TRY(fast_plan(shape, n_sub, k, &p));
+  if (!Q || !K || !V || !qsel || !idx || !beta || !Cv) return LC_ERR_INVALID_ARG;
+  if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 256 || workspace_bytes < p.total)
+    return LC_ERR_WORKSPACE;
+  LC_TRY(enter(h));
+  FastCtx c{h, static_cast<cudaStream_t>(stream)};
+  return run_fast(c, p, static_cast<uint8_t*>(workspace), Q, K, V, qsel, idx, beta, Cv,
+                  short_out);
 }
 
 lc_status lc_get_report(lc_handle h, int n_heads, int32_t* head_status, int32_t* nnls_iters,

@@ -37,6 +37,8 @@ struct KeyScoreParams {
   float scale;             // softmax scale (natural-log units)
   const float* lse_pad;    // [H][n_q_pad], +inf padding
   uint32_t* u_code;        // [H][T] order codes, atomicMax-merged (pre-zeroed)
+  int n_rows;              // mass mode: real query rows (later rows carry no mass)
+  float2* part;            // mass mode: [nsplit][H][T] base-2 (max, sum) per split
   uint32_t* err;
 };
 
@@ -82,6 +84,12 @@ cudaError_t launch_attn_stats(OperandMode mode, bool split_p, const CUtensorMap&
                               cudaStream_t st);
 cudaError_t launch_key_scores(OperandMode mode, const CUtensorMap& mK, const CUtensorMap& mQ,
                               const KeyScoreParams& p, int H, int nsplit, cudaStream_t st);
+// Key scores plus each key's column log mass in the same pass (bf16 modes):
+// per query split, p.part = (max_i b_ij, sum_i 2^(b_ij - max)) with
+// b_ij = s log2e q_i.k_j over the rows i < p.n_rows.
+cudaError_t launch_key_scores_mass(OperandMode mode, const CUtensorMap& mK,
+                                   const CUtensorMap& mQ, const KeyScoreParams& p, int H,
+                                   int nsplit, cudaStream_t st);
 cudaError_t launch_gram(OperandMode mode, bool with_r, const CUtensorMap& mKc,
                         const CUtensorMap& mQ, const CUtensorMap& mOhi, const CUtensorMap& mOlo,
                         const GramParams& p, int H, int nsplit, cudaStream_t st);
@@ -137,6 +145,19 @@ cudaError_t launch_reduce_gram(const float* part, float* out, int nsplit, int H,
 cudaError_t launch_mass_rows(const float* rowmax_pad, const float* lse_pad, float* rowsh2,
                              float* row_b, int H, int n_q, int n_q_pad, cudaStream_t st);
 cudaError_t launch_fill_colb2(float* colb2, int H, int t, int t_pad, cudaStream_t st);
+// L2[h][j] = log2 sum_z part_z.sum 2^(part_z.max) over the nsplit partials.
+cudaError_t launch_merge_key_lse(const float2* part, float* L2, int nsplit, int H, int T,
+                                 cudaStream_t st);
+// out[i] = in[i] * mul (padding values +-inf stay infinite).
+cudaError_t launch_scale_f32(const float* in, float* out, size_t n, float mul, cudaStream_t st);
+// idx[h][r] = short[h][pos[h][r]]; chosen[h][pos[h][r]] = 1 (pre-zeroed).
+cudaError_t launch_compose_idx(const int32_t* short_idx, const int32_t* pos, int32_t* idx,
+                               uint8_t* chosen, int H, int kt, int t, cudaStream_t st);
+// Uniform redistribution of the missing mass over the chosen shortlist keys:
+// beta[h][r] = ln(1 + Delta_h / (t m_j)), j = pos[h][r], with log2 m_j =
+// L2[h][j] and Delta_h the mass of the shortlist keys not chosen.
+cudaError_t launch_redistribute_beta(const float* L2, const uint8_t* chosen, const int32_t* pos,
+                                     float* beta, int H, int kt, int t, cudaStream_t st);
 
 struct SolveParams {
   int H, t, t_pad, d_v, max_iter;

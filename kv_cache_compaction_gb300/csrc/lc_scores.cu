@@ -181,7 +181,11 @@ struct KS2Layout {
   static constexpr int SMEM = 1024 + OFF_BAR + 128;
 };
 
-template <int D>
+// MASS = true: the same pass also reduces each key's column of unshifted
+// scores to its log mass, L2_j = log2 sum_{i < n_rows} 2^(s log2e q_i.k_j);
+// each query split writes its base-2 (max, sum) pair to p.part for
+// merge_key_lse.
+template <int D, bool MASS = false>
 __global__ void __launch_bounds__(320, 1)
     key_scores2_kernel(const __grid_constant__ CUtensorMap mK,
                        const __grid_constant__ CUtensorMap mQ, const KeyScoreParams p) {
@@ -285,7 +289,9 @@ __global__ void __launch_bounds__(320, 1)
     float u8[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) u8[e] = -kInf;
+    float mass_m = -kInf, mass_s = 0.f;  // MASS: running max and sum of 2^(b - max)
     const float2 sc2 = make_float2(p.scale, p.scale);
+    const float s2 = p.scale * kLog2e;
     bool ok = ntile > 0;
     for (int i = 0; ok && i < ntile; ++i) {
       const int s = i % L::NST, b = i & 1;
@@ -305,22 +311,58 @@ __global__ void __launch_bounds__(320, 1)
         u8[(2 * e) & 7] = fmaxf(u8[(2 * e) & 7], a.x);
         u8[(2 * e + 1) & 7] = fmaxf(u8[(2 * e + 1) & 7], a.y);
       }
+      if constexpr (MASS) {
+        // b = base-2 score; rows past n_rows (padding) carry no mass
+        float bm0 = -kInf, bm1 = -kInf;
+#pragma unroll
+        for (int e = 0; e < kBQ; e += 2) {
+          v[e] *= s2;
+          v[e + 1] *= s2;
+          bm0 = fmaxf(bm0, v[e]);
+          bm1 = fmaxf(bm1, v[e + 1]);
+        }
+        const int rem = p.n_rows - (t0i + i) * kBQ;
+        if (rem < kBQ) {
+          bm0 = bm1 = -kInf;
+#pragma unroll
+          for (int e = 0; e < kBQ; ++e) {
+            if (e >= rem) v[e] = -kInf;
+            bm0 = fmaxf(bm0, v[e]);
+          }
+        }
+        const float nm = fmaxf(mass_m, fmaxf(bm0, bm1));
+        if (nm > -kInf) {
+          float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+          for (int e = 0; e < kBQ; e += 2) {
+            a0 += ex2(v[e] - nm);
+            a1 += ex2(v[e + 1] - nm);
+          }
+          mass_s = mass_s * ex2(mass_m - nm) + (a0 + a1);
+          mass_m = nm;
+        }
+      }
       mbar_arrive(&q_empty[s]);
     }
     const float u = fmaxf(fmaxf(fmaxf(u8[0], u8[1]), fmaxf(u8[2], u8[3])),
                           fmaxf(fmaxf(u8[4], u8[5]), fmaxf(u8[6], u8[7])));
-    if (ok && key < p.T) atomicMax(p.u_code + static_cast<size_t>(h) * p.T + key, order_code(u));
+    if (ok && key < p.T) {
+      atomicMax(p.u_code + static_cast<size_t>(h) * p.T + key, order_code(u));
+      if constexpr (MASS)
+        p.part[(static_cast<size_t>(blockIdx.z) * gridDim.y + h) * p.T + key] =
+            make_float2(mass_m, mass_s);
+    }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tbase, 512);
 }
 
-template <int D>
+template <int D, bool MASS = false>
 cudaError_t launch_ks2_t(const CUtensorMap& mK, const CUtensorMap& mQ, const KeyScoreParams& p,
                          int H, int nsplit, cudaStream_t st) {
   using L = KS2Layout<D>;
-  auto kern = key_scores2_kernel<D>;
+  auto kern = key_scores2_kernel<D, MASS>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid((p.T + 2 * kBK - 1) / (2 * kBK), H, nsplit);
@@ -745,6 +787,90 @@ __global__ void fill_colb2_kernel(float* colb2, int H, int t, int t_pad) {
     colb2[i] = static_cast<int>(i % t_pad) < t ? 0.f : -kInf;
 }
 
+__global__ void merge_key_lse_kernel(const float2* part, float* L2, int nsplit, size_t n) {
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    float m = -kInf;
+    for (int z = 0; z < nsplit; ++z) m = fmaxf(m, part[z * n + i].x);
+    float sum = 0.f;
+    if (m > -kInf)
+      for (int z = 0; z < nsplit; ++z) {
+        const float2 q = part[z * n + i];
+        if (q.x > -kInf) sum += q.y * ex2(q.x - m);
+      }
+    L2[i] = m > -kInf ? m + log2f(sum) : -kInf;
+  }
+}
+
+__global__ void scale_f32_kernel(const float* in, float* out, size_t n, float mul) {
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x)
+    out[i] = in[i] * mul;
+}
+
+__global__ void compose_idx_kernel(const int32_t* short_idx, const int32_t* pos, int32_t* idx,
+                                   uint8_t* chosen, int H, int kt, int t) {
+  const size_t n = static_cast<size_t>(H) * t;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const size_t h = i / t;
+    const int r = pos[i];
+    const bool ok = r >= 0 && r < kt;
+    idx[i] = ok ? short_idx[h * kt + r] : -1;
+    if (ok) chosen[h * kt + r] = 1;
+  }
+}
+
+// Base-2 log-sum-exp of get(i) over i < n, whole block (256 threads).
+template <class F>
+__device__ float block_lse2_256(F get, int n, float* red) {
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  float m = -kInf;
+  for (int i = tid; i < n; i += 256) m = fmaxf(m, get(i));
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if (lane == 0) red[w] = m;
+  __syncthreads();
+  float M = -kInf;
+  for (int k = 0; k < 8; ++k) M = fmaxf(M, red[k]);
+  __syncthreads();
+  float sum = 0.f;
+  if (M > -kInf)
+    for (int i = tid; i < n; i += 256) sum += ex2(get(i) - M);
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  if (lane == 0) red[w] = sum;
+  __syncthreads();
+  float S = 0.f;
+  for (int k = 0; k < 8; ++k) S += red[k];
+  __syncthreads();
+  return M > -kInf ? M + log2f(S) : -kInf;
+}
+
+// One CTA per head.  D2 = log2 of the missing mass (the column masses of the
+// shortlist keys that were not chosen), then for each chosen key
+//   beta_j = ln(1 + 2^x),  x = D2 - log2 t - L2_j,
+// evaluated as x ln2 + ln(1 + 2^-x) for x > 0 (no overflow); no missing
+// mass gives beta = 0.
+__global__ void __launch_bounds__(256) redistribute_beta_kernel(const float* L2,
+                                                                const uint8_t* chosen,
+                                                                const int32_t* pos, float* beta,
+                                                                int kt, int t) {
+  __shared__ float red[8];
+  const int h = blockIdx.x, tid = threadIdx.x;
+  const float* Lh = L2 + static_cast<size_t>(h) * kt;
+  const uint8_t* ch = chosen + static_cast<size_t>(h) * kt;
+  const float D2 = block_lse2_256([&](int j) { return ch[j] ? -kInf : Lh[j]; }, kt, red);
+  const float log2t = log2f(static_cast<float>(t));
+  for (int r = tid; r < t; r += 256) {
+    const int j = pos[static_cast<size_t>(h) * t + r];
+    float b = 0.f;
+    if (D2 > -kInf && j >= 0 && j < kt) {
+      const float x = D2 - log2t - Lh[j];
+      b = x > 0.f ? x * kLn2 + log1pf(ex2(-x)) : log1pf(ex2(x));
+    }
+    beta[static_cast<size_t>(h) * t + r] = b;
+  }
+}
+
 inline int grid_for(size_t n, int block = 256) {
   size_t g = (n + block - 1) / block;
   if (g > 152 * 16) g = 152 * 16;
@@ -752,6 +878,42 @@ inline int grid_for(size_t n, int block = 256) {
 }
 
 }  // namespace
+
+cudaError_t launch_key_scores_mass(OperandMode mode, const CUtensorMap& mK,
+                                   const CUtensorMap& mQ, const KeyScoreParams& p, int H,
+                                   int nsplit, cudaStream_t st) {
+  if (!p.part || !p.u_code) return cudaErrorInvalidValue;
+  switch (mode) {
+    case kBF16d128: return launch_ks2_t<128, true>(mK, mQ, p, H, nsplit, st);
+    case kBF16d64: return launch_ks2_t<64, true>(mK, mQ, p, H, nsplit, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_merge_key_lse(const float2* part, float* L, int nsplit, int H, int T,
+                                 cudaStream_t st) {
+  const size_t n = static_cast<size_t>(H) * T;
+  merge_key_lse_kernel<<<grid_for(n), 256, 0, st>>>(part, L, nsplit, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scale_f32(const float* in, float* out, size_t n, float mul, cudaStream_t st) {
+  scale_f32_kernel<<<grid_for(n), 256, 0, st>>>(in, out, n, mul);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_compose_idx(const int32_t* short_idx, const int32_t* pos, int32_t* idx,
+                               uint8_t* chosen, int H, int kt, int t, cudaStream_t st) {
+  compose_idx_kernel<<<grid_for(static_cast<size_t>(H) * t), 256, 0, st>>>(short_idx, pos, idx,
+                                                                            chosen, H, kt, t);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_redistribute_beta(const float* L2, const uint8_t* chosen, const int32_t* pos,
+                                     float* beta, int H, int kt, int t, cudaStream_t st) {
+  redistribute_beta_kernel<<<H, 256, 0, st>>>(L2, chosen, pos, beta, kt, t);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_key_scores(OperandMode mode, const CUtensorMap& mK, const CUtensorMap& mQ,
                               const KeyScoreParams& p, int H, int nsplit, cudaStream_t st) {

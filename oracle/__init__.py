@@ -369,21 +369,29 @@ def redistribute_beta(Q, K, short, idx, scale):
     Over the n reference queries: m_j = (1/n) sum_i exp(s q_i.c_j) for each
     selected key, Delta = (1/n) sum_i [sum_{l in K'} exp(s q_i.k'_l) -
     sum_{j in C_k} exp(s q_i.c_j)], and beta_j = log((m_j + Delta/t) / m_j).
-    Computed with one common shift of every exponent (beta is invariant under
-    it).  -> beta [t]."""
+    C_k is a subset of K' (the page notes this), so the bracket equals the
+    sum over the dropped shortlist keys K' \\ C_k term by term; it is
+    evaluated that way, which has no cancellation when the dropped keys carry
+    little of the mass (no dropped key gives Delta = 0 and beta = 0 exactly).
+    Every exponent is shifted by one common constant (beta is invariant
+    under it).  -> beta [t]."""
     Q, K = _f64(Q), _f64(K)
     short = np.asarray(short, np.int64)
     idx = np.asarray(idx, np.int64)
+    if not np.all(np.isin(idx, short)):
+        raise ValueError("the selected keys must be shortlist keys")
+    dropped = np.setdiff1d(short, idx)
     t = idx.size
     n = Q.shape[0]
     M = lse_over(Q, K[short], scale).max()  # >= every exponent below
-    tot = 0.0
     m = np.zeros(t)
+    delta = 0.0
     for a, b in _chunks(n):
-        tot += np.exp(scale * (Q[a:b] @ K[short].T) - M).sum()
         m += np.exp(scale * (Q[a:b] @ K[idx].T) - M).sum(axis=0)
+        if dropped.size:
+            delta += np.exp(scale * (Q[a:b] @ K[dropped].T) - M).sum()
     m /= n
-    delta = tot / n - m.sum()
+    delta /= n
     return np.log((m + delta / t) / m)
 
 

@@ -14,6 +14,7 @@ unbiased compact cache has mass t instead of T, which is why beta exists).
 """
 from __future__ import annotations
 
+import decimal
 import itertools
 import math
 
@@ -379,6 +380,24 @@ def check_redistribute(o):
     _close(o.redistribute_beta(Z, K, short, idx, s), np.full(t, math.log(short.size / t)),
            1e-12, "q = 0")
     assert np.array_equal(o.direct_values(K, idx), K[idx])
+    # dropped keys carrying ~1e-14 of the mass: the definition evaluated in
+    # 50-digit decimal arithmetic (a float64 difference of the two sums
+    # loses most of Delta's digits here)
+    sc = 0.5
+    Q3 = np.array([[1.0, 0.3], [1.0, -0.7], [1.0, 2.0]])
+    K3 = np.array([[0.0, 0.0], [-70.0, 0.0], [-66.0, 0.1], [-64.0, -0.1]])
+    sh3, id3 = np.array([0, 1, 2, 3]), np.array([0, 1])
+    with decimal.localcontext() as ctx:
+        ctx.prec = 50
+        ex = [[(decimal.Decimal(sc) * (decimal.Decimal(float(Q3[i, 0])) * decimal.Decimal(float(K3[j, 0]))
+                + decimal.Decimal(float(Q3[i, 1])) * decimal.Decimal(float(K3[j, 1])))).exp()
+               for j in range(4)] for i in range(3)]
+        nD = decimal.Decimal(3)
+        mD = [sum(ex[i][j] for i in range(3)) / nD for j in id3]
+        totD = sum(ex[i][j] for i in range(3) for j in sh3) / nD
+        dD = totD - sum(mD)
+        ref = np.array([float(((mj + dD / 2) / mj).ln()) for mj in mD])
+    _close(o.redistribute_beta(Q3, K3, sh3, id3, sc), ref, 1e-12, "beta, tiny dropped mass")
 
 
 ALL_CHECKS = [

@@ -89,3 +89,34 @@ def test_null_handle_and_status_strings(lib):
     for code in range(8):
         assert lib.lc_status_string(code)
     assert lib.lc_destroy(None) == 1
+
+
+@pytest.mark.parametrize("kw,n_sub,k,code", [
+    ({}, 256, 4, 0),
+    ({}, 32768, 1, 0),
+    ({}, 0, 4, 1),                 # empty query subset
+    ({}, 32769, 4, 1),             # more subset rows than queries
+    ({}, 256, 0, 1),
+    ({"in_dtype": 1, "d": 64}, 256, 4, 2),   # fp32 inputs: bf16 only
+    ({"d": 96}, 256, 4, 2),
+    ({"t": 0}, 256, 4, 1),
+])
+def test_fast_workspace_query_validates(lib, kw, n_sub, k, code):
+    n = ctypes.c_size_t(0)
+    s = _shape(**kw)
+    assert lib.lc_fast_workspace_bytes(ctypes.byref(s), n_sub, k, ctypes.byref(n)) == code
+    if code == 0:
+        assert n.value > 0
+
+
+def test_fast_workspace_grows_with_the_shortlist(lib):
+    a, b = ctypes.c_size_t(), ctypes.c_size_t()
+    s = _shape()
+    lib.lc_fast_workspace_bytes(ctypes.byref(s), 256, 1, ctypes.byref(a))
+    lib.lc_fast_workspace_bytes(ctypes.byref(s), 256, 8, ctypes.byref(b))
+    assert b.value > a.value
+    # k t beyond T caps the shortlist at T
+    c8, c64 = ctypes.c_size_t(), ctypes.c_size_t()
+    lib.lc_fast_workspace_bytes(ctypes.byref(s), 256, 32, ctypes.byref(c8))
+    lib.lc_fast_workspace_bytes(ctypes.byref(s), 256, 64, ctypes.byref(c64))
+    assert c8.value == c64.value

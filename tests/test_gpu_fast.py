@@ -1,0 +1,150 @@
+"""Parity of the fast compaction path (two-pass shortlist selection, uniform
+redistribution of the missing mass, direct values) with the float64 oracle's
+compact_head_fast on the same seeded inputs and the same query subsets.
+
+Both selections are compared as sets: they must agree exactly except for keys
+whose oracle scores tie with the selection threshold within the score
+tolerance (rounding may order such keys either way).  When a head's shortlist
+or selection differs that way, the downstream values are not comparable and
+the head stops there.  beta is gated at 1e-3 relative (denominator floored at
+1), C_v must equal V[idx] exactly."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from gpu_util import FIT_REL, SCORE_ABS, beta_err, compactor, dev_i32, host, inputs
+
+pytestmark = pytest.mark.gpu
+
+# (workload, query-subset size, shortlist factor k)
+CASES = {
+    "d128_ragged": (synth.workload("cfg2", H=2, T=300, t=20, seed=7), 40, 4),
+    "d64_ragged": (synth.workload("cfg2", H=2, T=257, d=64, t=33, seed=8), 50, 3),
+    "tiny_capped": (synth.workload("cfg2", H=1, G=1, T=5, t=3, seed=9), 2, 4),
+    "k1_no_missing_mass": (synth.workload("cfg2", H=2, T=700, G=2, t=160, seed=10), 64, 1),
+    "shortlist_resident": (synth.workload("cfg2", H=2, T=1100, G=2, t=64, seed=14), 100, 4),
+    "shortlist_streamed": (synth.workload("cfg2", H=2, T=1024, G=4, t=128, seed=12), 256, 4),
+    "t300_k3": (synth.workload("cfg2", H=1, T=2000, G=3, t=300, seed=13), 128, 3),
+    "iid_all_queries": (synth.workload("cfg2", H=1, T=640, G=2, t=64, kind="iid", seed=11),
+                        None, 5),
+}
+
+
+@pytest.fixture(scope="module")
+def comp():
+    return compactor()
+
+
+def draw_subsets(w, n_sub, seed):
+    """Seeded query subsets, one per head, drawn without replacement."""
+    rng = np.random.default_rng(seed)
+    return np.stack([rng.choice(w.n_q, n_sub, replace=False) for _ in range(w.H)]).astype(np.int32)
+
+
+def _near_tie_only(got, ref, u, n_keep):
+    """got == ref, or they differ only in keys whose score ties the n_keep-th
+    largest within the score tolerance."""
+    if np.array_equal(got, ref):
+        return True
+    tau = np.sort(u)[::-1][n_keep - 1]
+    diff = np.setxor1d(got, ref)
+    assert np.all(np.abs(u[diff] - tau) <= SCORE_ABS), "selection differs beyond near-ties"
+    return False
+
+
+def check_head(r, short, idx, beta, Cv, t, kt):
+    """One head of the GPU fast path against the oracle's result r. Returns
+    True when every stage was compared."""
+    assert short.shape == (kt,) and np.all(np.diff(short) > 0)
+    if not _near_tie_only(short, r["short"], r["u1"], kt):
+        return False
+    assert np.all(np.diff(idx) > 0)
+    assert np.all(np.isin(idx, short))
+    if not _near_tie_only(idx, r["idx"], r["u2"], t):
+        return False
+    err = beta_err(beta, r["beta"])
+    assert np.all(np.isfinite(beta)) and err <= FIT_REL, f"beta err {err:.2e}"
+    assert np.array_equal(Cv, r["Cv"].astype(np.float32)), "C_v is not V[idx]"
+    return True
+
+
+def run_case(comp, w, n_sub, k, heads=None, qseed=0):
+    d, Q, K, V = inputs(w)
+    n_sub = w.n_q if n_sub is None else n_sub
+    qsel = draw_subsets(w, n_sub, qseed)
+    idx, beta, Cv, short = (host(x) for x in comp.compact_layer_fast(
+        Q, K, V, dev_i32(qsel), w.t, k, with_shortlist=True))
+    rep = comp.report(w.H)
+    assert rep.device_error_bits == 0
+    kt = min(k * w.t, w.T)
+    full = 0
+    for h in (range(w.H) if heads is None else heads):
+        r = oracle.compact_head_fast(d["Q"][h], d["K"][h], d["V"][h], qsel[h], w.t, k,
+                                     w.softmax_scale)
+        full += check_head(r, short[h], idx[h], beta[h], Cv[h], w.t, kt)
+    return full
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_fast_path_small(comp, name):
+    w, n_sub, k = CASES[name]
+    assert run_case(comp, w, n_sub, k) >= 1, "no head compared end to end"
+
+
+def test_k1_gives_zero_beta(comp):
+    """With k = 1 the shortlist is the selection: no missing mass, beta = 0
+    exactly."""
+    w, n_sub, _ = CASES["k1_no_missing_mass"]
+    _, Q, K, V = inputs(w)
+    qsel = draw_subsets(w, n_sub, 0)
+    idx, beta, _, short = (host(x) for x in comp.compact_layer_fast(
+        Q, K, V, dev_i32(qsel), w.t, 1, with_shortlist=True))
+    assert np.array_equal(idx, short)
+    assert np.all(beta == 0)
+
+
+def test_beta_nonnegative_and_ordered(comp):
+    """Redistribution only adds mass: beta >= 0, and it falls as a key's own
+    mass grows (beta_j = log1p(Delta / (t m_j)))."""
+    w, n_sub, k = CASES["shortlist_streamed"]
+    d, Q, K, V = inputs(w)
+    qsel = draw_subsets(w, n_sub, 3)
+    idx, beta, _ = (host(x) for x in comp.compact_layer_fast(Q, K, V, dev_i32(qsel), w.t, k))
+    for h in range(w.H):
+        assert np.all(beta[h] >= 0)
+        # oracle column masses of the GPU's own selection order the GPU's beta
+        Kc = d["K"][h][idx[h]].astype(np.float64)
+        S = w.softmax_scale * (d["Q"][h].astype(np.float64) @ Kc.T)
+        logm = np.log(np.exp(S - S.max()).sum(axis=0))
+        order = np.argsort(logm)
+        sep = np.diff(logm[order]) > 1e-3
+        assert np.all(np.diff(beta[h][order])[sep] <= 1e-6)
+
+
+def test_reruns_are_bitwise_identical(comp):
+    w, n_sub, k = CASES["t300_k3"]
+    _, Q, K, V = inputs(w)
+    qs = dev_i32(draw_subsets(w, n_sub, 1))
+    a = [host(x) for x in comp.compact_layer_fast(Q, K, V, qs, w.t, k)]
+    b = [host(x) for x in comp.compact_layer_fast(Q, K, V, qs, w.t, k)]
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+
+
+# ---- full sizes, in the launch configuration the benchmark uses
+@pytest.mark.parametrize("name,heads", [("cfg2", None), ("cfg3", (0, 5))])
+def test_fast_path_full_size(comp, name, heads):
+    """Every head of the 8-head T = 4096 layer; sampled heads of the
+    T = 8192, n_q = 32768 layer; 256-query subsets, shortlist 4t."""
+    w = synth.workload(name)
+    assert run_case(comp, w, 256, 4, heads=heads, qseed=17) >= 1
+
+
+def test_rejects_fp32_inputs(comp):
+    w = synth.workload("cfg1")
+    _, Q, K, V = inputs(w)
+    import kv_cache_compaction_gb300 as lc
+    with pytest.raises(lc.LCError) as e:
+        comp.compact_layer_fast(Q, K, V, dev_i32(np.zeros((w.H, 4), np.int32)), w.t, 4)
+    assert e.value.code == 2

@@ -99,9 +99,22 @@ def _delta_not_shared(o):
     o.redistribute_beta = f
 
 
+def _delta_by_difference(o):
+    # Delta as the float64 difference of the shortlist and selected sums
+    def f(Q, K, short, idx, scale):
+        Q, K = np.asarray(Q, float), np.asarray(K, float)
+        S_all = scale * (Q @ K[np.asarray(short)].T)
+        S_sel = scale * (Q @ K[np.asarray(idx)].T)
+        M = S_all.max()
+        m = np.exp(S_sel - M).mean(axis=0)
+        delta = np.exp(S_all - M).sum(axis=1).mean() - m.sum()
+        return np.log((m + delta / len(idx)) / m)
+    o.redistribute_beta = f
+
+
 MUTANTS = [_no_scale, _unnormalised_output, _score_plus_lse, _score_min, _ties_high,
            _no_stepback, _mass_unshifted, _weights_no_bias, _ols_diag, _second_pass_full_lse,
-           _delta_not_shared]
+           _delta_not_shared, _delta_by_difference]
 
 
 @pytest.mark.parametrize("mutate", MUTANTS, ids=lambda f: f.__name__)
