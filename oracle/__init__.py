@@ -20,7 +20,11 @@ Sources (page title, then section / equation):
 * [KVC] "KV compaction" (bkal01 blog) -- section "Fast KV Compaction via
   Attention Matching": output- and mass-matching equations, the q = 0 argument
   for beta, the three steps (top keys by attention, beta by NNLS on the mass
-  equation, C_v by OLS on the output equation), C_k a subset of K.
+  equation, C_v by OLS on the output equation), C_k a subset of K; sections
+  "Attempt #3: Two-Pass", "Choosing beta", "Choosing C_v" (fast path,
+  held-out errors).
+* [LC] §3.1 "Handling Subsequent Tokens" Eq. (4)-(5) and Appendix A.2
+  (decode-time consumer); §3.2 Eq. (7) (farthest-first diversifiers).
 
 Readings taken where the pages leave a step open (each is also listed in the
 design notes):
@@ -37,6 +41,13 @@ design notes):
   over the keys with w_j > 0; C_v = (X^T X)^-1 X^T O by Cholesky; keys with
   w_j = 0 keep their original value row.  If the Cholesky factorisation fails
   a ridge of 1e-8 * mean(diag) is added once and the status says so.
+
+* Decode consumer: row r of the queries sees the compacted entries whose
+  beta is finite and the first n_vis[r] appended tokens (a causal mask given
+  as a count per row); a row that sees nothing has log Z = -inf and output 0.
+* Held-out errors: mass error = mean over held-out queries of
+  |log Z_cmp - log Z_full|, output error = mean of ||A_cmp - A_full||_2.
+* Farthest-first ties go to the lower key index.
 
 Parity is pinned for every function here by the CPU tests (brute force on tiny
 inputs, closed forms, library cross-checks, invariants); see tests/.
@@ -406,3 +417,102 @@ def compact_head_fast(Q, K, V, qsel, t, k, scale):
     r["beta"] = redistribute_beta(Q, K, r["short"], r["idx"], scale)
     r["Cv"] = direct_values(V, r["idx"])
     return r
+
+
+# ------------------------------------------------------ decode consumer -----
+# [LC] §3.1 "Handling Subsequent Tokens", Eq. (4)-(5), and Appendix A.2
+# "Normalizer Computation and Storage": the compacted document branch (biased
+# logits, padded slots excluded) and the branch of tokens appended after
+# compaction (no bias, causal visibility) are each reduced to an output and a
+# log-normaliser, then merged with the shared normaliser in log space.
+def branch_attention(Q, K, V, bias, valid, scale):
+    """Output and log-normaliser of one branch for every row of Q.
+
+    scores = s q.k_j (+ bias_j), entries with valid_j = False excluded.
+    Returns (out [n, d_v], log_z [n]); a row with no valid entry has
+    log_z = -inf and out = 0 (its branch carries no mass)."""
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    n = Q.shape[0]
+    valid = np.broadcast_to(np.asarray(valid, bool), (n, K.shape[0]))
+    out = np.zeros((n, V.shape[1]))
+    log_z = np.full(n, -np.inf)
+    for a, b in _chunks(n):
+        S = scale * (Q[a:b] @ K.T)
+        if bias is not None:
+            S = S + _f64(bias)[None, :]
+        S = np.where(valid[a:b], S, -np.inf)
+        mm = S.max(axis=1) if S.shape[1] else np.full(b - a, -np.inf)
+        has = np.isfinite(mm)
+        E = np.zeros_like(S)
+        E[has] = np.exp(S[has] - mm[has, None])
+        z = E.sum(axis=1)
+        log_z[a:b][has] = mm[has] + np.log(z[has])
+        out[a:b][has] = (E[has] @ V) / z[has, None]
+    return out, log_z
+
+
+def combine_attention(Q, Ck, beta, Cv, Knew, Vnew, n_vis, scale):
+    """Attention of queries over a compacted cache plus appended tokens
+    ([LC] Eq. (4)-(5)).  Row r sees the compacted entries with finite beta
+    and the first n_vis[r] appended tokens.  Z_cmp and Z_new are the
+    branches' normalisers; A = (Z_cmp A_cmp + Z_new A_new) / (Z_cmp + Z_new)
+    with the weights formed from log-normalisers.  -> (A [n, d_v], log_z)."""
+    beta = _f64(beta)
+    n = np.asarray(Q).shape[0]
+    doc_out, doc_lz = branch_attention(Q, Ck, Cv, np.where(np.isfinite(beta), beta, 0.0),
+                                       np.isfinite(beta)[None, :], scale)
+    n_new = np.asarray(Knew).shape[0]
+    vis = np.arange(n_new)[None, :] < np.asarray(n_vis)[:, None]
+    new_out, new_lz = branch_attention(Q, Knew, Vnew, None, vis, scale)
+    tot = np.logaddexp(doc_lz, new_lz)
+    A = np.zeros_like(doc_out)
+    ok = np.isfinite(tot)
+    wd = np.exp(doc_lz[ok] - tot[ok])
+    wn = np.exp(new_lz[ok] - tot[ok])
+    A[ok] = wd[:, None] * doc_out[ok] + wn[:, None] * new_out[ok]
+    assert A.shape[0] == n
+    return A, tot
+
+
+def heldout_errors(Qh, K, V, Ck, beta, Cv, scale):
+    """Quality of a compaction on held-out queries ([KVC] "Choosing beta" and
+    "Choosing C_v": the mass and the attention-output reconstruction errors).
+
+    Per query, the full cache gives (A_full, log Z_full) and the compacted
+    cache (no appended tokens) gives (A_cmp, log Z_cmp).  Returns
+    (mass_err, out_err) = (mean_i |log Z_cmp - log Z_full|,
+                           mean_i ||A_cmp - A_full||_2)."""
+    Qh = _f64(Qh)
+    _, lse, O = full_stats(Qh, K, V, scale)
+    beta = _f64(beta)
+    A, lz = branch_attention(Qh, Ck, Cv, np.where(np.isfinite(beta), beta, 0.0),
+                             np.isfinite(beta)[None, :], scale)
+    return float(np.mean(np.abs(lz - lse))), float(np.mean(np.linalg.norm(A - O, axis=1)))
+
+
+# ------------------------------------------------ farthest-first traversal --
+def farthest_first(K, seeds, M):
+    """Diversifier selection by farthest-first traversal ([LC] §3.2 Eq. (7),
+    after Gonzalez 1985): starting from the index set S = seeds, repeatedly add
+    i* = argmax_{i not in S} min_{j in S} ||k_i - k_j||^2 until |S| = M.
+    Ties go to the lower index.  Returns the added indices in the order
+    chosen (M - |seeds| of them; fewer if the keys run out)."""
+    K = _f64(K)
+    S = [int(s) for s in seeds]
+    if not S:
+        raise ValueError("farthest-first traversal needs at least one seed")
+    N = K.shape[0]
+    taken = np.zeros(N, bool)
+    taken[S] = True
+    mind = np.full(N, np.inf)
+    for j in S:
+        mind = np.minimum(mind, ((K - K[j]) ** 2).sum(axis=1))
+    added = []
+    while len(S) < M and not taken.all():
+        cand = np.where(taken, -np.inf, mind)
+        i = int(np.argmax(cand))  # first maximum = lowest index
+        added.append(i)
+        S.append(i)
+        taken[i] = True
+        mind = np.minimum(mind, ((K - K[i]) ** 2).sum(axis=1))
+    return np.asarray(added, np.int64)

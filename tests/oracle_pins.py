@@ -400,10 +400,118 @@ def check_redistribute(o):
     _close(o.redistribute_beta(Q3, K3, sh3, id3, sc), ref, 1e-12, "beta, tiny dropped mass")
 
 
+# ------------------------------------------------------- decode consumer ---
+def check_combine_single_softmax(o):
+    """[LC] Eq. (5) is one softmax over the compacted entries (with their
+    biases) and the visible appended tokens (without): against loops over
+    that single softmax; no appended token gives the document branch alone;
+    every compacted entry dropped (beta = -inf) gives the appended branch
+    alone; a row that sees nothing has log Z = -inf."""
+    rng = _rng(51)
+    n, t, n_new, d, dv = 5, 4, 3, 3, 2
+    Q = rng.normal(size=(n, d))
+    Ck = rng.normal(size=(t, d))
+    Cv = rng.normal(size=(t, dv))
+    beta = np.array([0.3, -np.inf, -1.2, 2.0])
+    Kn = rng.normal(size=(n_new, d))
+    Vn = rng.normal(size=(n_new, dv))
+    n_vis = np.array([0, 1, 2, 3, 3])
+    s = 0.7
+    A, lz = o.combine_attention(Q, Ck, beta, Cv, Kn, Vn, n_vis, s)
+    for i in range(n):
+        logits, vals = [], []
+        for j in range(t):
+            if np.isfinite(beta[j]):
+                logits.append(s * float(Q[i] @ Ck[j]) + beta[j])
+                vals.append(Cv[j])
+        for m in range(n_vis[i]):
+            logits.append(s * float(Q[i] @ Kn[m]))
+            vals.append(Vn[m])
+        ex = [math.exp(x) for x in logits]
+        z = sum(ex)
+        _close(lz[i], math.log(z), 1e-12, "combined log Z")
+        _close(A[i], sum(e * v for e, v in zip(ex, vals)) / z, 1e-12, "combined output")
+    A0, lz0 = o.combine_attention(Q, Ck, beta, Cv, Kn, Vn, np.zeros(n, int), s)
+    Ab, lzb = o.branch_attention(Q, Ck, Cv, np.where(np.isfinite(beta), beta, 0.0),
+                                 np.isfinite(beta)[None, :], s)
+    _close(A0, Ab, 1e-12, "no appended token: document branch")
+    _close(lz0, lzb, 1e-12, "no appended token: document log Z")
+    An, lzn = o.combine_attention(Q, Ck, np.full(t, -np.inf), Cv, Kn, Vn, n_vis, s)
+    assert np.isneginf(lzn[0]) and np.all(An[0] == 0), "empty row"
+    Bn, lzbn = o.branch_attention(Q[1:], Kn, Vn, None,
+                                  np.arange(n_new)[None, :] < n_vis[1:, None], s)
+    _close(An[1:], Bn, 1e-12, "all entries dropped: appended branch")
+    _close(lzn[1:], lzbn, 1e-12, "all entries dropped: appended log Z")
+
+
+def check_heldout_errors(o):
+    """Held-out mass and output errors: zero for the identity compaction
+    (C_k = K, beta = 0, C_v = V); against loops on a tiny head otherwise."""
+    rng = _rng(52)
+    n, T, d = 6, 7, 3
+    Q = rng.normal(size=(n, d))
+    K = rng.normal(size=(T, d))
+    V = rng.normal(size=(T, 2))
+    s = 0.9
+    me, oe = o.heldout_errors(Q, K, V, K, np.zeros(T), V, s)
+    _close([me, oe], [0.0, 0.0], 1e-12, "identity compaction")
+    idx = np.array([1, 4, 6])
+    beta = np.array([0.5, -0.25, 1.0])
+    Cv = rng.normal(size=(3, 2))
+    me, oe = o.heldout_errors(Q, K, V, K[idx], beta, Cv, s)
+    mref, oref = 0.0, 0.0
+    for i in range(n):
+        ef = [math.exp(s * float(Q[i] @ K[j])) for j in range(T)]
+        ec = [math.exp(s * float(Q[i] @ K[j]) + b) for j, b in zip(idx, beta)]
+        Af = sum(e * V[j] for e, j in zip(ef, range(T))) / sum(ef)
+        Ac = sum(e * c for e, c in zip(ec, Cv)) / sum(ec)
+        mref += abs(math.log(sum(ec)) - math.log(sum(ef))) / n
+        oref += float(np.linalg.norm(Ac - Af)) / n
+    _close([me, oe], [mref, oref], 1e-12, "held-out errors vs loops")
+
+
+# ------------------------------------------------ farthest-first traversal -
+def check_farthest_first(o):
+    """Farthest-first traversal against a from-scratch recomputation of every
+    step; the chosen distances never increase; and on tiny sets the result
+    is within the traversal's factor-2 bound of the exhaustive optimum of
+    the k-center problem it approximates (Gonzalez 1985)."""
+    rng = _rng(53)
+    K = rng.normal(size=(40, 3))
+    seeds = [5, 17]
+    added = o.farthest_first(K, seeds, 12)
+    S = list(seeds)
+    prev = np.inf
+    for i in added:
+        best, arg = -1.0, -1
+        for c in range(K.shape[0]):
+            if c in S:
+                continue
+            dmin = min(float(((K[c] - K[j]) ** 2).sum()) for j in S)
+            if dmin > best:
+                best, arg = dmin, c
+        assert i == arg, f"step chose {i}, expected {arg}"
+        assert best <= prev + 1e-12, "chosen distance increased"
+        prev = best
+        S.append(i)
+    assert len(added) == 10 and len(set(S)) == 12
+    # factor-2 bound on the k-center radius (radius in plain distance)
+    P = rng.normal(size=(11, 2))
+    k = 3
+    sel = [0] + list(o.farthest_first(P, [0], k))
+    rad = max(min(np.linalg.norm(P[c] - P[j]) for j in sel) for c in range(len(P)))
+    opt = min(max(min(np.linalg.norm(P[c] - P[j]) for j in comb) for c in range(len(P)))
+              for comb in itertools.combinations(range(len(P)), k))
+    assert rad <= 2 * opt + 1e-12, f"radius {rad} > 2 x optimum {opt}"
+    # all keys taken: the traversal stops
+    assert len(o.farthest_first(K[:4], [0], 10)) == 3
+
+
 ALL_CHECKS = [
     check_full_stats_brute, check_full_stats_closed_forms, check_key_scores_brute,
     check_select, check_mass_system_brute, check_nnls_bruteforce, check_nnls_scipy, check_nnls_planted_and_kkt,
     check_nnls_q_zero_and_caps, check_compact_weights, check_ols, check_t_equals_T,
     check_fit_reduces_error, check_two_pass_brute, check_two_pass_full_shortlist,
-    check_redistribute,
+    check_redistribute, check_combine_single_softmax, check_heldout_errors,
+    check_farthest_first,
 ]

@@ -112,9 +112,46 @@ def _delta_by_difference(o):
     o.redistribute_beta = f
 
 
+def _combine_unbiased(o):
+    # the compacted branch without its biases
+    orig = o.combine_attention
+
+    def f(Q, Ck, beta, Cv, Knew, Vnew, n_vis, scale):
+        b = np.asarray(beta, float)
+        return orig(Q, Ck, np.where(np.isfinite(b), 0.0, b), Cv, Knew, Vnew, n_vis, scale)
+    o.combine_attention = f
+
+
+def _mass_error_signed(o):
+    # the mean log-mass difference without the absolute value
+    def f(Qh, K, V, Ck, beta, Cv, scale):
+        _, lse, O = o.full_stats(Qh, K, V, scale)
+        b = np.asarray(beta, float)
+        A, lz = o.branch_attention(Qh, Ck, Cv, b, np.ones((1, len(b)), bool), scale)
+        return float(np.mean(lz - lse)), float(np.mean(np.linalg.norm(A - O, axis=1)))
+    o.heldout_errors = f
+
+
+def _farthest_by_sum(o):
+    # farthest from the sum of distances to the set instead of the nearest
+    def f(K, seeds, M):
+        K = np.asarray(K, float)
+        S = [int(x) for x in seeds]
+        out = []
+        while len(S) < M and len(S) < K.shape[0]:
+            tot = sum(((K - K[j]) ** 2).sum(axis=1) for j in S)
+            tot[S] = -np.inf
+            i = int(np.argmax(tot))
+            out.append(i)
+            S.append(i)
+        return np.asarray(out, np.int64)
+    o.farthest_first = f
+
+
 MUTANTS = [_no_scale, _unnormalised_output, _score_plus_lse, _score_min, _ties_high,
            _no_stepback, _mass_unshifted, _weights_no_bias, _ols_diag, _second_pass_full_lse,
-           _delta_not_shared, _delta_by_difference]
+           _delta_not_shared, _delta_by_difference, _combine_unbiased, _mass_error_signed,
+           _farthest_by_sum]
 
 
 @pytest.mark.parametrize("mutate", MUTANTS, ids=lambda f: f.__name__)
