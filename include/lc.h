@@ -168,6 +168,41 @@ lc_status lc_compact_layer_fast(lc_handle h, const lc_shape* shape, const void* 
                                 int32_t* idx, float* beta, float* Cv, int32_t* short_out,
                                 void* workspace, size_t workspace_bytes, void* stream);
 
+/* Attention of queries over a compacted cache plus tokens appended after it
+ * ("Latent Compaction with Test-Time Training", §3.1 "Handling Subsequent
+ * Tokens", Eq. (4)-(5), and Appendix A.2): per KV head h and query row r,
+ *   A = (Z_cmp A_cmp + Z_new A_new) / (Z_cmp + Z_new),
+ * the compacted branch with logits scale q.Ck_j + beta_j over the entries
+ * with finite beta_j, the appended branch with logits scale q.Knew_m over
+ * m < n_vis[h][r] (no bias); log_z = log(Z_cmp + Z_new) (-inf and A = 0 for
+ * a row that sees nothing).
+ *   q [H][n][d], Ck [H][t][d], Knew, Vnew [H][n_new][d]: bfloat16;
+ *   beta [H][t], Cv [H][t][d]: float32; n_vis [H][n] int32 (NULL: every row
+ *   sees all n_new appended tokens); outputs A [H][n][d] and log_z [H][n]
+ *   (NULL allowed) float32.  d = 64 or 128; scale <= 0 means 1/sqrt(d).
+ *   Knew and Vnew may be NULL when n_new = 0.  Device pointers; no
+ *   workspace. */
+lc_status lc_compact_attention(lc_handle h, int n_heads, int n, int t, int n_new, int d,
+                               float scale, const void* q, const void* Ck, const float* beta,
+                               const float* Cv, const void* Knew, const void* Vnew,
+                               const int32_t* n_vis, float* A, float* log_z, void* stream);
+
+/* Quality of a compaction on held-out queries ("KV compaction" blog,
+ * "Choosing beta" and "Choosing C_v": mass and attention-output
+ * reconstruction errors).  shape->n_q is the number of held-out query rows
+ * Qh [H][n_q][d] (bfloat16 only), shape->t the compacted size; the compacted
+ * cache is (K[idx], beta, Cv) as lc_compact_layer returns it.  Per head:
+ *   mass_err[h] = mean_r |log Z_cmp(q_r) - log Z_full(q_r)|,
+ *   out_err[h]  = mean_r ||A_cmp(q_r) - A_full(q_r)||_2,
+ * the full-cache side from step 1 over all T keys, the compacted side from
+ * lc_compact_attention with no appended tokens.  Outputs are device float32
+ * [H]; the workspace has lc_heldout_workspace_bytes(shape) bytes. */
+lc_status lc_heldout_workspace_bytes(const lc_shape* shape, size_t* bytes);
+lc_status lc_heldout_errors(lc_handle h, const lc_shape* shape, const void* Qh, const void* K,
+                            const void* V, const int32_t* idx, const float* beta,
+                            const float* Cv, float* mass_err, float* out_err, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
 /* Per-head outcome of the last lc_fit_only / lc_compact_layer on this handle:
  * head_status[H] (lc_status values), nnls_iters[H] and device error bits.
  * Synchronises `stream`.  Any pointer may be NULL. */

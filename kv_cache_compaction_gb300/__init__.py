@@ -36,7 +36,8 @@ EXPORTS = [
     "lc_select_topt", "lc_fit_only", "lc_compact_layer", "lc_host_workspace_bytes",
     "lc_compact_layer_host", "lc_get_report", "lc_profile_enable", "lc_profile_read",
     "lc_select_topt_noalloc", "lc_status_string", "lc_fast_workspace_bytes",
-    "lc_compact_layer_fast",
+    "lc_compact_layer_fast", "lc_compact_attention", "lc_heldout_workspace_bytes",
+    "lc_heldout_errors",
 ]
 
 LC_BF16, LC_FP32 = 0, 1
@@ -82,6 +83,10 @@ def load_library(path: str = LIB_PATH):
         "lc_fast_workspace_bytes": ([sp, i32, i32, ctypes.POINTER(sz)], i32),
         "lc_compact_layer_fast": ([vp, sp, vp, vp, vp, vp, i32, i32, vp, vp, vp, vp, vp, sz, vp],
                                   i32),
+        "lc_compact_attention": ([vp, i32, i32, i32, i32, i32, ctypes.c_float, vp, vp, vp, vp,
+                                  vp, vp, vp, vp, vp, vp], i32),
+        "lc_heldout_workspace_bytes": ([sp, ctypes.POINTER(sz)], i32),
+        "lc_heldout_errors": ([vp, sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
         "lc_get_report": ([vp, i32, vp, vp, vp, vp], i32),
         "lc_profile_enable": ([vp, i32], i32),
         "lc_profile_read": ([vp, i32, vp, vp, vp, vp], i32),
@@ -292,6 +297,44 @@ class Compactor:
                                               ws.numel(), self._stream()),
                "lc_compact_layer_fast")
         return (idx, beta, Cv, short) if with_shortlist else (idx, beta, Cv)
+
+    def compact_attention(self, q, Ck, beta, Cv, Knew=None, Vnew=None, n_vis=None,
+                          scale: float = 0.0):
+        """Attention of q [H, n, d] over a compacted cache (Ck bf16 [H, t, d],
+        beta, Cv fp32) plus appended tokens (Knew, Vnew bf16 [H, n_new, d];
+        row r sees the first n_vis[h, r] of them, all if n_vis is None):
+        (A [H, n, d] fp32, log_z [H, n] fp32)."""
+        torch = self._torch
+        self._check_inputs(q, Ck, beta, Cv, Knew, Vnew, n_vis)
+        H, n, d = q.shape
+        t = int(Ck.shape[1])
+        n_new = 0 if Knew is None else int(Knew.shape[1])
+        A = self._empty((H, n, d), torch.float32)
+        lz = self._empty((H, n), torch.float32)
+        _check(self.lib.lc_compact_attention(self.handle, H, n, t, n_new, d, scale, _ptr(q),
+                                             _ptr(Ck), _ptr(beta), _ptr(Cv), _ptr(Knew),
+                                             _ptr(Vnew), _ptr(n_vis), _ptr(A), _ptr(lz),
+                                             self._stream()), "lc_compact_attention")
+        return A, lz
+
+    def heldout_errors(self, Qh, K, V, idx, beta, Cv, scale: float = 0.0):
+        """Mean |log Z_cmp - log Z_full| and mean ||A_cmp - A_full|| per head
+        on held-out queries Qh for the compaction (idx, beta, Cv)."""
+        torch = self._torch
+        self._check_inputs(Qh, K, V, idx, beta, Cv)
+        s = self.shape(Qh, K, int(idx.shape[1]), scale)
+        n = ctypes.c_size_t()
+        _check(self.lib.lc_heldout_workspace_bytes(ctypes.byref(s), ctypes.byref(n)),
+               "lc_heldout_workspace_bytes")
+        ws = self.workspace(n.value)
+        H = Qh.shape[0]
+        me = self._empty((H,), torch.float32)
+        oe = self._empty((H,), torch.float32)
+        _check(self.lib.lc_heldout_errors(self.handle, ctypes.byref(s), _ptr(Qh), _ptr(K), _ptr(V),
+                                          _ptr(idx), _ptr(beta), _ptr(Cv), _ptr(me), _ptr(oe),
+                                          _ptr(ws), ws.numel(), self._stream()),
+               "lc_heldout_errors")
+        return me, oe
 
     def profile(self, on: bool):
         """Turn per-kernel CUDA-event timing of the library's launches on/off."""

@@ -1049,6 +1049,118 @@ lc_status lc_compact_layer_fast(lc_handle h, const lc_shape* shape, const void* 
                   short_out);
 }
 
+lc_status lc_compact_attention(lc_handle h, int n_heads, int n, int t, int n_new, int d,
+                               float scale, const void* q, const void* Ck, const float* beta,
+                               const float* Cv, const void* Knew, const void* Vnew,
+                               const int32_t* n_vis, float* A, float* log_z, void* stream) {
+  if (n_heads < 1 || n_heads > kMaxHeads || n < 1 || t < 0 || n_new < 0) return LC_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return LC_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale)) return LC_ERR_INVALID_ARG;
+  if (!q || !A || (t > 0 && (!Ck || !beta || !Cv)) || (n_new > 0 && (!Knew || !Vnew)))
+    return LC_ERR_INVALID_ARG;
+  LC_TRY(enter(h));
+  CompactAttnParams p{};
+  p.n = n;
+  p.t = t;
+  p.n_new = n_new;
+  p.scale = scale > 0.f ? scale : 1.f / std::sqrt(static_cast<float>(d));
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.Ck = static_cast<const __nv_bfloat16*>(Ck);
+  p.beta = beta;
+  p.Cv = Cv;
+  p.Knew = static_cast<const __nv_bfloat16*>(Knew);
+  p.Vnew = static_cast<const __nv_bfloat16*>(Vnew);
+  p.n_vis = n_vis;
+  p.A = A;
+  p.log_z = log_z;
+  FastCtx c{h, static_cast<cudaStream_t>(stream)};
+  LC_PROF(c, "compact_attention", 1);
+  LC_CUDA(launch_compact_attention(d, p, n_heads, c.st));
+  return LC_OK;
+}
+
+namespace {
+// Held-out evaluation: step-1 statistics and the compacted attention of the
+// held-out rows, placed after the compaction plan's own workspace.
+struct HeldoutPlan {
+  Plan p;
+  size_t lse, O, ck, A, lz, total;
+};
+
+lc_status heldout_plan(const lc_shape* s, HeldoutPlan* out) {
+  LC_TRY(validate(s));
+  if (s->in_dtype != LC_BF16) return LC_ERR_UNSUPPORTED;
+  HeldoutPlan hp{};
+  hp.p = make_plan(s);
+  size_t off = hp.p.total;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = round_up(off + bytes, 256);
+    return o;
+  };
+  const size_t H = s->n_kv_heads, n = s->n_q, d = s->d, t = s->t;
+  hp.lse = take(H * n * 4);
+  hp.O = take(H * n * d * 4);
+  hp.ck = take(H * t * d * 2);
+  hp.A = take(H * n * d * 4);
+  hp.lz = take(H * n * 4);
+  hp.total = off;
+  *out = hp;
+  return LC_OK;
+}
+}  // namespace
+
+lc_status lc_heldout_workspace_bytes(const lc_shape* shape, size_t* bytes) {
+  HeldoutPlan hp;
+  LC_TRY(heldout_plan(shape, &hp));
+  if (!bytes) return LC_ERR_INVALID_ARG;
+  *bytes = hp.total;
+  return LC_OK;
+}
+
+lc_status lc_heldout_errors(lc_handle h, const lc_shape* shape, const void* Qh, const void* K,
+                            const void* V, const int32_t* idx, const float* beta,
+                            const float* Cv, float* mass_err, float* out_err, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  HeldoutPlan hp;
+  LC_TRY(heldout_plan(shape, &hp));
+  if (!Qh || !K || !V || !idx || !beta || !Cv || !mass_err || !out_err) return LC_ERR_INVALID_ARG;
+  if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 256 || workspace_bytes < hp.total)
+    return LC_ERR_WORKSPACE;
+  LC_TRY(enter(h));
+  const Plan& p = hp.p;
+  Ctx c{h, p, static_cast<uint8_t*>(workspace), static_cast<cudaStream_t>(stream)};
+  LC_CUDA(cudaMemsetAsync(h->d_err, 0, sizeof(uint32_t), c.st));
+  const void *qop, *kop;
+  LC_TRY(prepare_operands(c, Qh, K, V, true, &qop, &kop));
+  LC_TRY(run_pass1(c, qop, kop, nullptr, c.at<float>(hp.lse), c.at<float>(hp.O), false));
+  {
+    LC_PROF(c, "gather_keys", 1);
+    LC_CUDA(launch_gather_rows(K, c.ws + hp.ck, idx, p.H, p.T, p.t, p.t, p.d * 2, c.st));
+  }
+  CompactAttnParams a{};
+  a.n = p.n_q;
+  a.t = p.t;
+  a.n_new = 0;
+  a.scale = p.scale;
+  a.q = static_cast<const __nv_bfloat16*>(Qh);
+  a.Ck = c.at<__nv_bfloat16>(hp.ck);
+  a.beta = beta;
+  a.Cv = Cv;
+  a.A = c.at<float>(hp.A);
+  a.log_z = c.at<float>(hp.lz);
+  {
+    LC_PROF(c, "compact_attention", 1);
+    LC_CUDA(launch_compact_attention(p.d, a, p.H, c.st));
+  }
+  {
+    LC_PROF(c, "heldout_reduce", 1);
+    LC_CUDA(launch_heldout_reduce(p.d, c.at<float>(hp.A), c.at<float>(hp.lz), c.at<float>(hp.O),
+                                  c.at<float>(hp.lse), p.H, p.n_q, mass_err, out_err, c.st));
+  }
+  return LC_OK;
+}
+
 lc_status lc_get_report(lc_handle h, int n_heads, int32_t* head_status, int32_t* nnls_iters,
                         uint32_t* device_error_bits, void* stream) {
   if (!h || n_heads < 1 || n_heads > kMaxHeads) return LC_ERR_INVALID_ARG;

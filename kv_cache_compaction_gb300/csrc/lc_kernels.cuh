@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -158,6 +159,26 @@ cudaError_t launch_compose_idx(const int32_t* short_idx, const int32_t* pos, int
 // L2[h][j] and Delta_h the mass of the shortlist keys not chosen.
 cudaError_t launch_redistribute_beta(const float* L2, const uint8_t* chosen, const int32_t* pos,
                                      float* beta, int H, int kt, int t, cudaStream_t st);
+
+// Attention over a compacted cache plus appended tokens (decode consumer).
+struct CompactAttnParams {
+  int n, t, n_new;
+  float scale;                 // softmax scale (natural-log units)
+  const __nv_bfloat16* q;      // [H][n][d]
+  const __nv_bfloat16* Ck;     // [H][t][d]
+  const float* beta;           // [H][t]; -inf excludes the entry
+  const float* Cv;             // [H][t][d]
+  const __nv_bfloat16* Knew;   // [H][n_new][d]
+  const __nv_bfloat16* Vnew;   // [H][n_new][d]
+  const int32_t* n_vis;        // [H][n] appended tokens visible to each row, or null (all)
+  float* A;                    // [H][n][d]
+  float* log_z;                // [H][n] or null
+};
+cudaError_t launch_compact_attention(int d, const CompactAttnParams& p, int H, cudaStream_t st);
+// mass_err[h] = mean_i |lz - lse|, out_err[h] = mean_i ||A_i - O_i|| over n rows.
+cudaError_t launch_heldout_reduce(int d, const float* A, const float* lz, const float* O,
+                                  const float* lse, int H, int n, float* mass_err, float* out_err,
+                                  cudaStream_t st);
 
 struct SolveParams {
   int H, t, t_pad, d_v, max_iter;

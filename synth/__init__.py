@@ -194,6 +194,34 @@ def make(w: Workload, heads=None):
     return res
 
 
+def heldout_queries(w: Workload, K: np.ndarray, n: int, seed: int) -> np.ndarray:
+    """Held-out queries for the keys K [h, T, d] of a drawn layer, from the
+    workload's own query recipe (peaked: 0.5 * a random key of the head plus
+    N(0, 1) noise; iid: N(0, 1)) with a separate seed.  -> [h, n, d]."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    rnd = bf16_round if w.dtype == "bf16" else (lambda a: np.asarray(a, np.float32))
+    out = []
+    for Kh in np.asarray(K, np.float32):
+        if w.kind == "peaked":
+            src = rng.integers(0, Kh.shape[0], size=n)
+            q = 0.5 * Kh[src] + rng.standard_normal((n, Kh.shape[1]), dtype=np.float32)
+        else:
+            q = rng.standard_normal((n, Kh.shape[1]), dtype=np.float32)
+        out.append(rnd(q))
+    return np.stack(out)
+
+
+def appended_tokens(w: Workload, n_new: int, seed: int):
+    """Keys and values of tokens appended after compaction (question and
+    generated tokens), N(0, 1), bf16-exact for bf16 workloads.
+    -> (K_new, V_new), each [H, n_new, d]."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    rnd = bf16_round if w.dtype == "bf16" else (lambda a: np.asarray(a, np.float32))
+    Kn = rnd(rng.standard_normal((w.H, n_new, w.d), dtype=np.float32))
+    Vn = rnd(rng.standard_normal((w.H, n_new, w.d), dtype=np.float32))
+    return Kn, Vn
+
+
 def tie_heavy_scores(n_heads: int, T: int, seed: int, levels=(0.0, -1.0, -2.0)) -> np.ndarray:
     """Score arrays whose values come from a small set, so many keys tie."""
     rng = np.random.Generator(np.random.PCG64(seed))

@@ -120,3 +120,32 @@ def test_fast_workspace_grows_with_the_shortlist(lib):
     lib.lc_fast_workspace_bytes(ctypes.byref(s), 256, 32, ctypes.byref(c8))
     lib.lc_fast_workspace_bytes(ctypes.byref(s), 256, 64, ctypes.byref(c64))
     assert c8.value == c64.value
+
+
+def test_compact_attention_validates_before_any_device_work(lib):
+    vp = ctypes.c_void_p(16)  # never dereferenced: validation fails first
+    args = dict(n_heads=2, n=4, t=3, n_new=0, d=128)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return lib.lc_compact_attention(None, a["n_heads"], a["n"], a["t"], a["n_new"], a["d"],
+                                        ctypes.c_float(kw.get("scale", 0.0)), vp, vp, vp, vp,
+                                        None, None, None, vp, None, None)
+    assert call(n=0) == 1
+    assert call(n_heads=0) == 1
+    assert call(t=-1) == 1
+    assert call(n_new=2) == 1          # appended tokens without Knew / Vnew
+    assert call(d=96) == 2
+    assert call(scale=float("nan")) == 1
+    assert call() == 1                 # valid arguments, null handle
+
+
+def test_heldout_workspace_query(lib):
+    n = ctypes.c_size_t(0)
+    s = _shape(n_q=4096)
+    assert lib.lc_heldout_workspace_bytes(ctypes.byref(s), ctypes.byref(n)) == 0
+    base = ctypes.c_size_t(0)
+    lib.lc_workspace_bytes(ctypes.byref(s), ctypes.byref(base))
+    assert n.value > base.value
+    s = _shape(in_dtype=1, d=64)
+    assert lib.lc_heldout_workspace_bytes(ctypes.byref(s), ctypes.byref(n)) == 2
