@@ -203,6 +203,18 @@ lc_status lc_heldout_errors(lc_handle h, const lc_shape* shape, const void* Qh, 
                             const float* Cv, float* mass_err, float* out_err, void* workspace,
                             size_t workspace_bytes, void* stream);
 
+/* Diversifier selection by farthest-first traversal ("Latent Compaction with
+ * Test-Time Training", §3.2 Eq. (7), after Gonzalez 1985): per head, starting
+ * from the seed set S (seeds[h][0..n_seed), e.g. the anchors), repeatedly add
+ *   i* = argmax_{i not in S} min_{j in S} ||k_i - k_j||^2
+ * until |S| = M; ties go to the lower index.  K [H][T][d] bfloat16 (d = 64 or
+ * 128), seeds int32 (valid, distinct; an index outside [0, T) is ignored),
+ * out [H][M - n_seed] int32: the added keys in the order chosen (-1 past the
+ * point where no key is left).  1 <= n_seed <= M <= T.  Distances are fp32.
+ * Device pointers; no workspace. */
+lc_status lc_farthest_first(lc_handle h, int n_heads, int T, int d, const void* K,
+                            const int32_t* seeds, int n_seed, int M, int32_t* out, void* stream);
+
 /* Per-head outcome of the last lc_fit_only / lc_compact_layer on this handle:
  * head_status[H] (lc_status values), nnls_iters[H] and device error bits.
  * Synchronises `stream`.  Any pointer may be NULL. */

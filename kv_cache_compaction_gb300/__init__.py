@@ -37,7 +37,7 @@ EXPORTS = [
     "lc_compact_layer_host", "lc_get_report", "lc_profile_enable", "lc_profile_read",
     "lc_select_topt_noalloc", "lc_status_string", "lc_fast_workspace_bytes",
     "lc_compact_layer_fast", "lc_compact_attention", "lc_heldout_workspace_bytes",
-    "lc_heldout_errors",
+    "lc_heldout_errors", "lc_farthest_first",
 ]
 
 LC_BF16, LC_FP32 = 0, 1
@@ -87,6 +87,7 @@ def load_library(path: str = LIB_PATH):
                                   vp, vp, vp, vp, vp, vp], i32),
         "lc_heldout_workspace_bytes": ([sp, ctypes.POINTER(sz)], i32),
         "lc_heldout_errors": ([vp, sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
+        "lc_farthest_first": ([vp, i32, i32, i32, vp, vp, i32, i32, vp, vp], i32),
         "lc_get_report": ([vp, i32, vp, vp, vp, vp], i32),
         "lc_profile_enable": ([vp, i32], i32),
         "lc_profile_read": ([vp, i32, vp, vp, vp, vp], i32),
@@ -335,6 +336,18 @@ class Compactor:
                                           _ptr(ws), ws.numel(), self._stream()),
                "lc_heldout_errors")
         return me, oe
+
+    def farthest_first(self, K, seeds, M: int):
+        """Farthest-first traversal per head from the seeds [H, n_seed] int32
+        until M keys are selected: the added indices [H, M - n_seed] int32."""
+        torch = self._torch
+        self._check_inputs(K, seeds)
+        H, T, d = K.shape
+        n_seed = int(seeds.shape[1])
+        out = self._empty((H, max(M - n_seed, 0)), torch.int32)
+        _check(self.lib.lc_farthest_first(self.handle, H, T, d, _ptr(K), _ptr(seeds), n_seed, M,
+                                          _ptr(out), self._stream()), "lc_farthest_first")
+        return out
 
     def profile(self, on: bool):
         """Turn per-kernel CUDA-event timing of the library's launches on/off."""

@@ -1161,6 +1161,21 @@ lc_status lc_heldout_errors(lc_handle h, const lc_shape* shape, const void* Qh, 
   return LC_OK;
 }
 
+lc_status lc_farthest_first(lc_handle h, int n_heads, int T, int d, const void* K,
+                            const int32_t* seeds, int n_seed, int M, int32_t* out, void* stream) {
+  if (n_heads < 1 || n_heads > kMaxHeads || T < 1 || n_seed < 1 || M < n_seed || M > T)
+    return LC_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return LC_ERR_UNSUPPORTED;
+  if (!K || !seeds || (M > n_seed && !out)) return LC_ERR_INVALID_ARG;
+  if (M == n_seed) return LC_OK;
+  LC_TRY(enter(h));
+  FastCtx c{h, static_cast<cudaStream_t>(stream)};
+  LC_PROF(c, "farthest_first", 1);
+  LC_CUDA(launch_farthest_first(d, static_cast<const __nv_bfloat16*>(K), n_heads, T, seeds, n_seed,
+                                M - n_seed, out, c.st));
+  return LC_OK;
+}
+
 lc_status lc_get_report(lc_handle h, int n_heads, int32_t* head_status, int32_t* nnls_iters,
                         uint32_t* device_error_bits, void* stream) {
   if (!h || n_heads < 1 || n_heads > kMaxHeads) return LC_ERR_INVALID_ARG;

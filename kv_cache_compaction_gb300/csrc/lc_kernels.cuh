@@ -180,6 +180,12 @@ cudaError_t launch_heldout_reduce(int d, const float* A, const float* lz, const 
                                   const float* lse, int H, int n, float* mass_err, float* out_err,
                                   cudaStream_t st);
 
+// Farthest-first traversal per head (one thread-block cluster per head):
+// out[h][0..n_add) = the keys added after the n_seed seeds, in order.
+cudaError_t launch_farthest_first(int d, const __nv_bfloat16* K, int H, int T,
+                                  const int32_t* seeds, int n_seed, int n_add, int32_t* out,
+                                  cudaStream_t st);
+
 struct SolveParams {
   int H, t, t_pad, d_v, max_iter;
   const float* G;          // [H][t_pad][t_pad]

@@ -149,3 +149,17 @@ def test_heldout_workspace_query(lib):
     assert n.value > base.value
     s = _shape(in_dtype=1, d=64)
     assert lib.lc_heldout_workspace_bytes(ctypes.byref(s), ctypes.byref(n)) == 2
+
+
+def test_farthest_first_validates(lib):
+    vp = ctypes.c_void_p(16)  # never dereferenced: validation fails first
+
+    def call(H=2, T=100, d=128, n_seed=2, M=10, out=vp):
+        return lib.lc_farthest_first(None, H, T, d, vp, vp, n_seed, M, out, None)
+    assert call(n_seed=0) == 1
+    assert call(M=1) == 1          # fewer keys in all than seeds
+    assert call(M=101) == 1        # more than T
+    assert call(d=96) == 2
+    assert call(out=None) == 1
+    assert call(M=2, out=None) == 0  # nothing to add: no device work at all
+    assert call() == 1               # valid arguments, null handle

@@ -1,0 +1,109 @@
+"""Parity of the farthest-first traversal (diversifiers) with the float64
+oracle.  Each step takes an argmax of squared distances, which the GPU forms
+in fp32: every GPU step must be a valid choice given the seeds and the GPU's
+own earlier choices (its distance within fp32 rounding of the float64
+maximum, the key not yet selected), and the whole sequence must equal the
+oracle's as long as no step's best and second-best distances lie within that
+rounding."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from gpu_util import compactor, dev, dev_i32, host
+
+pytestmark = pytest.mark.gpu
+
+REL = 1e-5  # fp32 rounding of a sum of d squared differences, with margin
+
+
+@pytest.fixture(scope="module")
+def comp():
+    return compactor()
+
+
+def check_sequence(K, seeds, added, M):
+    K = np.asarray(K, np.float64)
+    T = K.shape[0]
+    ref = oracle.farthest_first(K, seeds, M)
+    taken = np.zeros(T, bool)
+    mind = np.full(T, np.inf)
+    for s in seeds:
+        taken[s] = True
+        mind = np.minimum(mind, ((K - K[s]) ** 2).sum(axis=1))
+    exact = True
+    n_left = T - len(seeds)
+    for step, i in enumerate(added):
+        if step >= n_left:
+            assert i == -1, "index past the end of the keys"
+            continue
+        assert 0 <= i < T and not taken[i], f"step {step}: invalid or repeated key {i}"
+        cand = np.where(taken, -np.inf, mind)
+        best = cand.max()
+        tol = REL * max(best, 1e-30)
+        assert cand[i] >= best - tol, f"step {step}: {cand[i]} < max {best}"
+        if exact:
+            top2 = np.sort(cand)[::-1][:2]
+            if len(top2) > 1 and top2[0] - top2[1] <= tol:
+                exact = False  # a near-tie: later steps may legitimately differ
+            else:
+                assert i == ref[step], f"step {step}: {i} vs oracle {ref[step]}"
+        taken[i] = True
+        mind = np.minimum(mind, ((K - K[i]) ** 2).sum(axis=1))
+    return exact
+
+
+def _run(comp, K, seeds, M):
+    out = host(comp.farthest_first(dev(K, "bf16"), dev_i32(seeds), M))
+    assert out.shape == (K.shape[0], M - seeds.shape[1])
+    return out
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_small_heads(comp, d):
+    w = synth.workload("cfg2", H=2, T=300, d=d, t=32, seed=70 + d)
+    K = synth.make(w)["K"]
+    rng = np.random.default_rng(d)
+    seeds = np.stack([rng.choice(w.T, 3, replace=False) for _ in range(w.H)]).astype(np.int32)
+    out = _run(comp, K, seeds, 40)
+    for h in range(w.H):
+        check_sequence(K[h], seeds[h], out[h], 40)
+
+
+def test_runs_out_of_keys(comp):
+    """M = T: the traversal takes every key once."""
+    w = synth.workload("cfg2", H=1, G=1, T=5, t=3, seed=9)
+    K = synth.make(w)["K"]
+    seeds = np.array([[2]], np.int32)
+    out = _run(comp, K, seeds, 5)
+    check_sequence(K[0], seeds[0], out[0], 5)
+    assert sorted(out[0].tolist() + [2]) == list(range(5))
+
+
+def test_benchmark_layer(comp):
+    """8 heads of T = 8192 (each head's keys resident across one cluster),
+    16 seeds per head (the head's top keys by the oracle's score on a query
+    sample stand in for anchors), 64 keys in all."""
+    w = synth.workload("cfg3")
+    d = synth.make(w)
+    rng = np.random.default_rng(71)
+    seeds = []
+    for h in range(w.H):
+        rows = rng.choice(w.n_q, 512, replace=False)
+        Qs = d["Q"][h][rows]
+        _, lse, _ = oracle.full_stats(Qs, d["K"][h], d["V"][h], w.softmax_scale)
+        seeds.append(oracle.select(oracle.key_scores(Qs, d["K"][h], lse, w.softmax_scale), 16))
+    seeds = np.stack(seeds).astype(np.int32)
+    out = _run(comp, d["K"], seeds, 64)
+    for h in range(w.H):
+        check_sequence(d["K"][h], seeds[h], out[h], 64)
+
+
+def test_long_context_streams_keys(comp):
+    """T = 131072 (too many keys to keep resident: they stream from memory at
+    every step), one head, 4 seeds, 24 keys in all."""
+    w = synth.workload("cfg5", H=1)
+    K = synth.make(w)["K"]
+    seeds = np.array([[0, 777, 50000, 131071]], np.int32)
+    out = _run(comp, K, seeds, 24)
+    check_sequence(K[0], seeds[0], out[0], 24)
