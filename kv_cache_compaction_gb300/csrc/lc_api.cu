@@ -599,11 +599,14 @@ struct FastPlan {
   int n_sub_pad, T_pad, kt_pad, n_q_pad, t_pad;
   float scale;
   int mass_units, mass_max;  // pass 2 scores: CTAs per query split, largest split
+  int sub_kb, sub_splits;    // pass 1 lse: key blocks per split, splits
+  int sl_chunk, sl_chunks;   // pass 2 lse: keys per resident chunk, chunks
   // workspace offsets (bytes)
   size_t qs, colb_all, lc2_sub, lse_sub;  // pass 1 over the query subset
   size_t ucode, shrt, kp, colb_short;     // scores, shortlist, its keys
   size_t lc2_q, lse_q, pos;               // pass 2 over all queries
   size_t part, L2, chosen;                // column masses of the shortlist keys
+  size_t part1, part3;                    // split partials of the two lse passes
   size_t total;
 };
 
@@ -628,6 +631,16 @@ lc_status fast_plan(const lc_shape* s, int n_sub, int k, FastPlan* out) {
   p.scale = s->scale > 0.f ? s->scale : 1.f / std::sqrt(static_cast<float>(s->d));
   p.mass_units = ((p.kt + 255) / 256) * p.H;
   p.mass_max = max_split(p.mass_units, 2, p.n_q_pad / 128);
+  {
+    // the subset's lse over all T keys: split the keys so that about two
+    // waves of CTAs run (the subset alone gives only n_sub/128 per head)
+    const int nkb = p.T_pad / 128, units = (p.n_sub_pad / 128) * p.H;
+    int ns = std::max(1, std::min(std::min(nkb, 64), (2 * 152 + units - 1) / units));
+    p.sub_kb = (nkb + ns - 1) / ns;
+    p.sub_splits = (nkb + p.sub_kb - 1) / p.sub_kb;
+    p.sl_chunk = p.kt_pad <= 256 ? p.kt_pad : (p.kt_pad % 256 == 0 ? 256 : 128);
+    p.sl_chunks = p.kt_pad / p.sl_chunk;
+  }
 
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -644,6 +657,8 @@ lc_status fast_plan(const lc_shape* s, int n_sub, int k, FastPlan* out) {
   p.shrt = take(H * p.kt * 4);
   p.kp = take(H * p.kt_pad * p.d * 2);
   p.colb_short = take(H * p.kt_pad * 4);
+  p.part1 = take(static_cast<size_t>(p.sub_splits) * H * p.n_sub_pad * 8);
+  p.part3 = p.sl_chunks > 1 ? take(static_cast<size_t>(p.sl_chunks) * H * p.n_q_pad * 8) : 0;
   p.lc2_q = take(H * p.n_q_pad * 4);
   p.lse_q = take(H * p.n_q_pad * 4);
   p.pos = take(H * p.t * 4);
@@ -697,14 +712,18 @@ lc_status run_fast(const FastCtx& c, const FastPlan& p, uint8_t* ws, const void*
   CompactLseParams cl{};
   cl.n_q = p.n_sub;
   cl.n_q_pad = p.n_sub_pad;
-  cl.t_pad = p.T_pad;
+  cl.t_pad = p.sub_kb * 128;
+  cl.key_stride = p.T_pad;
+  cl.part = reinterpret_cast<float2*>(ws + p.part1);
   cl.scale_log2 = s2;
   cl.colb2 = F(p.colb_all);
-  cl.lc2_pad = F(p.lc2_sub);
+  cl.lc2_pad = nullptr;
   cl.err = c.h->d_err;
   {
-    LC_PROF(c, "subset_lse", 2);
+    LC_PROF(c, "subset_lse", 3);
     LC_CUDA(launch_compact_lse(p.mode, mQs, mK, cl, p.H, c.st));
+    LC_CUDA(launch_merge_row_lse(cl.part, F(p.lc2_sub), p.sub_splits, p.H, p.n_sub, p.n_sub_pad,
+                                 c.st));
     LC_CUDA(launch_scale_f32(F(p.lc2_sub), F(p.lse_sub), H * p.n_sub_pad, kLn2, c.st));
   }
   KeyScoreParams ks{};
@@ -730,19 +749,22 @@ lc_status run_fast(const FastCtx& c, const FastPlan& p, uint8_t* ws, const void*
   }
 
   // ---- pass 2: every query scores the shortlist, normalised over it
+  // every query's lse over the shortlist: resident key chunks of at most
+  // 256, one partial per chunk when there are several
   cl.n_q = p.n_q;
   cl.n_q_pad = p.n_q_pad;
-  cl.t_pad = p.kt_pad;
+  cl.t_pad = p.sl_chunk;
+  cl.key_stride = p.kt_pad;
+  cl.part = p.sl_chunks > 1 ? reinterpret_cast<float2*>(ws + p.part3) : nullptr;
   cl.colb2 = F(p.colb_short);
   cl.lc2_pad = F(p.lc2_q);
   {
-    LC_PROF(c, "shortlist_lse", 2);
-    if (p.kt_pad <= 256) {
-      const int sp = best_split(p.H, c.h->sm_count, 1, p.n_q_pad / 128);
-      LC_CUDA(launch_compact_lse_resident(p.mode, mQ, mKp, cl, p.H, sp, c.st));
-    } else {
-      LC_CUDA(launch_compact_lse(p.mode, mQ, mKp, cl, p.H, c.st));
-    }
+    LC_PROF(c, "shortlist_lse", 3);
+    const int sp = best_split(p.H * p.sl_chunks, c.h->sm_count, 1, p.n_q_pad / 128);
+    LC_CUDA(launch_compact_lse_resident(p.mode, mQ, mKp, cl, p.H, sp, c.st));
+    if (cl.part)
+      LC_CUDA(launch_merge_row_lse(cl.part, F(p.lc2_q), p.sl_chunks, p.H, p.n_q, p.n_q_pad,
+                                   c.st));
     LC_CUDA(launch_scale_f32(F(p.lc2_q), F(p.lse_q), H * p.n_q_pad, kLn2, c.st));
   }
   {

@@ -961,7 +961,10 @@ __global__ void __launch_bounds__(192, 1)
   __shared__ volatile int abort_flag;
   const int warp = warp_id(), lane = lane_id();
   const int q0 = blockIdx.x * kBM, h = blockIdx.y;
-  const int nkb = p.t_pad / 128;
+  // key split z covers keys [key0, key0 + t_pad) of the key_stride padded keys
+  const int kstride = p.key_stride > 0 ? p.key_stride : p.t_pad;
+  const int key0 = blockIdx.z * p.t_pad;
+  const int nkb = max(0, min(p.t_pad, kstride - key0)) / 128;
   if (threadIdx.x == 0) {
     abort_flag = launch_aborted(p.err) ? 1 : 0;
     mbar_init(bar_q, 1);
@@ -989,7 +992,8 @@ __global__ void __launch_bounds__(192, 1)
         if (j >= 2 && !wait_bar(&k_empty[s], ((j >> 1) - 1) & 1, &abort_flag, p.err)) break;
         mbar_arrive_expect_tx(&k_full[s], L::KC_BYTES);
         for (int c = 0; c < L::NQC; ++c)
-          tma_load_3d(sK + s * L::KC_BYTES + c * 128 * 128, &mKc, &k_full[s], 64 * c, j * 128, h);
+          tma_load_3d(sK + s * L::KC_BYTES + c * 128 * 128, &mKc, &k_full[s], 64 * c,
+                      key0 + j * 128, h);
         issued = j + 1;
       }
       if (abort_flag) {
@@ -1025,7 +1029,7 @@ __global__ void __launch_bounds__(192, 1)
     const int wq = warp & 3;
     const int row = wq * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const float* cb = p.colb2 + static_cast<size_t>(h) * p.t_pad;
+    const float* cb = p.colb2 + static_cast<size_t>(h) * kstride + key0;
     float mref = -kInf, l = 0.f;
     bool ok = true;
     for (int j = 0; j < nkb; ++j) {
@@ -1058,9 +1062,14 @@ __global__ void __launch_bounds__(192, 1)
     }
     if (ok) {
       const int qr = q0 + row;
-      if (qr < p.n_q_pad)
-        p.lc2_pad[static_cast<size_t>(h) * p.n_q_pad + qr] =
-            (qr < p.n_q) ? mref + log2f(l) : kInf;
+      if (qr < p.n_q_pad) {
+        if (p.part)
+          p.part[(static_cast<size_t>(blockIdx.z) * gridDim.y + h) * p.n_q_pad + qr] =
+              make_float2(mref, l);
+        else
+          p.lc2_pad[static_cast<size_t>(h) * p.n_q_pad + qr] =
+              (qr < p.n_q) ? mref + log2f(l) : kInf;
+      }
     }
   }
   tc_fence_before();
@@ -1107,6 +1116,9 @@ __global__ void __launch_bounds__(320, 1)
   const int warp = warp_id(), lane = lane_id();
   const int h = blockIdx.y;
   const int nkb = p.t_pad / 128;
+  // key chunk z: keys [key0, key0 + t_pad) of the key_stride padded keys
+  const int kstride = p.key_stride > 0 ? p.key_stride : p.t_pad;
+  const int key0 = blockIdx.z * p.t_pad;
   const int ntiles_all = p.n_q_pad / kBM;
   const int t0 = blockIdx.x * tiles_per_split;
   const int nt = max(0, min(ntiles_all, t0 + tiles_per_split) - t0);
@@ -1132,8 +1144,9 @@ __global__ void __launch_bounds__(320, 1)
       mbar_arrive_expect_tx(k_full, nkb * 128 * D * 2 + p.t_pad * 4);
       for (int c = 0; c < L::NC; ++c)
         for (int j = 0; j < nkb; ++j)
-          tma_load_3d(sK + c * (p.t_pad * 128) + j * (128 * 128), &mKc, k_full, 64 * c, j * 128, h);
-      bulk_g2s(sCB, p.colb2 + static_cast<size_t>(h) * p.t_pad, p.t_pad * 4, k_full);
+          tma_load_3d(sK + c * (p.t_pad * 128) + j * (128 * 128), &mKc, k_full, 64 * c,
+                      key0 + j * 128, h);
+      bulk_g2s(sCB, p.colb2 + static_cast<size_t>(h) * kstride + key0, p.t_pad * 4, k_full);
       int issued = 0;
       for (int i = 0; i < nt; ++i) {
         const int s = i & 1;
@@ -1218,8 +1231,14 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_before();
       mbar_arrive(&s_free[g]);
       const int qr = (t0 + i) * kBM + row;
-      if (qr < p.n_q_pad)
-        p.lc2_pad[static_cast<size_t>(h) * p.n_q_pad + qr] = (qr < p.n_q) ? mref + log2f(l) : kInf;
+      if (qr < p.n_q_pad) {
+        if (p.part)
+          p.part[(static_cast<size_t>(blockIdx.z) * gridDim.y + h) * p.n_q_pad + qr] =
+              make_float2(mref, l);
+        else
+          p.lc2_pad[static_cast<size_t>(h) * p.n_q_pad + qr] =
+              (qr < p.n_q) ? mref + log2f(l) : kInf;
+      }
     }
   }
   tc_fence_before();
@@ -1271,7 +1290,8 @@ cudaError_t launch_cl_t(const CUtensorMap& mQ, const CUtensorMap& mKc, const Com
   auto kern = compact_lse_kernel<QK_BF16, D_QK>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
   if (e != cudaSuccess) return e;
-  dim3 grid((p.n_q + kBM - 1) / kBM, H);
+  const int kstride = p.key_stride > 0 ? p.key_stride : p.t_pad;
+  dim3 grid((p.n_q + kBM - 1) / kBM, H, (kstride + p.t_pad - 1) / p.t_pad);
   kern<<<grid, 192, L::SMEM, st>>>(mQ, mKc, p);
   return cudaGetLastError();
 }
@@ -1298,13 +1318,15 @@ cudaError_t launch_compact_lse_resident(OperandMode mode, const CUtensorMap& mQ,
                                         const CUtensorMap& mKc, const CompactLseParams& p, int H,
                                         int nsplit, cudaStream_t st) {
   if (p.t_pad > 256 || nsplit < 1) return cudaErrorInvalidValue;
+  const int kstride = p.key_stride > 0 ? p.key_stride : p.t_pad;
+  if (kstride % p.t_pad != 0 || (kstride > p.t_pad && !p.part)) return cudaErrorInvalidValue;
   const int ntiles = p.n_q_pad / kBM;
   const int tps = (ntiles + nsplit - 1) / nsplit;
   const int grid_x = (ntiles + tps - 1) / tps;
   auto go = [&](auto kern, int smem) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    kern<<<dim3(grid_x, H), 320, smem, st>>>(mQ, mKc, p, tps);
+    kern<<<dim3(grid_x, H, kstride / p.t_pad), 320, smem, st>>>(mQ, mKc, p, tps);
     return cudaGetLastError();
   };
   switch (mode) {

@@ -67,12 +67,18 @@ struct GramParams {
 };
 
 // Compact log mass per query: lc2_r = log2 sum_j 2^(s2 * S_rj + colb2_j).
+// Key splits (blockIdx.z): with key_stride > t_pad, CTA z takes keys
+// [z t_pad, (z + 1) t_pad) of key_stride padded keys (colb2 rows have
+// key_stride entries) and writes its base-2 (max, sum) per query to part
+// instead of lc2_pad; merge_row_lse combines the splits.
 struct CompactLseParams {
   int n_q, n_q_pad, t_pad;
   float scale_log2;
-  const float* colb2;      // [H][t_pad]
+  const float* colb2;      // [H][key_stride or t_pad]
   float* lc2_pad;          // [H][n_q_pad], +inf padding
   uint32_t* err;
+  int key_stride;          // 0: t_pad (no split)
+  float2* part;            // [nsplit][H][n_q_pad] or null
 };
 
 // Launchers (return cudaGetLastError()).
@@ -146,6 +152,10 @@ cudaError_t launch_reduce_gram(const float* part, float* out, int nsplit, int H,
 cudaError_t launch_mass_rows(const float* rowmax_pad, const float* lse_pad, float* rowsh2,
                              float* row_b, int H, int n_q, int n_q_pad, cudaStream_t st);
 cudaError_t launch_fill_colb2(float* colb2, int H, int t, int t_pad, cudaStream_t st);
+// lc2_pad[h][r] = log2 sum_z part_z.sum 2^(part_z.max) for r < n, +inf for
+// the padding rows n <= r < n_pad.
+cudaError_t launch_merge_row_lse(const float2* part, float* lc2_pad, int nsplit, int H, int n,
+                                 int n_pad, cudaStream_t st);
 // L2[h][j] = log2 sum_z part_z.sum 2^(part_z.max) over the nsplit partials.
 cudaError_t launch_merge_key_lse(const float2* part, float* L2, int nsplit, int H, int T,
                                  cudaStream_t st);

@@ -802,6 +802,26 @@ __global__ void merge_key_lse_kernel(const float2* part, float* L2, int nsplit, 
   }
 }
 
+__global__ void merge_row_lse_kernel(const float2* part, float* out, int nsplit, int n, int n_pad,
+                                     size_t total) {
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    if (static_cast<int>(i % n_pad) >= n) {
+      out[i] = kInf;
+      continue;
+    }
+    float m = -kInf;
+    for (int z = 0; z < nsplit; ++z) m = fmaxf(m, part[z * total + i].x);
+    float sum = 0.f;
+    if (m > -kInf)
+      for (int z = 0; z < nsplit; ++z) {
+        const float2 q = part[z * total + i];
+        if (q.x > -kInf) sum += q.y * ex2(q.x - m);
+      }
+    out[i] = m > -kInf ? m + log2f(sum) : -kInf;
+  }
+}
+
 __global__ void scale_f32_kernel(const float* in, float* out, size_t n, float mul) {
   for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<size_t>(gridDim.x) * blockDim.x)
@@ -894,6 +914,13 @@ cudaError_t launch_merge_key_lse(const float2* part, float* L, int nsplit, int H
                                  cudaStream_t st) {
   const size_t n = static_cast<size_t>(H) * T;
   merge_key_lse_kernel<<<grid_for(n), 256, 0, st>>>(part, L, nsplit, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_merge_row_lse(const float2* part, float* lc2_pad, int nsplit, int H, int n,
+                                 int n_pad, cudaStream_t st) {
+  const size_t total = static_cast<size_t>(H) * n_pad;
+  merge_row_lse_kernel<<<grid_for(total), 256, 0, st>>>(part, lc2_pad, nsplit, n, n_pad, total);
   return cudaGetLastError();
 }
 

@@ -26,6 +26,7 @@ CASES = {
     "shortlist_resident": (synth.workload("cfg2", H=2, T=1100, G=2, t=64, seed=14), 100, 4),
     "shortlist_streamed": (synth.workload("cfg2", H=2, T=1024, G=4, t=128, seed=12), 256, 4),
     "t300_k3": (synth.workload("cfg2", H=1, T=2000, G=3, t=300, seed=13), 128, 3),
+    "shortlist_chunks_of_128": (synth.workload("cfg2", H=2, T=700, G=2, t=100, seed=15), 96, 3),
     "iid_all_queries": (synth.workload("cfg2", H=1, T=640, G=2, t=64, kind="iid", seed=11),
                         None, 5),
 }
