@@ -320,295 +320,6 @@ __global__ void __launch_bounds__(192, 1)
 }
 
 // ---------------------------------------------------------------------------
-// Two-tile variant for bf16 inputs: one CTA owns 256 query rows as two tiles
-// A and B, each with its own softmax warpgroup, so the tensor core always has
-// the other tile's work while one warpgroup computes exponentials.  K and V
-// tiles stream through a 3-slot ring (load n: K_{n/2} if n is even, V_{n/2}
-// if odd).  Tensor memory: S_A, S_B, O_A, O_B, 128 columns each.  Warp roles:
-// 0 TMA, 1 MMA issue, 2..5 softmax of tile A, 6..9 softmax of tile B.
-template <int D>
-struct Attn2Layout {
-  static constexpr int NC = D / 64;
-  static constexpr int BN = 128;
-  static constexpr int Q_BYTES = kBM * D * 2;      // one tile
-  static constexpr int SLOT = BN * D * 2;          // one K or V tile
-  static constexpr int PCHUNK = kBM * 128;
-  static constexpr int P_BYTES = (BN / 64) * PCHUNK;
-  static constexpr int OFF_RING = 2 * Q_BYTES;
-  static constexpr int OFF_P = OFF_RING + 3 * SLOT;
-  static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
-  static constexpr int SMEM = 1024 + OFF_BAR + 256;
-};
-
-template <int D>
-__global__ void __launch_bounds__(320, 1)
-    attn_stats2_kernel(const __grid_constant__ CUtensorMap mQ,
-                       const __grid_constant__ CUtensorMap mK,
-                       const __grid_constant__ CUtensorMap mV, const AttnStatsParams p) {
-  using L = Attn2Layout<D>;
-  constexpr int BN = L::BN;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* base = align1024(smem_raw);
-  uint8_t* sQ = base;
-  uint8_t* sRing = base + L::OFF_RING;
-  uint8_t* sP = base + L::OFF_P;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base + L::OFF_BAR);
-  uint64_t* q_full = bars + 0;
-  uint64_t* r_full = bars + 1;    // [3]
-  uint64_t* r_empty = bars + 4;   // [3]
-  uint64_t* s_full = bars + 7;    // [2] tile A, B
-  uint64_t* s_free = bars + 9;    // [2]
-  uint64_t* p_full = bars + 11;   // [2]
-  uint64_t* pv_done = bars + 13;  // [2]
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 15);
-  __shared__ volatile int abort_flag;
-
-  const int warp = warp_id(), lane = lane_id();
-  const int q0 = blockIdx.x * (2 * kBM);
-  const int h = blockIdx.y;
-  const int nkt = (p.T + BN - 1) / BN;
-
-  if (threadIdx.x == 0) {
-    abort_flag = launch_aborted(p.err) ? 1 : 0;
-    mbar_init(q_full, 1);
-    for (int i = 0; i < 3; ++i) {
-      mbar_init(&r_full[i], 1);
-      mbar_init(&r_empty[i], 1);
-    }
-    for (int x = 0; x < 2; ++x) {
-      mbar_init(&s_full[x], 1);
-      mbar_init(&s_free[x], 128);
-      mbar_init(&p_full[x], 128);
-      mbar_init(&pv_done[x], 1);
-    }
-    fence_mbar_init();
-  }
-  if (warp == 1) tmem_alloc(tslot, 512);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tbase = *tslot;  // S_A 0, S_B 128, O_A 256, O_B 384
-
-  if (warp == 0) {
-    if (lane == 0) {
-      tma_prefetch_desc(&mQ);
-      tma_prefetch_desc(&mK);
-      tma_prefetch_desc(&mV);
-      mbar_arrive_expect_tx(q_full, 2 * L::Q_BYTES);
-      for (int x = 0; x < 2; ++x)
-        for (int c = 0; c < L::NC; ++c)
-          tma_load_3d(sQ + x * L::Q_BYTES + c * kBM * 128, &mQ, q_full, 64 * c, q0 + x * kBM, h);
-      int issued = 0;
-      for (int n = 0; n < 2 * nkt; ++n) {
-        const int sl = n % 3;
-        if (n >= 3 && !wait_bar(&r_empty[sl], ((n / 3) - 1) & 1, &abort_flag, p.err)) break;
-        uint8_t* dst = sRing + sl * L::SLOT;
-        mbar_arrive_expect_tx(&r_full[sl], L::SLOT);
-        const CUtensorMap* m = (n & 1) ? &mV : &mK;
-        for (int c = 0; c < L::NC; ++c)
-          tma_load_3d(dst + c * BN * 128, m, &r_full[sl], 64 * c, (n >> 1) * BN, h);
-        issued = n + 1;
-      }
-      if (abort_flag) {
-        for (int n = (issued > 3 ? issued - 3 : 0); n < issued; ++n) {
-          const uint64_t t0 = globaltimer_ns();
-          while (!mbar_try_wait(&r_full[n % 3], (n / 3) & 1) &&
-                 globaltimer_ns() - t0 < kWaitLimitNs) {
-          }
-        }
-      }
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_f16(kBM, BN, true, false, false);
-      constexpr uint32_t idesc_pv = idesc_f16(kBM, D, false, false, true);
-      bool ok = wait_bar(q_full, 0, &abort_flag, p.err);
-      // S_x(j) = Q_x K_j^T
-      auto issue_s = [&](int x, int j) {
-        const uint32_t aQ = smem_u32(sQ + x * L::Q_BYTES);
-        const uint32_t aK = smem_u32(sRing + ((2 * j) % 3) * L::SLOT);
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint64_t da = sdesc_sw128(aQ + (k >> 2) * (kBM * 128) + (k & 3) * 32, 16, 1024);
-          const uint64_t db = sdesc_sw128(aK + (k >> 2) * (BN * 128) + (k & 3) * 32, 16, 1024);
-          umma_f16_ss(tbase + x * 128, da, db, idesc_s, k > 0 ? 1u : 0u);
-        }
-        umma_commit(&s_full[x]);
-      };
-      // O_x += P_x V_j
-      auto issue_pv = [&](int x, int j) {
-        const uint32_t aP = smem_u32(sP + x * L::P_BYTES);
-        const uint32_t aV = smem_u32(sRing + ((2 * j + 1) % 3) * L::SLOT);
-#pragma unroll
-        for (int k = 0; k < BN / 16; ++k) {
-          const uint64_t dp = sdesc_sw128(aP + (k >> 2) * L::PCHUNK + (k & 3) * 32, 16, 1024);
-          const uint64_t dv = sdesc_sw128(aV + k * 2048, BN * 128, 1024);
-          umma_f16_ss(tbase + 256 + x * 128, dp, dv, idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
-        }
-        umma_commit(&pv_done[x]);
-      };
-      auto wait_ring = [&](int n) {
-        return wait_bar(&r_full[n % 3], (n / 3) & 1, &abort_flag, p.err);
-      };
-      if (ok && wait_ring(0)) {
-        tc_fence_after();
-        issue_s(0, 0);
-        issue_s(1, 0);
-        umma_commit(&r_empty[0]);
-      } else {
-        ok = false;
-      }
-      for (int j = 0; ok && j < nkt; ++j) {
-        // tile A: P.V, then its next scores
-        if (!wait_bar(&p_full[0], j & 1, &abort_flag, p.err) || !wait_ring(2 * j + 1)) break;
-        tc_fence_after();
-        issue_pv(0, j);
-        if (j + 1 < nkt) {
-          if (!wait_ring(2 * j + 2) || !wait_bar(&s_free[0], j & 1, &abort_flag, p.err)) break;
-          tc_fence_after();
-          issue_s(0, j + 1);
-        }
-        // tile B: P.V (frees V_j), then its next scores (frees K_{j+1})
-        if (!wait_bar(&p_full[1], j & 1, &abort_flag, p.err)) break;
-        tc_fence_after();
-        issue_pv(1, j);
-        umma_commit(&r_empty[(2 * j + 1) % 3]);
-        if (j + 1 < nkt) {
-          if (!wait_bar(&s_free[1], j & 1, &abort_flag, p.err)) break;
-          tc_fence_after();
-          issue_s(1, j + 1);
-          umma_commit(&r_empty[(2 * j + 2) % 3]);
-        }
-      }
-    }
-  } else {
-    // ------------------------------------------------------------ softmax
-    const int x = (warp - 2) >> 2;  // tile
-    const int wq = warp & 3;
-    const int row = wq * 32 + lane;
-    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t tS = tbase + x * 128, tO = tbase + 256 + x * 128;
-    uint8_t* sPx = sP + x * L::P_BYTES;
-    const float sl2 = p.scale_log2;
-    float m_ref = -kInf, m_true = -kInf, l = 0.f;
-    bool ok = true;
-    for (int j = 0; j < nkt; ++j) {
-      if (!wait_bar(&s_full[x], j & 1, &abort_flag, p.err)) { ok = false; break; }
-      tc_fence_after();
-      float xs[BN];
-      tmem_ld128(tS + lane_off, xs);
-      tc_fence_before();
-      mbar_arrive(&s_free[x]);
-      const int valid = p.T - j * BN;
-      if (valid < BN) {
-#pragma unroll
-        for (int k = 0; k < BN; ++k)
-          if (k >= valid) xs[k] = -kInf;
-      }
-      float m8[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) m8[e] = xs[e];
-#pragma unroll
-      for (int k = 8; k < BN; k += 8)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) m8[e] = fmaxf(m8[e], xs[k + e]);
-      const float mx =
-          fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * sl2;
-      m_true = fmaxf(m_true, mx);
-      const bool resc = mx > m_ref + 8.f;
-      const float new_ref = resc ? mx : m_ref;
-      const float alpha = resc ? ex2(m_ref - new_ref) : 1.f;
-      if (j > 0) {
-        if (!wait_bar(&pv_done[x], (j - 1) & 1, &abort_flag, p.err)) { ok = false; break; }
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, resc)) {
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            float o[32];
-            tmem_ld32(tO + lane_off + c * 32, o);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] *= alpha;
-            tmem_st32(tO + lane_off + c * 32, o);
-          }
-        }
-      }
-      m_ref = new_ref;
-      const float2 s2 = make_float2(sl2, sl2);
-      const float2 nm2 = make_float2(-m_ref, -m_ref);
-      float2 l4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                      make_float2(0.f, 0.f)};
-#pragma unroll
-      for (int c8 = 0; c8 < BN / 8; ++c8) {
-        float pv[8];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 a =
-              __ffma2_rn(make_float2(xs[c8 * 8 + 2 * e], xs[c8 * 8 + 2 * e + 1]), s2, nm2);
-          pv[2 * e] = ex2(a.x);
-          pv[2 * e + 1] = ex2(a.y);
-          l4[e] = __fadd2_rn(l4[e], make_float2(pv[2 * e], pv[2 * e + 1]));
-        }
-        const uint32_t off = (c8 >> 3) * L::PCHUNK + sw128_offset(row, (c8 & 7) * 8);
-        *reinterpret_cast<uint4*>(sPx + off) = pack8_f16(pv);
-      }
-      l = fmaf(l, alpha, ((l4[0].x + l4[0].y) + (l4[1].x + l4[1].y)) +
-                             ((l4[2].x + l4[2].y) + (l4[3].x + l4[3].y)));
-      fence_async_smem();
-      tc_fence_before();
-      mbar_arrive(&p_full[x]);
-    }
-    if (ok && wait_bar(&pv_done[x], (nkt - 1) & 1, &abort_flag, p.err)) {
-      tc_fence_after();
-      const int qr = q0 + x * kBM + row;
-      const size_t hq = static_cast<size_t>(h) * p.n_q;
-      const float inv_l = 1.f / l;
-      if (qr < p.n_q) {
-        const float m_nat = m_true * kLn2;
-        const float lse_nat = (m_ref + log2f(l)) * kLn2;
-        if (p.rowmax) p.rowmax[hq + qr] = m_nat;
-        if (p.lse) p.lse[hq + qr] = lse_nat;
-        if (p.rowmax_pad) p.rowmax_pad[static_cast<size_t>(h) * p.n_q_pad + qr] = m_nat;
-        if (p.lse_pad) p.lse_pad[static_cast<size_t>(h) * p.n_q_pad + qr] = lse_nat;
-      } else if (qr < p.n_q_pad) {
-        if (p.rowmax_pad) p.rowmax_pad[static_cast<size_t>(h) * p.n_q_pad + qr] = kInf;
-        if (p.lse_pad) p.lse_pad[static_cast<size_t>(h) * p.n_q_pad + qr] = kInf;
-      }
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        float o[32];
-        tmem_ld32(tO + lane_off + c * 32, o);
-        if (qr < p.n_q) {
-          const size_t off = (hq + qr) * D + c * 32;
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] *= inv_l;
-          if (p.O) {
-            float4* dst = reinterpret_cast<float4*>(p.O + off);
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-              dst[e] = make_float4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
-          }
-          if (p.O_hi) {
-            uint4* dh = reinterpret_cast<uint4*>(p.O_hi + off);
-            uint4* dl = reinterpret_cast<uint4*>(p.O_lo + off);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              uint4 hi, lo;
-              split8(o + 8 * e, hi, lo);
-              dh[e] = hi;
-              dl[e] = lo;
-            }
-          }
-        }
-      }
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) tmem_dealloc(tbase, 512);
-}
-
-// ---------------------------------------------------------------------------
 // Two-tile pass with P kept in tensor memory (bf16 inputs, P.V in one fp16
 // product).  One CTA owns 256 query rows as two tiles, each with its own
 // softmax warpgroup.  The softmax writes P_x (fp16 pairs) over the first 64
@@ -927,325 +638,6 @@ __global__ void __launch_bounds__(320, 1)
   if (warp == 1) tmem_dealloc(tbase, 512);
 }
 
-// ---------------------------------------------------------------------------
-// Compact log mass of each query under the fitted biases:
-//   lc2_r = log2 sum_j 2^(scale*log2e * S_rj + colb2_j)   (base-2 units)
-// i.e. the log-normaliser of the biased compact attention ("Latent Compaction
-// ...", §3.1 Eq. (2)-(4)).  Thread = query row; key blocks of 128 streamed.
-template <bool QK_BF16, int D_QK>
-struct CLLayout {
-  static constexpr int NQC = D_QK / 64;
-  static constexpr int Q_BYTES = kBM * D_QK * 2;
-  static constexpr int KC_BYTES = 128 * D_QK * 2;
-  static constexpr int OFF_K = Q_BYTES;
-  static constexpr int OFF_BAR = OFF_K + 2 * KC_BYTES;
-  static constexpr int SMEM = 1024 + OFF_BAR + 256;
-};
-
-template <bool QK_BF16, int D_QK>
-__global__ void __launch_bounds__(192, 1)
-    compact_lse_kernel(const __grid_constant__ CUtensorMap mQ,
-                       const __grid_constant__ CUtensorMap mKc, const CompactLseParams p) {
-  using L = CLLayout<QK_BF16, D_QK>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* base = align1024(smem_raw);
-  uint8_t* sQ = base;
-  uint8_t* sK = base + L::OFF_K;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base + L::OFF_BAR);
-  uint64_t* bar_q = bars;
-  uint64_t* k_full = bars + 1;   // [2]
-  uint64_t* k_empty = bars + 3;  // [2]
-  uint64_t* s_full = bars + 5;   // [2]
-  uint64_t* s_free = bars + 7;   // [2]
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 9);
-  __shared__ volatile int abort_flag;
-  const int warp = warp_id(), lane = lane_id();
-  const int q0 = blockIdx.x * kBM, h = blockIdx.y;
-  // key split z covers keys [key0, key0 + t_pad) of the key_stride padded keys
-  const int kstride = p.key_stride > 0 ? p.key_stride : p.t_pad;
-  const int key0 = blockIdx.z * p.t_pad;
-  const int nkb = max(0, min(p.t_pad, kstride - key0)) / 128;
-  if (threadIdx.x == 0) {
-    abort_flag = launch_aborted(p.err) ? 1 : 0;
-    mbar_init(bar_q, 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&k_full[i], 1);
-      mbar_init(&k_empty[i], 1);
-      mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 128);
-    }
-    fence_mbar_init();
-  }
-  if (warp == 1) tmem_alloc(tslot, 256);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tbase = *tslot;
-
-  if (warp == 0) {
-    if (lane == 0) {
-      mbar_arrive_expect_tx(bar_q, L::Q_BYTES);
-      for (int c = 0; c < L::NQC; ++c) tma_load_3d(sQ + c * kBM * 128, &mQ, bar_q, 64 * c, q0, h);
-      int issued = 0;
-      for (int j = 0; j < nkb; ++j) {
-        const int s = j & 1;
-        if (j >= 2 && !wait_bar(&k_empty[s], ((j >> 1) - 1) & 1, &abort_flag, p.err)) break;
-        mbar_arrive_expect_tx(&k_full[s], L::KC_BYTES);
-        for (int c = 0; c < L::NQC; ++c)
-          tma_load_3d(sK + s * L::KC_BYTES + c * 128 * 128, &mKc, &k_full[s], 64 * c,
-                      key0 + j * 128, h);
-        issued = j + 1;
-      }
-      if (abort_flag) {
-        for (int j = (issued > 2 ? issued - 2 : 0); j < issued; ++j) {
-          const uint64_t t0 = globaltimer_ns();
-          while (!mbar_try_wait(&k_full[j & 1], (j >> 1) & 1) &&
-                 globaltimer_ns() - t0 < kWaitLimitNs) {
-          }
-        }
-      }
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_f16(kBM, 128, QK_BF16, false, false);
-      bool ok = wait_bar(bar_q, 0, &abort_flag, p.err);
-      for (int j = 0; ok && j < nkb; ++j) {
-        const int s = j & 1;
-        if (!wait_bar(&k_full[s], (j >> 1) & 1, &abort_flag, p.err)) break;
-        if (j >= 2 && !wait_bar(&s_free[s], ((j >> 1) - 1) & 1, &abort_flag, p.err)) break;
-        tc_fence_after();
-        const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK + s * L::KC_BYTES);
-#pragma unroll
-        for (int k = 0; k < D_QK / 16; ++k) {
-          const uint64_t da = sdesc_sw128(aQ + (k >> 2) * (kBM * 128) + (k & 3) * 32, 16, 1024);
-          const uint64_t db = sdesc_sw128(aK + (k >> 2) * (128 * 128) + (k & 3) * 32, 16, 1024);
-          umma_f16_ss(tbase + s * 128, da, db, idesc, k > 0 ? 1u : 0u);
-        }
-        umma_commit(&s_full[s]);
-        umma_commit(&k_empty[s]);
-      }
-    }
-  } else {
-    const int wq = warp & 3;
-    const int row = wq * 32 + lane;
-    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const float* cb = p.colb2 + static_cast<size_t>(h) * kstride + key0;
-    float mref = -kInf, l = 0.f;
-    bool ok = true;
-    for (int j = 0; j < nkb; ++j) {
-      const int s = j & 1;
-      if (!wait_bar(&s_full[s], (j >> 1) & 1, &abort_flag, p.err)) { ok = false; break; }
-      tc_fence_after();
-      float x[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float v[32];
-        tmem_ld32(tbase + lane_off + s * 128 + c * 32, v);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) x[c * 32 + e] = v[e];
-      }
-      tc_fence_before();
-      mbar_arrive(&s_free[s]);
-      float mx = -kInf;
-#pragma unroll
-      for (int k = 0; k < 128; ++k) {
-        x[k] = fmaf(x[k], p.scale_log2, __ldg(cb + j * 128 + k));
-        mx = fmaxf(mx, x[k]);
-      }
-      const float nref = fmaxf(mref, mx);
-      if (nref > -kInf) {
-        l *= ex2(mref - nref);
-#pragma unroll
-        for (int k = 0; k < 128; ++k) l += ex2(x[k] - nref);
-        mref = nref;
-      }
-    }
-    if (ok) {
-      const int qr = q0 + row;
-      if (qr < p.n_q_pad) {
-        if (p.part)
-          p.part[(static_cast<size_t>(blockIdx.z) * gridDim.y + h) * p.n_q_pad + qr] =
-              make_float2(mref, l);
-        else
-          p.lc2_pad[static_cast<size_t>(h) * p.n_q_pad + qr] =
-              (qr < p.n_q) ? mref + log2f(l) : kInf;
-      }
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) tmem_dealloc(tbase, 256);
-}
-
-// Compact log mass, bf16 inputs with at most 256 selected keys: the scores of
-// a 128-query tile against all keys come from one chain of MMAs with N = t_pad
-// (C_k resident in shared memory for the whole CTA), and two epilogue
-// warpgroups take alternate tiles (S double-buffered in TMEM, 2 x 256
-// columns), each thread reducing its query's row with an online log-sum-exp.
-// CTAs are persistent over a contiguous range of query tiles of one head.
-template <int D>
-struct CL2Layout {
-  static constexpr int NC = D / 64;
-  static constexpr int KC_BYTES = 256 * D * 2;  // up to 256 keys
-  static constexpr int Q_BYTES = kBM * D * 2;
-  static constexpr int OFF_Q = KC_BYTES;
-  static constexpr int OFF_CB = OFF_Q + 2 * Q_BYTES;
-  static constexpr int OFF_BAR = OFF_CB + 256 * 4;
-  static constexpr int SMEM = 1024 + OFF_BAR + 256;
-};
-
-template <int D>
-__global__ void __launch_bounds__(320, 1)
-    compact_lse2_kernel(const __grid_constant__ CUtensorMap mQ,
-                        const __grid_constant__ CUtensorMap mKc, const CompactLseParams p,
-                        int tiles_per_split) {
-  using L = CL2Layout<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* base = align1024(smem_raw);
-  uint8_t* sK = base;
-  uint8_t* sQ = base + L::OFF_Q;
-  float* sCB = reinterpret_cast<float*>(base + L::OFF_CB);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base + L::OFF_BAR);
-  uint64_t* k_full = bars + 0;
-  uint64_t* q_full = bars + 1;   // [2]
-  uint64_t* q_empty = bars + 3;  // [2]
-  uint64_t* s_full = bars + 5;   // [2]
-  uint64_t* s_free = bars + 7;   // [2]
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 9);
-  __shared__ volatile int abort_flag;
-  const int warp = warp_id(), lane = lane_id();
-  const int h = blockIdx.y;
-  const int nkb = p.t_pad / 128;
-  // key chunk z: keys [key0, key0 + t_pad) of the key_stride padded keys
-  const int kstride = p.key_stride > 0 ? p.key_stride : p.t_pad;
-  const int key0 = blockIdx.z * p.t_pad;
-  const int ntiles_all = p.n_q_pad / kBM;
-  const int t0 = blockIdx.x * tiles_per_split;
-  const int nt = max(0, min(ntiles_all, t0 + tiles_per_split) - t0);
-  if (threadIdx.x == 0) {
-    abort_flag = launch_aborted(p.err) ? 1 : 0;
-    mbar_init(k_full, 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&q_full[i], 1);
-      mbar_init(&q_empty[i], 1);
-      mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 128);
-    }
-    fence_mbar_init();
-  }
-  if (warp == 1) tmem_alloc(tslot, 512);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tbase = *tslot;
-
-  if (warp == 0) {
-    if (lane == 0 && nt > 0) {
-      mbar_arrive_expect_tx(k_full, nkb * 128 * D * 2 + p.t_pad * 4);
-      for (int c = 0; c < L::NC; ++c)
-        for (int j = 0; j < nkb; ++j)
-          tma_load_3d(sK + c * (p.t_pad * 128) + j * (128 * 128), &mKc, k_full, 64 * c,
-                      key0 + j * 128, h);
-      bulk_g2s(sCB, p.colb2 + static_cast<size_t>(h) * kstride + key0, p.t_pad * 4, k_full);
-      int issued = 0;
-      for (int i = 0; i < nt; ++i) {
-        const int s = i & 1;
-        if (i >= 2 && !wait_bar(&q_empty[s], ((i >> 1) - 1) & 1, &abort_flag, p.err)) break;
-        mbar_arrive_expect_tx(&q_full[s], L::Q_BYTES);
-        for (int c = 0; c < L::NC; ++c)
-          tma_load_3d(sQ + s * L::Q_BYTES + c * kBM * 128, &mQ, &q_full[s], 64 * c,
-                      (t0 + i) * kBM, h);
-        issued = i + 1;
-      }
-      if (abort_flag) {
-        const uint64_t w0 = globaltimer_ns();
-        while (!mbar_try_wait(k_full, 0) && globaltimer_ns() - w0 < kWaitLimitNs) {
-        }
-        for (int i = (issued > 2 ? issued - 2 : 0); i < issued; ++i) {
-          const uint64_t w1 = globaltimer_ns();
-          while (!mbar_try_wait(&q_full[i & 1], (i >> 1) & 1) &&
-                 globaltimer_ns() - w1 < kWaitLimitNs) {
-          }
-        }
-      }
-    }
-  } else if (warp == 1) {
-    if (lane == 0 && nt > 0) {
-      const uint32_t idesc = idesc_f16(kBM, p.t_pad, true, false, false);
-      bool ok = wait_bar(k_full, 0, &abort_flag, p.err);
-      for (int i = 0; ok && i < nt; ++i) {
-        const int s = i & 1;
-        if (!wait_bar(&q_full[s], (i >> 1) & 1, &abort_flag, p.err)) break;
-        if (i >= 2 && !wait_bar(&s_free[s], ((i >> 1) - 1) & 1, &abort_flag, p.err)) break;
-        tc_fence_after();
-        const uint32_t aQ = smem_u32(sQ + s * L::Q_BYTES), aK = smem_u32(sK);
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint64_t da = sdesc_sw128(aQ + (k >> 2) * (kBM * 128) + (k & 3) * 32, 16, 1024);
-          const uint64_t db =
-              sdesc_sw128(aK + (k >> 2) * (p.t_pad * 128) + (k & 3) * 32, 16, 1024);
-          umma_f16_ss(tbase + s * 256, da, db, idesc, k > 0 ? 1u : 0u);
-        }
-        umma_commit(&s_full[s]);
-        umma_commit(&q_empty[s]);
-      }
-    }
-  } else {
-    const int g = (warp - 2) >> 2;
-    const int wq = warp & 3;
-    const int row = wq * 32 + lane;
-    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const float s2 = p.scale_log2;
-    bool ok = nt > g && wait_bar(k_full, 0, &abort_flag, p.err);
-    for (int i = g; ok && i < nt; i += 2) {
-      const int n = i >> 1;
-      if (!wait_bar(&s_full[g], n & 1, &abort_flag, p.err)) { ok = false; break; }
-      tc_fence_after();
-      float mref = -kInf, l = 0.f;
-      for (int c = 0; c < p.t_pad / 32; ++c) {
-        float v[32];
-        tmem_ld32(tbase + g * 256 + c * 32 + lane_off, v);
-        const float4* cb4 = reinterpret_cast<const float4*>(sCB + c * 32);
-        float mx = -kInf;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const float4 b = cb4[q];
-          v[4 * q] = fmaf(v[4 * q], s2, b.x);
-          v[4 * q + 1] = fmaf(v[4 * q + 1], s2, b.y);
-          v[4 * q + 2] = fmaf(v[4 * q + 2], s2, b.z);
-          v[4 * q + 3] = fmaf(v[4 * q + 3], s2, b.w);
-          mx = fmaxf(fmaxf(mx, fmaxf(v[4 * q], v[4 * q + 1])), fmaxf(v[4 * q + 2], v[4 * q + 3]));
-        }
-        const float nref = fmaxf(mref, mx);
-        if (nref > -kInf) {
-          float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            a0 += ex2(v[e] - nref);
-            a1 += ex2(v[e + 1] - nref);
-          }
-          l = l * ex2(mref - nref) + (a0 + a1);
-          mref = nref;
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(&s_free[g]);
-      const int qr = (t0 + i) * kBM + row;
-      if (qr < p.n_q_pad) {
-        if (p.part)
-          p.part[(static_cast<size_t>(blockIdx.z) * gridDim.y + h) * p.n_q_pad + qr] =
-              make_float2(mref, l);
-        else
-          p.lc2_pad[static_cast<size_t>(h) * p.n_q_pad + qr] =
-              (qr < p.n_q) ? mref + log2f(l) : kInf;
-      }
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) tmem_dealloc(tbase, 512);
-}
-
 template <bool QK_BF16, int D_QK, int D_V, int V_TERMS, int BN, int P_TERMS>
 cudaError_t launch_attn_t(const CUtensorMap& mQ, const CUtensorMap& mK, const CUtensorMap& mV,
                           const CUtensorMap& mVlo, const AttnStatsParams& p, int H,
@@ -1260,18 +652,6 @@ cudaError_t launch_attn_t(const CUtensorMap& mQ, const CUtensorMap& mK, const CU
 }
 
 template <int D>
-cudaError_t launch_attn2_t(const CUtensorMap& mQ, const CUtensorMap& mK, const CUtensorMap& mV,
-                           const AttnStatsParams& p, int H, cudaStream_t st) {
-  using L = Attn2Layout<D>;
-  auto kern = attn_stats2_kernel<D>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
-  if (e != cudaSuccess) return e;
-  dim3 grid((p.n_q + 2 * kBM - 1) / (2 * kBM), H);
-  kern<<<grid, 320, L::SMEM, st>>>(mQ, mK, mV, p);
-  return cudaGetLastError();
-}
-
-template <int D>
 cudaError_t launch_attn3_t(const CUtensorMap& mQ, const CUtensorMap& mK, const CUtensorMap& mV,
                            const AttnStatsParams& p, int H, cudaStream_t st) {
   using L = Attn3Layout<D>;
@@ -1280,19 +660,6 @@ cudaError_t launch_attn3_t(const CUtensorMap& mQ, const CUtensorMap& mK, const C
   if (e != cudaSuccess) return e;
   dim3 grid((p.n_q + 2 * kBM - 1) / (2 * kBM), H);
   kern<<<grid, 320, L::SMEM, st>>>(mQ, mK, mV, p);
-  return cudaGetLastError();
-}
-
-template <bool QK_BF16, int D_QK>
-cudaError_t launch_cl_t(const CUtensorMap& mQ, const CUtensorMap& mKc, const CompactLseParams& p,
-                        int H, cudaStream_t st) {
-  using L = CLLayout<QK_BF16, D_QK>;
-  auto kern = compact_lse_kernel<QK_BF16, D_QK>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
-  if (e != cudaSuccess) return e;
-  const int kstride = p.key_stride > 0 ? p.key_stride : p.t_pad;
-  dim3 grid((p.n_q + kBM - 1) / kBM, H, (kstride + p.t_pad - 1) / p.t_pad);
-  kern<<<grid, 192, L::SMEM, st>>>(mQ, mKc, p);
   return cudaGetLastError();
 }
 
@@ -1314,52 +681,11 @@ cudaError_t launch_attn_stats(OperandMode mode, bool split_p, const CUtensorMap&
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_compact_lse_resident(OperandMode mode, const CUtensorMap& mQ,
-                                        const CUtensorMap& mKc, const CompactLseParams& p, int H,
-                                        int nsplit, cudaStream_t st) {
-  if (p.t_pad > 256 || nsplit < 1) return cudaErrorInvalidValue;
-  const int kstride = p.key_stride > 0 ? p.key_stride : p.t_pad;
-  if (kstride % p.t_pad != 0 || (kstride > p.t_pad && !p.part)) return cudaErrorInvalidValue;
-  const int ntiles = p.n_q_pad / kBM;
-  const int tps = (ntiles + nsplit - 1) / nsplit;
-  const int grid_x = (ntiles + tps - 1) / tps;
-  auto go = [&](auto kern, int smem) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    kern<<<dim3(grid_x, H, kstride / p.t_pad), 320, smem, st>>>(mQ, mKc, p, tps);
-    return cudaGetLastError();
-  };
-  switch (mode) {
-    case kBF16d128: return go(compact_lse2_kernel<128>, CL2Layout<128>::SMEM);
-    case kBF16d64: return go(compact_lse2_kernel<64>, CL2Layout<64>::SMEM);
-    default: return cudaErrorInvalidValue;
-  }
-}
-
 int attn_stats_smem(OperandMode mode) {
   switch (mode) {
     case kBF16d128: return AttnLayout<128, 128, 1, 128, 2>::SMEM;
     case kBF16d64: return Attn3Layout<64>::SMEM;
     case kSplitF16d64: return AttnLayout<192, 64, 2, 64, 2>::SMEM;
-  }
-  return 0;
-}
-
-cudaError_t launch_compact_lse(OperandMode mode, const CUtensorMap& mQ, const CUtensorMap& mKc,
-                               const CompactLseParams& p, int H, cudaStream_t st) {
-  switch (mode) {
-    case kBF16d128: return launch_cl_t<true, 128>(mQ, mKc, p, H, st);
-    case kBF16d64: return launch_cl_t<true, 64>(mQ, mKc, p, H, st);
-    case kSplitF16d64: return launch_cl_t<false, 192>(mQ, mKc, p, H, st);
-  }
-  return cudaErrorInvalidValue;
-}
-
-int compact_lse_smem(OperandMode mode) {
-  switch (mode) {
-    case kBF16d128: return CLLayout<true, 128>::SMEM;
-    case kBF16d64: return CLLayout<true, 64>::SMEM;
-    case kSplitF16d64: return CLLayout<false, 192>::SMEM;
   }
   return 0;
 }
