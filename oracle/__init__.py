@@ -24,7 +24,9 @@ Sources (page title, then section / equation):
   "Attempt #3: Two-Pass", "Choosing beta", "Choosing C_v" (fast path,
   held-out errors).
 * [LC] §3.1 "Handling Subsequent Tokens" Eq. (4)-(5) and Appendix A.2
-  (decode-time consumer); §3.2 Eq. (7) (farthest-first diversifiers).
+  (decode-time consumer); §3.2 Eq. (7) (farthest-first diversifiers);
+  Appendix A.3 (the Attention Matching baseline: RMS attention key
+  selection, two bounded NNLS iterations with bounds [e^-3, e^3]).
 
 Readings taken where the pages leave a step open (each is also listed in the
 design notes):
@@ -48,6 +50,10 @@ design notes):
 * Held-out errors: mass error = mean over held-out queries of
   |log Z_cmp - log Z_full|, output error = mean of ||A_cmp - A_full||_2.
 * Farthest-first ties go to the lower key index.
+* Baseline variant: the RMS is over the group's reference queries; a bounded
+  iteration solves over the free weights with the pinned ones at their
+  bounds, then pins every free weight outside [lo, hi] at the bound it
+  crossed; two iterations from all-free, stopping early if nothing is pinned.
 
 Parity is pinned for every function here by the CPU tests (brute force on tiny
 inputs, closed forms, library cross-checks, invariants); see tests/.
@@ -516,3 +522,77 @@ def farthest_first(K, seeds, M):
         taken[i] = True
         mind = np.minimum(mind, ((K - K[i]) ** 2).sum(axis=1))
     return np.asarray(added, np.int64)
+
+
+# ------------------------------------------------- baseline AM variant -----
+# [LC] Appendix A.3 "Baselines and Budgets": the Attention Matching baseline
+# selects keys by RMS attention and fits the biases with two bounded
+# non-negative least-squares iterations, bounds [e^-3, e^3], then fits the
+# values by least squares.  Readings: the RMS runs over the reference queries
+# of the group; one bounded iteration solves the normal equations over the
+# free weights with the pinned ones held at their bounds and then pins every
+# free weight that left [lo, hi] at the bound it crossed (the first steps of
+# an active-set method for bound constraints), starting with every weight
+# free.
+def rms_key_scores(Q, K, lse, scale):
+    """u_j = log sqrt((1/n) sum_i p_ij^2), p_ij = exp(s q_i.k_j - lse_i): the
+    log of key j's RMS attention probability over the n queries."""
+    Q, K, lse = _f64(Q), _f64(K), _f64(lse)
+    n = Q.shape[0]
+    mx = np.full(K.shape[0], -np.inf)
+    for a, b in _chunks(n):
+        mx = np.maximum(mx, (2.0 * (scale * (Q[a:b] @ K.T) - lse[a:b, None])).max(axis=0))
+    acc = np.zeros(K.shape[0])
+    for a, b in _chunks(n):
+        acc += np.exp(2.0 * (scale * (Q[a:b] @ K.T) - lse[a:b, None]) - mx[None, :]).sum(axis=0)
+    return 0.5 * (mx + np.log(acc) - np.log(n))
+
+
+def bounded_ls(G, c, lo, hi, iters):
+    """Bounded least squares from the normal equations (G = A^T A, c = A^T b):
+    `iters` iterations of [solve G_FF w_F = c_F - G_FB w_B over the free set
+    F with the pinned set B at its bounds; pin every free w_j outside
+    [lo, hi] at the bound it crossed], starting with F = all.  Stops early
+    when an iteration pins nothing.  -> (w, iterations run)."""
+    G, c = _f64(G), _f64(c)
+    t = c.size
+    w = np.zeros(t)
+    free = np.ones(t, bool)
+    it = 0
+    while it < iters and free.any():
+        it += 1
+        F = np.flatnonzero(free)
+        B = np.flatnonzero(~free)
+        rhs = c[F] - G[np.ix_(F, B)] @ w[B]
+        x = _chol_solve(G[np.ix_(F, F)], rhs)
+        if x is None:  # not positive definite: the same ridge as the OLS fallback
+            M = G[np.ix_(F, F)]
+            x = _chol_solve(M + 1e-8 * float(np.mean(np.diag(M))) * np.eye(F.size), rhs)
+        w[F] = x
+        low = free & (w < lo)
+        high = free & (w > hi)
+        w[low] = lo
+        w[high] = hi
+        if not (low.any() or high.any()):
+            break
+        free &= ~(low | high)
+    return w, it
+
+
+def compact_head_variant(Q, K, V, t, scale, iters=2, lo=np.exp(-3.0), hi=np.exp(3.0)):
+    """The baseline AM variant for one KV head: full statistics, RMS key
+    scores, top-t selection, bounded biases (two iterations, [e^-3, e^3]),
+    least-squares values over all t keys (every w_j > 0)."""
+    m, lse, O = full_stats(Q, K, V, scale)
+    u = rms_key_scores(Q, K, lse, scale)
+    idx = select(u, t)
+    Kc = _f64(K)[idx]
+    G, c, bb = mass_system(Q, Kc, m, lse, scale)
+    w, it = bounded_ls(G, c, lo, hi, iters)
+    beta = np.log(w)
+    sup, H, R = output_system(Q, Kc, w, O, scale)
+    C, st = ols(H, R)
+    Cv = _f64(V)[idx].copy()
+    Cv[sup] = C
+    return {"m": m, "lse": lse, "O": O, "u": u, "idx": idx, "w": w, "beta": beta, "Cv": Cv,
+            "iters": it, "ols_status": st, "G": G, "c": c}

@@ -507,11 +507,95 @@ def check_farthest_first(o):
     assert len(o.farthest_first(K[:4], [0], 10)) == 3
 
 
+# ------------------------------------------------- baseline AM variant -----
+def check_rms_scores(o):
+    """RMS key scores against loops over the softmax probabilities; the RMS
+    lies between the largest probability / sqrt(n) and the largest."""
+    rng = _rng(81)
+    n, T, d = 9, 7, 3
+    Q = rng.normal(size=(n, d)) * 2
+    K = rng.normal(size=(T, d))
+    s = 0.6
+    _, lse, _ = o.full_stats(Q, K, np.zeros((T, 1)), s)
+    u = o.rms_key_scores(Q, K, lse, s)
+    for j in range(T):
+        ps = []
+        for i in range(n):
+            z = sum(math.exp(s * float(Q[i] @ K[l])) for l in range(T))
+            ps.append(math.exp(s * float(Q[i] @ K[j])) / z)
+        rms = math.sqrt(sum(p * p for p in ps) / n)
+        _close(u[j], math.log(rms), 1e-12, "RMS score vs loops")
+        assert max(ps) / math.sqrt(n) - 1e-15 <= rms <= max(ps) + 1e-15
+
+
+def check_bounded_ls(o):
+    """Bounded least squares: one iteration is the clipped unconstrained
+    solution (numpy lstsq on the design matrix); two iterations re-solve the
+    free weights with the pinned ones at their bounds (lstsq again); an
+    interior solution is returned unchanged; when the two iterations reach
+    the optimum it equals scipy's bounded-variable least squares and
+    satisfies the bound-constrained KKT conditions."""
+    from scipy.optimize import lsq_linear
+    rng = _rng(82)
+    lo, hi = math.exp(-3), math.exp(3)
+    for trial in range(20):
+        A = np.abs(rng.normal(size=(30, 5)))
+        wtrue = np.exp(rng.uniform(-5, 5, size=5))
+        b = A @ wtrue + 0.1 * rng.normal(size=30)
+        G, c = A.T @ A, A.T @ b
+        x0 = np.linalg.lstsq(A, b, rcond=None)[0]
+        w1, _ = o.bounded_ls(G, c, lo, hi, 1)
+        _close(w1, np.clip(x0, lo, hi), 1e-8 * max(1, np.abs(x0).max()), "one iteration")
+        pinned = (x0 < lo) | (x0 > hi)
+        w2, it = o.bounded_ls(G, c, lo, hi, 2)
+        if pinned.any() and not pinned.all():
+            F = ~pinned
+            wp = np.clip(x0, lo, hi)
+            xf = np.linalg.lstsq(A[:, F], b - A[:, pinned] @ wp[pinned], rcond=None)[0]
+            ref = wp.copy()
+            ref[F] = np.clip(xf, lo, hi)
+            _close(w2, ref, 1e-7 * max(1, np.abs(xf).max()), "two iterations")
+            g = G @ w2 - c
+            inside = (w2 > lo) & (w2 < hi)
+            kkt = (np.all(np.abs(g[inside]) <= 1e-6 * np.abs(c).max())
+                   and np.all(g[w2 == lo] >= -1e-6 * np.abs(c).max())
+                   and np.all(g[w2 == hi] <= 1e-6 * np.abs(c).max()))
+            if kkt:
+                ws = lsq_linear(A, b, bounds=(lo, hi), method="bvls", tol=1e-14).x
+                _close(w2, ws, 1e-6 * max(1, np.abs(ws).max()), "optimum vs BVLS")
+        if not pinned.any():
+            _close(w2, x0, 1e-8 * max(1, np.abs(x0).max()), "interior solution")
+            assert it == 1
+    # an exact interior solution comes back after one iteration
+    A = np.abs(rng.normal(size=(30, 4)))
+    wi = np.exp(rng.uniform(-1, 1, size=4))
+    w, it = o.bounded_ls(A.T @ A, A.T @ (A @ wi), lo, hi, 2)
+    _close(w, wi, 1e-9, "interior solution")
+    assert it == 1
+    # every weight pushed below the lower bound: all pinned there
+    w, it = o.bounded_ls(np.eye(3), -np.ones(3), lo, hi, 2)
+    _close(w, np.full(3, lo), 0.0, "all at the lower bound")
+
+
+def check_variant_t_equals_T(o):
+    """The baseline variant keeping every key: w = 1 lies inside [e^-3, e^3],
+    so beta = 0 and C_v = V."""
+    rng = _rng(83)
+    T, d, n_q = 10, 4, 30
+    K = rng.standard_normal((T, d))
+    Q = 0.5 * K[rng.integers(0, T, n_q)] + rng.standard_normal((n_q, d))
+    V = rng.standard_normal((T, 2))
+    r = o.compact_head_variant(Q, K, V, T, 1 / math.sqrt(d))
+    assert list(r["idx"]) == list(range(T))
+    _close(r["w"], np.ones(T), 1e-8, "variant t=T: w = 1")
+    _close(r["Cv"], V, 1e-6, "variant t=T: C_v = V")
+
+
 ALL_CHECKS = [
     check_full_stats_brute, check_full_stats_closed_forms, check_key_scores_brute,
     check_select, check_mass_system_brute, check_nnls_bruteforce, check_nnls_scipy, check_nnls_planted_and_kkt,
     check_nnls_q_zero_and_caps, check_compact_weights, check_ols, check_t_equals_T,
     check_fit_reduces_error, check_two_pass_brute, check_two_pass_full_shortlist,
     check_redistribute, check_combine_single_softmax, check_heldout_errors,
-    check_farthest_first,
+    check_farthest_first, check_rms_scores, check_bounded_ls, check_variant_t_equals_T,
 ]

@@ -148,10 +148,39 @@ def _farthest_by_sum(o):
     o.farthest_first = f
 
 
+def _rms_as_mean(o):
+    # mean attention probability instead of its root mean square
+    def f(Q, K, lse, scale):
+        Q, K, lse = np.asarray(Q, float), np.asarray(K, float), np.asarray(lse, float)
+        P = np.exp(scale * (Q @ K.T) - lse[:, None])
+        return np.log(P.mean(axis=0))
+    o.rms_key_scores = f
+
+
+def _bounded_pins_at_zero(o):
+    # the re-solve holds the pinned weights at 0 instead of their bounds
+    def f(G, c, lo, hi, iters):
+        G, c = np.asarray(G, float), np.asarray(c, float)
+        w = np.zeros(c.size)
+        free = np.ones(c.size, bool)
+        it = 0
+        while it < iters and free.any():
+            it += 1
+            F = np.flatnonzero(free)
+            w[F] = np.linalg.solve(G[np.ix_(F, F)], c[F])
+            low, high = free & (w < lo), free & (w > hi)
+            if not (low.any() or high.any()):
+                break
+            w[low], w[high] = 0.0, 0.0
+            free &= ~(low | high)
+        return np.clip(w, lo, hi), it
+    o.bounded_ls = f
+
+
 MUTANTS = [_no_scale, _unnormalised_output, _score_plus_lse, _score_min, _ties_high,
            _no_stepback, _mass_unshifted, _weights_no_bias, _ols_diag, _second_pass_full_lse,
            _delta_not_shared, _delta_by_difference, _combine_unbiased, _mass_error_signed,
-           _farthest_by_sum]
+           _farthest_by_sum, _rms_as_mean, _bounded_pins_at_zero]
 
 
 @pytest.mark.parametrize("mutate", MUTANTS, ids=lambda f: f.__name__)
