@@ -215,6 +215,28 @@ lc_status lc_heldout_errors(lc_handle h, const lc_shape* shape, const void* Qh, 
 lc_status lc_farthest_first(lc_handle h, int n_heads, int T, int d, const void* K,
                             const int32_t* seeds, int n_seed, int M, int32_t* out, void* stream);
 
+/* The Attention Matching baseline variant ("Latent Compaction with Test-Time
+ * Training", Appendix A.3): steps 1-5 with
+ *  - step 2 as RMS attention: u_j = log sqrt((1/n_q) sum_i p_ij^2),
+ *    p_ij = exp(S_ij - lse_i), top t as in step 3;
+ *  - step 4 as bounded least squares, w in [e^-3, e^3]: each iteration
+ *    solves the mass system over the free weights with the pinned ones at
+ *    their bounds, then pins every free weight outside the box at the bound
+ *    it crossed; shape->nnls_max_iter iterations (0 = two, the page's
+ *    setting), from all-free, stopping early when nothing is pinned;
+ *  - step 5 unchanged (every w_j > 0, so every key takes part).
+ * bfloat16 inputs only.  Outputs and report as lc_compact_layer; the
+ * workspace has lc_baseline_workspace_bytes(shape) bytes.
+ * lc_key_scores_rms is the RMS step alone (lse [H][n_q] given, u [H][T]). */
+lc_status lc_baseline_workspace_bytes(const lc_shape* shape, size_t* bytes);
+lc_status lc_compact_layer_baseline(lc_handle h, const lc_shape* shape, const void* Q,
+                                    const void* K, const void* V, int32_t* idx, float* w,
+                                    float* beta, float* Cv, void* workspace,
+                                    size_t workspace_bytes, void* stream);
+lc_status lc_key_scores_rms(lc_handle h, const lc_shape* shape, const void* Q, const void* K,
+                            const float* lse, float* u, void* workspace, size_t workspace_bytes,
+                            void* stream);
+
 /* Per-head outcome of the last lc_fit_only / lc_compact_layer on this handle:
  * head_status[H] (lc_status values), nnls_iters[H] and device error bits.
  * Synchronises `stream`.  Any pointer may be NULL. */

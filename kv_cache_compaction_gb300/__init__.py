@@ -37,7 +37,8 @@ EXPORTS = [
     "lc_compact_layer_host", "lc_get_report", "lc_profile_enable", "lc_profile_read",
     "lc_select_topt_noalloc", "lc_status_string", "lc_fast_workspace_bytes",
     "lc_compact_layer_fast", "lc_compact_attention", "lc_heldout_workspace_bytes",
-    "lc_heldout_errors", "lc_farthest_first",
+    "lc_heldout_errors", "lc_farthest_first", "lc_baseline_workspace_bytes",
+    "lc_compact_layer_baseline", "lc_key_scores_rms",
 ]
 
 LC_BF16, LC_FP32 = 0, 1
@@ -88,6 +89,9 @@ def load_library(path: str = LIB_PATH):
         "lc_heldout_workspace_bytes": ([sp, ctypes.POINTER(sz)], i32),
         "lc_heldout_errors": ([vp, sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
         "lc_farthest_first": ([vp, i32, i32, i32, vp, vp, i32, i32, vp, vp], i32),
+        "lc_baseline_workspace_bytes": ([sp, ctypes.POINTER(sz)], i32),
+        "lc_compact_layer_baseline": ([vp, sp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
+        "lc_key_scores_rms": ([vp, sp, vp, vp, vp, vp, vp, sz, vp], i32),
         "lc_get_report": ([vp, i32, vp, vp, vp, vp], i32),
         "lc_profile_enable": ([vp, i32], i32),
         "lc_profile_read": ([vp, i32, vp, vp, vp, vp], i32),
@@ -348,6 +352,42 @@ class Compactor:
         _check(self.lib.lc_farthest_first(self.handle, H, T, d, _ptr(K), _ptr(seeds), n_seed, M,
                                           _ptr(out), self._stream()), "lc_farthest_first")
         return out
+
+    def _baseline_ws(self, s):
+        n = ctypes.c_size_t()
+        _check(self.lib.lc_baseline_workspace_bytes(ctypes.byref(s), ctypes.byref(n)),
+               "lc_baseline_workspace_bytes")
+        return self.workspace(n.value)
+
+    def key_scores_rms(self, Q, K, lse, scale: float = 0.0):
+        """RMS key scores u[h, j] = log sqrt(mean_i p_ij^2) (bf16 Q, K)."""
+        torch = self._torch
+        self._check_inputs(Q, K, lse)
+        s = self.shape(Q, K, 1, scale)
+        ws = self._baseline_ws(s)
+        u = self._empty((K.shape[0], K.shape[1]), torch.float32)
+        _check(self.lib.lc_key_scores_rms(self.handle, ctypes.byref(s), _ptr(Q), _ptr(K),
+                                          _ptr(lse), _ptr(u), _ptr(ws), ws.numel(),
+                                          self._stream()), "lc_key_scores_rms")
+        return u
+
+    def compact_layer_baseline(self, Q, K, V, t: int, scale: float = 0.0, iters: int = 0):
+        """The baseline variant (RMS key scores, bounded biases in
+        [e^-3, e^3] with `iters` iterations, 0 = two): (idx, w, beta, Cv)."""
+        torch = self._torch
+        self._check_inputs(Q, K, V)
+        s = self.shape(Q, K, t, scale, iters)
+        ws = self._baseline_ws(s)
+        H, _, d = Q.shape
+        idx = self._empty((H, t), torch.int32)
+        w = self._empty((H, t), torch.float32)
+        beta = self._empty((H, t), torch.float32)
+        Cv = self._empty((H, t, d), torch.float32)
+        _check(self.lib.lc_compact_layer_baseline(self.handle, ctypes.byref(s), _ptr(Q), _ptr(K),
+                                                  _ptr(V), _ptr(idx), _ptr(w), _ptr(beta),
+                                                  _ptr(Cv), _ptr(ws), ws.numel(),
+                                                  self._stream()), "lc_compact_layer_baseline")
+        return idx, w, beta, Cv
 
     def profile(self, on: bool):
         """Turn per-kernel CUDA-event timing of the library's launches on/off."""

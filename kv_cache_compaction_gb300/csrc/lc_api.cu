@@ -421,9 +421,42 @@ lc_status run_pass2(const Ctx& c, const void* qop, const void* kop) {
   return LC_OK;
 }
 
+// Step 2 as RMS attention (bf16 operands): merged base-2 column masses of
+// the squared probabilities into L2, then order codes of u = log RMS in the
+// workspace's ucode (and u as floats when given).
+lc_status run_pass2_rms(const Ctx& c, const void* qop, const void* kop, float2* part, float* L2,
+                        float* u) {
+  const Plan& p = c.p;
+  CUtensorMap mQ, mK;
+  if (!make_map(&mQ, qop, true, p.d_qk, p.n_q, p.H, 128)) return LC_ERR_CUDA;
+  if (!make_map(&mK, kop, true, p.d_qk, p.T, p.H, 128)) return LC_ERR_CUDA;
+  const int nqt = p.n_q_pad / 128;
+  int split = best_split(((p.T + 255) / 256) * p.H, c.h->sm_count, 1, p.ks_max);
+  const int tiles = (nqt + split - 1) / split;
+  split = (nqt + tiles - 1) / tiles;
+  KeyScoreParams k{};
+  k.n_q_pad = p.n_q_pad;
+  k.T = p.T;
+  k.tiles_per_split = tiles;
+  k.scale = p.scale;
+  k.lse_pad = c.at<float>(p.lse_pad);
+  k.part = part;
+  k.err = c.h->d_err;
+  {
+    LC_PROF(c, "key_scores_rms", 3);
+    LC_CUDA(launch_key_scores_rms(p.mode, mK, mQ, k, p.H, split, c.st));
+    LC_CUDA(launch_merge_key_lse(part, L2, split, p.H, p.T, c.st));
+    LC_CUDA(launch_rms_finish(L2, p.n_q, c.at<uint32_t>(p.ucode), u,
+                              static_cast<size_t>(p.H) * p.T, c.st));
+  }
+  return LC_OK;
+}
+
 // Steps 4-5 from the workspace's m_pad, lse_pad, O hi/lo and the given idx.
+// bounded_iters > 0: step 4 as the bounded variant (w in [e^-3, e^3], that
+// many iterations) instead of the NNLS.
 lc_status run_fit(const Ctx& c, const void* qop, const void* kop, const void* V,
-                  const int32_t* idx, float* w, float* beta, float* Cv) {
+                  const int32_t* idx, float* w, float* beta, float* Cv, int bounded_iters = 0) {
   const Plan& p = c.p;
   const size_t H = p.H;
   const int row_bytes = p.d_qk * 2;
@@ -501,7 +534,11 @@ lc_status run_fit(const Ctx& c, const void* qop, const void* kop, const void* V,
   sp.head_status = c.h->d_status;
   sp.head_iters = c.h->d_iters;
   sp.err = c.h->d_err;
-  {
+  if (bounded_iters > 0) {
+    LC_PROF(c, "bounded_ls", 1);
+    sp.max_iter = bounded_iters;
+    LC_CUDA(launch_bounded_ls(sp, std::exp(-3.f), std::exp(3.f), c.st));
+  } else {
     LC_PROF(c, "nnls", 1);
     LC_CUDA(launch_nnls(sp, c.st));
   }
@@ -1196,6 +1233,82 @@ lc_status lc_farthest_first(lc_handle h, int n_heads, int T, int d, const void* 
   LC_CUDA(launch_farthest_first(d, static_cast<const __nv_bfloat16*>(K), n_heads, T, seeds, n_seed,
                                 M - n_seed, out, c.st));
   return LC_OK;
+}
+
+namespace {
+// The baseline variant's extra workspace: per-split column partials and the
+// merged column masses of the RMS pass, after the compaction plan's own.
+struct BaselinePlan {
+  Plan p;
+  size_t part, L2, total;
+};
+
+lc_status baseline_plan(const lc_shape* s, BaselinePlan* out) {
+  LC_TRY(validate(s));
+  if (s->in_dtype != LC_BF16) return LC_ERR_UNSUPPORTED;
+  BaselinePlan bp{};
+  bp.p = make_plan(s);
+  size_t off = bp.p.total;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = round_up(off + bytes, 256);
+    return o;
+  };
+  const size_t H = s->n_kv_heads, T = s->T;
+  bp.part = take(static_cast<size_t>(bp.p.ks_max) * H * T * 8);
+  bp.L2 = take(H * T * 4);
+  bp.total = off;
+  *out = bp;
+  return LC_OK;
+}
+}  // namespace
+
+lc_status lc_baseline_workspace_bytes(const lc_shape* shape, size_t* bytes) {
+  BaselinePlan bp;
+  LC_TRY(baseline_plan(shape, &bp));
+  if (!bytes) return LC_ERR_INVALID_ARG;
+  *bytes = bp.total;
+  return LC_OK;
+}
+
+lc_status lc_key_scores_rms(lc_handle h, const lc_shape* shape, const void* Q, const void* K,
+                            const float* lse, float* u, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+  BaselinePlan bp;
+  LC_TRY(baseline_plan(shape, &bp));
+  if (!Q || !K || !lse || !u) return LC_ERR_INVALID_ARG;
+  if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 256 || workspace_bytes < bp.total)
+    return LC_ERR_WORKSPACE;
+  LC_TRY(enter(h));
+  const Plan& p = bp.p;
+  Ctx c{h, p, static_cast<uint8_t*>(workspace), static_cast<cudaStream_t>(stream)};
+  LC_CUDA(launch_pad_rows(lse, c.at<float>(p.lse_pad), p.H, p.n_q, p.n_q_pad, kInf, c.st));
+  return run_pass2_rms(c, Q, K, c.at<float2>(bp.part), c.at<float>(bp.L2), u);
+}
+
+lc_status lc_compact_layer_baseline(lc_handle h, const lc_shape* shape, const void* Q,
+                                    const void* K, const void* V, int32_t* idx, float* w,
+                                    float* beta, float* Cv, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
+  BaselinePlan bp;
+  LC_TRY(baseline_plan(shape, &bp));
+  if (!Q || !K || !V || !idx || !w || !beta || !Cv) return LC_ERR_INVALID_ARG;
+  if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 256 || workspace_bytes < bp.total)
+    return LC_ERR_WORKSPACE;
+  LC_TRY(enter(h));
+  const Plan& p = bp.p;
+  Ctx c{h, p, static_cast<uint8_t*>(workspace), static_cast<cudaStream_t>(stream)};
+  LC_TRY(reset_report(c));
+  const void *qop, *kop;
+  LC_TRY(prepare_operands(c, Q, K, V, true, &qop, &kop));
+  LC_TRY(run_pass1(c, qop, kop, nullptr, nullptr, nullptr, true));
+  LC_TRY(run_pass2_rms(c, qop, kop, c.at<float2>(bp.part), c.at<float>(bp.L2), nullptr));
+  {
+    LC_PROF(c, "select_topt", 1);
+    LC_CUDA(launch_select_topt(c.at<uint32_t>(p.ucode), p.H, p.T, p.t, idx, c.st));
+  }
+  const int iters = shape->nnls_max_iter > 0 ? shape->nnls_max_iter : 2;
+  return run_fit(c, qop, kop, V, idx, w, beta, Cv, iters);
 }
 
 lc_status lc_get_report(lc_handle h, int n_heads, int32_t* head_status, int32_t* nnls_iters,

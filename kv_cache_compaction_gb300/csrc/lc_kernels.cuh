@@ -97,6 +97,15 @@ cudaError_t launch_key_scores(OperandMode mode, const CUtensorMap& mK, const CUt
 cudaError_t launch_key_scores_mass(OperandMode mode, const CUtensorMap& mK,
                                    const CUtensorMap& mQ, const KeyScoreParams& p, int H,
                                    int nsplit, cudaStream_t st);
+// RMS key scores (bf16 modes): per query split, p.part = (max_i b_ij,
+// sum_i 2^(b_ij - max)), b_ij = 2 log2e (s q_i.k_j - lse_pad_i).
+cudaError_t launch_key_scores_rms(OperandMode mode, const CUtensorMap& mK,
+                                  const CUtensorMap& mQ, const KeyScoreParams& p, int H,
+                                  int nsplit, cudaStream_t st);
+// From the merged L2 of the RMS pass over n_rows queries: u = log RMS
+// probability, as order codes (and floats when u is not null).
+cudaError_t launch_rms_finish(const float* L2, int n_rows, uint32_t* code, float* u, size_t n,
+                              cudaStream_t st);
 cudaError_t launch_gram(OperandMode mode, bool with_r, const CUtensorMap& mKc,
                         const CUtensorMap& mQ, const CUtensorMap& mOhi, const CUtensorMap& mOlo,
                         const GramParams& p, int H, int nsplit, cudaStream_t st);
@@ -211,6 +220,8 @@ struct SolveParams {
   uint32_t* err;
 };
 cudaError_t launch_nnls(const SolveParams& p, cudaStream_t st);
+// Bounded least squares w in [lo, hi], p.max_iter iterations (see the kernel).
+cudaError_t launch_bounded_ls(const SolveParams& p, float lo, float hi, cudaStream_t st);
 size_t solver_smem(int t);  // dynamic shared memory of the solver kernels
 
 struct OlsParams {

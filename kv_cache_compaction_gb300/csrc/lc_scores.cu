@@ -181,11 +181,14 @@ struct KS2Layout {
   static constexpr int SMEM = 1024 + OFF_BAR + 128;
 };
 
-// MASS = true: the same pass also reduces each key's column of unshifted
-// scores to its log mass, L2_j = log2 sum_{i < n_rows} 2^(s log2e q_i.k_j);
-// each query split writes its base-2 (max, sum) pair to p.part for
-// merge_key_lse.
-template <int D, bool MASS = false>
+// MODE 0: key scores only.  MODE 1 (mass): the same pass also reduces each
+// key's column of unshifted scores to its log mass,
+// L2_j = log2 sum_{i < n_rows} 2^(s log2e q_i.k_j).  MODE 2 (RMS): instead of
+// the max, each key's column of squared probabilities,
+// L2_j = log2 sum_i 2^(2 log2e a_ij), a_ij = s q_i.k_j - lse_i (padding rows,
+// lse = +inf, drop out).  Modes 1 and 2 write one base-2 (max, sum) pair per
+// query split to p.part for merge_key_lse.
+template <int D, int MODE = 0>
 __global__ void __launch_bounds__(320, 1)
     key_scores2_kernel(const __grid_constant__ CUtensorMap mK,
                        const __grid_constant__ CUtensorMap mQ, const KeyScoreParams p) {
@@ -289,7 +292,7 @@ __global__ void __launch_bounds__(320, 1)
     float u8[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) u8[e] = -kInf;
-    float mass_m = -kInf, mass_s = 0.f;  // MASS: running max and sum of 2^(b - max)
+    float mass_m = -kInf, mass_s = 0.f;  // modes 1, 2: running max and sum of 2^(b - max)
     const float2 sc2 = make_float2(p.scale, p.scale);
     const float s2 = p.scale * kLog2e;
     bool ok = ntile > 0;
@@ -308,10 +311,34 @@ __global__ void __launch_bounds__(320, 1)
         const float2 l2 = lt[e];
         const float2 a = __ffma2_rn(make_float2(v[2 * e], v[2 * e + 1]), sc2,
                                     make_float2(-l2.x, -l2.y));
-        u8[(2 * e) & 7] = fmaxf(u8[(2 * e) & 7], a.x);
-        u8[(2 * e + 1) & 7] = fmaxf(u8[(2 * e + 1) & 7], a.y);
+        if constexpr (MODE == 2) {
+          v[2 * e] = a.x * (2.f * kLog2e);
+          v[2 * e + 1] = a.y * (2.f * kLog2e);
+        } else {
+          u8[(2 * e) & 7] = fmaxf(u8[(2 * e) & 7], a.x);
+          u8[(2 * e + 1) & 7] = fmaxf(u8[(2 * e + 1) & 7], a.y);
+        }
       }
-      if constexpr (MASS) {
+      if constexpr (MODE == 2) {
+        float bm0 = -kInf, bm1 = -kInf;
+#pragma unroll
+        for (int e = 0; e < kBQ; e += 2) {
+          bm0 = fmaxf(bm0, v[e]);
+          bm1 = fmaxf(bm1, v[e + 1]);
+        }
+        const float nm = fmaxf(mass_m, fmaxf(bm0, bm1));
+        if (nm > -kInf) {
+          float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+          for (int e = 0; e < kBQ; e += 2) {
+            a0 += ex2(v[e] - nm);
+            a1 += ex2(v[e + 1] - nm);
+          }
+          mass_s = mass_s * ex2(mass_m - nm) + (a0 + a1);
+          mass_m = nm;
+        }
+      }
+      if constexpr (MODE == 1) {
         // b = base-2 score; rows past n_rows (padding) carry no mass
         float bm0 = -kInf, bm1 = -kInf;
 #pragma unroll
@@ -347,8 +374,8 @@ __global__ void __launch_bounds__(320, 1)
     const float u = fmaxf(fmaxf(fmaxf(u8[0], u8[1]), fmaxf(u8[2], u8[3])),
                           fmaxf(fmaxf(u8[4], u8[5]), fmaxf(u8[6], u8[7])));
     if (ok && key < p.T) {
-      atomicMax(p.u_code + static_cast<size_t>(h) * p.T + key, order_code(u));
-      if constexpr (MASS)
+      if constexpr (MODE != 2) atomicMax(p.u_code + static_cast<size_t>(h) * p.T + key, order_code(u));
+      if constexpr (MODE != 0)
         p.part[(static_cast<size_t>(blockIdx.z) * gridDim.y + h) * p.T + key] =
             make_float2(mass_m, mass_s);
     }
@@ -358,11 +385,11 @@ __global__ void __launch_bounds__(320, 1)
   if (warp == 1) tmem_dealloc(tbase, 512);
 }
 
-template <int D, bool MASS = false>
+template <int D, int MODE = 0>
 cudaError_t launch_ks2_t(const CUtensorMap& mK, const CUtensorMap& mQ, const KeyScoreParams& p,
                          int H, int nsplit, cudaStream_t st) {
   using L = KS2Layout<D>;
-  auto kern = key_scores2_kernel<D, MASS>;
+  auto kern = key_scores2_kernel<D, MODE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid((p.T + 2 * kBK - 1) / (2 * kBK), H, nsplit);
@@ -822,6 +849,18 @@ __global__ void merge_row_lse_kernel(const float2* part, float* out, int nsplit,
   }
 }
 
+// u_j = log of the RMS probability = (L2_j ln 2 - ln n) / 2, as an order
+// code for the selection and optionally as a float.
+__global__ void rms_finish_kernel(const float* L2, float half_log_n, uint32_t* code, float* u,
+                                  size_t n) {
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const float v = 0.5f * L2[i] * kLn2 - half_log_n;
+    if (code) code[i] = order_code(v);
+    if (u) u[i] = v;
+  }
+}
+
 __global__ void scale_f32_kernel(const float* in, float* out, size_t n, float mul) {
   for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<size_t>(gridDim.x) * blockDim.x)
@@ -904,10 +943,28 @@ cudaError_t launch_key_scores_mass(OperandMode mode, const CUtensorMap& mK,
                                    int nsplit, cudaStream_t st) {
   if (!p.part || !p.u_code) return cudaErrorInvalidValue;
   switch (mode) {
-    case kBF16d128: return launch_ks2_t<128, true>(mK, mQ, p, H, nsplit, st);
-    case kBF16d64: return launch_ks2_t<64, true>(mK, mQ, p, H, nsplit, st);
+    case kBF16d128: return launch_ks2_t<128, 1>(mK, mQ, p, H, nsplit, st);
+    case kBF16d64: return launch_ks2_t<64, 1>(mK, mQ, p, H, nsplit, st);
     default: return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t launch_key_scores_rms(OperandMode mode, const CUtensorMap& mK,
+                                  const CUtensorMap& mQ, const KeyScoreParams& p, int H,
+                                  int nsplit, cudaStream_t st) {
+  if (!p.part) return cudaErrorInvalidValue;
+  switch (mode) {
+    case kBF16d128: return launch_ks2_t<128, 2>(mK, mQ, p, H, nsplit, st);
+    case kBF16d64: return launch_ks2_t<64, 2>(mK, mQ, p, H, nsplit, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_rms_finish(const float* L2, int n_rows, uint32_t* code, float* u, size_t n,
+                              cudaStream_t st) {
+  rms_finish_kernel<<<grid_for(n), 256, 0, st>>>(L2, 0.5f * logf(static_cast<float>(n_rows)),
+                                                 code, u, n);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_merge_key_lse(const float2* part, float* L, int nsplit, int H, int T,

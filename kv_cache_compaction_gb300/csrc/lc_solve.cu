@@ -829,6 +829,102 @@ __global__ void __launch_bounds__(kThreads, 1) nnls_bpp_kernel(const SolveParams
 }
 
 
+// Bounded variant of step 4 ("Latent Compaction with Test-Time Training",
+// Appendix A.3: the Attention Matching baseline's bounded NNLS iterations,
+// bounds [lo, hi] = [e^-3, e^3]).  Each iteration solves G_FF w_F =
+// c_F - G_FB w_B over the free set F with the pinned set B at its bounds
+// (G_FF factored directly), then pins every free weight outside [lo, hi] at
+// the bound it crossed; it starts with every weight free and stops after
+// p.max_iter iterations or when an iteration pins nothing.
+__global__ void __launch_bounds__(kThreads, 1)
+    bounded_ls_kernel(const SolveParams p, float lo, float hi) {
+  extern __shared__ float dyn[];
+  __shared__ int redi[33];
+  __shared__ int bad;
+  const int h = blockIdx.x, tid = threadIdx.x, warp = warp_id(), lane = lane_id();
+  const int t = p.t, tp = p.t_pad;
+  const int n_pad = (t + kBS - 1) / kBS * kBS;
+  SolverSmem sm = carve(dyn, n_pad);
+  float* S = sm.S ? sm.S : p.mat + static_cast<size_t>(h) * tp * tp;
+  float* x = sm.vec;
+  float* cv = x + n_pad;
+  float* xb = cv + n_pad;   // pinned weights at their bounds, 0 elsewhere
+  float* aux = xb + n_pad;
+  int* freev = sm.ivec;
+  int* Fidx = freev + n_pad;
+  int* pin = Fidx + n_pad;
+  const float* G = p.G + static_cast<size_t>(h) * tp * tp;
+
+  for (int j = tid; j < n_pad; j += kThreads) {
+    cv[j] = j < t ? p.c[static_cast<size_t>(h) * tp + j] : 0.f;
+    freev[j] = j < t;
+    x[j] = 0.f;
+    xb[j] = 0.f;
+  }
+  __syncthreads();
+  int status = LC_OK_STATUS, it = 0;
+  while (it < p.max_iter) {
+    const int nF = block_compact(freev, Fidx, t, redi);
+    if (nF == 0) break;
+    ++it;
+    const int NBf = (nF + kBS - 1) / kBS;
+    gather_packed(S, NBf, nF, [&](int a, int b) {
+      return G[static_cast<size_t>(Fidx[a]) * tp + Fidx[b]];
+    });
+    // right-hand side c_F - G_FB w_B, one warp per free row
+    for (int a = warp; a < NBf * kBS; a += kWarps) {
+      float acc = 0.f;
+      if (a < nF) {
+        const float* g = G + static_cast<size_t>(Fidx[a]) * tp;
+        for (int k = lane; k < t; k += 32) acc = fmaf(g[k], xb[k], acc);
+      }
+      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(kFull, acc, o);
+      if (lane == 0) aux[a] = a < nF ? cv[Fidx[a]] - acc : 0.f;
+    }
+    __syncthreads();
+    if (!cta_cholesky(S, sm.dinv, NBf, &bad)) status = LC_SINGULAR_STATUS;
+    cta_solve1(S, sm.dinv, NBf, aux);
+    for (int a = tid; a < nF; a += kThreads) x[Fidx[a]] = aux[a];
+    __syncthreads();
+    // pin the free weights that left the box
+    int npin = 0;
+    for (int j = tid; j < t; j += kThreads) {
+      int f = 0;
+      if (freev[j]) {
+        if (x[j] < lo) {
+          x[j] = lo;
+          f = 1;
+        } else if (x[j] > hi) {
+          x[j] = hi;
+          f = 1;
+        }
+      }
+      pin[j] = f;
+      npin += f;
+    }
+    npin = block_sum_int(npin, redi);
+    if (npin == 0) break;
+    for (int j = tid; j < t; j += kThreads)
+      if (pin[j]) {
+        freev[j] = 0;
+        xb[j] = x[j];
+      }
+    __syncthreads();
+  }
+  for (int j = tid; j < tp; j += kThreads) {
+    const float wj = j < t ? fminf(fmaxf(x[j], lo), hi) : 0.f;
+    if (j < t) {
+      p.w[static_cast<size_t>(h) * t + j] = wj;
+      p.beta[static_cast<size_t>(h) * t + j] = logf(wj);
+    }
+    p.colb2[static_cast<size_t>(h) * tp + j] = j < t ? log2f(wj) : -kInf;
+  }
+  if (tid == 0) {
+    p.head_status[h] = status;
+    p.head_iters[h] = it;
+  }
+}
+
 // Step 5, part 1: factor the output system (identity rows for zero-weight
 // keys and padding) into the packed blocks in p.mat, reciprocal diagonal in
 // p.dinv; the right-hand sides of those rows become the original values.
@@ -958,6 +1054,16 @@ cudaError_t launch_nnls(const SolveParams& p, cudaStream_t st) {
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   nnls_bpp_kernel<<<p.H, kThreads, smem, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bounded_ls(const SolveParams& p, float lo, float hi, cudaStream_t st) {
+  const size_t smem = solver_smem(p.t);
+  cudaError_t e = cudaFuncSetAttribute(bounded_ls_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  bounded_ls_kernel<<<p.H, kThreads, smem, st>>>(p, lo, hi);
   return cudaGetLastError();
 }
 

@@ -163,3 +163,13 @@ def test_farthest_first_validates(lib):
     assert call(out=None) == 1
     assert call(M=2, out=None) == 0  # nothing to add: no device work at all
     assert call() == 1               # valid arguments, null handle
+
+
+def test_baseline_workspace_query(lib):
+    n, base = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    s = _shape()
+    assert lib.lc_baseline_workspace_bytes(ctypes.byref(s), ctypes.byref(n)) == 0
+    lib.lc_workspace_bytes(ctypes.byref(s), ctypes.byref(base))
+    assert n.value > base.value
+    s = _shape(in_dtype=1, d=64)
+    assert lib.lc_baseline_workspace_bytes(ctypes.byref(s), ctypes.byref(n)) == 2
