@@ -25,11 +25,11 @@
 // One CTA (512 threads) per head.  Matrices are stored as packed
 // lower-triangular 32x32 blocks (row stride 33), in shared memory when the
 // system has at most 256 unknowns, in the L2-resident workspace otherwise.
-// Cholesky is blocked right-looking: the diagonal block is factored in
-// registers by one warp with shuffles, its inverse is formed explicitly, and
-// the panel, the trailing update and both triangular solves are small
-// data-parallel products with those inverses -- no dependent chains through
-// memory.
+// Cholesky is blocked right-looking with one block of look-ahead: the
+// diagonal block is factored in registers by one warp with shuffles, the
+// panel rows are solved by substitution against it (reciprocal diagonal
+// kept; explicit block inverses lost accuracy at kappa ~ 1e6), and the
+// trailing update is a register-tiled 32x32x32 warp product.
 #include "lc_common.cuh"
 #include "lc_kernels.cuh"
 
