@@ -50,6 +50,10 @@ def args_():
                     help="steps of the two-pass / redistribution path (0: skip)")
     ap.add_argument("--fast-n-sub", type=int, default=256)
     ap.add_argument("--fast-k", type=int, default=4)
+    ap.add_argument("--sweep-layers", type=int, default=36,
+                    help="layers of the full-model sweep timed through the pipelined "
+                         "multi-layer call (0: skip)")
+    ap.add_argument("--sweep-steps", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0,
                     help="seconds of oracle work for the cpu_baseline sample")
@@ -330,6 +334,37 @@ def main():
             qkt[k] = {"tflops": tf, "frac_of_peak": tf / pk["bf16_tflops_sustained"],
                       "ms": ms}
 
+    # end to end through the host-buffer entry point
+    e2e = None
+    if a.e2e_steps > 0:
+        pinned = [tuple(x.pin_memory() for x in L) for L in layers_host]
+        hout = (torch.empty((H, t), dtype=torch.int32).pin_memory(),
+                torch.empty((H, t)).pin_memory(), torch.empty((H, t)).pin_memory(),
+                torch.empty((H, t, dd)).pin_memory())
+        for i in range(2):
+            Q, K, V = pinned[i % N_LAYERS]
+            comp.compact_layer_host(Q, K, V, t, hout)
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(a.e2e_steps):
+            Q, K, V = pinned[i % N_LAYERS]
+            comp.compact_layer_host(Q, K, V, t, hout)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms_e2e = e0.elapsed_time(e1) / a.e2e_steps
+        if dist:
+            tt = torch.tensor([ms_e2e], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            ms_e2e = float(tt.item())
+        h2d = sum(x.numel() * x.element_size() for x in pinned[0])
+        d2h = sum(x.numel() * x.element_size() for x in hout)
+        e2e = {"value": ms_e2e / world, "unit": "ms", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h}
+
     # the fast path (two-pass selection, redistributed beta, direct values)
     # on the same layers, 256-query subsets drawn per layer
     fast = None
@@ -369,36 +404,41 @@ def main():
                 "launches_per_step": sum(v[1] for v in fk.values()) / 20,
                 "per_kernel_ms": {k: v[0] / 20 for k, v in fk.items()}}
 
-    # end to end through the host-buffer entry point
-    e2e = None
-    if a.e2e_steps > 0:
-        pinned = [tuple(x.pin_memory() for x in L) for L in layers_host]
-        hout = (torch.empty((H, t), dtype=torch.int32).pin_memory(),
-                torch.empty((H, t)).pin_memory(), torch.empty((H, t)).pin_memory(),
-                torch.empty((H, t, dd)).pin_memory())
-        for i in range(2):
-            Q, K, V = pinned[i % N_LAYERS]
-            comp.compact_layer_host(Q, K, V, t, hout)
-        if dist:
-            dist.barrier()
+    # the full-model sweep (36 layers of the benchmark shape) through the
+    # pipelined multi-layer call; the layers cycle over the drawn ones
+    sweep = None
+    if a.sweep_layers > 0:
+        L = a.sweep_layers
+        SQ = torch.empty((L,) + tuple(layers[0][0].shape), dtype=torch.bfloat16, device=dev)
+        SK = torch.empty((L,) + tuple(layers[0][1].shape), dtype=torch.bfloat16, device=dev)
+        SV = torch.empty((L,) + tuple(layers[0][2].shape), dtype=torch.bfloat16, device=dev)
+        for l in range(L):
+            SQ[l].copy_(layers[l % N_LAYERS][0])
+            SK[l].copy_(layers[l % N_LAYERS][1])
+            SV[l].copy_(layers[l % N_LAYERS][2])
+        sout = (torch.empty((L, H, t), dtype=torch.int32, device=dev),
+                torch.empty((L, H, t), dtype=torch.float32, device=dev),
+                torch.empty((L, H, t), dtype=torch.float32, device=dev),
+                torch.empty((L, H, t, dd), dtype=torch.float32, device=dev))
+        comp.compact_layers(SQ, SK, SV, t, out=sout)
         torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for i in range(a.e2e_steps):
-            Q, K, V = pinned[i % N_LAYERS]
-            comp.compact_layer_host(Q, K, V, t, hout)
-        e1.record(stream)
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(a.sweep_steps):
+            comp.compact_layers(SQ, SK, SV, t, out=sout)
+        s1.record(stream)
         torch.cuda.synchronize()
-        ms_e2e = e0.elapsed_time(e1) / a.e2e_steps
-        if dist:
-            tt = torch.tensor([ms_e2e], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            ms_e2e = float(tt.item())
-        h2d = sum(x.numel() * x.element_size() for x in pinned[0])
-        d2h = sum(x.numel() * x.element_size() for x in hout)
-        e2e = {"value": ms_e2e / world, "unit": "ms", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h}
+        rep = comp.report(L * H)
+        if rep.device_error_bits:
+            raise RuntimeError("device error in the layer sweep")
+        ms_sweep = s0.elapsed_time(s1) / a.sweep_steps
+        sweep = {"workload": f"cfg4: {L} layers of the benchmark shape (inputs cycle over "
+                             f"{N_LAYERS} drawn layers), one pipelined call",
+                 "layers": L, "ms": ms_sweep, "ms_per_layer": ms_sweep / L,
+                 "serial_ms_per_layer": ms_step, "speedup_vs_serial": ms_step * L / ms_sweep,
+                 "steps": a.sweep_steps}
+        del SQ, SK, SV, sout
 
     cpu = None
     if rank == 0 and world == 1 and not a.no_cpu_baseline:
@@ -415,7 +455,7 @@ def main():
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": config_dict(w, world), "roofline": roof, "qkt": qkt,
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
-            "per_kernel": per_kernel, "fast_path": fast, "layer_tflops": fl["layer"] / (ms_step * 1e-3) / 1e12,
+            "per_kernel": per_kernel, "fast_path": fast, "sweep": sweep, "layer_tflops": fl["layer"] / (ms_step * 1e-3) / 1e12,
             "wall_s_timed": wall_s,
         }
         print(json.dumps(line), flush=True)

@@ -237,6 +237,21 @@ lc_status lc_key_scores_rms(lc_handle h, const lc_shape* shape, const void* Q, c
                             const float* lse, float* u, void* workspace, size_t workspace_bytes,
                             void* stream);
 
+/* lc_compact_layer for n_layers layers stored one after another (Q
+ * [L][H][n_q][d], K and V [L][H][T][d], idx [L][H][t], w and beta [L][H][t],
+ * Cv [L][H][t][d]) in one call, pipelined across layers: the latency-bound
+ * solves of layer l (steps 4-5, a CTA per head) run on a second stream of
+ * the handle while steps 1-3 and the mass system of layer l + 1 fill the
+ * rest of the GPU.  Two workspaces alternate between layers
+ * (lc_layers_workspace_bytes).  Results equal separate lc_compact_layer
+ * calls; the report (lc_get_report with n_heads = L*H, L*H <= 4096) holds
+ * every layer's per-head outcome in layer order.  Returns once the work is
+ * enqueued; `stream` waits for all of it. */
+lc_status lc_layers_workspace_bytes(const lc_shape* shape, int n_layers, size_t* bytes);
+lc_status lc_compact_layers(lc_handle h, const lc_shape* shape, int n_layers, const void* Q,
+                            const void* K, const void* V, int32_t* idx, float* w, float* beta,
+                            float* Cv, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Per-head outcome of the last lc_fit_only / lc_compact_layer on this handle:
  * head_status[H] (lc_status values), nnls_iters[H] and device error bits.
  * Synchronises `stream`.  Any pointer may be NULL. */

@@ -38,7 +38,8 @@ EXPORTS = [
     "lc_select_topt_noalloc", "lc_status_string", "lc_fast_workspace_bytes",
     "lc_compact_layer_fast", "lc_compact_attention", "lc_heldout_workspace_bytes",
     "lc_heldout_errors", "lc_farthest_first", "lc_baseline_workspace_bytes",
-    "lc_compact_layer_baseline", "lc_key_scores_rms",
+    "lc_compact_layer_baseline", "lc_key_scores_rms", "lc_layers_workspace_bytes",
+    "lc_compact_layers",
 ]
 
 LC_BF16, LC_FP32 = 0, 1
@@ -92,6 +93,8 @@ def load_library(path: str = LIB_PATH):
         "lc_baseline_workspace_bytes": ([sp, ctypes.POINTER(sz)], i32),
         "lc_compact_layer_baseline": ([vp, sp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
         "lc_key_scores_rms": ([vp, sp, vp, vp, vp, vp, vp, sz, vp], i32),
+        "lc_layers_workspace_bytes": ([sp, i32, ctypes.POINTER(sz)], i32),
+        "lc_compact_layers": ([vp, sp, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
         "lc_get_report": ([vp, i32, vp, vp, vp, vp], i32),
         "lc_profile_enable": ([vp, i32], i32),
         "lc_profile_read": ([vp, i32, vp, vp, vp, vp], i32),
@@ -257,6 +260,28 @@ class Compactor:
         _check(self.lib.lc_compact_layer(self.handle, ctypes.byref(s), _ptr(Q), _ptr(K), _ptr(V),
                                          _ptr(idx), _ptr(w), _ptr(beta), _ptr(Cv), _ptr(ws),
                                          ws.numel(), self._stream()), "lc_compact_layer")
+        return idx, w, beta, Cv
+
+    def compact_layers(self, Q, K, V, t: int, scale: float = 0.0, nnls_max_iter: int = 0,
+                       out=None):
+        """compact_layer for L layers in one pipelined call: Q [L, H, n_q, d],
+        K, V [L, H, T, d] -> (idx [L, H, t], w, beta [L, H, t], Cv [L, H, t, d])."""
+        torch = self._torch
+        self._check_inputs(Q, K, V)
+        L, H, _, d = Q.shape
+        s = self.shape(Q[0], K[0], t, scale, nnls_max_iter)
+        n = ctypes.c_size_t()
+        _check(self.lib.lc_layers_workspace_bytes(ctypes.byref(s), L, ctypes.byref(n)),
+               "lc_layers_workspace_bytes")
+        ws = self.workspace(n.value)
+        if out is None:
+            out = (self._empty((L, H, t), torch.int32), self._empty((L, H, t), torch.float32),
+                   self._empty((L, H, t), torch.float32), self._empty((L, H, t, d), torch.float32))
+        idx, w, beta, Cv = out
+        _check(self.lib.lc_compact_layers(self.handle, ctypes.byref(s), L, _ptr(Q), _ptr(K),
+                                          _ptr(V), _ptr(idx), _ptr(w), _ptr(beta), _ptr(Cv),
+                                          _ptr(ws), ws.numel(), self._stream()),
+               "lc_compact_layers")
         return idx, w, beta, Cv
 
     def compact_layer_host(self, Q, K, V, t: int, out, scale: float = 0.0, nnls_max_iter: int = 0):

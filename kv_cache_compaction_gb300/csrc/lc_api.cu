@@ -270,6 +270,9 @@ struct lc_context {
   cudaEvent_t ev_start = nullptr;
   cudaEvent_t ev_copy[kGroups] = {};
   cudaEvent_t ev_p1[kGroups] = {};
+  // multi-layer entry point: the solve stream and its hand-off events
+  cudaStream_t fit_st = nullptr;
+  cudaEvent_t ev_mass[2] = {}, ev_fit[2] = {}, ev_begin = nullptr;
 };
 
 namespace {
@@ -453,13 +456,25 @@ lc_status run_pass2_rms(const Ctx& c, const void* qop, const void* kop, float2* 
 }
 
 // Steps 4-5 from the workspace's m_pad, lse_pad, O hi/lo and the given idx.
+lc_status run_fit_solve(const Ctx& c, const void* qop, const void* V, const int32_t* idx,
+                        float* w, float* beta, float* Cv, int bounded_iters, int status_off,
+                        const CUtensorMap& mKc, const CUtensorMap& mQ64, const CUtensorMap& mOhi,
+                        const CUtensorMap& mOlo, GramParams g, int g7_split, int g7_slabs,
+                        int r_split, int r_slabs);
+
 // bounded_iters > 0: step 4 as the bounded variant (w in [e^-3, e^3], that
-// many iterations) instead of the NNLS.
-lc_status run_fit(const Ctx& c, const void* qop, const void* kop, const void* V,
-                  const int32_t* idx, float* w, float* beta, float* Cv, int bounded_iters = 0) {
-  const Plan& p = c.p;
+// many iterations) instead of the NNLS.  The mass system is built on c's
+// stream; from the solve on, the work goes to `cs` (the same context, or one
+// on another stream that waits for `handoff`).  Per-head outcomes go to the
+// report at head offset status_off.
+lc_status run_fit(const Ctx& ca, const void* qop, const void* kop, const void* V,
+                  const int32_t* idx, float* w, float* beta, float* Cv, int bounded_iters = 0,
+                  const Ctx* cs = nullptr, cudaEvent_t handoff = nullptr, int status_off = 0) {
+  const Ctx* cp = &ca;
+  const Plan& p = ca.p;
   const size_t H = p.H;
   const int row_bytes = p.d_qk * 2;
+  const Ctx& c = ca;
   {
     LC_PROF(c, "gather_keys", 1);
     LC_CUDA(launch_gather_rows(kop, c.ws + p.kc, idx, p.H, p.T, p.t, p.t_pad, row_bytes, c.st));
@@ -517,6 +532,23 @@ lc_status run_fit(const Ctx& c, const void* qop, const void* kop, const void* V,
     LC_CUDA(launch_reduce_partials(c.at<float>(p.cpart), c.at<float>(p.c), g5_split, H * p.t_pad,
                                    c.st));
   }
+  if (cs && cs->st != ca.st) {
+    LC_CUDA(cudaEventRecord(handoff, ca.st));
+    LC_CUDA(cudaStreamWaitEvent(cs->st, handoff, 0));
+    cp = cs;
+  }
+  return run_fit_solve(*cp, qop, V, idx, w, beta, Cv, bounded_iters, status_off, mKc, mQ64, mOhi,
+                       mOlo, g, g7_split, g7_slabs, r_split, r_slabs);
+}
+
+// Steps 4 (solve) and 5 of run_fit.
+lc_status run_fit_solve(const Ctx& c, const void* qop, const void* V, const int32_t* idx,
+                        float* w, float* beta, float* Cv, int bounded_iters, int status_off,
+                        const CUtensorMap& mKc, const CUtensorMap& mQ64, const CUtensorMap& mOhi,
+                        const CUtensorMap& mOlo, GramParams g, int g7_split, int g7_slabs,
+                        int r_split, int r_slabs) {
+  const Plan& p = c.p;
+  const size_t H = p.H;
   SolveParams sp{};
   sp.H = p.H;
   sp.t = p.t;
@@ -531,8 +563,8 @@ lc_status run_fit(const Ctx& c, const void* qop, const void* kop, const void* V,
   sp.mat = c.at<float>(p.mat);
   sp.vec = c.at<float>(p.vec);
   sp.wbuf = c.at<float>(p.wbuf);
-  sp.head_status = c.h->d_status;
-  sp.head_iters = c.h->d_iters;
+  sp.head_status = c.h->d_status + status_off;
+  sp.head_iters = c.h->d_iters + status_off;
   sp.err = c.h->d_err;
   if (bounded_iters > 0) {
     LC_PROF(c, "bounded_ls", 1);
@@ -604,7 +636,7 @@ lc_status run_fit(const Ctx& c, const void* qop, const void* kop, const void* V,
   op.mat = c.at<float>(p.mat);
   op.dinv = c.at<float>(p.vec);
   op.Cv = Cv;
-  op.head_status = c.h->d_status;
+  op.head_status = c.h->d_status + status_off;
   op.err = c.h->d_err;
   {
     LC_PROF(c, "ols", 2);
@@ -881,6 +913,12 @@ lc_status lc_destroy(lc_handle h) {
   }
   if (h->ev_start) cudaEventDestroy(h->ev_start);
   if (h->copy_st) cudaStreamDestroy(h->copy_st);
+  for (int b = 0; b < 2; ++b) {
+    if (h->ev_mass[b]) cudaEventDestroy(h->ev_mass[b]);
+    if (h->ev_fit[b]) cudaEventDestroy(h->ev_fit[b]);
+  }
+  if (h->ev_begin) cudaEventDestroy(h->ev_begin);
+  if (h->fit_st) cudaStreamDestroy(h->fit_st);
   delete h;
   return LC_OK;
 }
@@ -1309,6 +1347,71 @@ lc_status lc_compact_layer_baseline(lc_handle h, const lc_shape* shape, const vo
   }
   const int iters = shape->nnls_max_iter > 0 ? shape->nnls_max_iter : 2;
   return run_fit(c, qop, kop, V, idx, w, beta, Cv, iters);
+}
+
+lc_status lc_layers_workspace_bytes(const lc_shape* shape, int n_layers, size_t* bytes) {
+  LC_TRY(validate(shape));
+  if (!bytes || n_layers < 1) return LC_ERR_INVALID_ARG;
+  *bytes = (n_layers > 1 ? 2 : 1) * make_plan(shape).total;
+  return LC_OK;
+}
+
+lc_status lc_compact_layers(lc_handle h, const lc_shape* shape, int n_layers, const void* Q,
+                            const void* K, const void* V, int32_t* idx, float* w, float* beta,
+                            float* Cv, void* workspace, size_t workspace_bytes, void* stream) {
+  LC_TRY(validate(shape));
+  if (n_layers < 1 || static_cast<long long>(n_layers) * shape->n_kv_heads > kMaxHeads)
+    return LC_ERR_INVALID_ARG;
+  if (!Q || !K || !V || !idx || !w || !beta || !Cv) return LC_ERR_INVALID_ARG;
+  const Plan p = make_plan(shape);
+  const int nb = n_layers > 1 ? 2 : 1;
+  if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 256 ||
+      workspace_bytes < nb * p.total)
+    return LC_ERR_WORKSPACE;
+  LC_TRY(enter(h));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (!h->fit_st) LC_CUDA(cudaStreamCreateWithFlags(&h->fit_st, cudaStreamNonBlocking));
+  if (!h->ev_begin) LC_CUDA(cudaEventCreateWithFlags(&h->ev_begin, cudaEventDisableTiming));
+  for (int b = 0; b < 2; ++b) {
+    if (!h->ev_mass[b]) LC_CUDA(cudaEventCreateWithFlags(&h->ev_mass[b], cudaEventDisableTiming));
+    if (!h->ev_fit[b]) LC_CUDA(cudaEventCreateWithFlags(&h->ev_fit[b], cudaEventDisableTiming));
+  }
+  const size_t H = p.H, LH = static_cast<size_t>(n_layers) * H;
+  LC_CUDA(cudaMemsetAsync(h->d_status, 0, sizeof(int32_t) * LH, st));
+  LC_CUDA(cudaMemsetAsync(h->d_iters, 0, sizeof(int32_t) * LH, st));
+  LC_CUDA(cudaMemsetAsync(h->d_err, 0, sizeof(uint32_t), st));
+  // the solve stream starts after the caller's earlier work and the resets
+  LC_CUDA(cudaEventRecord(h->ev_begin, st));
+  LC_CUDA(cudaStreamWaitEvent(h->fit_st, h->ev_begin, 0));
+  const size_t el = p.bf16_in ? 2 : 4;
+  const size_t qs = H * p.n_q * p.d * el, ks = H * p.T * p.d * el;
+  for (int l = 0; l < n_layers; ++l) {
+    const int b = l & 1;
+    uint8_t* wsb = static_cast<uint8_t*>(workspace) + b * p.total;
+    Ctx ca{h, p, wsb, st};
+    Ctx cs{h, p, wsb, h->fit_st};
+    // workspace b is free once layer l - 2 has finished its solve
+    if (l >= 2) LC_CUDA(cudaStreamWaitEvent(st, h->ev_fit[b], 0));
+    const void* Ql = static_cast<const uint8_t*>(Q) + l * qs;
+    const void* Kl = static_cast<const uint8_t*>(K) + l * ks;
+    const void* Vl = static_cast<const uint8_t*>(V) + l * ks;
+    int32_t* idxl = idx + l * H * p.t;
+    const void *qop, *kop;
+    LC_TRY(prepare_operands(ca, Ql, Kl, Vl, true, &qop, &kop));
+    LC_TRY(run_pass1(ca, qop, kop, nullptr, nullptr, nullptr, true));
+    LC_TRY(run_pass2(ca, qop, kop));
+    {
+      LC_PROF(ca, "select_topt", 1);
+      LC_CUDA(launch_select_topt(ca.at<uint32_t>(p.ucode), p.H, p.T, p.t, idxl, st));
+    }
+    LC_TRY(run_fit(ca, qop, kop, Vl, idxl, w + l * H * p.t, beta + l * H * p.t,
+                   Cv + l * H * p.t * p.d, 0, &cs, h->ev_mass[b], l * p.H));
+    LC_CUDA(cudaEventRecord(h->ev_fit[b], h->fit_st));
+  }
+  // the caller's stream resumes when the last solve is done (the solve
+  // stream is in order, so that covers every layer)
+  LC_CUDA(cudaStreamWaitEvent(st, h->ev_fit[(n_layers - 1) & 1], 0));
+  return LC_OK;
 }
 
 lc_status lc_get_report(lc_handle h, int n_heads, int32_t* head_status, int32_t* nnls_iters,

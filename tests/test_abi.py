@@ -173,3 +173,12 @@ def test_baseline_workspace_query(lib):
     assert n.value > base.value
     s = _shape(in_dtype=1, d=64)
     assert lib.lc_baseline_workspace_bytes(ctypes.byref(s), ctypes.byref(n)) == 2
+
+
+def test_layers_workspace_query(lib):
+    one, two = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    s = _shape()
+    assert lib.lc_layers_workspace_bytes(ctypes.byref(s), 1, ctypes.byref(one)) == 0
+    assert lib.lc_layers_workspace_bytes(ctypes.byref(s), 36, ctypes.byref(two)) == 0
+    assert two.value == 2 * one.value
+    assert lib.lc_layers_workspace_bytes(ctypes.byref(s), 0, ctypes.byref(one)) == 1
