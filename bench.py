@@ -39,6 +39,29 @@ WORKLOAD = "cfg3"
 N_LAYERS = 4
 
 
+def rank_layer_ids(rank: int, n_layers: int = N_LAYERS):
+    """Layer indices (generator seeds) a rank compacts: ranks own disjoint
+    layers, so per-GPU work is fixed as the job grows (weak scaling)."""
+    return [rank * n_layers + l for l in range(n_layers)]
+
+
+def max_over_ranks(x: float, dist=None, device=None) -> float:
+    """The largest value of x over all ranks: a step of the job takes as long
+    as its slowest rank."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(ms_step_max: float, world: int) -> float:
+    """ms per compacted layer over the whole job: each of the `world` ranks
+    compacts one layer per step."""
+    return ms_step_max / world
+
+
 def args_():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -257,7 +280,7 @@ def main():
     layers_host = []
     layers = []
     for l in range(N_LAYERS):
-        d = synth.make(w.layer(rank * N_LAYERS + l))
+        d = synth.make(w.layer(rank_layer_ids(rank)[l]))
         hq, hk, hv = up(d["Q"]), up(d["K"]), up(d["V"])
         layers_host.append((hq, hk, hv))
         layers.append((hq.to(dev), hk.to(dev), hv.to(dev)))
@@ -302,12 +325,8 @@ def main():
     comp.profile(False)
     kern = comp.profile_read()
     ms_total = ev0.elapsed_time(ev1)
-    ms_step = ms_total / a.steps
-    if dist:
-        tt = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_step = float(tt.item())
-    value = ms_step / world   # whole job: `world` layers per step
+    ms_step = max_over_ranks(ms_total / a.steps, dist, dev)
+    value = job_value(ms_step, world)
 
     # per-kernel breakdown (per step) and the dominant kernel's roofline
     pk = peaks()
@@ -355,14 +374,10 @@ def main():
             comp.compact_layer_host(Q, K, V, t, hout)
         e1.record(stream)
         torch.cuda.synchronize()
-        ms_e2e = e0.elapsed_time(e1) / a.e2e_steps
-        if dist:
-            tt = torch.tensor([ms_e2e], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            ms_e2e = float(tt.item())
+        ms_e2e = max_over_ranks(e0.elapsed_time(e1) / a.e2e_steps, dist, dev)
         h2d = sum(x.numel() * x.element_size() for x in pinned[0])
         d2h = sum(x.numel() * x.element_size() for x in hout)
-        e2e = {"value": ms_e2e / world, "unit": "ms", "h2d_bytes_per_step": h2d,
+        e2e = {"value": job_value(ms_e2e, world), "unit": "ms", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h}
 
     # the fast path (two-pass selection, redistributed beta, direct values)
