@@ -77,6 +77,8 @@ def args_():
                     help="layers of the full-model sweep timed through the pipelined "
                          "multi-layer call (0: skip)")
     ap.add_argument("--sweep-steps", type=int, default=3)
+    ap.add_argument("--quality-queries", type=int, default=4096,
+                    help="held-out queries per head for the quality comparison (0: skip)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0,
                     help="seconds of oracle work for the cpu_baseline sample")
@@ -281,6 +283,8 @@ def main():
     layers = []
     for l in range(N_LAYERS):
         d = synth.make(w.layer(rank_layer_ids(rank)[l]))
+        if l == 0:
+            K0 = d["K"]
         hq, hk, hv = up(d["Q"]), up(d["K"]), up(d["V"])
         layers_host.append((hq, hk, hv))
         layers.append((hq.to(dev), hk.to(dev), hv.to(dev)))
@@ -455,6 +459,35 @@ def main():
                  "steps": a.sweep_steps}
         del SQ, SK, SV, sout
 
+    # quality of three compactions of the first layer on held-out queries
+    # drawn from the same recipe: attention matching (NNLS beta, OLS values),
+    # the fast path (two-pass keys, redistributed beta, direct values) and
+    # the baseline variant (RMS keys, bounded beta, OLS values)
+    quality = None
+    if a.quality_queries > 0:
+        Qh = up(synth.heldout_queries(w, K0, a.quality_queries, 9001)).to(dev)
+        Q, K, V = layers[0]
+        qsel0 = torch.from_numpy(np.stack([
+            np.random.default_rng(2000 + h).choice(w.n_q, a.fast_n_sub, replace=False)
+            for h in range(H)]).astype(np.int32)).to(dev)
+
+        def errs(idx, beta, Cv):
+            me, oe = comp.heldout_errors(Qh, K, V, idx, beta, Cv)
+            return {"mass_err": float(me.mean()), "out_err": float(oe.mean())}
+
+        i1, _, b1, c1 = comp.compact_layer(Q, K, V, t)
+        i2, b2, c2 = comp.compact_layer_fast(Q, K, V, qsel0, t, a.fast_k)
+        i3, _, b3, c3 = comp.compact_layer_baseline(Q, K, V, t)
+        quality = {"heldout_queries_per_head": a.quality_queries,
+                   "definition": "per head mean |log Z_cmp - log Z_full| and mean "
+                                 "||A_cmp - A_full||_2 over held-out queries, averaged over heads",
+                   "attention_matching": errs(i1, b1, c1),
+                   "fast_path": errs(i2, b2, c2),
+                   "baseline_variant": errs(i3, b3, c3)}
+        torch.cuda.synchronize()
+        if comp.report(H).device_error_bits:
+            raise RuntimeError("device error in the quality comparison")
+
     cpu = None
     if rank == 0 and world == 1 and not a.no_cpu_baseline:
         ms_l, n, t_s = oracle_sample(a.cpu_budget)
@@ -470,7 +503,7 @@ def main():
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": config_dict(w, world), "roofline": roof, "qkt": qkt,
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
-            "per_kernel": per_kernel, "fast_path": fast, "sweep": sweep, "layer_tflops": fl["layer"] / (ms_step * 1e-3) / 1e12,
+            "per_kernel": per_kernel, "fast_path": fast, "sweep": sweep, "quality": quality, "layer_tflops": fl["layer"] / (ms_step * 1e-3) / 1e12,
             "wall_s_timed": wall_s,
         }
         print(json.dumps(line), flush=True)
