@@ -273,6 +273,9 @@ struct lc_context {
   // multi-layer entry point: the solve stream and its hand-off events
   cudaStream_t fit_st = nullptr;
   cudaEvent_t ev_mass[2] = {}, ev_fit[2] = {}, ev_begin = nullptr;
+  // step 5: the auxiliary stream of the output-system factorisation
+  cudaStream_t aux_st = nullptr;
+  cudaEvent_t ev_h = nullptr, ev_f = nullptr;
 };
 
 namespace {
@@ -602,28 +605,6 @@ lc_status run_fit_solve(const Ctx& c, const void* qop, const void* V, const int3
   g.Gpart = c.at<float>(p.hpart);
   g.cpart = nullptr;
   g.Rpart = c.at<float>(p.rpart);
-  if (p.all_pairs) {
-    {
-      LC_PROF(c, "gram_out", 1);
-      LC_CUDA(launch_gram_all_pairs(p.mode, mKc, mQ64, mOhi, mOlo, g, p.H, g7_split, c.st));
-    }
-    GramParams gr = g;
-    gr.r_only = 1;
-    gr.slabs_per_split = r_slabs;
-    LC_PROF(c, "gram_r", 1);
-    LC_CUDA(launch_gram_r(p.mode, mKc, mQ64, mOhi, mOlo, gr, p.H, r_split, c.st));
-  } else {
-    LC_PROF(c, "gram_out", 1);
-    LC_CUDA(launch_gram(p.mode, true, mKc, mQ64, mOhi, mOlo, g, p.H, g7_split, c.st));
-  }
-  {
-    LC_PROF(c, "reduce_out", 3);
-    LC_CUDA(launch_reduce_gram(c.at<float>(p.hpart), c.at<float>(p.Hm), g7_split, p.H, p.t_pad, c.st));
-    LC_CUDA(launch_reduce_partials(c.at<float>(p.rpart), c.at<float>(p.R), r_split,
-                                   H * p.t_pad * p.d, c.st));
-    LC_CUDA(launch_gather_v(V, p.bf16_in ? 0 : 1, idx, c.at<float>(p.vc), p.H, p.T, p.t, p.t_pad,
-                            p.d, c.st));
-  }
   OlsParams op{};
   op.H = p.H;
   op.t = p.t;
@@ -638,6 +619,67 @@ lc_status run_fit_solve(const Ctx& c, const void* qop, const void* V, const int3
   op.Cv = Cv;
   op.head_status = c.h->d_status + status_off;
   op.err = c.h->d_err;
+  if (p.all_pairs) {
+    // H first; its factorisation (a CTA per head) runs on the auxiliary
+    // stream while R is formed on the SMs left free
+    {
+      LC_PROF(c, "gram_out", 1);
+      LC_CUDA(launch_gram_all_pairs(p.mode, mKc, mQ64, mOhi, mOlo, g, p.H, g7_split, c.st));
+    }
+    {
+      LC_PROF(c, "reduce_out", 1);
+      LC_CUDA(launch_reduce_gram(c.at<float>(p.hpart), c.at<float>(p.Hm), g7_split, p.H, p.t_pad,
+                                 c.st));
+    }
+    lc_context* hc = c.h;
+    if (!hc->aux_st) LC_CUDA(cudaStreamCreateWithFlags(&hc->aux_st, cudaStreamNonBlocking));
+    if (!hc->ev_h) LC_CUDA(cudaEventCreateWithFlags(&hc->ev_h, cudaEventDisableTiming));
+    if (!hc->ev_f) LC_CUDA(cudaEventCreateWithFlags(&hc->ev_f, cudaEventDisableTiming));
+    LC_CUDA(cudaEventRecord(hc->ev_h, c.st));
+    LC_CUDA(cudaStreamWaitEvent(hc->aux_st, hc->ev_h, 0));
+    {
+      Ctx ca{c.h, c.p, c.ws, hc->aux_st};
+      LC_PROF(ca, "ols_factor", 1);
+      LC_CUDA(launch_ols_factor(op, hc->aux_st));
+    }
+    LC_CUDA(cudaEventRecord(hc->ev_f, hc->aux_st));
+    const int free_sms = std::max(1, c.h->sm_count - p.H);
+    int rs = best_split(p.H, free_sms, 1, p.r_max);
+    const int r_per = (p.n_q_pad / 64 + rs - 1) / rs;
+    rs = (p.n_q_pad / 64 + r_per - 1) / r_per;
+    GramParams gr = g;
+    gr.r_only = 1;
+    gr.slabs_per_split = r_per;
+    {
+      LC_PROF(c, "gram_r", 1);
+      LC_CUDA(launch_gram_r(p.mode, mKc, mQ64, mOhi, mOlo, gr, p.H, rs, c.st));
+    }
+    {
+      LC_PROF(c, "reduce_out", 2);
+      LC_CUDA(launch_reduce_partials(c.at<float>(p.rpart), c.at<float>(p.R), rs,
+                                     H * p.t_pad * p.d, c.st));
+      LC_CUDA(launch_gather_v(V, p.bf16_in ? 0 : 1, idx, c.at<float>(p.vc), p.H, p.T, p.t,
+                              p.t_pad, p.d, c.st));
+    }
+    LC_CUDA(cudaStreamWaitEvent(c.st, hc->ev_f, 0));
+    {
+      LC_PROF(c, "ols", 1);
+      LC_CUDA(launch_ols_solve(op, c.st));
+    }
+    return LC_OK;
+  }
+  {
+    LC_PROF(c, "gram_out", 1);
+    LC_CUDA(launch_gram(p.mode, true, mKc, mQ64, mOhi, mOlo, g, p.H, g7_split, c.st));
+  }
+  {
+    LC_PROF(c, "reduce_out", 3);
+    LC_CUDA(launch_reduce_gram(c.at<float>(p.hpart), c.at<float>(p.Hm), g7_split, p.H, p.t_pad, c.st));
+    LC_CUDA(launch_reduce_partials(c.at<float>(p.rpart), c.at<float>(p.R), r_split,
+                                   H * p.t_pad * p.d, c.st));
+    LC_CUDA(launch_gather_v(V, p.bf16_in ? 0 : 1, idx, c.at<float>(p.vc), p.H, p.T, p.t, p.t_pad,
+                            p.d, c.st));
+  }
   {
     LC_PROF(c, "ols", 2);
     LC_CUDA(launch_ols(op, c.st));
@@ -919,6 +961,9 @@ lc_status lc_destroy(lc_handle h) {
   }
   if (h->ev_begin) cudaEventDestroy(h->ev_begin);
   if (h->fit_st) cudaStreamDestroy(h->fit_st);
+  if (h->ev_h) cudaEventDestroy(h->ev_h);
+  if (h->ev_f) cudaEventDestroy(h->ev_f);
+  if (h->aux_st) cudaStreamDestroy(h->aux_st);
   delete h;
   return LC_OK;
 }

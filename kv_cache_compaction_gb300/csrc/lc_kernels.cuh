@@ -237,5 +237,10 @@ struct OlsParams {
   uint32_t* err;
 };
 cudaError_t launch_ols(const OlsParams& p, cudaStream_t st);
+// The two halves of launch_ols: the factor needs Hm and w only; the solve
+// also needs R and Vc (it substitutes the original values for the rows of
+// zero-weight keys).
+cudaError_t launch_ols_factor(const OlsParams& p, cudaStream_t st);
+cudaError_t launch_ols_solve(const OlsParams& p, cudaStream_t st);
 
 }  // namespace lc

@@ -940,9 +940,7 @@ __global__ void __launch_bounds__(kThreads, 1) ols_factor_kernel(const OlsParams
   float* gS = p.mat + static_cast<size_t>(h) * tp * tp;
   float* S = sm.S ? sm.S : gS;
   const float* Hm = p.Hm + static_cast<size_t>(h) * tp * tp;
-  float* B = p.R + static_cast<size_t>(h) * tp * dv;
   const float* w = p.w + static_cast<size_t>(h) * t;
-  const float* Vc = p.Vc + static_cast<size_t>(h) * tp * dv;
   float ridge = 0.f;
   int status = LC_OK_STATUS;
   for (int attempt = 0; attempt < 2; ++attempt) {
@@ -960,11 +958,6 @@ __global__ void __launch_bounds__(kThreads, 1) ols_factor_kernel(const OlsParams
     ridge = 1e-6f * block_sum_f(dsum, redf) / t;
   }
   LC_SOLVER_MARK(21);
-  for (int e = tid; e < n_pad * dv; e += kThreads) {
-    const int a = e / dv;
-    if (a >= t) B[e] = 0.f;
-    else if (!(w[a] > 0.f)) B[e] = Vc[e];
-  }
   // publish the factor for the solve kernel
   if (sm.S) {
     const size_t nel = static_cast<size_t>(NB * (NB + 1) / 2) * kBlk;
@@ -1001,6 +994,15 @@ __global__ void __launch_bounds__(kThreads, 1) ols_solve_kernel(const OlsParams 
   for (int a = tid; a < n_pad; a += kThreads) sm.dinv[a] = gd[a];
   float* B = p.R + static_cast<size_t>(h) * tp * dv;
   float* Cv = p.Cv + static_cast<size_t>(h) * t * dv;
+  const float* w = p.w + static_cast<size_t>(h) * t;
+  const float* Vc = p.Vc + static_cast<size_t>(h) * tp * dv;
+  // right-hand side of row a: R_a, the original value row where w_a = 0
+  // (identity row of the factor), 0 in the padding
+  auto rhs = [&](int a, int col) -> float {
+    if (a >= t) return 0.f;
+    const size_t e = static_cast<size_t>(a) * dv + col;
+    return w[a] > 0.f ? B[e] : Vc[e];
+  };
   if (sm.S) {
     const int warp = warp_id(), lane = lane_id(), rg = lane >> 2, cg = lane & 3;
     const int c0 = blockIdx.y * kBS;
@@ -1013,7 +1015,7 @@ __global__ void __launch_bounds__(kThreads, 1) ols_solve_kernel(const OlsParams 
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const int a = I * kBS + 4 * rg + i, q = ct * kBS + 8 * cg + j;
-        nb[i][j] = (I < NB && q < nc) ? -B[static_cast<size_t>(a) * dv + c0 + q] : 0.f;
+        nb[i][j] = (I < NB && q < nc) ? -rhs(a, c0 + q) : 0.f;
       }
     __syncthreads();
     LC_SOLVER_MARK(30);
@@ -1031,9 +1033,13 @@ __global__ void __launch_bounds__(kThreads, 1) ols_solve_kernel(const OlsParams 
     }
     return;
   }
-  __syncthreads();
   const int c0 = blockIdx.y * kBS;
   const int nc = min(kBS, dv - c0);
+  for (int e = tid; e < n_pad * nc; e += kThreads) {
+    const int a = e / nc, j = e % nc;
+    if (a >= t || !(w[a] > 0.f)) B[static_cast<size_t>(a) * dv + c0 + j] = rhs(a, c0 + j);
+  }
+  __syncthreads();
   cta_chol_solve(S, sm.dinv, NB, B + c0, dv, nc, sm.T, sm.T2);
   for (int e = tid; e < t * nc; e += kThreads) {
     const int a = e / nc, j = e % nc;
@@ -1067,18 +1073,30 @@ cudaError_t launch_bounded_ls(const SolveParams& p, float lo, float hi, cudaStre
   return cudaGetLastError();
 }
 
-cudaError_t launch_ols(const OlsParams& p, cudaStream_t st) {
+cudaError_t launch_ols_factor(const OlsParams& p, cudaStream_t st) {
   const size_t smem = solver_smem(p.t);
   cudaError_t e = cudaFuncSetAttribute(ols_factor_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(ols_solve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
   ols_factor_kernel<<<p.H, kThreads, smem, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ols_solve(const OlsParams& p, cudaStream_t st) {
+  const size_t smem = solver_smem(p.t);
+  cudaError_t e = cudaFuncSetAttribute(ols_solve_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
   ols_solve_kernel<<<dim3(p.H, (p.d_v + kBS - 1) / kBS), kThreads, smem, st>>>(p);
   return cudaGetLastError();
+}
+
+cudaError_t launch_ols(const OlsParams& p, cudaStream_t st) {
+  cudaError_t e = launch_ols_factor(p, st);
+  if (e != cudaSuccess) return e;
+  return launch_ols_solve(p, st);
 }
 
 }  // namespace lc
