@@ -174,11 +174,13 @@ struct KS2Layout {
   static constexpr int K_BYTES = kBK * D * 2;    // one key tile
   static constexpr int QCHUNK = kBQ * 128;
   static constexpr int Q_BYTES = NC * QCHUNK;
-  static constexpr int NST = 3;
+  // query stages in flight: as many as fit beside the two key tiles (four
+  // 32 KB stages for d = 128 keep about 28 B/clk of tile traffic per SM)
+  static constexpr int NST = D == 128 ? 4 : 6;
   static constexpr int OFF_Q = 2 * K_BYTES;
   static constexpr int OFF_L = OFF_Q + NST * Q_BYTES;
   static constexpr int OFF_BAR = OFF_L + NST * kBQ * 4;
-  static constexpr int SMEM = 1024 + OFF_BAR + 128;
+  static constexpr int SMEM = 1024 + OFF_BAR + 256;
 };
 
 // MODE 0: key scores only.  MODE 1 (mass): the same pass also reduces each
@@ -200,11 +202,11 @@ __global__ void __launch_bounds__(320, 1)
   float* sL = reinterpret_cast<float*>(base + L::OFF_L);
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + L::OFF_BAR);
   uint64_t* k_full = bars + 0;
-  uint64_t* q_full = bars + 1;   // [3]
-  uint64_t* q_empty = bars + 4;  // [3]
-  uint64_t* d_full = bars + 7;   // [2]
-  uint64_t* d_free = bars + 9;   // [2]
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 11);
+  uint64_t* q_full = bars + 1;                // [NST]
+  uint64_t* q_empty = bars + 1 + L::NST;      // [NST]
+  uint64_t* d_full = bars + 1 + 2 * L::NST;   // [2]
+  uint64_t* d_free = bars + 3 + 2 * L::NST;   // [2]
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 5 + 2 * L::NST);
   __shared__ volatile int abort_flag;
 
   const int warp = warp_id(), lane = lane_id();
