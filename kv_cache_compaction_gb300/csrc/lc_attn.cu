@@ -16,6 +16,12 @@
 #include "lc_common.cuh"
 #include "lc_kernels.cuh"
 
+// Pipeline marks for instrumented builds (clock reads at the steps of one
+// CTA); empty in the library.
+#ifndef LC_ATTN_MARK
+#define LC_ATTN_MARK(id, step) ((void)0)
+#endif
+
 namespace lc {
 namespace {
 
@@ -418,6 +424,7 @@ __global__ void __launch_bounds__(320, 1)
         const CUtensorMap* m = (n & 1) ? &mV : &mK;
         for (int c = 0; c < L::NC; ++c)
           tma_load_3d(dst + c * BN * 128, m, &r_full[sl], 64 * c, (n >> 1) * BN, h);
+        LC_ATTN_MARK((n & 1) ? 5 : 0, n >> 1);
         issued = n + 1;
       }
       if (abort_flag) {
@@ -446,6 +453,7 @@ __global__ void __launch_bounds__(320, 1)
           umma_f16_ss(tbase + x * 128, da, db, idesc_s, k > 0 ? 1u : 0u);
         }
         umma_commit(&s_full[x]);
+        LC_ATTN_MARK(1 + x, j);
       };
       // O_x += P_x V_j, P_x in tensor memory (16 keys = 8 columns per step)
       auto issue_pv = [&](int x, int j) {
@@ -457,6 +465,7 @@ __global__ void __launch_bounds__(320, 1)
                       (j > 0 || k > 0) ? 1u : 0u);
         }
         umma_commit(&pv_done[x]);
+        LC_ATTN_MARK(3 + x, j);
       };
       // Event loop over both tiles: S_x(0); then per j: P_x V_j once P_x(j)
       // is written, followed by S_x(j+1) once K_{j+1} has landed.  A ring
@@ -514,10 +523,13 @@ __global__ void __launch_bounds__(320, 1)
     float m_ref = -kInf, m_true = -kInf, l = 0.f;
     bool ok = true;
     for (int j = 0; j < nkt; ++j) {
+      if (wq == 2) LC_ATTN_MARK(8, j);
       if (!wait_bar(&s_full[x], j & 1, &abort_flag, p.err)) { ok = false; break; }
       tc_fence_after();
+      if (wq == 2) LC_ATTN_MARK(9, j);
       float xs[BN];
       tmem_ld128(tS + lane_off, xs);
+      if (wq == 2) LC_ATTN_MARK(10, j);
       const int valid = p.T - j * BN;
       if (valid < BN) {
 #pragma unroll
@@ -587,6 +599,7 @@ __global__ void __launch_bounds__(320, 1)
       }
       tc_fence_before();
       mbar_arrive(&p_full[x]);
+      if (wq == 2) LC_ATTN_MARK(13, j);
     }
     if (ok && wait_bar(&pv_done[x], (nkt - 1) & 1, &abort_flag, p.err)) {
       tc_fence_after();
