@@ -355,7 +355,16 @@ def main():
             ms = kern[k][0] / max(kern[k][1], 1)
             tf = f / (ms * 1e-3) / 1e12
             qkt[k] = {"tflops": tf, "frac_of_peak": tf / pk["bf16_tflops_sustained"],
-                      "ms": ms}
+                      "frac_of_burst": tf / pk["bf16_tflops"], "ms": ms}
+    # the two small memory-side kernels against HBM: the top-t select reads
+    # the scores u and writes idx; the key gather reads and writes t rows of K
+    hbm_bytes = {"select_topt": H * w.T * 4 + H * t * 4, "gather_keys": 2 * H * t * dd * 2}
+    hbm = {}
+    for k, nb in hbm_bytes.items():
+        if k in kern:
+            ms = kern[k][0] / max(kern[k][1], 1)
+            gbs = nb / (ms * 1e-3) / 1e9
+            hbm[k] = {"bytes": nb, "ms": ms, "gbs": gbs, "frac_of_hbm": gbs / pk["hbm_gbs"]}
 
     # end to end through the host-buffer entry point
     e2e = None
@@ -501,7 +510,7 @@ def main():
             "metric": METRIC, "value": value, "unit": "ms", "n_gpus": world, "steps": a.steps,
             "warmup": a.warmup, "ms_per_step": ms_step, "higher_is_better": False,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": config_dict(w, world), "roofline": roof, "qkt": qkt,
+            "config": config_dict(w, world), "roofline": roof, "qkt": qkt, "hbm": hbm,
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
             "per_kernel": per_kernel, "fast_path": fast, "sweep": sweep, "quality": quality, "layer_tflops": fl["layer"] / (ms_step * 1e-3) / 1e12,
             "wall_s_timed": wall_s,
