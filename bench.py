@@ -77,6 +77,9 @@ def args_():
                     help="layers of the full-model sweep timed through the pipelined "
                          "multi-layer call (0: skip)")
     ap.add_argument("--sweep-steps", type=int, default=3)
+    ap.add_argument("--long-steps", type=int, default=0,
+                    help="timed compactions of one long-context layer (T = 131072, "
+                         "t = 1024); 0 skips it (drawing its inputs takes about a minute)")
     ap.add_argument("--quality-queries", type=int, default=4096,
                     help="held-out queries per head for the quality comparison (0: skip)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -468,6 +471,44 @@ def main():
                  "steps": a.sweep_steps}
         del SQ, SK, SV, sout
 
+    # one long-context layer (T = 131072 keys, 524288 reference queries per KV
+    # head, t = 1024): heads 0-1 of the seeded draw, repeated to the layer's 8
+    # heads (same shapes and kernels; drawing all 8 takes minutes)
+    long_ctx = None
+    if a.long_steps > 0 and rank == 0:
+        w5 = synth.workload("cfg5")
+        d5 = synth.make(w5, heads=[0, 1])
+        rep_h = (w5.H + 1) // 2
+        Q5, K5, V5 = (up(np.concatenate([d5[k]] * rep_h)[: w5.H]).to(dev) for k in ("Q", "K", "V"))
+        del d5
+        comp.compact_layer(Q5, K5, V5, w5.t)
+        torch.cuda.synchronize()
+        comp.profile(True)
+        l0 = torch.cuda.Event(enable_timing=True)
+        l1 = torch.cuda.Event(enable_timing=True)
+        l0.record(stream)
+        for _ in range(a.long_steps):
+            comp.compact_layer(Q5, K5, V5, w5.t)
+        l1.record(stream)
+        torch.cuda.synchronize()
+        comp.profile(False)
+        k5 = comp.profile_read()
+        rep = comp.report(w5.H)
+        if rep.device_error_bits:
+            raise RuntimeError("device error in the long-context layer")
+        f5 = flops(w5)
+        pk5 = {k: v[0] / a.long_steps for k, v in k5.items()}
+        long_ctx = {
+            "workload": "cfg5: one layer, 8 KV heads x 4 query heads, T=131072, n_q=524288 "
+                        "per KV head, d=128, t=1024, bf16, 64 needles per head (heads 0-1 of "
+                        "the draw repeated to 8)",
+            "ms_per_layer": l0.elapsed_time(l1) / a.long_steps, "steps": a.long_steps,
+            "attn_stats_tflops": f5["attn_stats"] / (pk5["attn_stats"] * 1e-3) / 1e12,
+            "key_scores_tflops": f5["key_scores"] / (pk5["key_scores"] * 1e-3) / 1e12,
+            "layer_tflops": f5["layer"] / (l0.elapsed_time(l1) / a.long_steps * 1e-3) / 1e12,
+            "nnls_iters": rep.nnls_iters, "per_kernel_ms": pk5}
+        del Q5, K5, V5
+
     # quality of three compactions of the first layer on held-out queries
     # drawn from the same recipe: attention matching (NNLS beta, OLS values),
     # the fast path (two-pass keys, redistributed beta, direct values) and
@@ -512,7 +553,7 @@ def main():
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": config_dict(w, world), "roofline": roof, "qkt": qkt, "hbm": hbm,
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
-            "per_kernel": per_kernel, "fast_path": fast, "sweep": sweep, "quality": quality, "layer_tflops": fl["layer"] / (ms_step * 1e-3) / 1e12,
+            "per_kernel": per_kernel, "fast_path": fast, "sweep": sweep, "long_context": long_ctx, "quality": quality, "layer_tflops": fl["layer"] / (ms_step * 1e-3) / 1e12,
             "wall_s_timed": wall_s,
         }
         print(json.dumps(line), flush=True)
