@@ -696,8 +696,13 @@ __global__ void __launch_bounds__(kThreads, 1) nnls_bpp_kernel(const SolveParams
         }
         LC_SOLVER_MARK(11);
         __syncthreads();
-        // (G^-1)_DD = Y^T Y: tile pairs (0,0), (1,0), (1,1) summed over row blocks
+        // (G^-1)_DD = Y^T Y, lower tiles (0,0), (1,0), (1,1): one register-
+        // tiled product per (tile, 32-row block of Y), written to the dense
+        // scratch (unused here: the factor is in shared memory), then summed
+        // over the row blocks in ascending order -- the same result on every
+        // run, and exactly symmetric diagonal tiles.
         const int npair = nct == 2 ? 3 : 1;
+        float* Mpart = p.mat + static_cast<size_t>(h) * tp * tp;
         for (int task = warp; task < npair * NB; task += kWarps) {
           const int pr = task / NB, Ib = task % NB;
           const int ta = pr == 0 ? 0 : 1, tb = pr == 2 ? 1 : 0;
@@ -705,11 +710,22 @@ __global__ void __launch_bounds__(kThreads, 1) nnls_bpp_kernel(const SolveParams
           zero_acc(acc);
           const float* Yb = Yg + static_cast<size_t>(Ib) * kBS * kMaxD;
           warp_mm32<true, false>(Yb + ta * kBS, kMaxD, Yb + tb * kBS, kMaxD, acc);
-          float* Mt = blk(Ms, ta, tb);
+          float* dst = Mpart + static_cast<size_t>(task) * kBS * kBS;
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int j = 0; j < 8; ++j) atomicAdd(&Mt[(4 * rg + i) * kLD + 8 * cg + j], acc[i][j]);
+          for (int i = 0; i < 4; ++i) {
+            float4* d4 = reinterpret_cast<float4*>(dst + (4 * rg + i) * kBS + 8 * cg);
+            d4[0] = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+            d4[1] = make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
+          }
+        }
+        __syncthreads();
+        for (int e = tid; e < npair * kBS * kBS; e += kThreads) {
+          const int pr = e / (kBS * kBS), rc = e % (kBS * kBS);
+          const float* src = Mpart + static_cast<size_t>(pr * NB) * kBS * kBS + rc;
+          float sacc = 0.f;
+          for (int Ib = 0; Ib < NB; ++Ib) sacc += src[static_cast<size_t>(Ib) * kBS * kBS];
+          const int ta = pr == 0 ? 0 : 1, tb = pr == 2 ? 1 : 0;
+          blk(Ms, ta, tb)[(rc / kBS) * kLD + rc % kBS] = sacc;
         }
         __syncthreads();
         for (int q = nD + tid; q < NBs * kBS; q += kThreads)
