@@ -24,6 +24,12 @@ CASES = {
     "bf16_iid_d128": synth.workload("cfg2", H=1, T=640, G=2, t=64, kind="iid", seed=11),
     "bf16_t256": synth.workload("cfg2", H=2, T=1024, G=4, t=256, seed=12),
     "bf16_t300_ragged": synth.workload("cfg2", H=1, T=1100, G=3, t=300, seed=13),
+    # edge cases: a single kept key, a single cached key (t = T = 1), the
+    # fp32 path at ragged sizes, more than half the keys kept over several tiles
+    "bf16_t1": synth.workload("cfg2", H=2, T=200, G=1, t=1, seed=14),
+    "bf16_T1": synth.workload("cfg2", H=1, T=1, G=2, t=1, seed=15),
+    "fp32_ragged": synth.workload("cfg1", T=300, t=17, G=1, seed=16),
+    "bf16_split_p_ragged": synth.workload("cfg2", H=1, T=130, G=2, t=100, seed=17),
 }
 
 
