@@ -12,7 +12,11 @@
 // writes its row of E in the K-major layout the Gram products read, and
 // c_i = sum_r E_ir b_r is a per-thread dot product.  E is split into fp16
 // hi + lo and each Gram block is the sum of three tensor-core products
-// (hi.hi + hi.lo + lo.hi), which keeps fp32-level accuracy.
+// (hi.hi + hi.lo + lo.hi), which keeps fp32-level accuracy.  With two key
+// blocks per CTA the blocks G00 and G01 are formed together as 128 x 256
+// products (the second block's E rows follow the first's in shared memory),
+// six products per step instead of nine: issuing tensor-core instructions,
+// not executing them, limits these kernels.
 //
 // CTA kinds (blockIdx.x):
 //   [0, npairs)           key-block pair (bi <= bj): G[bi][bj], and c[bi]
@@ -838,6 +842,7 @@ __global__ void __launch_bounds__(320, 1)
     if (lane == 0 && nsl > 0) {
       constexpr uint32_t idesc_s = idesc_f16(128, kSL, true, false, false);
       constexpr uint32_t idesc_g = idesc_f16(128, 128, false, false, false);
+      constexpr uint32_t idesc_g2 = idesc_f16(128, 256, false, false, false);
       constexpr uint32_t idesc_r = idesc_f16(128, D, false, false, true);
       bool ok = wait_bar(k_full, 0, &abort_flag, p.err);
       auto issue_s = [&](int i) {  // scores of slab i for both key blocks
@@ -858,9 +863,11 @@ __global__ void __launch_bounds__(320, 1)
       };
       auto issue_g = [&](int i) {  // Gram blocks (or R) of slab i
         tc_fence_after();
+        // E tiles [E0 hi, E1 hi, E0 lo, E1 lo]: E1 follows E0, so one
+        // 256-row operand covers both key blocks
         const uint32_t eb = smem_u32(sE + ebuf(i) * 4 * L::E_BLK);
-        const uint32_t e0h = eb, e0l = eb + L::E_BLK;
-        const uint32_t e1h = eb + 2 * L::E_BLK, e1l = eb + 3 * L::E_BLK;
+        const uint32_t e0h = eb, e1h = eb + L::E_BLK;
+        const uint32_t e0l = eb + 2 * L::E_BLK, e1l = eb + 3 * L::E_BLK;
         if constexpr (!RM) {
 #pragma unroll
           for (int k = 0; k < kSL / 16; ++k) {
@@ -870,12 +877,10 @@ __global__ void __launch_bounds__(320, 1)
             const uint64_t a0l = sdesc_sw128(e0l + o, 16, 1024);
             const uint64_t a1h = sdesc_sw128(e1h + o, 16, 1024);
             const uint64_t a1l = sdesc_sw128(e1l + o, 16, 1024);
-            umma_f16_ss(tbase + 128, a0h, a0h, idesc_g, acc0);
-            umma_f16_ss(tbase + 128, a0h, a0l, idesc_g, 1u);
-            umma_f16_ss(tbase + 128, a0l, a0h, idesc_g, 1u);
-            umma_f16_ss(tbase + 256, a0h, a1h, idesc_g, acc0);
-            umma_f16_ss(tbase + 256, a0h, a1l, idesc_g, 1u);
-            umma_f16_ss(tbase + 256, a0l, a1h, idesc_g, 1u);
+            // G00 | G01 (TMEM columns 128..383) as 128 x 256 products
+            umma_f16_ss(tbase + 128, a0h, a0h, idesc_g2, acc0);
+            umma_f16_ss(tbase + 128, a0h, a0l, idesc_g2, 1u);
+            umma_f16_ss(tbase + 128, a0l, a0h, idesc_g2, 1u);
             umma_f16_ss(tbase + 384, a1h, a1h, idesc_g, acc0);
             umma_f16_ss(tbase + 384, a1h, a1l, idesc_g, 1u);
             umma_f16_ss(tbase + 384, a1l, a1h, idesc_g, 1u);
@@ -950,8 +955,8 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_after();
       const float* rs = sRows + (i & 1) * (L::ROW_STAGE / 4);
       const float* rb = rs + kSL;
-      uint8_t* sEh = sE + ebuf(i) * 4 * L::E_BLK + b * 2 * L::E_BLK;
-      uint8_t* sEl = sEh + L::E_BLK;
+      uint8_t* sEh = sE + ebuf(i) * 4 * L::E_BLK + b * L::E_BLK;
+      uint8_t* sEl = sEh + 2 * L::E_BLK;
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {  // 32 query columns at a time
         float x[32];
