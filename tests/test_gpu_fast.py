@@ -29,6 +29,11 @@ CASES = {
     "shortlist_chunks_of_128": (synth.workload("cfg2", H=2, T=700, G=2, t=100, seed=15), 96, 3),
     "iid_all_queries": (synth.workload("cfg2", H=1, T=640, G=2, t=64, kind="iid", seed=11),
                         None, 5),
+    # edge cases: one kept key (iid inputs: with peaked ones the best
+    # second-pass scores tie within fp32 rounding); one cached key and a
+    # one-query subset
+    "t1": (synth.workload("cfg2", H=2, T=200, G=1, t=1, kind="iid", seed=18), 8, 4),
+    "T1": (synth.workload("cfg2", H=1, T=1, G=2, t=1, seed=17), 1, 2),
 }
 
 
@@ -62,7 +67,11 @@ def check_head(r, short, idx, beta, Cv, t, kt):
         return False
     assert np.all(np.diff(idx) > 0)
     assert np.all(np.isin(idx, short))
-    if not _near_tie_only(idx, r["idx"], r["u2"], t):
+    # second-pass scores are given per shortlist position: place them at
+    # their keys (the shortlists are equal here) so keys index them
+    u2 = np.full(int(short.max()) + 1, -np.inf)
+    u2[r["short"]] = r["u2"]
+    if not _near_tie_only(idx, r["idx"], u2, t):
         return False
     err = beta_err(beta, r["beta"])
     assert np.all(np.isfinite(beta)) and err <= FIT_REL, f"beta err {err:.2e}"
