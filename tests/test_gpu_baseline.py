@@ -19,6 +19,10 @@ CASES = {
     "t_over_128": synth.workload("cfg2", H=2, T=700, G=2, t=160, seed=10),
     "iid": synth.workload("cfg2", H=1, T=640, G=2, t=64, kind="iid", seed=11),
     "t256": synth.workload("cfg2", H=2, T=1024, G=4, t=256, seed=12),
+    # edge cases: one kept key (its bias meets the upper bound e^3); one
+    # cached key
+    "t1": synth.workload("cfg2", H=2, T=200, G=1, t=1, kind="iid", seed=18),
+    "T1": synth.workload("cfg2", H=1, T=1, G=2, t=1, seed=17),
 }
 
 
