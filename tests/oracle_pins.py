@@ -295,6 +295,49 @@ def check_t_equals_T(o):
     _close(X @ r["Cv"], r["O"], 1e-6, "t=T: compact output = full")
 
 
+def _softmax_rows(L):
+    L = L - L.max(axis=1, keepdims=True)
+    E = np.exp(L)
+    return E / E.sum(axis=1, keepdims=True)
+
+
+def check_fit_zero_weight_branch(o):
+    """Steps 4-5 through ``fit_head`` on a planted problem whose NNLS solution
+    has zeros: the mass targets are b = A w* with w* >= 0 and three zero
+    weights, the output targets O = X C* with X the compact softmax over the
+    keys with w*_j > 0 ("KV compaction" blog, output equation; "Latent
+    Compaction with Test-Time Training" Eq. (2)-(3)).  Then w = w*, beta is
+    -inf exactly on the zeros, C_v on the support is the least-squares fit of
+    O on X restricted to the support (numpy's SVD solver, = C*), and every row
+    off the support is the key's original value row, bit for bit."""
+    rng = _rng(62)
+    T, d, dv, n_q, t = 16, 4, 3, 60, 8
+    K = rng.standard_normal((T, d))
+    Q = 1.5 * rng.standard_normal((n_q, d))
+    V = rng.standard_normal((T, dv))
+    s = 0.7
+    idx = np.array([0, 2, 3, 5, 8, 9, 12, 14])
+    logit = s * Q @ K[idx].T
+    m = logit.max(axis=1) + 0.3          # any per-row shift defines the same fit
+    A = np.exp(logit - m[:, None])
+    ws = np.abs(rng.standard_normal(t)) + 0.2
+    off = np.array([1, 4, 6])
+    ws[off] = 0.0
+    lse = m + np.log(A @ ws)
+    sup = np.flatnonzero(ws > 0)
+    X = _softmax_rows(logit[:, sup] + np.log(ws[sup])[None, :])
+    Cs = rng.standard_normal((sup.size, dv))
+    O = X @ Cs
+    r = o.fit_head(Q, K, V, idx, m, lse, O, s)
+    _close(r["w"], ws, 1e-9, "planted weights with zeros")
+    assert np.all(r["w"][off] == 0.0), "a zero weight came back nonzero"
+    assert np.all(np.isneginf(r["beta"][off])), "beta of a zero weight is not -inf"
+    Cref, *_ = np.linalg.lstsq(X, O, rcond=None)
+    _close(r["Cv"][sup], Cref, 1e-8, "C_v on the support vs SVD least squares")
+    _close(Cref, Cs, 1e-8, "planted values (test is not testing)")
+    assert np.array_equal(r["Cv"][off], V[idx[off]]), "off-support rows are not V[idx]"
+
+
 def check_fit_reduces_error(o):
     """With t < T the fitted beta and C_v match mass and output better than
     keeping the selected keys unchanged (beta = 0, C_v = V[idx])."""
@@ -595,6 +638,7 @@ ALL_CHECKS = [
     check_full_stats_brute, check_full_stats_closed_forms, check_key_scores_brute,
     check_select, check_mass_system_brute, check_nnls_bruteforce, check_nnls_scipy, check_nnls_planted_and_kkt,
     check_nnls_q_zero_and_caps, check_compact_weights, check_ols, check_t_equals_T,
+    check_fit_zero_weight_branch,
     check_fit_reduces_error, check_two_pass_brute, check_two_pass_full_shortlist,
     check_redistribute, check_combine_single_softmax, check_heldout_errors,
     check_farthest_first, check_rms_scores, check_bounded_ls, check_variant_t_equals_T,

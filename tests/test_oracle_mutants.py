@@ -177,10 +177,33 @@ def _bounded_pins_at_zero(o):
     o.bounded_ls = f
 
 
+def _off_support_zeroed(o):
+    # rows of C_v off the support set to 0 instead of the original values
+    orig = o.fit_head
+
+    def f(Q, K, V, idx, m, lse, O, scale, max_outer=0, max_inner=0):
+        r = orig(Q, K, V, idx, m, lse, O, scale, max_outer, max_inner)
+        r["Cv"][~(r["w"] > 0)] = 0.0
+        return r
+    o.fit_head = f
+
+
+def _support_ignored(o):
+    # zero weights replaced by a small positive weight before the output fit,
+    # so every kept key enters the least squares
+    orig = o.output_system
+
+    def f(Q, Kc, w, O, scale):
+        w = np.asarray(w, float)
+        return orig(Q, Kc, np.where(w > 0, w, 1e-3), O, scale)
+    o.output_system = f
+
+
 MUTANTS = [_no_scale, _unnormalised_output, _score_plus_lse, _score_min, _ties_high,
            _no_stepback, _mass_unshifted, _weights_no_bias, _ols_diag, _second_pass_full_lse,
            _delta_not_shared, _delta_by_difference, _combine_unbiased, _mass_error_signed,
-           _farthest_by_sum, _rms_as_mean, _bounded_pins_at_zero]
+           _farthest_by_sum, _rms_as_mean, _bounded_pins_at_zero, _off_support_zeroed,
+           _support_ignored]
 
 
 @pytest.mark.parametrize("mutate", MUTANTS, ids=lambda f: f.__name__)
