@@ -41,8 +41,15 @@ design notes):
   outer steps and t inner steps per outer step.
 * The OLS design matrix is the compact softmax X = softmax_j(s q.C_kj + beta_j)
   over the keys with w_j > 0; C_v = (X^T X)^-1 X^T O by Cholesky; keys with
-  w_j = 0 keep their original value row.  If the Cholesky factorisation fails
-  a ridge of 1e-8 * mean(diag) is added once and the status says so.
+  w_j = 0 keep their original value row.
+* Singular systems (the pages give no ridge): when a Cholesky factorisation
+  breaks down, a ridge of 1e-6 * mean(diag) of the system being factored is
+  added once and the status says so (1e-6 rather than less, so that the
+  same rule also regularises a single-precision factorisation).
+* A kept key whose vector equals that of a kept key at an earlier position
+  has w = 0: its column of A equals the earlier one's, so the NNLS minimiser
+  is not unique, and this is the one Lawson-Hanson reaches with argmax ties
+  going to the lower index (the later copy never enters the passive set).
 
 * Decode consumer: row r of the queries sees the compacted entries whose
   beta is finite and the first n_vis[r] appended tokens (a causal mask given
@@ -181,6 +188,12 @@ def _chol_solve(M, r):
     return np.linalg.solve(L.T, np.linalg.solve(L, r))
 
 
+def ridge(M):
+    """The ridge added to a system whose Cholesky factorisation broke down:
+    1e-6 times the mean of its diagonal."""
+    return 1e-6 * float(np.mean(np.diag(M))) if M.size else 0.0
+
+
 def nnls_tolerance(c, t, eps=np.finfo(np.float64).eps):
     return 10.0 * eps * t * float(np.max(np.abs(c))) if c.size else 0.0
 
@@ -198,7 +211,9 @@ def nnls_lh(G, c, max_outer=0, max_inner=0, tol=None):
     otherwise w moves toward z by the largest step that keeps w >= 0 and the
     indices that reach zero leave P.  Should the index that just joined get
     z_j <= 0 (no progress possible in exact arithmetic, so a rounding effect)
-    it leaves again and is not retried until w changes.
+    it leaves again and is not retried until w changes.  A passive system
+    whose factorisation breaks down is solved with the ridge of ``ridge``
+    added and the status is SINGULAR.
 
     Returns (w, info) with info = {"outer", "inner", "status"}.
     """
@@ -211,6 +226,7 @@ def nnls_lh(G, c, max_outer=0, max_inner=0, tol=None):
     P = np.zeros(t, dtype=bool)
     blocked = np.zeros(t, dtype=bool)
     status = NOT_CONVERGED
+    singular = False
     outer = inner_total = 0
     while outer < max_outer:
         g = c - G @ w
@@ -225,9 +241,13 @@ def nnls_lh(G, c, max_outer=0, max_inner=0, tol=None):
         for _ in range(max_inner):
             inner_total += 1
             idx = np.flatnonzero(P)
-            zP = _chol_solve(G[np.ix_(idx, idx)], c[idx])
+            GP = G[np.ix_(idx, idx)]
+            zP = _chol_solve(GP, c[idx])
             if zP is None:
-                return w, {"outer": outer, "inner": inner_total, "status": SINGULAR}
+                singular = True
+                zP = _chol_solve(GP + ridge(GP) * np.eye(idx.size), c[idx])
+                if zP is None:
+                    return w, {"outer": outer, "inner": inner_total, "status": SINGULAR}
             z = np.zeros(t)
             z[idx] = zP
             if np.all(zP > 0):
@@ -252,6 +272,8 @@ def nnls_lh(G, c, max_outer=0, max_inner=0, tol=None):
             blocked[:] = False
         else:
             return w, {"outer": outer, "inner": inner_total, "status": NOT_CONVERGED}
+    if singular and status == OK:
+        status = SINGULAR
     return w, {"outer": outer, "inner": inner_total, "status": status}
 
 
@@ -286,27 +308,38 @@ def output_system(Q, Kc, w, O, scale):
 
 
 def ols(H, R):
-    """C = H^-1 R by Cholesky; on breakdown a ridge of 1e-8 * mean(diag H) is
-    added once.  Returns (C, status)."""
+    """C = H^-1 R by Cholesky; on breakdown the ridge of ``ridge`` (1e-6 *
+    mean(diag H)) is added once.  Returns (C, status)."""
     H, R = _f64(H), _f64(R)
     C = _chol_solve(H, R)
     if C is not None:
         return C, OK
-    lam = 1e-8 * float(np.mean(np.diag(H)))
-    C = _chol_solve(H + lam * np.eye(H.shape[0]), R)
+    C = _chol_solve(H + ridge(H) * np.eye(H.shape[0]), R)
     if C is None:
         C = np.zeros_like(R)
     return C, SINGULAR
 
 
 # ------------------------------------------------------------ one head ------
+def later_duplicates(Kc):
+    """True for each kept key whose vector equals (value for value; -0 equals
+    +0) the vector of a kept key at an earlier position."""
+    Kc = np.asarray(Kc)
+    dup = np.zeros(Kc.shape[0], dtype=bool)
+    for j in range(1, Kc.shape[0]):
+        dup[j] = bool(np.any(np.all(Kc[:j] == Kc[j], axis=1)))
+    return dup
+
+
 def fit_head(Q, K, V, idx, m, lse, O, scale, max_outer=0, max_inner=0):
     """Steps 4-5 for one head given the selected keys and the full statistics:
     returns dict(w, beta, Cv, nnls=info, ols_status)."""
     idx = np.asarray(idx, np.int64)
     Kc = _f64(K)[idx]
     G, c, bb = mass_system(Q, Kc, m, lse, scale)
-    w, info = nnls_lh(G, c, max_outer, max_inner)
+    keep = np.flatnonzero(~later_duplicates(Kc))
+    w = np.zeros(idx.size)
+    w[keep], info = nnls_lh(G[np.ix_(keep, keep)], c[keep], max_outer, max_inner)
     with np.errstate(divide="ignore"):
         beta = np.log(w)
     sup, H, R = output_system(Q, Kc, w, O, scale)
@@ -567,7 +600,7 @@ def bounded_ls(G, c, lo, hi, iters):
         x = _chol_solve(G[np.ix_(F, F)], rhs)
         if x is None:  # not positive definite: the same ridge as the OLS fallback
             M = G[np.ix_(F, F)]
-            x = _chol_solve(M + 1e-8 * float(np.mean(np.diag(M))) * np.eye(F.size), rhs)
+            x = _chol_solve(M + ridge(M) * np.eye(F.size), rhs)
         w[F] = x
         low = free & (w < lo)
         high = free & (w > hi)

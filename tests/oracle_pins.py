@@ -267,10 +267,25 @@ def check_ols(o):
     Cs = rng.standard_normal((t, d))
     C2, _ = o.ols(X.T @ X, X.T @ (X @ Cs))
     _close(C2, Cs, 1e-7, "planted OLS solution")
-    # duplicated column: singular, ridge fallback, finite answer
+    # duplicated column: singular, ridge fallback; the ridge solution tends to
+    # the minimum-norm least-squares solution (SVD) as the ridge shrinks, which
+    # splits the coefficient evenly between the two equal columns
     Xd = np.concatenate([X, X[:, :1]], axis=1)
     C3, st = o.ols(Xd.T @ Xd, Xd.T @ Ot)
     assert st == o.SINGULAR and np.all(np.isfinite(C3))
+    # In the SVD basis a ridge lam scales the coefficient along singular value
+    # sv by sv^2 / (sv^2 + lam), so both the coefficients and the fitted
+    # outputs move by at most lam / sv_min^2 (smallest nonzero sv) relative.
+    Cmn, *_ = np.linalg.lstsq(Xd, Ot, rcond=None)
+    sv = np.linalg.svd(Xd, compute_uv=False)
+    lam = 1e-6 * float(np.mean(np.diag(Xd.T @ Xd)))
+    bound = lam / sv[sv > 1e-10 * sv[0]].min() ** 2
+    assert bound < 0.1, "ridge bound too loose (test is not testing)"
+    assert np.linalg.norm(C3 - Cmn) <= 1.01 * bound * np.linalg.norm(Cmn), \
+        "ridge fallback vs minimum-norm least squares"
+    assert np.linalg.norm(Xd @ (C3 - Cmn)) <= 1.01 * bound * np.linalg.norm(Xd @ Cmn), \
+        "ridge fallback: fitted outputs"
+    _close(C3[0], C3[t], 1e-9 * np.abs(C3).max(), "equal columns share the coefficient")
 
 
 # ------------------------------------------------------------ end to end ----
@@ -336,6 +351,47 @@ def check_fit_zero_weight_branch(o):
     _close(r["Cv"][sup], Cref, 1e-8, "C_v on the support vs SVD least squares")
     _close(Cref, Cs, 1e-8, "planted values (test is not testing)")
     assert np.array_equal(r["Cv"][off], V[idx[off]]), "off-support rows are not V[idx]"
+
+
+def check_fit_duplicate_keys(o):
+    """Two kept keys with equal vectors give equal columns of A, so the NNLS
+    minimiser is not unique.  Lawson-Hanson with argmax ties going to the
+    lower index never lets the later copy into the passive set: on a system
+    whose rows and columns are duplicated by index (bitwise equal) it returns
+    w = 0 there and the distinct-column solution elsewhere.  ``fit_head``
+    gives the same: w = 0 and beta = -inf at the later copy, its C_v row the
+    original value row, the other weights equal to the exhaustive NNLS over
+    supports of the distinct columns and C_v on the support equal to SVD
+    least squares."""
+    rng = _rng(63)
+    A, b = _random_problem(rng, 14, 5)
+    G0, c0 = A.T @ A, A.T @ b
+    p = [0, 1, 2, 1, 3, 4]
+    w, info = o.nnls_lh(G0[np.ix_(p, p)], c0[p])
+    assert w[3] == 0.0, "the later copy entered the passive set"
+    _close(w[[0, 1, 2, 4, 5]], _nnls_by_supports(A, b), 1e-8, "duplicated system vs distinct")
+
+    T, d, dv, n_q = 10, 3, 2, 40
+    K = rng.standard_normal((T, d))
+    K[7] = K[2]
+    Q = 0.5 * K[rng.integers(0, T, n_q)] + rng.standard_normal((n_q, d))
+    V = rng.standard_normal((T, dv))
+    s = 0.8
+    idx = np.array([1, 2, 4, 7, 9])
+    m, lse, O = o.full_stats(Q, K, V, s)
+    r = o.fit_head(Q, K, V, idx, m, lse, O, s)
+    assert r["w"][3] == 0.0 and np.isneginf(r["beta"][3]), "later copy has a weight"
+    assert np.array_equal(r["Cv"][3], V[7]), "later copy's value row changed"
+    keep = [0, 1, 2, 4]
+    Ad = np.array([[math.exp(s * float(Q[i] @ K[j]) - m[i]) for j in idx[keep]]
+                   for i in range(n_q)])
+    bd = np.exp(lse - m)
+    _close(r["w"][keep], _nnls_by_supports(Ad, bd), 1e-8 * max(1.0, r["w"].max()),
+           "weights vs exhaustive NNLS on the distinct keys")
+    sup = np.flatnonzero(r["w"] > 0)
+    X = _softmax_rows(s * Q @ K[idx[sup]].T + np.log(r["w"][sup])[None, :])
+    Cref, *_ = np.linalg.lstsq(X, O, rcond=None)
+    _close(r["Cv"][sup], Cref, 1e-7 * max(1.0, np.abs(Cref).max()), "C_v with a duplicate")
 
 
 def check_fit_reduces_error(o):
@@ -638,7 +694,7 @@ ALL_CHECKS = [
     check_full_stats_brute, check_full_stats_closed_forms, check_key_scores_brute,
     check_select, check_mass_system_brute, check_nnls_bruteforce, check_nnls_scipy, check_nnls_planted_and_kkt,
     check_nnls_q_zero_and_caps, check_compact_weights, check_ols, check_t_equals_T,
-    check_fit_zero_weight_branch,
+    check_fit_zero_weight_branch, check_fit_duplicate_keys,
     check_fit_reduces_error, check_two_pass_brute, check_two_pass_full_shortlist,
     check_redistribute, check_combine_single_softmax, check_heldout_errors,
     check_farthest_first, check_rms_scores, check_bounded_ls, check_variant_t_equals_T,

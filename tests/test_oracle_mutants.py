@@ -199,11 +199,32 @@ def _support_ignored(o):
     o.output_system = f
 
 
+def _duplicate_keeps_later(o):
+    # of two equal kept keys, the earlier one dropped instead of the later one
+    def later(Kc):
+        Kc = np.asarray(Kc)
+        dup = np.zeros(Kc.shape[0], dtype=bool)
+        for j in range(Kc.shape[0] - 1):
+            dup[j] = bool(np.any(np.all(Kc[j + 1:] == Kc[j], axis=1)))
+        return dup
+    o.later_duplicates = later
+
+
+def _no_ridge(o):
+    # a failed factorisation gives zeros instead of the ridge solution
+    orig = o.ols
+
+    def f(H, R):
+        C, st = orig(H, R)
+        return (np.zeros_like(C), st) if st == o.SINGULAR else (C, st)
+    o.ols = f
+
+
 MUTANTS = [_no_scale, _unnormalised_output, _score_plus_lse, _score_min, _ties_high,
            _no_stepback, _mass_unshifted, _weights_no_bias, _ols_diag, _second_pass_full_lse,
            _delta_not_shared, _delta_by_difference, _combine_unbiased, _mass_error_signed,
            _farthest_by_sum, _rms_as_mean, _bounded_pins_at_zero, _off_support_zeroed,
-           _support_ignored]
+           _support_ignored, _duplicate_keeps_later, _no_ridge]
 
 
 @pytest.mark.parametrize("mutate", MUTANTS, ids=lambda f: f.__name__)
