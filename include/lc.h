@@ -40,6 +40,11 @@
  *    are recorded per head and read back with lc_get_report().
  *  - Outputs are finite except beta_j = -inf where w_j = 0 (key j keeps a
  *    zero weight, so it never receives attention).
+ *  - Two kept keys with equal vectors (value for value, -0 = +0) give equal
+ *    columns of the mass system, whose minimiser is then not unique: the
+ *    copy at the later position of idx gets w = 0 and keeps its own value
+ *    row, the minimiser an active-set method reaches when ties in its choice
+ *    of index go to the lower index.
  *  - A handle may be used by one host thread at a time; calls that share a
  *    workspace must not overlap on the device.
  */
@@ -60,8 +65,10 @@ typedef enum {
   LC_ERR_WORKSPACE = 3,      /* workspace too small or misaligned */
   LC_ERR_CUDA = 4,           /* a CUDA runtime/driver call failed */
   LC_ERR_NOT_CONVERGED = 5,  /* NNLS hit its iteration cap (outputs finite) */
-  LC_ERR_SINGULAR = 6,       /* a Cholesky factorisation broke down; a ridge
-                                of 1e-6 * mean(diag) was added once */
+  LC_ERR_SINGULAR = 6,       /* a Cholesky factorisation of an n x n system
+                                broke down (a pivot that is not positive); a
+                                ridge of n * 2^-20 * mean(diag) was added once
+                                and the outputs are that ridge solution's */
   LC_ERR_TIMEOUT = 7         /* a device-side wait gave up (internal error) */
 } lc_status;
 
@@ -113,7 +120,10 @@ lc_status lc_select_topt(lc_handle h, int n_heads, int T, int t, const float* u,
  * LC_NOALLOC_MAX_SCORES 32-bit codes (4 MiB) compiled into the library, held
  * on every GPU that loads it until the process exits.  Works on the current
  * CUDA device; the first call on a device looks up the array's address and
- * should come before any stream capture.  n_heads*T above
+ * should come before any stream capture.  The address is kept per device
+ * with the ID of the context it belongs to; after the device's context is
+ * reset (cudaDeviceReset) the next call looks it up again, and that call too
+ * belongs before any capture.  n_heads*T above
  * LC_NOALLOC_MAX_SCORES returns LC_ERR_UNSUPPORTED and enqueues nothing.
  * Calls that overlap on the GPU share the array and race: serialise them.
  * No cudaMalloc, cudaFree or allocating library call is made. */

@@ -459,8 +459,9 @@ lc_status run_pass2_rms(const Ctx& c, const void* qop, const void* kop, float2* 
 }
 
 // Steps 4-5 from the workspace's m_pad, lse_pad, O hi/lo and the given idx.
-lc_status run_fit_solve(const Ctx& c, const void* qop, const void* V, const int32_t* idx,
-                        float* w, float* beta, float* Cv, int bounded_iters, int status_off,
+lc_status run_fit_solve(const Ctx& c, const void* qop, const void* kop, const void* V,
+                        const int32_t* idx, float* w, float* beta, float* Cv, int bounded_iters,
+                        int status_off,
                         const CUtensorMap& mKc, const CUtensorMap& mQ64, const CUtensorMap& mOhi,
                         const CUtensorMap& mOlo, GramParams g, int g7_split, int g7_slabs,
                         int r_split, int r_slabs);
@@ -540,13 +541,14 @@ lc_status run_fit(const Ctx& ca, const void* qop, const void* kop, const void* V
     LC_CUDA(cudaStreamWaitEvent(cs->st, handoff, 0));
     cp = cs;
   }
-  return run_fit_solve(*cp, qop, V, idx, w, beta, Cv, bounded_iters, status_off, mKc, mQ64, mOhi,
+  return run_fit_solve(*cp, qop, kop, V, idx, w, beta, Cv, bounded_iters, status_off, mKc, mQ64, mOhi,
                        mOlo, g, g7_split, g7_slabs, r_split, r_slabs);
 }
 
 // Steps 4 (solve) and 5 of run_fit.
-lc_status run_fit_solve(const Ctx& c, const void* qop, const void* V, const int32_t* idx,
-                        float* w, float* beta, float* Cv, int bounded_iters, int status_off,
+lc_status run_fit_solve(const Ctx& c, const void* qop, const void* kop, const void* V,
+                        const int32_t* idx, float* w, float* beta, float* Cv, int bounded_iters,
+                        int status_off,
                         const CUtensorMap& mKc, const CUtensorMap& mQ64, const CUtensorMap& mOhi,
                         const CUtensorMap& mOlo, GramParams g, int g7_split, int g7_slabs,
                         int r_split, int r_slabs) {
@@ -569,6 +571,10 @@ lc_status run_fit_solve(const Ctx& c, const void* qop, const void* V, const int3
   sp.head_status = c.h->d_status + status_off;
   sp.head_iters = c.h->d_iters + status_off;
   sp.err = c.h->d_err;
+  sp.krows = kop;
+  sp.idx = idx;
+  sp.T = p.T;
+  sp.k_row_bytes = p.d_qk * 2;
   if (bounded_iters > 0) {
     LC_PROF(c, "bounded_ls", 1);
     sp.max_iter = bounded_iters;

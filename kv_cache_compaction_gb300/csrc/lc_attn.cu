@@ -16,12 +16,6 @@
 #include "lc_common.cuh"
 #include "lc_kernels.cuh"
 
-// Pipeline marks for instrumented builds (clock reads at the steps of one
-// CTA); empty in the library.
-#ifndef LC_ATTN_MARK
-#define LC_ATTN_MARK(id, step) ((void)0)
-#endif
-
 namespace lc {
 namespace {
 
@@ -66,7 +60,8 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* s_free = s_full + 2;            // [2]
   uint64_t* p_full = s_free + 2;
   uint64_t* pv_done = p_full + 1;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(pv_done + 1);
+  uint64_t* mma_drain = pv_done + 1;  // MMA completion before exit
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(mma_drain + 1);
   __shared__ volatile int abort_flag;
 
   const int warp = warp_id(), lane = lane_id();
@@ -87,6 +82,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     mbar_init(p_full, 128);
     mbar_init(pv_done, 1);
+    mbar_init(mma_drain, 1);
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(tslot, 512);
@@ -121,15 +117,11 @@ __global__ void __launch_bounds__(192, 1)
                         j * BN, h);
         issued = j + 1;
       }
-      // On abort, let the copies already in flight land before the CTA exits.
-      if (abort_flag) {
-        for (int j = (issued > L::NST ? issued - L::NST : 0); j < issued; ++j) {
-          const uint64_t t0 = globaltimer_ns();
-          while (!mbar_try_wait(&kv_full[j % L::NST], (j / L::NST) & 1) &&
-                 globaltimer_ns() - t0 < kWaitLimitNs) {
-          }
-        }
-      }
+      // the copies in flight land before the CTA exits, also when the pipeline
+      // was abandoned after a wait gave up elsewhere in the CTA
+      drain_wait(bar_q, 0);
+      for (int j = (issued > L::NST ? issued - L::NST : 0); j < issued; ++j)
+        drain_wait(&kv_full[j % L::NST], (j / L::NST) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -320,6 +312,7 @@ __global__ void __launch_bounds__(192, 1)
       }
     }
   }
+  if (warp == 1 && lane_id() == 0) drain_mma(mma_drain);
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tbase, 512);
@@ -378,7 +371,8 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* s_full = bars + 1 + 2 * NS;   // [2] tile A, B
   uint64_t* p_full = bars + 3 + 2 * NS;   // [2]
   uint64_t* pv_done = bars + 5 + 2 * NS;  // [2]
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 7 + 2 * NS);
+  uint64_t* mma_drain = bars + 7 + 2 * NS;  // MMA completion before exit
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(mma_drain + 1);
   __shared__ volatile int abort_flag;
 
   const int warp = warp_id(), lane = lane_id();
@@ -398,6 +392,7 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&p_full[x], 128);
       mbar_init(&pv_done[x], 1);
     }
+    mbar_init(mma_drain, 1);
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(tslot, 512);
@@ -424,17 +419,13 @@ __global__ void __launch_bounds__(320, 1)
         const CUtensorMap* m = (n & 1) ? &mV : &mK;
         for (int c = 0; c < L::NC; ++c)
           tma_load_3d(dst + c * BN * 128, m, &r_full[sl], 64 * c, (n >> 1) * BN, h);
-        LC_ATTN_MARK((n & 1) ? 5 : 0, n >> 1);
         issued = n + 1;
       }
-      if (abort_flag) {
-        for (int n = (issued > NS ? issued - NS : 0); n < issued; ++n) {
-          const uint64_t t0 = globaltimer_ns();
-          while (!mbar_try_wait(&r_full[n % NS], (n / NS) & 1) &&
-                 globaltimer_ns() - t0 < kWaitLimitNs) {
-          }
-        }
-      }
+      // the copies in flight land before the CTA exits, also when the pipeline
+      // was abandoned after a wait gave up elsewhere in the CTA
+      drain_wait(q_full, 0);
+      for (int n = (issued > NS ? issued - NS : 0); n < issued; ++n)
+        drain_wait(&r_full[n % NS], (n / NS) & 1);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -453,7 +444,6 @@ __global__ void __launch_bounds__(320, 1)
           umma_f16_ss(tbase + x * 128, da, db, idesc_s, k > 0 ? 1u : 0u);
         }
         umma_commit(&s_full[x]);
-        LC_ATTN_MARK(1 + x, j);
       };
       // O_x += P_x V_j, P_x in tensor memory (16 keys = 8 columns per step)
       auto issue_pv = [&](int x, int j) {
@@ -465,7 +455,6 @@ __global__ void __launch_bounds__(320, 1)
                       (j > 0 || k > 0) ? 1u : 0u);
         }
         umma_commit(&pv_done[x]);
-        LC_ATTN_MARK(3 + x, j);
       };
       // Event loop over both tiles: S_x(0); then per j: P_x V_j once P_x(j)
       // is written, followed by S_x(j+1) once K_{j+1} has landed.  A ring
@@ -523,13 +512,10 @@ __global__ void __launch_bounds__(320, 1)
     float m_ref = -kInf, m_true = -kInf, l = 0.f;
     bool ok = true;
     for (int j = 0; j < nkt; ++j) {
-      if (wq == 2) LC_ATTN_MARK(8, j);
       if (!wait_bar(&s_full[x], j & 1, &abort_flag, p.err)) { ok = false; break; }
       tc_fence_after();
-      if (wq == 2) LC_ATTN_MARK(9, j);
       float xs[BN];
       tmem_ld128(tS + lane_off, xs);
-      if (wq == 2) LC_ATTN_MARK(10, j);
       const int valid = p.T - j * BN;
       if (valid < BN) {
 #pragma unroll
@@ -599,7 +585,6 @@ __global__ void __launch_bounds__(320, 1)
       }
       tc_fence_before();
       mbar_arrive(&p_full[x]);
-      if (wq == 2) LC_ATTN_MARK(13, j);
     }
     if (ok && wait_bar(&pv_done[x], (nkt - 1) & 1, &abort_flag, p.err)) {
       tc_fence_after();
@@ -646,6 +631,7 @@ __global__ void __launch_bounds__(320, 1)
       }
     }
   }
+  if (warp == 1 && lane_id() == 0) drain_mma(mma_drain);
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tbase, 512);

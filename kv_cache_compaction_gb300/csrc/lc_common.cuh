@@ -111,6 +111,26 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
   }
 }
 
+// Bounded wait on the way out of a kernel: returns once the phase of `bar`
+// with the given parity has completed, or after kWaitLimitNs; abort flags are
+// not consulted (the point is to let work already in flight finish).
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity) && globaltimer_ns() - t0 < kWaitLimitNs) {
+  }
+}
+
+// Run by the thread that issued a kernel's tensor-core operations, after its
+// last issue and before the CTA frees its tensor memory: commits every
+// operation it issued to `bar` (an mbarrier of count 1 used for nothing else)
+// and waits, bounded, for them to complete.  Then no MMA still reads or
+// writes tensor or shared memory when the CTA frees them, also when a wait
+// elsewhere in the CTA gave up early and the pipeline was abandoned midway.
+__device__ __forceinline__ void drain_mma(uint64_t* bar) {
+  umma_commit(bar);
+  drain_wait(bar, 0);
+}
+
 // True if an earlier CTA of this launch (or an earlier launch of this call)
 // already timed out.
 __device__ __forceinline__ bool launch_aborted(const uint32_t* err) {

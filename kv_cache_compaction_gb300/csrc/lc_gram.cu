@@ -29,12 +29,6 @@
 #include "lc_common.cuh"
 #include "lc_kernels.cuh"
 
-// Phase marks for instrumented builds (clock reads at pipeline events); empty
-// in the library.
-#ifndef LC_GRAM_MARK
-#define LC_GRAM_MARK(id, slab) ((void)0)
-#endif
-
 namespace lc {
 namespace {
 
@@ -86,7 +80,8 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* s_free = bars + 7;    // [2]
   uint64_t* e_full = bars + 9;
   uint64_t* e_free = bars + 10;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 11);
+  uint64_t* mma_drain = bars + 11;  // MMA completion before exit
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(mma_drain + 1);
   __shared__ volatile int abort_flag;
 
   const int warp = warp_id(), lane = lane_id();
@@ -124,6 +119,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     mbar_init(e_full, 128);
     mbar_init(e_free, 1);
+    mbar_init(mma_drain, 1);
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(tslot, 512);
@@ -165,14 +161,11 @@ __global__ void __launch_bounds__(192, 1)
         if (with_c) bulk_g2s(rw + kSL * 4, p.row_b + roff, kSL * 4, &st_full[s]);
         issued = i + 1;
       }
-      if (abort_flag) {
-        for (int i = (issued > L::NST ? issued - L::NST : 0); i < issued; ++i) {
-          const uint64_t t0 = globaltimer_ns();
-          while (!mbar_try_wait(&st_full[i % L::NST], (i / L::NST) & 1) &&
-                 globaltimer_ns() - t0 < kWaitLimitNs) {
-          }
-        }
-      }
+      // the copies in flight land before the CTA exits, also when the pipeline
+      // was abandoned after a wait gave up elsewhere in the CTA
+      drain_wait(k_full, 0);
+      for (int i = (issued > L::NST ? issued - L::NST : 0); i < issued; ++i)
+        drain_wait(&st_full[i % L::NST], (i / L::NST) & 1);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
@@ -330,6 +323,7 @@ __global__ void __launch_bounds__(192, 1)
       }
     }
   }
+  if (warp == 1 && lane_id() == 0) drain_mma(mma_drain);
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tbase, 512);
@@ -384,7 +378,8 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* e_full = bars + 9;    // [2]
   uint64_t* e_free = bars + 11;   // [2]
   uint64_t* done = bars + 13;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 14);
+  uint64_t* mma_drain = bars + 14;  // MMA completion before exit
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(mma_drain + 1);
   float* cx = reinterpret_cast<float*>(base + L::OFF_CX);
   __shared__ volatile int abort_flag;
 
@@ -428,6 +423,7 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&e_free[i], 1);
     }
     mbar_init(done, 1);
+    mbar_init(mma_drain, 1);
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(tslot, 512);
@@ -449,7 +445,6 @@ __global__ void __launch_bounds__(320, 1)
       for (int i = 0; i < nsl; ++i) {
         const int s = i & 1;
         if (i >= 2 && !wait_bar(&st_empty[s], ((i >> 1) - 1) & 1, &abort_flag, p.err)) break;
-        LC_GRAM_MARK(10, i);
         uint8_t* st = sRing + s * stage_bytes;
         const int r0 = (s0 + i) * kSL;
         mbar_arrive_expect_tx(&st_full[s], bytes);
@@ -464,14 +459,11 @@ __global__ void __launch_bounds__(320, 1)
         }
         issued = i + 1;
       }
-      if (abort_flag) {
-        for (int i = (issued > 2 ? issued - 2 : 0); i < issued; ++i) {
-          const uint64_t t0 = globaltimer_ns();
-          while (!mbar_try_wait(&st_full[i & 1], (i >> 1) & 1) &&
-                 globaltimer_ns() - t0 < kWaitLimitNs) {
-          }
-        }
-      }
+      // the copies in flight land before the CTA exits, also when the pipeline
+      // was abandoned after a wait gave up elsewhere in the CTA
+      drain_wait(k_full, 0);
+      for (int i = (issued > 2 ? issued - 2 : 0); i < issued; ++i)
+        drain_wait(&st_full[i & 1], (i >> 1) & 1);
     }
   } else if (warp == 1) {
     if (lane == 0 && nsl > 0) {
@@ -542,13 +534,10 @@ __global__ void __launch_bounds__(320, 1)
       while (ok && ng < nsl) {
         if (ns < nsl && mbar_test_wait(&st_full[ns & 1], (ns >> 1) & 1) &&
             (ns < 2 || mbar_test_wait(&s_free[ns & 1], ((ns >> 1) - 1) & 1))) {
-          LC_GRAM_MARK(3, ns);
           issue_s(ns++);
           t_last = globaltimer_ns();
         } else if (ng < ns && mbar_test_wait(&e_full[ng & 1], (ng >> 1) & 1)) {
-          LC_GRAM_MARK(1, ng);
           issue_g(ng++);
-          LC_GRAM_MARK(2, ng - 1);
           t_last = globaltimer_ns();
         } else if ((++spins & 63u) == 0) {
           if (abort_flag) break;
@@ -596,7 +585,6 @@ __global__ void __launch_bounds__(320, 1)
         asm volatile("prefetch.global.L1 [%0];" ::"l"(rb + 32));
       }
       if (!wait_bar(&s_full[g], n & 1, &abort_flag, p.err)) { ok = false; break; }
-      LC_GRAM_MARK(20, i);
       tc_fence_after();
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {  // 32 query columns at a time
@@ -617,7 +605,6 @@ __global__ void __launch_bounds__(320, 1)
           mbar_arrive(&s_free[g]);
         } else {
           if (n > 0 && !wait_bar(&e_free[g], (n - 1) & 1, &abort_flag, p.err)) { ok = false; break; }
-          LC_GRAM_MARK(21, i);
         }
 #pragma unroll
         for (int q8 = 0; q8 < 4; ++q8) {
@@ -650,7 +637,6 @@ __global__ void __launch_bounds__(320, 1)
         }
       }
       if (!ok) break;
-      LC_GRAM_MARK(23, i);
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(&e_full[g]);
@@ -687,6 +673,7 @@ __global__ void __launch_bounds__(320, 1)
       }
     }
   }
+  if (warp == 1 && lane_id() == 0) drain_mma(mma_drain);
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tbase, 512);
@@ -742,7 +729,8 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* e_full = bars + 15;   // [2]
   uint64_t* e_free = bars + 17;   // [2]
   uint64_t* done = bars + 19;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 20);
+  uint64_t* mma_drain = bars + 20;  // MMA completion before exit
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(mma_drain + 1);
   __shared__ volatile int abort_flag;
 
   const int warp = warp_id(), lane = lane_id();
@@ -777,6 +765,7 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&e_free[i], 1);
     }
     mbar_init(done, 1);
+    mbar_init(mma_drain, 1);
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(tslot, 512);
@@ -823,20 +812,15 @@ __global__ void __launch_bounds__(320, 1)
         }
         no = RM ? i + 1 : 0;
       }
-      if (abort_flag) {
-        // let the copies in flight land before the CTA exits
-        auto drain = [&](uint64_t* full, int n) {
-          for (int i = (n > 2 ? n - 2 : 0); i < n; ++i) {
-            const uint64_t t0 = globaltimer_ns();
-            while (!mbar_try_wait(&full[i & 1], (i >> 1) & 1) &&
-                   globaltimer_ns() - t0 < kWaitLimitNs) {
-            }
-          }
-        };
-        drain(st_full, nq);
-        drain(r_full, nr);
-        drain(o_full, no);
-      }
+      // the copies in flight land before the CTA exits, also when the pipeline
+      // was abandoned after a wait gave up elsewhere in the CTA
+      auto drain = [&](uint64_t* full, int n) {
+        for (int i = (n > 2 ? n - 2 : 0); i < n; ++i) drain_wait(&full[i & 1], (i >> 1) & 1);
+      };
+      drain_wait(k_full, 0);
+      drain(st_full, nq);
+      drain(r_full, nr);
+      drain(o_full, no);
     }
   } else if (warp == 1) {
     if (lane == 0 && nsl > 0) {
@@ -1027,6 +1011,7 @@ __global__ void __launch_bounds__(320, 1)
       }
     }
   }
+  if (warp == 1 && lane_id() == 0) drain_mma(mma_drain);
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tbase, 512);

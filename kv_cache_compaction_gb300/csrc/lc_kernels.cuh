@@ -218,6 +218,11 @@ struct SolveParams {
   int32_t* head_status;    // [H]
   int32_t* head_iters;     // [H]
   uint32_t* err;
+  // Kept-key rows for the duplicate check of the NNLS (null: no check): the
+  // key operand [H][T][k_row_bytes / 2] of 16-bit elements and the selection.
+  const void* krows;
+  const int32_t* idx;      // [H][t]
+  int T, k_row_bytes;
 };
 cudaError_t launch_nnls(const SolveParams& p, cudaStream_t st);
 // Bounded least squares w in [lo, hi], p.max_iter iterations (see the kernel).

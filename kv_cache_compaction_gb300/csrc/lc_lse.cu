@@ -49,7 +49,8 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* k_empty = bars + 3;  // [2]
   uint64_t* s_full = bars + 5;   // [2]
   uint64_t* s_free = bars + 7;   // [2]
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 9);
+  uint64_t* mma_drain = bars + 9;  // MMA completion before exit
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(mma_drain + 1);
   __shared__ volatile int abort_flag;
   const int warp = warp_id(), lane = lane_id();
   const int q0 = blockIdx.x * kBM, h = blockIdx.y;
@@ -66,6 +67,7 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&s_full[i], 1);
       mbar_init(&s_free[i], 128);
     }
+    mbar_init(mma_drain, 1);
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(tslot, 256);
@@ -88,14 +90,11 @@ __global__ void __launch_bounds__(192, 1)
                       key0 + j * 128, h);
         issued = j + 1;
       }
-      if (abort_flag) {
-        for (int j = (issued > 2 ? issued - 2 : 0); j < issued; ++j) {
-          const uint64_t t0 = globaltimer_ns();
-          while (!mbar_try_wait(&k_full[j & 1], (j >> 1) & 1) &&
-                 globaltimer_ns() - t0 < kWaitLimitNs) {
-          }
-        }
-      }
+      // the copies in flight land before the CTA exits, also when the pipeline
+      // was abandoned after a wait gave up elsewhere in the CTA
+      drain_wait(bar_q, 0);
+      for (int j = (issued > 2 ? issued - 2 : 0); j < issued; ++j)
+        drain_wait(&k_full[j & 1], (j >> 1) & 1);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -164,6 +163,7 @@ __global__ void __launch_bounds__(192, 1)
       }
     }
   }
+  if (warp == 1 && lane_id() == 0) drain_mma(mma_drain);
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tbase, 256);
@@ -203,7 +203,8 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* q_empty = bars + 3;  // [2]
   uint64_t* s_full = bars + 5;   // [2]
   uint64_t* s_free = bars + 7;   // [2]
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 9);
+  uint64_t* mma_drain = bars + 9;  // MMA completion before exit
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(mma_drain + 1);
   __shared__ volatile int abort_flag;
   const int warp = warp_id(), lane = lane_id();
   const int h = blockIdx.y;
@@ -223,6 +224,7 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&s_full[i], 1);
       mbar_init(&s_free[i], 128);
     }
+    mbar_init(mma_drain, 1);
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(tslot, 512);
@@ -249,17 +251,11 @@ __global__ void __launch_bounds__(320, 1)
                       (t0 + i) * kBM, h);
         issued = i + 1;
       }
-      if (abort_flag) {
-        const uint64_t w0 = globaltimer_ns();
-        while (!mbar_try_wait(k_full, 0) && globaltimer_ns() - w0 < kWaitLimitNs) {
-        }
-        for (int i = (issued > 2 ? issued - 2 : 0); i < issued; ++i) {
-          const uint64_t w1 = globaltimer_ns();
-          while (!mbar_try_wait(&q_full[i & 1], (i >> 1) & 1) &&
-                 globaltimer_ns() - w1 < kWaitLimitNs) {
-          }
-        }
-      }
+      // the copies in flight land before the CTA exits, also when the pipeline
+      // was abandoned after a wait gave up elsewhere in the CTA
+      drain_wait(k_full, 0);
+      for (int i = (issued > 2 ? issued - 2 : 0); i < issued; ++i)
+        drain_wait(&q_full[i & 1], (i >> 1) & 1);
     }
   } else if (warp == 1) {
     if (lane == 0 && nt > 0) {
@@ -333,6 +329,7 @@ __global__ void __launch_bounds__(320, 1)
       }
     }
   }
+  if (warp == 1 && lane_id() == 0) drain_mma(mma_drain);
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tbase, 512);

@@ -53,7 +53,8 @@ __global__ void __launch_bounds__(192, 2)
   uint64_t* q_empty = bars + 3;  // [2]
   uint64_t* d_full = bars + 5;   // [2]
   uint64_t* d_free = bars + 7;   // [2]
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 9);
+  uint64_t* mma_drain = bars + 9;  // MMA completion before exit
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(mma_drain + 1);
   __shared__ volatile int abort_flag;
 
   const int warp = warp_id(), lane = lane_id();
@@ -71,6 +72,7 @@ __global__ void __launch_bounds__(192, 2)
       mbar_init(&d_full[i], 1);
       mbar_init(&d_free[i], 128);
     }
+    mbar_init(mma_drain, 1);
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(tslot, 256);
@@ -95,14 +97,11 @@ __global__ void __launch_bounds__(192, 2)
                  &q_full[s]);
         issued = i + 1;
       }
-      if (abort_flag) {
-        for (int i = (issued > 2 ? issued - 2 : 0); i < issued; ++i) {
-          const uint64_t tt = globaltimer_ns();
-          while (!mbar_try_wait(&q_full[i & 1], (i >> 1) & 1) &&
-                 globaltimer_ns() - tt < kWaitLimitNs) {
-          }
-        }
-      }
+      // the copies in flight land before the CTA exits, also when the pipeline
+      // was abandoned after a wait gave up elsewhere in the CTA
+      drain_wait(k_full, 0);
+      for (int i = (issued > 2 ? issued - 2 : 0); i < issued; ++i)
+        drain_wait(&q_full[i & 1], (i >> 1) & 1);
     }
   } else if (warp == 1) {
     if (lane == 0 && ntile > 0) {
@@ -158,6 +157,7 @@ __global__ void __launch_bounds__(192, 2)
                           fmaxf(fmaxf(u8[4], u8[5]), fmaxf(u8[6], u8[7])));
     if (ok && key < p.T) atomicMax(p.u_code + static_cast<size_t>(h) * p.T + key, order_code(u));
   }
+  if (warp == 1 && lane_id() == 0) drain_mma(mma_drain);
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tbase, 256);
@@ -206,7 +206,8 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* q_empty = bars + 1 + L::NST;      // [NST]
   uint64_t* d_full = bars + 1 + 2 * L::NST;   // [2]
   uint64_t* d_free = bars + 3 + 2 * L::NST;   // [2]
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 5 + 2 * L::NST);
+  uint64_t* mma_drain = bars + 5 + 2 * L::NST;  // MMA completion before exit
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(mma_drain + 1);
   __shared__ volatile int abort_flag;
 
   const int warp = warp_id(), lane = lane_id();
@@ -226,6 +227,7 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&d_full[b], 1);
       mbar_init(&d_free[b], 256);
     }
+    mbar_init(mma_drain, 1);
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(tslot, 512);
@@ -253,14 +255,11 @@ __global__ void __launch_bounds__(320, 1)
                  &q_full[s]);
         issued = i + 1;
       }
-      if (abort_flag) {
-        for (int i = (issued > L::NST ? issued - L::NST : 0); i < issued; ++i) {
-          const uint64_t tt = globaltimer_ns();
-          while (!mbar_try_wait(&q_full[i % L::NST], (i / L::NST) & 1) &&
-                 globaltimer_ns() - tt < kWaitLimitNs) {
-          }
-        }
-      }
+      // the copies in flight land before the CTA exits, also when the pipeline
+      // was abandoned after a wait gave up elsewhere in the CTA
+      drain_wait(k_full, 0);
+      for (int i = (issued > L::NST ? issued - L::NST : 0); i < issued; ++i)
+        drain_wait(&q_full[i % L::NST], (i / L::NST) & 1);
     }
   } else if (warp == 1) {
     if (lane == 0 && ntile > 0) {
@@ -382,6 +381,7 @@ __global__ void __launch_bounds__(320, 1)
             make_float2(mass_m, mass_s);
     }
   }
+  if (warp == 1 && lane_id() == 0) drain_mma(mma_drain);
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tbase, 512);

@@ -33,12 +33,6 @@
 #include "lc_common.cuh"
 #include "lc_kernels.cuh"
 
-// Phase marks for instrumented builds (clock reads between phases); empty in
-// the library.
-#ifndef LC_SOLVER_MARK
-#define LC_SOLVER_MARK(id) ((void)0)
-#endif
-
 namespace lc {
 namespace {
 
@@ -180,16 +174,13 @@ __device__ __noinline__ bool cta_cholesky(float* S, float* dinv, int NB, int* ba
       for (int c = 0; c < kBS; ++c) row[c] = x[c];
     }
     __syncthreads();
-    LC_SOLVER_MARK(40);
     // trailing update; warp 0 takes the next diagonal block and factors it
     const int m = NB - K - 1;
     if (m > 0) {
       if (warp == 0) {
         tile_update(S, K + 1, K + 1, K);
         __syncwarp();
-        LC_SOLVER_MARK(41);
         diag_factor(S, dinv, K + 1, bad);
-        LC_SOLVER_MARK(42);
       } else if (warp % 4 != 0) {
         // warps 4, 8, 12 share a scheduler with warp 0 and stay idle, so
         // the diagonal factorisation -- the critical path -- issues alone
@@ -206,7 +197,6 @@ __device__ __noinline__ bool cta_cholesky(float* S, float* dinv, int NB, int* ba
       }
     }
     __syncthreads();
-    LC_SOLVER_MARK(43);
   }
   const bool ok = *bad == 0;
   __syncthreads();
@@ -302,7 +292,6 @@ __device__ __noinline__ void cta_chol_solve(const float* S, const float* dinv, i
     }
   }
 }
-
 
 // Solve L L^T x = v (passes as in cta_chol_solve) for one right-hand side v
 // in shared memory (NB*32 entries).  Step K: warp 0 solves block K with one
@@ -526,7 +515,7 @@ struct SolverSmem {
   float* S;      // packed blocks (resident) or null
   float* dinv;   // reciprocal diagonal of L
   float* vec;    // 4 * n_pad floats
-  int* ivec;     // 3 * n_pad ints
+  int* ivec;     // 4 * n_pad ints
   float* T;      // 32 * kMaxRhs floats
   float* T2;     // 32 * kMaxRhs floats
 };
@@ -537,7 +526,7 @@ __host__ __device__ inline size_t solver_smem_bytes(int n_pad) {
   size_t b = 0;
   if (resident) b += static_cast<size_t>(NB * (NB + 1) / 2) * kBlk * 4;
   b += static_cast<size_t>(n_pad) * 4;
-  b += 4ull * n_pad * 4 + 3ull * n_pad * 4;
+  b += 4ull * n_pad * 4 + 4ull * n_pad * 4;
   b += 2ull * kBS * kMaxRhs * 4;
   return b;
 }
@@ -556,7 +545,7 @@ __device__ SolverSmem carve(float* dyn, int n_pad) {
   s.vec = p;
   p += 4 * n_pad;
   s.ivec = reinterpret_cast<int*>(p);
-  p += 3 * n_pad;
+  p += 4 * n_pad;
   s.T = p;
   s.T2 = p + kBS * kMaxRhs;
   return s;
@@ -580,6 +569,93 @@ __device__ void gather_packed(float* S, int NB, int n, F src) {
   }
 }
 
+// Ridge added once to an n x n system whose factorisation broke down (a
+// pivot that is not positive), from the sum of its diagonal: n * 2^-20 *
+// mean(diag) = 2^-20 * diag_sum.  On a rank-deficient system the rounding
+// errors of the factorisation add up coherently to about n unit roundoffs of
+// the diagonal (all queries at q = 0 give a rank-one mass system whose
+// leftover block after one elimination step is a constant of that size), so
+// the ridge scales with n to stay above them.
+__device__ __forceinline__ float ridge_of(float diag_sum, int n) {
+  return n > 0 ? diag_sum * 9.5367431640625e-7f : 0.f;
+}
+
+// 32-bit word of a key row with -0 folded onto +0 in both 16-bit halves, so
+// that equal words mean equal values.
+__device__ __forceinline__ uint32_t canon16x2(uint32_t x) {
+  if ((x & 0x7fffu) == 0) x &= 0xffff0000u;
+  if ((x & 0x7fff0000u) == 0) x &= 0x0000ffffu;
+  return x;
+}
+
+// dup[j] = 1 for each kept key j whose operand row equals, value for value,
+// the row of a kept key at an earlier position (dup must be zero on entry).
+// Such a key's column of the mass system equals the earlier key's, so the
+// NNLS minimiser is not unique; the later copy is held at w = 0, the
+// minimiser Lawson-Hanson reaches with its argmax ties going to the lower
+// index.  Rows are hashed (one warp per row, eight rows in flight per warp,
+// at most 96 words a row), each key's hash is compared with the earlier
+// keys' and a hash match is confirmed on the full rows.  hsh: t words.
+__device__ void mark_later_duplicates(const SolveParams& p, int h, int* dup, uint32_t* hsh) {
+  const int t = p.t, warp = warp_id(), lane = lane_id();
+  const int nw = p.k_row_bytes / 4;
+  const uint32_t* K = static_cast<const uint32_t*>(p.krows);
+  const int32_t* idx = p.idx + static_cast<size_t>(h) * t;
+  auto row = [&](int j) {
+    return K + (static_cast<size_t>(h) * p.T + static_cast<size_t>(idx[j])) * nw;
+  };
+  constexpr int kRows = 8;
+  for (int j0 = warp * kRows; j0 < t; j0 += kWarps * kRows) {
+    uint32_t acc[kRows];
+#pragma unroll
+    for (int u = 0; u < kRows; ++u) {
+      acc[u] = 0u;
+      const int j = j0 + u;
+      if (j < t) {
+        const uint32_t* r = row(j);
+#pragma unroll
+        for (int q = 0; q < 3; ++q) {
+          const int k = lane + 32 * q;
+          if (k < nw) {
+            uint32_t x = canon16x2(__ldg(r + k)) ^ (0x9e3779b9u * static_cast<uint32_t>(k + 1));
+            x *= 0x85ebca6bu;
+            x ^= x >> 13;
+            x *= 0xc2b2ae35u;
+            x ^= x >> 16;
+            acc[u] += x;
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kRows; ++u) {
+      uint32_t a = acc[u];
+      for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(kFull, a, o);
+      if (lane == 0 && j0 + u < t) hsh[j0 + u] = a;
+    }
+  }
+  __syncthreads();
+  for (int j = 1 + warp; j < t; j += kWarps) {
+    const uint32_t hj = hsh[j];
+    bool found = false;
+    for (int base = 0; base < j && !found; base += 32) {
+      const int jp = base + lane;
+      unsigned m = __ballot_sync(kFull, jp < j && hsh[jp] == hj);
+      while (m != 0u && !found) {
+        const int c = base + __ffs(m) - 1;
+        m &= m - 1u;
+        const uint32_t* a = row(j);
+        const uint32_t* b = row(c);
+        bool eq = true;
+        for (int k = lane; k < nw; k += 32) eq = eq && canon16x2(a[k]) == canon16x2(b[k]);
+        found = __all_sync(kFull, eq);
+      }
+    }
+    if (lane == 0) dup[j] = found ? 1 : 0;
+  }
+  __syncthreads();
+}
+
 // Step 4 for one head (one CTA).
 //
 // G is factored once (L L^T = G) and z0 = G^-1 c.  For an active set D
@@ -590,11 +666,17 @@ __device__ void gather_packed(float* S, int NB, int n, F src) {
 // in registers), (G^-1)_DD = Y^T Y and G^-1 E_D mu = L^-T (Y mu), so a step
 // costs one forward solve with |D| columns, a |D| x |D| Cholesky and one
 // backward solve with a single column -- no refactorisation.  Systems with
-// more than 256 unknowns, a G that is not positive definite in fp32, or an
-// active set larger than 64 factor G_FF directly at every step instead.
+// more than 256 unknowns, a G that is not positive definite in fp32 even with
+// the ridge, or an active set larger than 64 factor G_FF directly at every
+// step instead.  Later copies of a kept key (mark_later_duplicates) stay at
+// w = 0: their rows and columns of the factored matrix are the identity's and
+// they never enter the passive or the active index lists.  A factorisation
+// that breaks down (a pivot that is not positive) is redone once with the
+// ridge of ridge_of, and the head's status becomes LC_ERR_SINGULAR.
 __global__ void __launch_bounds__(kThreads, 1) nnls_bpp_kernel(const SolveParams p) {
   extern __shared__ float dyn[];
   __shared__ int redi[33];
+  __shared__ float redf[33];
   __shared__ int bad;
   const int h = blockIdx.x, tid = threadIdx.x, warp = warp_id(), lane = lane_id();
   const int rg = lane >> 2, cg = lane & 3;
@@ -610,6 +692,7 @@ __global__ void __launch_bounds__(kThreads, 1) nnls_bpp_kernel(const SolveParams
   int* F = sm.ivec;
   int* Didx = F + n_pad;
   int* flip = Didx + n_pad;
+  int* dup = flip + n_pad;
   float* Yg = p.wbuf + static_cast<size_t>(h) * tp * kMaxD;  // Y spilled for Y^T Y
   // small system in the first staging buffer
   float* Ms = sm.T;
@@ -617,31 +700,53 @@ __global__ void __launch_bounds__(kThreads, 1) nnls_bpp_kernel(const SolveParams
   float* mu = ds + 2 * kBS;
   const float* G = p.G + static_cast<size_t>(h) * tp * tp;
 
+  for (int j = tid; j < n_pad; j += kThreads) dup[j] = 0;
+  __syncthreads();
+  if (p.krows) mark_later_duplicates(p, h, dup, reinterpret_cast<uint32_t*>(aux));
   for (int j = tid; j < n_pad; j += kThreads) {
-    cv[j] = j < t ? p.c[static_cast<size_t>(h) * tp + j] : 0.f;
-    F[j] = j < t;
+    const bool live = j < t && !dup[j];
+    cv[j] = live ? p.c[static_cast<size_t>(h) * tp + j] : 0.f;
+    F[j] = live;
     x[j] = 0.f;
   }
   __syncthreads();
   int status = LC_OK_STATUS;
   bool direct = sm.S == nullptr;
   if (!direct) {
-    gather_packed(S, NB, t, [&](int a, int b) { return G[static_cast<size_t>(a) * tp + b]; });
-    __syncthreads();
-    LC_SOLVER_MARK(0);
-    direct = !cta_cholesky(S, sm.dinv, NB, &bad);
-    LC_SOLVER_MARK(1);
+    float ridge = 0.f;
+    for (int attempt = 0; attempt < 2; ++attempt) {
+      gather_packed(S, NB, t, [&](int a, int b) {
+        if (dup[a] || dup[b]) return (a == b) ? 1.f : 0.f;
+        return G[static_cast<size_t>(a) * tp + b] + (a == b ? ridge : 0.f);
+      });
+      __syncthreads();
+      if (cta_cholesky(S, sm.dinv, NB, &bad)) break;
+      if (attempt == 1) {
+        direct = true;
+        break;
+      }
+      status = LC_SINGULAR_STATUS;
+      float dsum = 0.f;
+      int cnt = 0;
+      for (int a = tid; a < t; a += kThreads)
+        if (!dup[a]) {
+          dsum += G[static_cast<size_t>(a) * tp + a];
+          ++cnt;
+        }
+      dsum = block_sum_f(dsum, redf);
+      cnt = block_sum_int(cnt, redi);
+      ridge = ridge_of(dsum, cnt);
+    }
   }
   if (!direct) {
     for (int j = tid; j < n_pad; j += kThreads) z0[j] = cv[j];
     __syncthreads();
     cta_solve1(S, sm.dinv, NB, z0);
-    LC_SOLVER_MARK(3);
   }
   int ninf_best = t + 1, backup = 3, it = 0;
   bool converged = false;
   for (it = 0; it < p.max_iter; ++it) {
-    for (int j = tid; j < n_pad; j += kThreads) flip[j] = (j < t) && !F[j];
+    for (int j = tid; j < n_pad; j += kThreads) flip[j] = (j < t) && !F[j] && !dup[j];
     __syncthreads();
     const int nD = block_compact(flip, Didx, t, redi);
     if (!direct && nD > kMaxD) direct = true;
@@ -653,7 +758,6 @@ __global__ void __launch_bounds__(kThreads, 1) nnls_bpp_kernel(const SolveParams
         const int nct = nD > kBS ? 2 : 1;
         const int NBs = nct;
         for (int e = tid; e < 3 * kBlk; e += kThreads) Ms[e] = 0.f;
-        LC_SOLVER_MARK(10);
         // Y = L^-1 E_D, one warp per column: lane r keeps the running
         // right-hand side of row r of every block; block K is solved
         // lane-parallel (x_k broadcast by shuffle) and its product with the
@@ -694,7 +798,6 @@ __global__ void __launch_bounds__(kThreads, 1) nnls_bpp_kernel(const SolveParams
             }
           }
         }
-        LC_SOLVER_MARK(11);
         __syncthreads();
         // (G^-1)_DD = Y^T Y, lower tiles (0,0), (1,0), (1,1): one register-
         // tiled product per (tile, 32-row block of Y), written to the dense
@@ -734,7 +837,6 @@ __global__ void __launch_bounds__(kThreads, 1) nnls_bpp_kernel(const SolveParams
         __syncthreads();
         if (!cta_cholesky(Ms, ds, NBs, &bad)) status = LC_SINGULAR_STATUS;
         cta_solve1(Ms, ds, NBs, mu);
-        LC_SOLVER_MARK(12);
         // v = Y mu, then x = z0 + L^-T v
         for (int a = tid; a < n_pad; a += kThreads) {
           const float4* yr = reinterpret_cast<const float4*>(Yg + static_cast<size_t>(a) * kMaxD);
@@ -758,23 +860,31 @@ __global__ void __launch_bounds__(kThreads, 1) nnls_bpp_kernel(const SolveParams
       // direct: factor G_FF
       const int nF = block_compact(F, Didx, t, redi);
       const int NBf = (nF + kBS - 1) / kBS;
-      gather_packed(S, NBf, nF, [&](int a, int b) {
-        return G[static_cast<size_t>(Didx[a]) * tp + Didx[b]];
-      });
+      float ridge = 0.f;
+      for (int attempt = 0; attempt < 2; ++attempt) {
+        gather_packed(S, NBf, nF, [&](int a, int b) {
+          return G[static_cast<size_t>(Didx[a]) * tp + Didx[b]] + (a == b ? ridge : 0.f);
+        });
+        __syncthreads();
+        if (cta_cholesky(S, sm.dinv, NBf, &bad)) break;
+        status = LC_SINGULAR_STATUS;
+        if (attempt == 1) break;  // keep the factor with its non-positive pivots set to 1
+        float dsum = 0.f;
+        for (int a = tid; a < nF; a += kThreads) dsum += G[static_cast<size_t>(Didx[a]) * tp + Didx[a]];
+        ridge = ridge_of(block_sum_f(dsum, redf), nF);
+      }
       for (int a = tid; a < NBf * kBS; a += kThreads) aux[a] = a < nF ? cv[Didx[a]] : 0.f;
       __syncthreads();
-      if (!cta_cholesky(S, sm.dinv, NBf, &bad)) status = LC_SINGULAR_STATUS;
       cta_solve1(S, sm.dinv, NBf, aux);
       for (int j = tid; j < n_pad; j += kThreads) x[j] = 0.f;
       __syncthreads();
       for (int a = tid; a < nF; a += kThreads) x[Didx[a]] = aux[a];
       __syncthreads();
       // the active rows for the dual check below
-      for (int j = tid; j < n_pad; j += kThreads) flip[j] = (j < t) && !F[j];
+      for (int j = tid; j < n_pad; j += kThreads) flip[j] = (j < t) && !F[j] && !dup[j];
       __syncthreads();
       block_compact(flip, Didx, t, redi);
     }
-    LC_SOLVER_MARK(13);
     // infeasible set: x_j < 0 on F; on D, y_j = (G x - c)_j < -tol with tol a
     // few ulps of the terms of y_j
     for (int j = tid; j < n_pad; j += kThreads) flip[j] = (j < t) && F[j] && x[j] < 0.f;
@@ -807,7 +917,6 @@ __global__ void __launch_bounds__(kThreads, 1) nnls_bpp_kernel(const SolveParams
         maxj = j;
       }
     cnt = block_sum_int(cnt, redi);
-    LC_SOLVER_MARK(14);
     if (cnt == 0) {
       converged = true;
       break;
@@ -844,18 +953,20 @@ __global__ void __launch_bounds__(kThreads, 1) nnls_bpp_kernel(const SolveParams
   }
 }
 
-
 // Bounded variant of step 4 ("Latent Compaction with Test-Time Training",
 // Appendix A.3: the Attention Matching baseline's bounded NNLS iterations,
 // bounds [lo, hi] = [e^-3, e^3]).  Each iteration solves G_FF w_F =
 // c_F - G_FB w_B over the free set F with the pinned set B at its bounds
 // (G_FF factored directly), then pins every free weight outside [lo, hi] at
 // the bound it crossed; it starts with every weight free and stops after
-// p.max_iter iterations or when an iteration pins nothing.
+// p.max_iter iterations or when an iteration pins nothing.  A factorisation
+// that breaks down is redone once with the ridge of ridge_of (status
+// LC_ERR_SINGULAR).
 __global__ void __launch_bounds__(kThreads, 1)
     bounded_ls_kernel(const SolveParams p, float lo, float hi) {
   extern __shared__ float dyn[];
   __shared__ int redi[33];
+  __shared__ float redf[33];
   __shared__ int bad;
   const int h = blockIdx.x, tid = threadIdx.x, warp = warp_id(), lane = lane_id();
   const int t = p.t, tp = p.t_pad;
@@ -884,9 +995,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (nF == 0) break;
     ++it;
     const int NBf = (nF + kBS - 1) / kBS;
-    gather_packed(S, NBf, nF, [&](int a, int b) {
-      return G[static_cast<size_t>(Fidx[a]) * tp + Fidx[b]];
-    });
     // right-hand side c_F - G_FB w_B, one warp per free row
     for (int a = warp; a < NBf * kBS; a += kWarps) {
       float acc = 0.f;
@@ -897,8 +1005,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(kFull, acc, o);
       if (lane == 0) aux[a] = a < nF ? cv[Fidx[a]] - acc : 0.f;
     }
-    __syncthreads();
-    if (!cta_cholesky(S, sm.dinv, NBf, &bad)) status = LC_SINGULAR_STATUS;
+    float ridge = 0.f;
+    for (int attempt = 0; attempt < 2; ++attempt) {
+      gather_packed(S, NBf, nF, [&](int a, int b) {
+        return G[static_cast<size_t>(Fidx[a]) * tp + Fidx[b]] + (a == b ? ridge : 0.f);
+      });
+      __syncthreads();
+      if (cta_cholesky(S, sm.dinv, NBf, &bad)) break;
+      status = LC_SINGULAR_STATUS;
+      if (attempt == 1) break;
+      float dsum = 0.f;
+      for (int a = tid; a < nF; a += kThreads) dsum += G[static_cast<size_t>(Fidx[a]) * tp + Fidx[a]];
+      ridge = ridge_of(block_sum_f(dsum, redf), nF);
+    }
     cta_solve1(S, sm.dinv, NBf, aux);
     for (int a = tid; a < nF; a += kThreads) x[Fidx[a]] = aux[a];
     __syncthreads();
@@ -947,6 +1066,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 __global__ void __launch_bounds__(kThreads, 1) ols_factor_kernel(const OlsParams p) {
   extern __shared__ float dyn[];
   __shared__ float redf[33];
+  __shared__ int redi[33];
   __shared__ int bad;
   const int h = blockIdx.x, tid = threadIdx.x;
   const int t = p.t, tp = p.t_pad, dv = p.d_v;
@@ -965,15 +1085,19 @@ __global__ void __launch_bounds__(kThreads, 1) ols_factor_kernel(const OlsParams
       return Hm[static_cast<size_t>(a) * tp + b] + (a == b ? ridge : 0.f);
     });
     __syncthreads();
-    LC_SOLVER_MARK(20);
     if (cta_cholesky(S, sm.dinv, NB, &bad)) break;
     status = LC_SINGULAR_STATUS;
     float dsum = 0.f;
+    int cnt = 0;
     for (int a = tid; a < t; a += kThreads)
-      dsum += (w[a] > 0.f) ? Hm[static_cast<size_t>(a) * tp + a] : 0.f;
-    ridge = 1e-6f * block_sum_f(dsum, redf) / t;
+      if (w[a] > 0.f) {
+        dsum += Hm[static_cast<size_t>(a) * tp + a];
+        ++cnt;
+      }
+    dsum = block_sum_f(dsum, redf);
+    cnt = block_sum_int(cnt, redi);
+    ridge = ridge_of(dsum, cnt);
   }
-  LC_SOLVER_MARK(21);
   // publish the factor for the solve kernel
   if (sm.S) {
     const size_t nel = static_cast<size_t>(NB * (NB + 1) / 2) * kBlk;
@@ -1034,10 +1158,8 @@ __global__ void __launch_bounds__(kThreads, 1) ols_solve_kernel(const OlsParams 
         nb[i][j] = (I < NB && q < nc) ? -rhs(a, c0 + q) : 0.f;
       }
     __syncthreads();
-    LC_SOLVER_MARK(30);
     reg_tri_solve<true>(S, sm.dinv, NB, nct, nb, sm.T2);
     reg_tri_solve<false>(S, sm.dinv, NB, nct, nb, sm.T2);
-    LC_SOLVER_MARK(31);
     if (I < NB) {
 #pragma unroll
       for (int i = 0; i < 4; ++i)

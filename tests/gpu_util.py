@@ -71,3 +71,57 @@ def beta_err(b_gpu, b_ref) -> float:
 def inputs(w: synth.Workload, heads=None):
     d = synth.make(w, heads)
     return d, dev(d["Q"], w.dtype), dev(d["K"], w.dtype), dev(d["V"], w.dtype)
+
+
+def near_tie_swap(got, ref, u, n_keep, where=""):
+    """Check that the selections ``got`` and ``ref`` (ascending key indices)
+    agree except for keys whose reference score ties the n_keep-th largest
+    within the score tolerance (rounding may order such keys either way).
+    Returns the overlap |got & ref| / n_keep."""
+    got, ref = np.asarray(got), np.asarray(ref)
+    if not np.array_equal(got, ref):
+        tau = np.sort(np.asarray(u))[::-1][n_keep - 1]
+        diff = np.setxor1d(got, ref)
+        assert np.all(np.abs(np.asarray(u)[diff] - tau) <= SCORE_ABS), \
+            f"{where}: selection differs beyond near-ties"
+    return np.intersect1d(got, ref).size / n_keep
+
+
+def gate_fit(wg, bg, cg, ref, where=""):
+    """w, beta and C_v of one head against the oracle's fit ``ref``."""
+    assert relf(wg, ref["w"]) <= FIT_REL, f"{where} w relF {relf(wg, ref['w']):.2e}"
+    assert beta_err(bg, ref["beta"]) <= FIT_REL, f"{where} beta {beta_err(bg, ref['beta']):.2e}"
+    assert relf(cg, ref["Cv"]) <= FIT_REL, f"{where} Cv relF {relf(cg, ref['Cv']):.2e}"
+
+
+def check_layer_fits(comp, w, Q, K, V, refs, idx, wg, bg, cg):
+    """Steps 3-5 of a GPU compaction, head by head, against the oracle's
+    compaction of each head (``refs``: head -> oracle.compact_head result).
+
+    Heads whose selection equals the oracle's compare w, beta and C_v
+    directly.  Where a near-tie made the selections differ, the GPU's fit
+    is compared on the oracle's own selection and statistics instead,
+    through lc_fit_only: every head gets its fit compared, and every oracle
+    input still comes from the generator or the oracle.  Returns the
+    selection overlaps."""
+    overlaps, refit = {}, []
+    for h, r in refs.items():
+        overlaps[h] = near_tie_swap(idx[h], r["idx"], r["u"], w.t, f"head {h}")
+        if overlaps[h] == 1.0:
+            gate_fit(wg[h], bg[h], cg[h], r, f"head {h}")
+        else:
+            refit.append(h)
+    if refit:
+        sel = [refs[h] for h in refit]
+        wf, bf, cf = comp.fit_only(Q[refit], K[refit], V[refit],
+                                   dev_i32(np.stack([r["idx"] for r in sel])),
+                                   dev_f32(np.stack([r["m"] for r in sel])),
+                                   dev_f32(np.stack([r["lse"] for r in sel])),
+                                   dev_f32(np.stack([r["O"] for r in sel])))
+        rep = comp.report(len(refit))
+        assert rep.device_error_bits == 0
+        wf, bf, cf = host(wf), host(bf), host(cf)
+        for i, h in enumerate(refit):
+            assert rep.head_status[i] == 0, f"head {h} refit status {rep.head_status[i]}"
+            gate_fit(wf[i], bf[i], cf[i], refs[h], f"head {h} (on the oracle's selection)")
+    return overlaps
