@@ -43,9 +43,11 @@ design notes):
   over the keys with w_j > 0; C_v = (X^T X)^-1 X^T O by Cholesky; keys with
   w_j = 0 keep their original value row.
 * Singular systems (the pages give no ridge): when a Cholesky factorisation
-  breaks down, a ridge of 1e-6 * mean(diag) of the system being factored is
-  added once and the status says so (1e-6 rather than less, so that the
-  same rule also regularises a single-precision factorisation).
+  of an n x n system breaks down, a ridge of n * 2^-20 * mean(diag) is added
+  once and the status says so.  The size scaling is what lets the same rule
+  work in single precision: on a rank-deficient system the rounding errors
+  of a factorisation add up coherently to about n unit roundoffs of the
+  diagonal, which the ridge must exceed.
 * A kept key whose vector equals that of a kept key at an earlier position
   has w = 0: its column of A equals the earlier one's, so the NNLS minimiser
   is not unique, and this is the one Lawson-Hanson reaches with argmax ties
@@ -189,9 +191,9 @@ def _chol_solve(M, r):
 
 
 def ridge(M):
-    """The ridge added to a system whose Cholesky factorisation broke down:
-    1e-6 times the mean of its diagonal."""
-    return 1e-6 * float(np.mean(np.diag(M))) if M.size else 0.0
+    """The ridge added to an n x n system whose Cholesky factorisation broke
+    down: n * 2^-20 times the mean of its diagonal."""
+    return M.shape[0] * 2.0 ** -20 * float(np.mean(np.diag(M))) if M.size else 0.0
 
 
 def nnls_tolerance(c, t, eps=np.finfo(np.float64).eps):
@@ -308,8 +310,8 @@ def output_system(Q, Kc, w, O, scale):
 
 
 def ols(H, R):
-    """C = H^-1 R by Cholesky; on breakdown the ridge of ``ridge`` (1e-6 *
-    mean(diag H)) is added once.  Returns (C, status)."""
+    """C = H^-1 R by Cholesky; on breakdown the ridge of ``ridge`` (n * 2^-20
+    * mean(diag H)) is added once.  Returns (C, status)."""
     H, R = _f64(H), _f64(R)
     C = _chol_solve(H, R)
     if C is not None:

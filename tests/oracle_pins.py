@@ -278,7 +278,7 @@ def check_ols(o):
     # outputs move by at most lam / sv_min^2 (smallest nonzero sv) relative.
     Cmn, *_ = np.linalg.lstsq(Xd, Ot, rcond=None)
     sv = np.linalg.svd(Xd, compute_uv=False)
-    lam = 1e-6 * float(np.mean(np.diag(Xd.T @ Xd)))
+    lam = Xd.shape[1] * 2.0 ** -20 * float(np.mean(np.diag(Xd.T @ Xd)))
     bound = lam / sv[sv > 1e-10 * sv[0]].min() ** 2
     assert bound < 0.1, "ridge bound too loose (test is not testing)"
     assert np.linalg.norm(C3 - Cmn) <= 1.01 * bound * np.linalg.norm(Cmn), \
