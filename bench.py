@@ -80,6 +80,8 @@ def args_():
     ap.add_argument("--long-steps", type=int, default=2,
                     help="timed compactions of one long-context layer (T = 131072, "
                          "t = 1024); 0 skips it (drawing its inputs takes about a minute)")
+    ap.add_argument("--select-steps", type=int, default=20,
+                    help="timed top-t selections of 8 x 2^22 scores (0: skip)")
     ap.add_argument("--quality-queries", type=int, default=4096,
                     help="held-out queries per head for the quality comparison (0: skip)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -383,6 +385,48 @@ def main():
             ms = kern[k][0] / max(kern[k][1], 1)
             gbs = nb / (ms * 1e-3) / 1e9
             hbm[k] = {"bytes": nb, "ms": ms, "gbs": gbs, "frac_of_hbm": gbs / pk["hbm_gbs"]}
+
+    # the top-t select on long score arrays (the sampled-threshold path of
+    # lc_select_topt): 8 heads x 2^22 fp32 scores, t = 1024, two arrays used
+    # in turn (2 x 134 MB) so that no call finds its scores in L2
+    if a.select_steps > 0:
+        Hs, Ts, ts = 8, 1 << 22, 1024
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(11)
+        us = [-20.0 * torch.rand((Hs, Ts), generator=gen, device=dev) for _ in range(2)]
+        for i in range(3):
+            comp.select_topt(us[i % 2], ts)
+        torch.cuda.synchronize()
+        q0 = torch.cuda.Event(enable_timing=True)
+        q1 = torch.cuda.Event(enable_timing=True)
+        q0.record(stream)
+        for i in range(a.select_steps):
+            comp.select_topt(us[i % 2], ts)
+        q1.record(stream)
+        torch.cuda.synchronize()
+        ms_sel = q0.elapsed_time(q1) / a.select_steps
+        comp.profile_read()
+        comp.profile(True)
+        for i in range(a.select_steps):
+            comp.select_topt(us[i % 2], ts)
+        torch.cuda.synchronize()
+        comp.profile(False)
+        sk = comp.profile_read()
+        stage_ms = {k: v[0] / max(v[1], 1) for k, v in sk.items()}
+        nb = Hs * Ts * 4 + Hs * ts * 4
+        filt = None
+        if "select_filter" in stage_ms:
+            fb = Hs * Ts * 4
+            fg = fb / (stage_ms["select_filter"] * 1e-3) / 1e9
+            filt = {"bytes": fb, "ms": stage_ms["select_filter"], "gbs": fg,
+                    "frac_of_hbm": fg / pk["hbm_gbs"]}
+        hbm.setdefault("select_topt", {})["large_n_sweep"] = {
+            "workload": f"{Hs} heads x {Ts} fp32 scores (uniform in [-20, 0]), t = {ts}, "
+                        "two arrays in turn (> L2)",
+            "bytes": nb, "ms": ms_sel, "gbs": nb / (ms_sel * 1e-3) / 1e9,
+            "frac_of_hbm": nb / (ms_sel * 1e-3) / 1e9 / pk["hbm_gbs"],
+            "steps": a.select_steps, "stage_ms": stage_ms, "filter_kernel": filt}
+        del us
 
     # end to end through the host-buffer entry point
     e2e = None

@@ -66,8 +66,10 @@ struct Plan {
   // workspace offsets (bytes)
   size_t qop, kop, vhi, vlo;            // operand copies (16-bit)
   size_t m_pad, lse_pad, ohi, olo;      // step-1 results
-  size_t ucode, idx;                    // steps 2-3
-  size_t kc, rowsh2, rowb, colb2, lc2;  // fit inputs
+  size_t ucode, idx, selw;              // steps 2-3 (selw: wide-select scratch)
+  bool selw_on;                         // step 3 through the wide path
+  size_t kc, khash;                     // kept-key rows and their hashes
+  size_t rowsh2, rowb, colb2, lc2;      // fit inputs
   size_t gpart, cpart, G, c;            // mass system
   size_t hpart, rpart, Hm, R, vc;       // output system
   size_t mat, vec, wbuf;                // solver scratch
@@ -174,8 +176,11 @@ Plan make_plan(const lc_shape* s) {
   p.ohi = take(H * p.n_q * p.d * 2);
   p.olo = take(H * p.n_q * p.d * 2);
   p.ucode = take(H * p.T * 4);
+  p.selw_on = select_wide_applies(p.T, p.t);
+  p.selw = take(p.selw_on ? select_wide_bytes(p.H) : 0);
   p.idx = take(H * p.t * 4);
   p.kc = take(H * p.t_pad * p.d_qk * 2);
+  p.khash = take(H * p.t_pad * 4);
   p.rowsh2 = take(H * p.n_q_pad * 4);
   p.rowb = take(H * p.n_q_pad * 4);
   p.colb2 = take(H * p.t_pad * 4);
@@ -459,9 +464,8 @@ lc_status run_pass2_rms(const Ctx& c, const void* qop, const void* kop, float2* 
 }
 
 // Steps 4-5 from the workspace's m_pad, lse_pad, O hi/lo and the given idx.
-lc_status run_fit_solve(const Ctx& c, const void* qop, const void* kop, const void* V,
-                        const int32_t* idx, float* w, float* beta, float* Cv, int bounded_iters,
-                        int status_off,
+lc_status run_fit_solve(const Ctx& c, const void* qop, const void* V, const int32_t* idx,
+                        float* w, float* beta, float* Cv, int bounded_iters, int status_off,
                         const CUtensorMap& mKc, const CUtensorMap& mQ64, const CUtensorMap& mOhi,
                         const CUtensorMap& mOlo, GramParams g, int g7_split, int g7_slabs,
                         int r_split, int r_slabs);
@@ -481,7 +485,8 @@ lc_status run_fit(const Ctx& ca, const void* qop, const void* kop, const void* V
   const Ctx& c = ca;
   {
     LC_PROF(c, "gather_keys", 1);
-    LC_CUDA(launch_gather_rows(kop, c.ws + p.kc, idx, p.H, p.T, p.t, p.t_pad, row_bytes, c.st));
+    LC_CUDA(launch_gather_rows(kop, c.ws + p.kc, idx, p.H, p.T, p.t, p.t_pad, row_bytes, c.st,
+                               c.at<uint32_t>(p.khash)));
   }
   CUtensorMap mQ64, mKc, mOhi, mOlo;
   if (!make_map(&mQ64, qop, p.bf16_in, p.d_qk, p.n_q, p.H, 64)) return LC_ERR_CUDA;
@@ -541,14 +546,13 @@ lc_status run_fit(const Ctx& ca, const void* qop, const void* kop, const void* V
     LC_CUDA(cudaStreamWaitEvent(cs->st, handoff, 0));
     cp = cs;
   }
-  return run_fit_solve(*cp, qop, kop, V, idx, w, beta, Cv, bounded_iters, status_off, mKc, mQ64, mOhi,
+  return run_fit_solve(*cp, qop, V, idx, w, beta, Cv, bounded_iters, status_off, mKc, mQ64, mOhi,
                        mOlo, g, g7_split, g7_slabs, r_split, r_slabs);
 }
 
 // Steps 4 (solve) and 5 of run_fit.
-lc_status run_fit_solve(const Ctx& c, const void* qop, const void* kop, const void* V,
-                        const int32_t* idx, float* w, float* beta, float* Cv, int bounded_iters,
-                        int status_off,
+lc_status run_fit_solve(const Ctx& c, const void* qop, const void* V, const int32_t* idx,
+                        float* w, float* beta, float* Cv, int bounded_iters, int status_off,
                         const CUtensorMap& mKc, const CUtensorMap& mQ64, const CUtensorMap& mOhi,
                         const CUtensorMap& mOlo, GramParams g, int g7_split, int g7_slabs,
                         int r_split, int r_slabs) {
@@ -571,9 +575,8 @@ lc_status run_fit_solve(const Ctx& c, const void* qop, const void* kop, const vo
   sp.head_status = c.h->d_status + status_off;
   sp.head_iters = c.h->d_iters + status_off;
   sp.err = c.h->d_err;
-  sp.krows = kop;
-  sp.idx = idx;
-  sp.T = p.T;
+  sp.krows = c.ws + p.kc;
+  sp.khash = c.at<uint32_t>(p.khash);
   sp.k_row_bytes = p.d_qk * 2;
   if (bounded_iters > 0) {
     LC_PROF(c, "bounded_ls", 1);
@@ -691,6 +694,19 @@ lc_status run_fit_solve(const Ctx& c, const void* qop, const void* kop, const vo
     LC_CUDA(launch_ols(op, c.st));
   }
   return LC_OK;
+}
+
+// Step 3 in the pipeline, from the order codes of the key scores: the wide
+// path for long heads, else one CTA per head.
+cudaError_t select_step(const Ctx& c, int32_t* idx, cudaStream_t st) {
+  const Plan& p = c.p;
+  if (!p.selw_on) return launch_select_topt(c.at<uint32_t>(p.ucode), p.H, p.T, p.t, idx, st);
+  for (int stage = 0; stage < 3; ++stage) {
+    const cudaError_t e = launch_select_wide_codes(c.at<uint32_t>(p.ucode), p.H, p.T, p.t, idx,
+                                                   c.ws + p.selw, c.h->sm_count, stage, st);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 lc_status reset_report(const Ctx& c) {
@@ -1021,6 +1037,15 @@ lc_status lc_select_topt(lc_handle h, int n_heads, int T, int t, const float* u,
   LC_TRY(enter(h));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint32_t* code = static_cast<uint32_t*>(workspace);
+  if (select_wide_applies(T, t) && (reinterpret_cast<uintptr_t>(u) & 15) == 0 &&
+      workspace_bytes >= select_wide_bytes(n_heads)) {
+    static const char* const kStage[3] = {"select_sample", "select_filter", "select_final"};
+    for (int stage = 0; stage < 3; ++stage) {
+      ProfScope prof(h, st, kStage[stage], 1);
+      LC_CUDA(launch_select_wide_scores(u, n_heads, T, t, idx, workspace, h->sm_count, stage, st));
+    }
+    return LC_OK;
+  }
   LC_CUDA(launch_encode_scores(u, code, static_cast<size_t>(n_heads) * T, st));
   LC_CUDA(launch_select_topt(code, n_heads, T, t, idx, st));
   return LC_OK;
@@ -1062,8 +1087,8 @@ lc_status lc_compact_layer(lc_handle h, const lc_shape* shape, const void* Q, co
   LC_TRY(run_pass1(c, qop, kop, nullptr, nullptr, nullptr, true));
   LC_TRY(run_pass2(c, qop, kop));
   {
-    LC_PROF(c, "select_topt", 1);
-    LC_CUDA(launch_select_topt(c.at<uint32_t>(p.ucode), p.H, p.T, p.t, idx, c.st));
+    LC_PROF(c, "select_topt", c.p.selw_on ? 3 : 1);
+    LC_CUDA(select_step(c, idx, c.st));
   }
   return run_fit(c, qop, kop, V, idx, w, beta, Cv);
 }
@@ -1160,8 +1185,8 @@ lc_status lc_compact_layer_host(lc_handle h, const lc_shape* shape, const void* 
     int32_t* idx = reinterpret_cast<int32_t*>(dIdx);
     LC_TRY(run_pass2(c, dQ, dK));
     {
-      LC_PROF(c, "select_topt", 1);
-      LC_CUDA(launch_select_topt(c.at<uint32_t>(p.ucode), p.H, p.T, p.t, idx, st));
+      LC_PROF(c, "select_topt", c.p.selw_on ? 3 : 1);
+      LC_CUDA(select_step(c, idx, st));
     }
     LC_TRY(run_fit(c, dQ, dK, dV, idx, reinterpret_cast<float*>(dW), reinterpret_cast<float*>(dB),
                    reinterpret_cast<float*>(dC)));
@@ -1393,8 +1418,8 @@ lc_status lc_compact_layer_baseline(lc_handle h, const lc_shape* shape, const vo
   LC_TRY(run_pass1(c, qop, kop, nullptr, nullptr, nullptr, true));
   LC_TRY(run_pass2_rms(c, qop, kop, c.at<float2>(bp.part), c.at<float>(bp.L2), nullptr));
   {
-    LC_PROF(c, "select_topt", 1);
-    LC_CUDA(launch_select_topt(c.at<uint32_t>(p.ucode), p.H, p.T, p.t, idx, c.st));
+    LC_PROF(c, "select_topt", c.p.selw_on ? 3 : 1);
+    LC_CUDA(select_step(c, idx, c.st));
   }
   const int iters = shape->nnls_max_iter > 0 ? shape->nnls_max_iter : 2;
   return run_fit(c, qop, kop, V, idx, w, beta, Cv, iters);
@@ -1452,8 +1477,8 @@ lc_status lc_compact_layers(lc_handle h, const lc_shape* shape, int n_layers, co
     LC_TRY(run_pass1(ca, qop, kop, nullptr, nullptr, nullptr, true));
     LC_TRY(run_pass2(ca, qop, kop));
     {
-      LC_PROF(ca, "select_topt", 1);
-      LC_CUDA(launch_select_topt(ca.at<uint32_t>(p.ucode), p.H, p.T, p.t, idxl, st));
+      LC_PROF(ca, "select_topt", ca.p.selw_on ? 3 : 1);
+      LC_CUDA(select_step(ca, idxl, st));
     }
     LC_TRY(run_fit(ca, qop, kop, Vl, idxl, w + l * H * p.t, beta + l * H * p.t,
                    Cv + l * H * p.t * p.d, 0, &cs, h->ev_mass[b], l * p.H));

@@ -111,6 +111,21 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
   }
 }
 
+// One 32-bit word of a row of 16-bit elements, folded into a row hash: -0 is
+// mapped onto +0 in both halves (so that equal values hash equally), then
+// the word is mixed with its position.  A row's hash is the sum of its
+// words' mixes.
+__device__ __forceinline__ uint32_t row_word_mix(uint32_t x, int pos) {
+  if ((x & 0x7fffu) == 0) x &= 0xffff0000u;
+  if ((x & 0x7fff0000u) == 0) x &= 0x0000ffffu;
+  x ^= 0x9e3779b9u * static_cast<uint32_t>(pos + 1);
+  x *= 0x85ebca6bu;
+  x ^= x >> 13;
+  x *= 0xc2b2ae35u;
+  x ^= x >> 16;
+  return x;
+}
+
 // Bounded wait on the way out of a kernel: returns once the phase of `bar`
 // with the given parity has completed, or after kWaitLimitNs; abort flags are
 // not consulted (the point is to let work already in flight finish).

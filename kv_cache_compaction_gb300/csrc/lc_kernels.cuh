@@ -147,8 +147,33 @@ cudaError_t launch_decode_scores(const uint32_t* code, float* u, size_t n, cudaS
 cudaError_t launch_encode_scores(const float* u, uint32_t* code, size_t n, cudaStream_t st);
 cudaError_t launch_select_topt(const uint32_t* code, int H, int T, int t, int32_t* idx,
                                cudaStream_t st);
+
+// Step 3 for long heads (T >= kWideMinT, T % 4 == 0, 16-byte aligned input,
+// t <= 1024): sampled threshold, a streaming filter over all SMs and an exact
+// selection among the candidates, with the single-CTA selection over the
+// whole head as fallback; same result as launch_select_topt.  The scratch
+// (select_wide_bytes) holds a threshold, a count and a candidate list per
+// head.  _codes reads order codes, _scores fp32 scores.  `stage` 0, 1, 2
+// launches the sample, the filter and the final selection; all three, in
+// order, make one selection.
+struct WideScratch {
+  uint32_t* theta;
+  int* count;
+  uint32_t* cand_code;
+  int32_t* cand_idx;
+};
+constexpr int kWideMinT = 65536;
+bool select_wide_applies(int T, int t);
+size_t select_wide_bytes(int H);
+cudaError_t launch_select_wide_codes(const uint32_t* code, int H, int T, int t, int32_t* idx,
+                                     void* scratch, int sm_count, int stage, cudaStream_t st);
+cudaError_t launch_select_wide_scores(const float* u, int H, int T, int t, int32_t* idx,
+                                      void* scratch, int sm_count, int stage, cudaStream_t st);
+// Row r of head h of dst = row idx[h][r] of src (zero rows past t); with
+// `hash`, also a hash of each gathered row into hash[h * t_pad + r].
 cudaError_t launch_gather_rows(const void* src, void* dst, const int32_t* idx, int H, int T,
-                               int t, int t_pad, int row_bytes, cudaStream_t st);
+                               int t, int t_pad, int row_bytes, cudaStream_t st,
+                               uint32_t* hash = nullptr);
 cudaError_t launch_gather_v(const void* V, int in_dtype, const int32_t* idx, float* Vc, int H,
                             int T, int t, int t_pad, int d, cudaStream_t st);
 cudaError_t launch_reduce_partials(const float* part, float* out, int nsplit, size_t n,
@@ -219,10 +244,11 @@ struct SolveParams {
   int32_t* head_iters;     // [H]
   uint32_t* err;
   // Kept-key rows for the duplicate check of the NNLS (null: no check): the
-  // key operand [H][T][k_row_bytes / 2] of 16-bit elements and the selection.
+  // gathered key operand [H][t_pad][k_row_bytes / 2] (16-bit elements) and
+  // the hash of each row (launch_gather_rows).
   const void* krows;
-  const int32_t* idx;      // [H][t]
-  int T, k_row_bytes;
+  const uint32_t* khash;   // [H][t_pad]
+  int k_row_bytes;
 };
 cudaError_t launch_nnls(const SolveParams& p, cudaStream_t st);
 // Bounded least squares w in [lo, hi], p.max_iter iterations (see the kernel).

@@ -411,188 +411,6 @@ cudaError_t launch_ks_t(const CUtensorMap& mK, const CUtensorMap& mQ, const KeyS
   return cudaGetLastError();
 }
 
-// ------------------------------------------------------------------ select
-constexpr int kSelThreads = 1024;
-
-__device__ __forceinline__ int block_exclusive_scan(int v, int* tmp, int& total) {
-  // tmp: 32 ints of shared memory
-  const int lane = lane_id(), w = warp_id();
-  int x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) tmp[w] = x;
-  __syncthreads();
-  if (w == 0) {
-    int s = tmp[lane];
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, s, o);
-      if (lane >= o) s += y;
-    }
-    tmp[lane] = s;  // inclusive over warps
-  }
-  __syncthreads();
-  const int before_warp = w > 0 ? tmp[w - 1] : 0;
-  total = tmp[31];
-  __syncthreads();
-  return before_warp + x - v;
-}
-
-// One CTA per head.  CPT > 0: thread i holds codes [CPT i, CPT i + CPT) in
-// registers (T <= 1024 CPT); CPT == 0: codes are re-read from global memory
-// in each pass.  Four 8-bit radix passes find the code of the t-th largest;
-// equal bins within a thread's run are counted before the shared atomic.
-template <int CPT>
-__global__ void __launch_bounds__(kSelThreads)
-    select_topt_kernel(const uint32_t* __restrict__ code, int T, int t, int32_t* __restrict__ idx) {
-  __shared__ int hist[256];
-  __shared__ int tmp[32];
-  __shared__ uint32_t s_prefix;
-  __shared__ int s_need;
-  const int h = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
-  const uint32_t* c = code + static_cast<size_t>(h) * T;
-  constexpr int R = CPT > 0 ? CPT : 1;
-  uint32_t v[R];
-  const int chunk = CPT > 0 ? CPT : (T + kSelThreads - 1) / kSelThreads;
-  const int j0 = min(T, tid * chunk), j1 = min(T, j0 + chunk);
-  if constexpr (CPT > 0) {
-    if (j0 + CPT <= T && CPT % 4 == 0 && (reinterpret_cast<uintptr_t>(c + j0) & 15) == 0) {
-#pragma unroll
-      for (int q = 0; q < CPT / 4; ++q) {
-        const uint4 u = reinterpret_cast<const uint4*>(c + j0)[q];
-        v[4 * q] = u.x;
-        v[4 * q + 1] = u.y;
-        v[4 * q + 2] = u.z;
-        v[4 * q + 3] = u.w;
-      }
-    } else {
-#pragma unroll
-      for (int k = 0; k < CPT; ++k) v[k] = j0 + k < j1 ? c[j0 + k] : 0u;
-    }
-  }
-  auto get = [&](int k) -> uint32_t {
-    if constexpr (CPT > 0) return v[k];
-    else return c[j0 + k];
-  };
-  uint32_t prefix = 0, mask = 0;
-  int need = t;  // rank (from the top) still to locate inside the current bucket
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int b = tid; b < 256; b += kSelThreads) hist[b] = 0;
-    __syncthreads();
-    int run_bin = -1, run_cnt = 0;
-    const int n = j1 - j0;
-#pragma unroll
-    for (int k = 0; k < (CPT > 0 ? CPT : 1); ++k) {
-      if constexpr (CPT > 0) {
-        if (k < n) {
-          const uint32_t x = get(k);
-          if ((x & mask) == prefix) {
-            const int bin = static_cast<int>((x >> shift) & 255u);
-            if (bin == run_bin) {
-              ++run_cnt;
-            } else {
-              if (run_cnt) atomicAdd(&hist[run_bin], run_cnt);
-              run_bin = bin;
-              run_cnt = 1;
-            }
-          }
-        }
-      }
-    }
-    if constexpr (CPT == 0) {
-      for (int k = 0; k < n; ++k) {
-        const uint32_t x = get(k);
-        if ((x & mask) == prefix) {
-          const int bin = static_cast<int>((x >> shift) & 255u);
-          if (bin == run_bin) {
-            ++run_cnt;
-          } else {
-            if (run_cnt) atomicAdd(&hist[run_bin], run_cnt);
-            run_bin = bin;
-            run_cnt = 1;
-          }
-        }
-      }
-    }
-    if (run_cnt) atomicAdd(&hist[run_bin], run_cnt);
-    __syncthreads();
-    if (tid < 32) {
-      // lane l owns bins 255-8l .. 248-8l; locate the bin holding rank `need`
-      // counted from the top
-      int cnt[8], own = 0;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        cnt[k] = hist[255 - 8 * lane - k];
-        own += cnt[k];
-      }
-      int incl = own;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      const int excl = incl - own;
-      const uint32_t hit = __ballot_sync(0xffffffffu, incl >= need);
-      const int src = hit ? __ffs(hit) - 1 : 31;
-      if (lane == src) {
-        int acc = excl, b = 255 - 8 * lane - 7;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          if (acc + cnt[k] >= need) {
-            b = 255 - 8 * lane - k;
-            break;
-          }
-          acc += cnt[k];
-        }
-        s_prefix = prefix | (static_cast<uint32_t>(b) << shift);
-        s_need = need - acc;
-      }
-    }
-    __syncthreads();
-    prefix = s_prefix;
-    need = s_need;
-    mask |= 255u << shift;
-    __syncthreads();
-  }
-  // prefix = code of the t-th largest; take all larger codes and the first
-  // `need` (lowest-index) codes equal to it.
-  const uint32_t tau = prefix;
-  const int n = j1 - j0;
-  int gt = 0, eq = 0;
-  if constexpr (CPT > 0) {
-#pragma unroll
-    for (int k = 0; k < CPT; ++k)
-      if (k < n) {
-        gt += v[k] > tau;
-        eq += v[k] == tau;
-      }
-  } else {
-    for (int k = 0; k < n; ++k) {
-      const uint32_t x = get(k);
-      gt += x > tau;
-      eq += x == tau;
-    }
-  }
-  int tot;
-  const int eq_before = block_exclusive_scan(eq, tmp, tot);
-  const int take_eq = max(0, min(eq, need - eq_before));
-  const int out0 = block_exclusive_scan(gt + take_eq, tmp, tot);
-  int o = out0, te = 0;
-  int32_t* dst = idx + static_cast<size_t>(h) * t;
-  if constexpr (CPT > 0) {
-#pragma unroll
-    for (int k = 0; k < CPT; ++k)
-      if (k < n && (v[k] > tau || (v[k] == tau && te++ < take_eq)) && o < t) dst[o++] = j0 + k;
-  } else {
-    for (int k = 0; k < n; ++k) {
-      const uint32_t x = get(k);
-      if ((x > tau || (x == tau && te++ < take_eq)) && o < t) dst[o++] = j0 + k;
-    }
-  }
-}
 
 // ------------------------------------------------------------ small kernels
 __global__ void convert_bf16_f16_kernel(const __nv_bfloat16* in, __half* out, size_t n) {
@@ -670,9 +488,11 @@ __global__ void encode_kernel(const float* u, uint32_t* code, size_t n) {
 }
 
 // dst[h][r] = src[h][idx[h][r]] for r < t, zero rows for t <= r < t_pad.
-// One warp per destination row, 16-byte moves.
+// One warp per destination row, 16-byte moves; with `hash` set, also the
+// row's hash (row_word_mix over its 32-bit words, 16-bit elements) into
+// hash[h * t_pad + r].
 __global__ void gather_rows_kernel(const uint8_t* src, uint8_t* dst, const int32_t* idx, int H,
-                                   int T, int t, int t_pad, int row_bytes) {
+                                   int T, int t, int t_pad, int row_bytes, uint32_t* hash) {
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = lane_id();
   if (gw >= H * t_pad) return;
@@ -680,11 +500,21 @@ __global__ void gather_rows_kernel(const uint8_t* src, uint8_t* dst, const int32
   uint4* d = reinterpret_cast<uint4*>(dst + static_cast<size_t>(gw) * row_bytes);
   const int n16 = row_bytes / 16;
   const int j = r < t ? idx[static_cast<size_t>(h) * t + r] : -1;
+  uint32_t acc = 0u;
   if (j >= 0 && j < T) {
     const uint4* s = reinterpret_cast<const uint4*>(src + (static_cast<size_t>(h) * T + j) * row_bytes);
-    for (int k = lane; k < n16; k += 32) d[k] = s[k];
+    for (int k = lane; k < n16; k += 32) {
+      const uint4 v = s[k];
+      d[k] = v;
+      acc += row_word_mix(v.x, 4 * k) + row_word_mix(v.y, 4 * k + 1) +
+             row_word_mix(v.z, 4 * k + 2) + row_word_mix(v.w, 4 * k + 3);
+    }
   } else {
     for (int k = lane; k < n16; k += 32) d[k] = make_uint4(0, 0, 0, 0);
+  }
+  if (hash) {
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) hash[gw] = acc;
   }
 }
 
@@ -1020,19 +850,6 @@ int key_scores_smem(OperandMode mode) {
   return 0;
 }
 
-cudaError_t launch_select_topt(const uint32_t* code, int H, int T, int t, int32_t* idx,
-                               cudaStream_t st) {
-  if (T <= 4 * kSelThreads)
-    select_topt_kernel<4><<<H, kSelThreads, 0, st>>>(code, T, t, idx);
-  else if (T <= 8 * kSelThreads)
-    select_topt_kernel<8><<<H, kSelThreads, 0, st>>>(code, T, t, idx);
-  else if (T <= 32 * kSelThreads)
-    select_topt_kernel<32><<<H, kSelThreads, 0, st>>>(code, T, t, idx);
-  else
-    select_topt_kernel<0><<<H, kSelThreads, 0, st>>>(code, T, t, idx);
-  return cudaGetLastError();
-}
-
 cudaError_t launch_convert_bf16_to_f16(const __nv_bfloat16* in, __half* out, size_t n,
                                        cudaStream_t st) {
   convert_bf16_f16_kernel<<<grid_for(n / 8 + 1), 256, 0, st>>>(in, out, n);
@@ -1073,11 +890,11 @@ cudaError_t launch_encode_scores(const float* u, uint32_t* code, size_t n, cudaS
 }
 
 cudaError_t launch_gather_rows(const void* src, void* dst, const int32_t* idx, int H, int T,
-                               int t, int t_pad, int row_bytes, cudaStream_t st) {
+                               int t, int t_pad, int row_bytes, cudaStream_t st, uint32_t* hash) {
   const int warps = H * t_pad;
   gather_rows_kernel<<<(warps * 32 + 255) / 256, 256, 0, st>>>(
       static_cast<const uint8_t*>(src), static_cast<uint8_t*>(dst), idx, H, T, t, t_pad,
-      row_bytes);
+      row_bytes, hash);
   return cudaGetLastError();
 }
 

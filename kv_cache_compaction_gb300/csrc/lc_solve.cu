@@ -580,60 +580,20 @@ __device__ __forceinline__ float ridge_of(float diag_sum, int n) {
   return n > 0 ? diag_sum * 9.5367431640625e-7f : 0.f;
 }
 
-// 32-bit word of a key row with -0 folded onto +0 in both 16-bit halves, so
-// that equal words mean equal values.
-__device__ __forceinline__ uint32_t canon16x2(uint32_t x) {
-  if ((x & 0x7fffu) == 0) x &= 0xffff0000u;
-  if ((x & 0x7fff0000u) == 0) x &= 0x0000ffffu;
-  return x;
-}
-
 // dup[j] = 1 for each kept key j whose operand row equals, value for value,
 // the row of a kept key at an earlier position (dup must be zero on entry).
 // Such a key's column of the mass system equals the earlier key's, so the
 // NNLS minimiser is not unique; the later copy is held at w = 0, the
 // minimiser Lawson-Hanson reaches with its argmax ties going to the lower
-// index.  Rows are hashed (one warp per row, eight rows in flight per warp,
-// at most 96 words a row), each key's hash is compared with the earlier
-// keys' and a hash match is confirmed on the full rows.  hsh: t words.
+// index.  The gather of the kept keys hashed each row; each key's hash is
+// compared with the earlier keys' and a match is confirmed on the full
+// gathered rows.  hsh: t words of shared memory.
 __device__ void mark_later_duplicates(const SolveParams& p, int h, int* dup, uint32_t* hsh) {
   const int t = p.t, warp = warp_id(), lane = lane_id();
   const int nw = p.k_row_bytes / 4;
-  const uint32_t* K = static_cast<const uint32_t*>(p.krows);
-  const int32_t* idx = p.idx + static_cast<size_t>(h) * t;
-  auto row = [&](int j) {
-    return K + (static_cast<size_t>(h) * p.T + static_cast<size_t>(idx[j])) * nw;
-  };
-  constexpr int kRows = 8;
-  for (int j0 = warp * kRows; j0 < t; j0 += kWarps * kRows) {
-    uint32_t acc[kRows];
-#pragma unroll
-    for (int u = 0; u < kRows; ++u) {
-      acc[u] = 0u;
-      const int j = j0 + u;
-      if (j < t) {
-        const uint32_t* r = row(j);
-#pragma unroll
-        for (int q = 0; q < 3; ++q) {
-          const int k = lane + 32 * q;
-          if (k < nw) {
-            uint32_t x = canon16x2(__ldg(r + k)) ^ (0x9e3779b9u * static_cast<uint32_t>(k + 1));
-            x *= 0x85ebca6bu;
-            x ^= x >> 13;
-            x *= 0xc2b2ae35u;
-            x ^= x >> 16;
-            acc[u] += x;
-          }
-        }
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kRows; ++u) {
-      uint32_t a = acc[u];
-      for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(kFull, a, o);
-      if (lane == 0 && j0 + u < t) hsh[j0 + u] = a;
-    }
-  }
+  const uint32_t* K = static_cast<const uint32_t*>(p.krows) + static_cast<size_t>(h) * p.t_pad * nw;
+  const uint32_t* hg = p.khash + static_cast<size_t>(h) * p.t_pad;
+  for (int j = threadIdx.x; j < t; j += kThreads) hsh[j] = hg[j];
   __syncthreads();
   for (int j = 1 + warp; j < t; j += kWarps) {
     const uint32_t hj = hsh[j];
@@ -644,10 +604,11 @@ __device__ void mark_later_duplicates(const SolveParams& p, int h, int* dup, uin
       while (m != 0u && !found) {
         const int c = base + __ffs(m) - 1;
         m &= m - 1u;
-        const uint32_t* a = row(j);
-        const uint32_t* b = row(c);
+        const uint32_t* a = K + static_cast<size_t>(j) * nw;
+        const uint32_t* b = K + static_cast<size_t>(c) * nw;
         bool eq = true;
-        for (int k = lane; k < nw; k += 32) eq = eq && canon16x2(a[k]) == canon16x2(b[k]);
+        for (int k = lane; k < nw; k += 32)
+          eq = eq && row_word_mix(a[k], k) == row_word_mix(b[k], k);
         found = __all_sync(kFull, eq);
       }
     }

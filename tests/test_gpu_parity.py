@@ -81,7 +81,22 @@ SELECT_CASES = [
     ("signed_zero", lambda: synth.tie_heavy_scores(2, 300, 3, levels=(0.0, -0.0, -1.0)), [5, 150]),
     ("long", lambda: synth.continuous_scores(2, 131072, 4), [1024]),
     ("single", lambda: synth.continuous_scores(1, 1, 5), [1]),
+    # long heads take the sampled-threshold path; these cases drive its
+    # branches: candidates found (several t, 2^20 keys), too many
+    # candidates (ties everywhere), too few (the high scores sit exactly at
+    # the sampled positions, so the sample overestimates the threshold)
+    ("wide_continuous", lambda: synth.continuous_scores(3, 1 << 20, 6), [1, 100, 1024]),
+    ("wide_ties", lambda: synth.tie_heavy_scores(2, 131072, 7), [1, 1024]),
+    ("wide_sample_misjudged", lambda: _sampled_positions_high(2, 131072), [1024]),
 ]
+
+
+def _sampled_positions_high(n_heads, T, stride=8):
+    """Scores 0 except at every stride-th key, where they rise with the key:
+    a strided sample sees only the high values."""
+    u = np.zeros((n_heads, T), np.float32)
+    u[:, ::stride] = 1.0 + 1e-3 * np.arange(T // stride, dtype=np.float32)
+    return u
 
 
 @pytest.mark.parametrize("case", SELECT_CASES, ids=lambda c: c[0])
