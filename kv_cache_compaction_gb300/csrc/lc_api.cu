@@ -703,7 +703,8 @@ cudaError_t select_step(const Ctx& c, int32_t* idx, cudaStream_t st) {
   if (!p.selw_on) return launch_select_topt(c.at<uint32_t>(p.ucode), p.H, p.T, p.t, idx, st);
   for (int stage = 0; stage < 3; ++stage) {
     const cudaError_t e = launch_select_wide_codes(c.at<uint32_t>(p.ucode), p.H, p.T, p.t, idx,
-                                                   c.ws + p.selw, c.h->sm_count, stage, st);
+                                                   c.ws + p.selw, c.h->sm_count, c.h->d_err,
+                                                   stage, st);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -1042,7 +1043,8 @@ lc_status lc_select_topt(lc_handle h, int n_heads, int T, int t, const float* u,
     static const char* const kStage[3] = {"select_sample", "select_filter", "select_final"};
     for (int stage = 0; stage < 3; ++stage) {
       ProfScope prof(h, st, kStage[stage], 1);
-      LC_CUDA(launch_select_wide_scores(u, n_heads, T, t, idx, workspace, h->sm_count, stage, st));
+      LC_CUDA(launch_select_wide_scores(u, n_heads, T, t, idx, workspace, h->sm_count, h->d_err,
+                                        stage, st));
     }
     return LC_OK;
   }

@@ -161,14 +161,17 @@ struct WideScratch {
   int* count;
   uint32_t* cand_code;
   int32_t* cand_idx;
+  uint32_t* err;  // error word of the handle (a timed-out wait sets a bit)
 };
 constexpr int kWideMinT = 65536;
 bool select_wide_applies(int T, int t);
 size_t select_wide_bytes(int H);
 cudaError_t launch_select_wide_codes(const uint32_t* code, int H, int T, int t, int32_t* idx,
-                                     void* scratch, int sm_count, int stage, cudaStream_t st);
+                                     void* scratch, int sm_count, uint32_t* err, int stage,
+                                     cudaStream_t st);
 cudaError_t launch_select_wide_scores(const float* u, int H, int T, int t, int32_t* idx,
-                                      void* scratch, int sm_count, int stage, cudaStream_t st);
+                                      void* scratch, int sm_count, uint32_t* err, int stage,
+                                      cudaStream_t st);
 // Row r of head h of dst = row idx[h][r] of src (zero rows past t); with
 // `hash`, also a hash of each gathered row into hash[h * t_pad + r].
 cudaError_t launch_gather_rows(const void* src, void* dst, const int32_t* idx, int H, int T,
