@@ -81,7 +81,9 @@ def args_():
                     help="timed compactions of one long-context layer (T = 131072, "
                          "t = 1024); 0 skips it (drawing its inputs takes about a minute)")
     ap.add_argument("--select-steps", type=int, default=20,
-                    help="timed top-t selections of 8 x 2^24 scores (0: skip)")
+                    help="timed top-t selections of 8 x 2^select-log2t scores (0: skip)")
+    ap.add_argument("--select-log2t", type=int, default=24,
+                    help="log2 of the scores per head in the select sweep")
     ap.add_argument("--quality-queries", type=int, default=4096,
                     help="held-out queries per head for the quality comparison (0: skip)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -387,10 +389,10 @@ def main():
             hbm[k] = {"bytes": nb, "ms": ms, "gbs": gbs, "frac_of_hbm": gbs / pk["hbm_gbs"]}
 
     # the top-t select on long score arrays (the sampled-threshold path of
-    # lc_select_topt): 8 heads x 2^24 fp32 scores, t = 1024, two arrays used
-    # in turn (2 x 537 MB) so that no call finds its scores in L2
+    # lc_select_topt): 8 heads x 2^24 fp32 scores by default, t = 1024, two
+    # arrays used in turn (2 x 537 MB) so that no call finds its scores in L2
     if a.select_steps > 0:
-        Hs, Ts, ts = 8, 1 << 24, 1024
+        Hs, Ts, ts = 8, 1 << a.select_log2t, 1024
         gen = torch.Generator(device=dev)
         gen.manual_seed(11)
         us = [-20.0 * torch.rand((Hs, Ts), generator=gen, device=dev) for _ in range(2)]
