@@ -145,8 +145,10 @@ Plan make_plan(const lc_shape* s) {
   p.ks_max = max_split(((p.T + 255) / 256) * p.H, 2, nqt);
   p.all_pairs = p.bf16_in && p.nblk == 2;
   if (p.all_pairs) {
-    // long CTAs: at most two waves of a 160-SM device
-    const int cap = std::max(1, std::min(max_split(p.H, 1, slabs), 320 / p.H));
+    // long CTAs: at most two waves of a 160-SM device, but no CTA sums more
+    // than kGramChain slabs in one accumulator
+    const int cap = std::max(gram_min_split(slabs),
+                             std::max(1, std::min(max_split(p.H, 1, slabs), 320 / p.H)));
     p.g5_max = p.g7_max = cap;
     p.r_max = cap;
   } else {
@@ -503,8 +505,11 @@ lc_status run_fit(const Ctx& ca, const void* qop, const void* kop, const void* V
   }
   const int slabs = p.n_q_pad / 64;
   const int npairs = p.nblk * (p.nblk + 1) / 2;
+  // the all-pairs kernels hold one accumulator per block: their chains are
+  // bounded by the split alone
+  const int min_split = p.all_pairs ? gram_min_split(slabs) : 1;
   auto split_of = [&](int units, int cap, int* per) {
-    int sp = best_split(units, c.h->sm_count, 1, cap);
+    int sp = std::max(min_split, best_split(units, c.h->sm_count, 1, cap));
     *per = (slabs + sp - 1) / sp;
     return (slabs + *per - 1) / *per;
   };
@@ -653,7 +658,7 @@ lc_status run_fit_solve(const Ctx& c, const void* qop, const void* V, const int3
     }
     LC_CUDA(cudaEventRecord(hc->ev_f, hc->aux_st));
     const int free_sms = std::max(1, c.h->sm_count - p.H);
-    int rs = best_split(p.H, free_sms, 1, p.r_max);
+    int rs = std::max(gram_min_split(p.n_q_pad / 64), best_split(p.H, free_sms, 1, p.r_max));
     const int r_per = (p.n_q_pad / 64 + rs - 1) / rs;
     rs = (p.n_q_pad / 64 + r_per - 1) / r_per;
     GramParams gr = g;

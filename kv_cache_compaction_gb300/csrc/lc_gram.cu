@@ -53,6 +53,42 @@ struct GramLayout {
   static constexpr int SMEM = 1024 + OFF_BAR + 128;
 };
 
+// Adds the finished chunk's accumulator into the CTA's running sum, NCOL
+// columns of this thread's tensor-memory lane, 16 at a time.
+template <int NCOL>
+__device__ __forceinline__ void fold_acc(uint32_t tsum, uint32_t tchunk) {
+#pragma unroll 1
+  for (int c = 0; c < NCOL / 16; ++c) {
+    float a[16], b[16];
+    tmem_ld16(tsum + c * 16, a);
+    tmem_ld16(tchunk + c * 16, b);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) a[e] += b[e];
+    tmem_st16(tsum + c * 16, a);
+  }
+}
+
+// Writes this thread's row of the CTA's partial: the running sum, plus the
+// last chunk's accumulator when there was more than one chunk.
+template <int NCOL>
+__device__ __forceinline__ void store_acc_row(uint32_t tsum, uint32_t tchunk, bool add_chunk,
+                                              float* dst) {
+#pragma unroll
+  for (int c = 0; c < NCOL / 32; ++c) {
+    float v[32];
+    tmem_ld32(tsum + c * 32, v);
+    if (add_chunk) {
+      float w[32];
+      tmem_ld32(tchunk + c * 32, w);
+#pragma unroll
+      for (int e = 0; e < 32; ++e) v[e] += w[e];
+    }
+    float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) d4[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+  }
+}
+
 template <bool QK_BF16, int D_QK, int D_V, int NST>
 __global__ void __launch_bounds__(192, 1)
     gram_kernel(const __grid_constant__ CUtensorMap mKc, const __grid_constant__ CUtensorMap mQ,
@@ -81,7 +117,8 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* e_full = bars + 9;
   uint64_t* e_free = bars + 10;
   uint64_t* mma_drain = bars + 11;  // MMA completion before exit
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(mma_drain + 1);
+  uint64_t* acc_free = bars + 12;   // a chunk's accumulator folded into the sum
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 13);
   __shared__ volatile int abort_flag;
 
   const int warp = warp_id(), lane = lane_id();
@@ -120,6 +157,7 @@ __global__ void __launch_bounds__(192, 1)
     mbar_init(e_full, 128);
     mbar_init(e_free, 1);
     mbar_init(mma_drain, 1);
+    mbar_init(acc_free, 128);
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(tslot, 512);
@@ -127,7 +165,10 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tslot;
-  const uint32_t tAcc = tbase + 256;  // G block or R block
+  // G block or R block: chunk 0 (of kGramChain slabs) accumulates at column
+  // 256 and stays there as the running sum; later chunks at column 384
+  const uint32_t tAcc = tbase + 256;
+  const uint32_t tChunk = tbase + 384;
 
   if (warp == 0) {
     // ---------------------------------------------------------- producer
@@ -197,8 +238,16 @@ __global__ void __launch_bounds__(192, 1)
       for (int i = 0; ok && i < nsl; ++i) {
         if (kPrefetchS && i + 1 < nsl && !issue_s(i + 1)) break;
         if (!wait_bar(e_full, i & 1, &abort_flag, p.err)) break;
+        const int ch = i / kGramChain;
+        // chunk ch - 1 has been folded into the sum before chunk ch reuses
+        // its accumulator
+        if (i % kGramChain == 0 && ch >= 2 &&
+            !wait_bar(acc_free, (ch - 2) & 1, &abort_flag, p.err))
+          break;
         tc_fence_after();
         const int s = i % L::NST;
+        const uint32_t tA = ch == 0 ? tAcc : tChunk;
+        const bool cont = i % kGramChain > 0;
         const uint32_t eih = smem_u32(sEih), eil = smem_u32(sEil);
         if (!is_r) {
           const uint32_t ejh = two ? smem_u32(sEjh) : eih;
@@ -206,12 +255,12 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
           for (int k = 0; k < kSL / 16; ++k) {
             const uint32_t o = k * 32;
-            const uint32_t acc0 = (i > 0 || k > 0) ? 1u : 0u;
-            umma_f16_ss(tAcc, sdesc_sw128(eih + o, 16, 1024), sdesc_sw128(ejh + o, 16, 1024),
+            const uint32_t acc0 = (cont || k > 0) ? 1u : 0u;
+            umma_f16_ss(tA, sdesc_sw128(eih + o, 16, 1024), sdesc_sw128(ejh + o, 16, 1024),
                         idesc_g, acc0);
-            umma_f16_ss(tAcc, sdesc_sw128(eih + o, 16, 1024), sdesc_sw128(ejl + o, 16, 1024),
+            umma_f16_ss(tA, sdesc_sw128(eih + o, 16, 1024), sdesc_sw128(ejl + o, 16, 1024),
                         idesc_g, 1u);
-            umma_f16_ss(tAcc, sdesc_sw128(eil + o, 16, 1024), sdesc_sw128(ejh + o, 16, 1024),
+            umma_f16_ss(tA, sdesc_sw128(eil + o, 16, 1024), sdesc_sw128(ejh + o, 16, 1024),
                         idesc_g, 1u);
           }
         } else {
@@ -220,12 +269,12 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
           for (int k = 0; k < kSL / 16; ++k) {
             const uint32_t o = k * 32;
-            const uint32_t acc0 = (i > 0 || k > 0) ? 1u : 0u;
+            const uint32_t acc0 = (cont || k > 0) ? 1u : 0u;
             const uint64_t doh = sdesc_sw128(aO + k * 2048, L::QCHUNK, 1024);
             const uint64_t dol = sdesc_sw128(aOl + k * 2048, L::QCHUNK, 1024);
-            umma_f16_ss(tAcc, sdesc_sw128(eih + o, 16, 1024), doh, idesc_r, acc0);
-            umma_f16_ss(tAcc, sdesc_sw128(eih + o, 16, 1024), dol, idesc_r, 1u);
-            umma_f16_ss(tAcc, sdesc_sw128(eil + o, 16, 1024), doh, idesc_r, 1u);
+            umma_f16_ss(tA, sdesc_sw128(eih + o, 16, 1024), doh, idesc_r, acc0);
+            umma_f16_ss(tA, sdesc_sw128(eih + o, 16, 1024), dol, idesc_r, 1u);
+            umma_f16_ss(tA, sdesc_sw128(eil + o, 16, 1024), doh, idesc_r, 1u);
           }
         }
         umma_commit(&st_empty[s]);
@@ -246,6 +295,17 @@ __global__ void __launch_bounds__(192, 1)
     bool ok = nsl > 0;
     for (int i = 0; ok && i < nsl; ++i) {
       const int b = i & 1, s = i % L::NST;
+      // slab i - 1 closed chunk ch >= 1: once its products are complete,
+      // fold it into the sum so that chunk ch + 1 can reuse its accumulator
+      if (i >= 2 * kGramChain && (i - 1) % kGramChain == kGramChain - 1) {
+        if (!wait_bar(e_free, (i - 1) & 1, &abort_flag, p.err)) { ok = false; break; }
+        tc_fence_after();
+        if (!is_r) fold_acc<128>(tAcc + lane_off, tChunk + lane_off);
+        else fold_acc<D_V>(tAcc + lane_off, tChunk + lane_off);
+        tc_fence_before();
+        mbar_arrive(acc_free);
+      }
+      float cs = 0.f;  // the slab's share of c
       if (!wait_bar(&s_full[b], (i >> 1) & 1, &abort_flag, p.err)) { ok = false; break; }
       tc_fence_after();
       float xi[kSL], xj[kSL];
@@ -275,7 +335,7 @@ __global__ void __launch_bounds__(192, 1)
         for (int e = 0; e < 8; ++e) {
           const float sh = rs[c8 * 8 + e];
           e8[e] = ex2(fmaf(xi[c8 * 8 + e], s2, cbi) - sh);
-          if (with_c) cacc = fmaf(e8[e], rb[c8 * 8 + e], cacc);
+          if (with_c) cs = fmaf(e8[e], rb[c8 * 8 + e], cs);
         }
         uint4 hi, lo;
         split8(e8, hi, lo);
@@ -293,33 +353,21 @@ __global__ void __launch_bounds__(192, 1)
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(e_full);
+      cacc += cs;
     }
     if (ok && nsl > 0 && wait_bar(e_free, (nsl - 1) & 1, &abort_flag, p.err)) {
       tc_fence_after();
       const int H = gridDim.y;
       const size_t zh = static_cast<size_t>(z) * H + h;
       const int key = bi * 128 + j;
+      const bool chunks = nsl > kGramChain;  // the last chunk is still apart
       if (!is_r) {
-        float* dst = p.Gpart + (zh * p.t_pad + key) * p.t_pad + bj * 128;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float v[32];
-          tmem_ld32(tAcc + lane_off + c * 32, v);
-          float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) d4[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
-        }
+        store_acc_row<128>(tAcc + lane_off, tChunk + lane_off, chunks,
+                           p.Gpart + (zh * p.t_pad + key) * p.t_pad + bj * 128);
         if (with_c) p.cpart[zh * p.t_pad + key] = cacc;
       } else {
-        float* dst = p.Rpart + (zh * p.t_pad + key) * p.d_v;
-#pragma unroll
-        for (int c = 0; c < D_V / 32; ++c) {
-          float v[32];
-          tmem_ld32(tAcc + lane_off + c * 32, v);
-          float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) d4[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
-        }
+        store_acc_row<D_V>(tAcc + lane_off, tChunk + lane_off, chunks,
+                           p.Rpart + (zh * p.t_pad + key) * p.d_v);
       }
     }
   }
@@ -379,7 +427,8 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* e_free = bars + 11;   // [2]
   uint64_t* done = bars + 13;
   uint64_t* mma_drain = bars + 14;  // MMA completion before exit
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(mma_drain + 1);
+  uint64_t* acc_free = bars + 15;   // a chunk's accumulator folded into the sum
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 16);
   float* cx = reinterpret_cast<float*>(base + L::OFF_CX);
   __shared__ volatile int abort_flag;
 
@@ -424,6 +473,7 @@ __global__ void __launch_bounds__(320, 1)
     }
     mbar_init(done, 1);
     mbar_init(mma_drain, 1);
+    mbar_init(acc_free, 128);
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(tslot, 512);
@@ -431,7 +481,10 @@ __global__ void __launch_bounds__(320, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tslot;
+  // chunk 0 (of kGramChain slabs) accumulates at column 256 and stays there
+  // as the running sum; later chunks at column 384
   const uint32_t tAcc = tbase + 256;
+  const uint32_t tChunk = tbase + 384;
 
   if (warp == 0) {
     if (lane == 0 && nsl > 0) {
@@ -494,18 +547,20 @@ __global__ void __launch_bounds__(320, 1)
         tc_fence_after();
         const uint32_t eb = smem_u32(sE + g * e_buf);
         const uint32_t eih = eb, eil = eb + L::E_BLK;
+        const uint32_t tA = i < kGramChain ? tAcc : tChunk;
+        const bool cont = i % kGramChain > 0;
         if (!is_r) {
           const uint32_t ejh = two ? eb + 2 * L::E_BLK : eih;
           const uint32_t ejl = two ? eb + 3 * L::E_BLK : eil;
 #pragma unroll
           for (int k = 0; k < kSL / 16; ++k) {
             const uint32_t o = k * 32;
-            const uint32_t acc0 = (i > 0 || k > 0) ? 1u : 0u;
-            umma_f16_ss(tAcc, sdesc_sw128(eih + o, 16, 1024), sdesc_sw128(ejh + o, 16, 1024),
+            const uint32_t acc0 = (cont || k > 0) ? 1u : 0u;
+            umma_f16_ss(tA, sdesc_sw128(eih + o, 16, 1024), sdesc_sw128(ejh + o, 16, 1024),
                         idesc_g, acc0);
-            umma_f16_ss(tAcc, sdesc_sw128(eih + o, 16, 1024), sdesc_sw128(ejl + o, 16, 1024),
+            umma_f16_ss(tA, sdesc_sw128(eih + o, 16, 1024), sdesc_sw128(ejl + o, 16, 1024),
                         idesc_g, 1u);
-            umma_f16_ss(tAcc, sdesc_sw128(eil + o, 16, 1024), sdesc_sw128(ejh + o, 16, 1024),
+            umma_f16_ss(tA, sdesc_sw128(eil + o, 16, 1024), sdesc_sw128(ejh + o, 16, 1024),
                         idesc_g, 1u);
           }
         } else {
@@ -514,16 +569,22 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
           for (int k = 0; k < kSL / 16; ++k) {
             const uint32_t o = k * 32;
-            const uint32_t acc0 = (i > 0 || k > 0) ? 1u : 0u;
+            const uint32_t acc0 = (cont || k > 0) ? 1u : 0u;
             const uint64_t doh = sdesc_sw128(aO + k * 2048, L::QCHUNK, 1024);
             const uint64_t dol = sdesc_sw128(aOl + k * 2048, L::QCHUNK, 1024);
-            umma_f16_ss(tAcc, sdesc_sw128(eih + o, 16, 1024), doh, idesc_r, acc0);
-            umma_f16_ss(tAcc, sdesc_sw128(eih + o, 16, 1024), dol, idesc_r, 1u);
-            umma_f16_ss(tAcc, sdesc_sw128(eil + o, 16, 1024), doh, idesc_r, 1u);
+            umma_f16_ss(tA, sdesc_sw128(eih + o, 16, 1024), doh, idesc_r, acc0);
+            umma_f16_ss(tA, sdesc_sw128(eih + o, 16, 1024), dol, idesc_r, 1u);
+            umma_f16_ss(tA, sdesc_sw128(eil + o, 16, 1024), doh, idesc_r, 1u);
           }
           umma_commit(&st_empty[g]);  // the O slab feeds the products above
         }
         umma_commit(&e_free[g]);
+      };
+      // a chunk's first products wait until the previous chunk has been
+      // folded into the sum (its accumulator is reused)
+      auto acc_ready = [&](int i) {
+        const int ch = i / kGramChain;
+        return i % kGramChain != 0 || ch < 2 || mbar_test_wait(acc_free, (ch - 2) & 1);
       };
       // Event loop: the scores of a slab are issued as soon as its query slab
       // is loaded and its S buffer has been read (up to two slabs ahead of
@@ -536,7 +597,7 @@ __global__ void __launch_bounds__(320, 1)
             (ns < 2 || mbar_test_wait(&s_free[ns & 1], ((ns >> 1) - 1) & 1))) {
           issue_s(ns++);
           t_last = globaltimer_ns();
-        } else if (ng < ns && mbar_test_wait(&e_full[ng & 1], (ng >> 1) & 1)) {
+        } else if (ng < ns && mbar_test_wait(&e_full[ng & 1], (ng >> 1) & 1) && acc_ready(ng)) {
           issue_g(ng++);
           t_last = globaltimer_ns();
         } else if ((++spins & 63u) == 0) {
@@ -569,10 +630,28 @@ __global__ void __launch_bounds__(320, 1)
     uint8_t* sEil = eb + L::E_BLK;
     uint8_t* sEjh = eb + 2 * L::E_BLK;
     uint8_t* sEjl = eb + 3 * L::E_BLK;
+    // slab e closed chunk ch >= 1 (not the last): once its products are
+    // complete, fold it into the sum so that chunk ch + 1 can reuse its
+    // accumulator.  The group that formed slab e does this, before its next
+    // slab or after its last one.
+    auto closes_chunk = [&](int e) {
+      return e >= 2 * kGramChain - 1 && e % kGramChain == kGramChain - 1 && e < nsl - 1;
+    };
+    auto fold = [&](int e) -> bool {
+      if (!wait_bar(&e_free[g], (e >> 1) & 1, &abort_flag, p.err)) return false;
+      tc_fence_after();
+      if (!is_r) fold_acc<128>(tAcc + lane_off, tChunk + lane_off);
+      else fold_acc<D>(tAcc + lane_off, tChunk + lane_off);
+      tc_fence_before();
+      mbar_arrive(acc_free);
+      return true;
+    };
     float cacc = 0.f;
     bool ok = nsl > 0;
     for (int i = g; ok && i < nsl; i += 2) {
       const int n = i >> 1;  // this group's n-th slab
+      if (i >= 2 && closes_chunk(i - 2) && !fold(i - 2)) { ok = false; break; }
+      float cs = 0.f;  // the slab's share of c
       // per-query shifts (and mass) of this slab, read through L1: every
       // thread of the group reads the same 64 values
       const size_t roff = static_cast<size_t>(h) * p.n_q_pad + static_cast<size_t>(s0 + i) * kSL;
@@ -620,7 +699,7 @@ __global__ void __launch_bounds__(320, 1)
                                  b4[2 * q8 + 1].x, b4[2 * q8 + 1].y, b4[2 * q8 + 1].z,
                                  b4[2 * q8 + 1].w};
 #pragma unroll
-            for (int e = 0; e < 8; ++e) cacc = fmaf(e8[e], b8[e], cacc);
+            for (int e = 0; e < 8; ++e) cs = fmaf(e8[e], b8[e], cs);
           }
           uint4 hi, lo;
           split8(e8, hi, lo);
@@ -640,7 +719,11 @@ __global__ void __launch_bounds__(320, 1)
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(&e_full[g]);
+      cacc += cs;
     }
+    // a chunk closed by this group's last slab (the next chunk has one slab)
+    if (ok && nsl >= 2 && ((nsl - 2) & 1) == g && closes_chunk(nsl - 2) && !fold(nsl - 2))
+      ok = false;
     // combine the groups' partial c and publish the block accumulator
     if (with_c && g == 1) cx[j] = cacc;
     asm volatile("bar.sync 1, 256;" ::: "memory");
@@ -649,27 +732,14 @@ __global__ void __launch_bounds__(320, 1)
       const int H = gridDim.y;
       const size_t zh = static_cast<size_t>(z) * H + h;
       const int key = bi * 128 + j;
+      const bool chunks = nsl > kGramChain;  // the last chunk is still apart
       if (!is_r) {
-        float* dst = p.Gpart + (zh * p.t_pad + key) * p.t_pad + bj * 128;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float v[32];
-          tmem_ld32(tAcc + lane_off + c * 32, v);
-          float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) d4[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
-        }
+        store_acc_row<128>(tAcc + lane_off, tChunk + lane_off, chunks,
+                           p.Gpart + (zh * p.t_pad + key) * p.t_pad + bj * 128);
         if (with_c) p.cpart[zh * p.t_pad + key] = cacc + (nsl > 1 ? cx[j] : 0.f);
       } else {
-        float* dst = p.Rpart + (zh * p.t_pad + key) * p.d_v;
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          float v[32];
-          tmem_ld32(tAcc + lane_off + c * 32, v);
-          float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) d4[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
-        }
+        store_acc_row<D>(tAcc + lane_off, tChunk + lane_off, chunks,
+                         p.Rpart + (zh * p.t_pad + key) * p.d_v);
       }
     }
   }

@@ -49,6 +49,20 @@ struct KeyScoreParams {
 //   G[bi,bj] += E_bi E_bj^T   (hi/lo split, three products)
 //   c[bi]    += E_bi b         (diagonal blocks, when row_b != null)
 //   R[bi]    += E_bi O         (diagonal blocks, when O maps given)
+//
+// The tensor core adds each product into its fp32 accumulator with
+// truncation, so a long chain of additions drifts low: about 2.6e-7 of the
+// sum per query slab summed (three products of four k-steps each), 2e-4
+// after 2048 slabs.  One accumulator therefore sums at most kGramChain
+// slabs.  The per-block kernels hold two in tensor memory: the first
+// chunk's becomes the CTA's running sum, and each later chunk, summed in
+// the second, is added into it (fp32, round to nearest, tensor memory to
+// registers and back) before the next chunk starts.  The launches whose
+// tensor memory has no room for the second take at least
+// gram_min_split(slabs) query splits, reduced afterwards in fp32.
+constexpr int kGramChain = 64;  // power of two
+inline int gram_min_split(int slabs) { return (slabs + kGramChain - 1) / kGramChain; }
+
 struct GramParams {
   int n_q_pad, n_q;
   int t_pad;

@@ -1,17 +1,22 @@
 """Parity at the full sizes of the benchmark configurations, in the launch
 configuration the benchmark uses (one compact_layer call over all heads of a
-layer).  The oracle recomputes sampled outputs: whole heads where it finishes
-in seconds (cfg2 every head, cfg3 and cfg4 sampled heads and layers), single
-query rows and properties of the GPU's own outputs where the layer is too
-large for a float64 CPU pass (cfg5, 131072 keys).  Every expected value comes
+layer).  The oracle recomputes whole heads where it finishes in seconds (cfg2
+and cfg3 every head, cfg4 sampled layers); for the long-context layer (cfg5,
+131072 keys) head 0's oracle compaction is stored (tests/golden/, written by
+a script that calls only the oracle), and the rest is checked on single query
+rows and on properties of the GPU's own outputs.  Every expected value comes
 from the generator or the oracle."""
+import hashlib
+import os
+
 import numpy as np
 import pytest
 
 import oracle
 import synth
-from gpu_util import (FIT_REL, LSE_ABS, O_REL, SCORE_ABS, beta_err, compactor, dev, dev_f32,
-                      dev_i32, host, inputs, relf)
+from gpu_util import (FIT_REL, LSE_ABS, O_REL, SCORE_ABS, beta_err, check_layer_fits,
+                      compactor, dev, dev_f32, dev_i32, gate_fit, host, inputs, near_tie_swap,
+                      relf)
 
 pytestmark = pytest.mark.gpu
 
@@ -21,24 +26,10 @@ def comp():
     return compactor()
 
 
-def _check_head(w, d, h, idx, wg, bg, cg, m=None, lse=None):
-    """One head of a GPU compaction against the oracle's compaction of it."""
-    r = oracle.compact_head(d["Q"][h], d["K"][h], d["V"][h], w.t, w.softmax_scale)
-    if lse is not None:
-        assert np.max(np.abs(lse - r["lse"])) <= LSE_ABS, f"head {h} lse"
-        assert np.max(np.abs(m - r["m"])) <= LSE_ABS, f"head {h} rowmax"
-    if not np.array_equal(idx, r["idx"]):
-        # only keys whose oracle scores tie within the score tolerance may swap
-        tau = np.sort(r["u"])[::-1][w.t - 1]
-        diff = np.setxor1d(idx, r["idx"])
-        assert np.all(np.abs(r["u"][diff] - tau) <= SCORE_ABS), f"head {h}: selection differs"
-        return
-    assert relf(wg, r["w"]) <= FIT_REL, f"head {h} w relF {relf(wg, r['w']):.2e}"
-    assert beta_err(bg, r["beta"]) <= FIT_REL, f"head {h} beta {beta_err(bg, r['beta']):.2e}"
-    assert relf(cg, r["Cv"]) <= FIT_REL, f"head {h} Cv relF {relf(cg, r['Cv']):.2e}"
-
-
 def _layer(comp, w, heads_checked, with_stats=True):
+    """One compact_layer call over every head of the layer, then the checked
+    heads against the oracle: row statistics, selection (exact up to
+    near-ties) and the fit of every checked head (check_layer_fits)."""
     d, Q, K, V = inputs(w)
     stats = None
     if with_stats:
@@ -48,9 +39,15 @@ def _layer(comp, w, heads_checked, with_stats=True):
     rep = comp.report(w.H)
     assert rep.device_error_bits == 0
     assert all(s == 0 for s in rep.head_status), rep.head_status
+    refs = {}
     for h in heads_checked:
-        kw = {} if stats is None else {"m": stats[0][h], "lse": stats[1][h]}
-        _check_head(w, d, h, idx[h], wg[h], bg[h], cg[h], **kw)
+        r = oracle.compact_head(d["Q"][h], d["K"][h], d["V"][h], w.t, w.softmax_scale)
+        if stats is not None:
+            assert np.max(np.abs(stats[1][h] - r["lse"])) <= LSE_ABS, f"head {h} lse"
+            assert np.max(np.abs(stats[0][h] - r["m"])) <= LSE_ABS, f"head {h} rowmax"
+        refs[h] = r
+    overlaps = check_layer_fits(comp, w, Q, K, V, refs, idx, wg, bg, cg)
+    print(f"{w.name}: selection overlap per head {overlaps}")
 
 
 def test_cfg2_full_layer_every_head(comp):
@@ -59,9 +56,10 @@ def test_cfg2_full_layer_every_head(comp):
     _layer(comp, w, range(w.H))
 
 
-def test_cfg3_layer_sampled_heads(comp):
-    """The benchmark layer (T = 8192, n_q = 32768, t = 256), heads 0 and 5."""
-    _layer(comp, synth.workload("cfg3"), (0, 5))
+def test_cfg3_full_layer_every_head(comp):
+    """The benchmark layer (T = 8192, n_q = 32768, t = 256), every head."""
+    w = synth.workload("cfg3")
+    _layer(comp, w, range(w.H))
 
 
 @pytest.mark.parametrize("layer", [0, 35])
@@ -158,3 +156,48 @@ def test_cfg5_fit_t1024(comp):
     assert relf(wg, r["w"]) <= FIT_REL, f"w relF {relf(wg, r['w']):.2e}"
     assert beta_err(bg, r["beta"]) <= FIT_REL, f"beta {beta_err(bg, r['beta']):.2e}"
     assert relf(cg, r["Cv"]) <= FIT_REL, f"Cv relF {relf(cg, r['Cv']):.2e}"
+
+
+GOLDEN_CFG5 = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "cfg5_head0.npz")
+
+
+def _inputs_digest(d, h):
+    dig = hashlib.sha256()
+    for k in ("Q", "K", "V"):
+        dig.update(synth.bf16_bits(d[k][h]).tobytes())
+    return dig.hexdigest()
+
+
+def test_cfg5_head0_against_stored_oracle(comp, cfg5):
+    """Head 0 of the long-context layer (131072 keys, 524288 queries, t = 1024)
+    against the float64 oracle's compaction of the same head, stored by
+    tests/golden/make_cfg5_head0.py (a little over an hour of host time, so
+    it is not recomputed here): key scores within the score tolerance, row
+    statistics of the stored sample rows, the selection exact up to
+    near-ties, and w, beta and C_v within the fit tolerance.  Where a near-tie
+    made the selections differ, the GPU's fit is compared on the oracle's
+    selection instead (lc_fit_only, from the GPU's own step-1 statistics as
+    in lc_compact_layer)."""
+    g = np.load(GOLDEN_CFG5)
+    w, d = cfg5["w"], cfg5["d"]
+    assert _inputs_digest(d, 0) == str(g["inputs_sha256"]), "the generator drew another layer"
+    assert int(g["nnls_status"]) == 0 and int(g["ols_status"]) == 0
+    err = float(np.max(np.abs(cfg5["u"][0] - g["u"])))
+    assert err <= SCORE_ABS, f"max |u_gpu - u| = {err:.2e}"
+    rows = g["rows"]
+    assert np.max(np.abs(cfg5["lse"][0][rows] - g["lse"])) <= LSE_ABS
+    assert np.max(np.abs(cfg5["m"][0][rows] - g["m"])) <= LSE_ABS
+    idx, wg, bg, cg = (x[0] for x in cfg5["out"])
+    ref = {"w": g["w"], "beta": g["beta"], "Cv": g["Cv"]}
+    overlap = near_tie_swap(idx, g["idx"], g["u"], w.t, "cfg5 head 0")
+    print(f"cfg5 head 0: selection overlap {overlap:.4f}")
+    if overlap == 1.0:
+        gate_fit(wg, bg, cg, ref, "cfg5 head 0")
+        return
+    wf, bf, cf = comp.fit_only(dev(d["Q"][:1], w.dtype), dev(d["K"][:1], w.dtype),
+                               dev(d["V"][:1], w.dtype), dev_i32(g["idx"][None]),
+                               dev_f32(cfg5["m"][:1]), dev_f32(cfg5["lse"][:1]),
+                               dev_f32(cfg5["O"][:1]))
+    rep = comp.report(1)
+    assert rep.device_error_bits == 0 and rep.head_status[0] == 0, rep
+    gate_fit(host(wf)[0], host(bf)[0], host(cf)[0], ref, "cfg5 head 0 (on the oracle's selection)")
