@@ -551,20 +551,63 @@ __device__ SolverSmem carve(float* dyn, int n_pad) {
   return s;
 }
 
-// Packed lower blocks of M_ab = src(a, b) for a, b < n and the identity
-// beyond n: one warp per matrix row, one lane per column, independent loads.
-template <class F>
-__device__ void gather_packed(float* S, int NB, int n, F src) {
+// Packed lower blocks of M_ab = fix(a, b, src[map(a) * ld + map(b)]) for
+// a, b < n and the identity beyond n (S in shared or global memory), one
+// warp per matrix row, one lane per column.
+template <class Map, class Fix>
+__device__ void gather_packed(float* S, int NB, int n, const float* src, int ld, Map map,
+                              Fix fix) {
   const int lane = lane_id();
-  for (int task = warp_id(); task < NB * kBS; task += kWarps) {
-    const int I = task / kBS, r = task % kBS, a = task;
-#pragma unroll 4
+  for (int a = warp_id(); a < NB * kBS; a += kWarps) {
+    const int I = a / kBS, r = a % kBS;
     for (int J = 0; J <= I; ++J) {
       const int b = J * kBS + lane;
-      float v;
-      if (a < n && b < n) v = src(a, b);
-      else v = (a == b) ? 1.f : 0.f;
-      blk(S, I, J)[r * kLD + lane] = v;
+      blk(S, I, J)[r * kLD + lane] =
+          (a < n && b < n) ? fix(a, b, src[static_cast<size_t>(map(a)) * ld + map(b)])
+                           : (a == b ? 1.f : 0.f);
+    }
+  }
+}
+
+// The same for the unpermuted rows and columns of a system of at most 256
+// unknowns (NB <= 8; ld a multiple of 4 and at least NB * 32).  The copy is
+// bound by load latency and by the instructions per element, so a warp takes
+// four rows at a time, each lane loading 16-byte pieces (columns 4l..4l+3 of
+// the two 128-column halves), and applies fix as it stores.
+template <class Fix>
+__device__ void gather_packed_rows(float* S, int NB, int n, const float* src, int ld, Fix fix) {
+  const int lane = lane_id();
+  const int rows = NB * kBS;
+  const int c0 = 4 * (lane % 8), Jl = lane / 8;  // column piece and block within a half
+  for (int a0 = warp_id(); a0 < rows; a0 += 4 * kWarps) {
+    float4 v[4][2];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int a = a0 + q * kWarps, I = a / kBS;
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const bool need = a < n && a < rows && hf * 4 + Jl <= I && (hf * 4 + Jl) * kBS + c0 < n;
+        v[q][hf] = need ? *reinterpret_cast<const float4*>(src + static_cast<size_t>(a) * ld +
+                                                          hf * 128 + 4 * lane)
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int a = a0 + q * kWarps, I = a / kBS, r = a % kBS;
+      if (a >= rows) break;
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const int J = hf * 4 + Jl;
+        if (J > I) continue;
+        const float e4[4] = {v[q][hf].x, v[q][hf].y, v[q][hf].z, v[q][hf].w};
+        float* dst = blk(S, I, J) + r * kLD + c0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int b = J * kBS + c0 + e;
+          dst[e] = (a < n && b < n) ? fix(a, b, e4[e]) : (a == b ? 1.f : 0.f);
+        }
+      }
     }
   }
 }
@@ -676,9 +719,9 @@ __global__ void __launch_bounds__(kThreads, 1) nnls_bpp_kernel(const SolveParams
   if (!direct) {
     float ridge = 0.f;
     for (int attempt = 0; attempt < 2; ++attempt) {
-      gather_packed(S, NB, t, [&](int a, int b) {
+      gather_packed_rows(S, NB, t, G, tp, [&](int a, int b, float v) {
         if (dup[a] || dup[b]) return (a == b) ? 1.f : 0.f;
-        return G[static_cast<size_t>(a) * tp + b] + (a == b ? ridge : 0.f);
+        return v + (a == b ? ridge : 0.f);
       });
       __syncthreads();
       if (cta_cholesky(S, sm.dinv, NB, &bad)) break;
@@ -823,9 +866,8 @@ __global__ void __launch_bounds__(kThreads, 1) nnls_bpp_kernel(const SolveParams
       const int NBf = (nF + kBS - 1) / kBS;
       float ridge = 0.f;
       for (int attempt = 0; attempt < 2; ++attempt) {
-        gather_packed(S, NBf, nF, [&](int a, int b) {
-          return G[static_cast<size_t>(Didx[a]) * tp + Didx[b]] + (a == b ? ridge : 0.f);
-        });
+        gather_packed(S, NBf, nF, G, tp, [&](int a) { return Didx[a]; },
+                      [&](int a, int b, float v) { return v + (a == b ? ridge : 0.f); });
         __syncthreads();
         if (cta_cholesky(S, sm.dinv, NBf, &bad)) break;
         status = LC_SINGULAR_STATUS;
@@ -968,9 +1010,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     float ridge = 0.f;
     for (int attempt = 0; attempt < 2; ++attempt) {
-      gather_packed(S, NBf, nF, [&](int a, int b) {
-        return G[static_cast<size_t>(Fidx[a]) * tp + Fidx[b]] + (a == b ? ridge : 0.f);
-      });
+      gather_packed(S, NBf, nF, G, tp, [&](int a) { return Fidx[a]; },
+                    [&](int a, int b, float v) { return v + (a == b ? ridge : 0.f); });
       __syncthreads();
       if (cta_cholesky(S, sm.dinv, NBf, &bad)) break;
       status = LC_SINGULAR_STATUS;
@@ -1038,20 +1079,27 @@ __global__ void __launch_bounds__(kThreads, 1) ols_factor_kernel(const OlsParams
   float* S = sm.S ? sm.S : gS;
   const float* Hm = p.Hm + static_cast<size_t>(h) * tp * tp;
   const float* w = p.w + static_cast<size_t>(h) * t;
+  // keys with w > 0 (the support), staged so that the gather's loads do not
+  // wait on loads of w
+  int* live = sm.ivec;
+  for (int j = tid; j < n_pad; j += kThreads) live[j] = j < t && w[j] > 0.f;
+  __syncthreads();
   float ridge = 0.f;
   int status = LC_OK_STATUS;
   for (int attempt = 0; attempt < 2; ++attempt) {
-    gather_packed(S, NB, t, [&](int a, int b) {
-      if (!(w[a] > 0.f) || !(w[b] > 0.f)) return (a == b) ? 1.f : 0.f;
-      return Hm[static_cast<size_t>(a) * tp + b] + (a == b ? ridge : 0.f);
-    });
+    auto fix = [&](int a, int b, float v) {
+      if (!live[a] || !live[b]) return (a == b) ? 1.f : 0.f;
+      return v + (a == b ? ridge : 0.f);
+    };
+    if (sm.S) gather_packed_rows(S, NB, t, Hm, tp, fix);
+    else gather_packed(S, NB, t, Hm, tp, [](int a) { return a; }, fix);
     __syncthreads();
     if (cta_cholesky(S, sm.dinv, NB, &bad)) break;
     status = LC_SINGULAR_STATUS;
     float dsum = 0.f;
     int cnt = 0;
     for (int a = tid; a < t; a += kThreads)
-      if (w[a] > 0.f) {
+      if (live[a]) {
         dsum += Hm[static_cast<size_t>(a) * tp + a];
         ++cnt;
       }
@@ -1085,10 +1133,15 @@ __global__ void __launch_bounds__(kThreads, 1) ols_solve_kernel(const OlsParams 
   const float* gS = p.mat + static_cast<size_t>(h) * tp * tp;
   const float* S = gS;
   if (sm.S) {
+    // the published factor by asynchronous 16-byte copies, all in flight
+    // at once (a copy loop of loads and stores waits on every load)
     const size_t nel = static_cast<size_t>(NB * (NB + 1) / 2) * kBlk;
-    const float4* src = reinterpret_cast<const float4*>(gS);
-    float4* dst = reinterpret_cast<float4*>(sm.S);
-    for (size_t e = tid; e < nel / 4; e += kThreads) dst[e] = src[e];
+    for (size_t e = tid; e < nel / 4; e += kThreads)
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(
+                       __cvta_generic_to_shared(sm.S + 4 * e))),
+                   "l"(__cvta_generic_to_global(gS + 4 * e))
+                   : "memory");
+    asm volatile("cp.async.wait_all;" ::: "memory");
     S = sm.S;
   }
   const float* gd = p.dinv + static_cast<size_t>(h) * tp;
@@ -1111,13 +1164,42 @@ __global__ void __launch_bounds__(kThreads, 1) ols_solve_kernel(const OlsParams 
     const int nct = 1;
     const int I = warp / nct, ct = warp % nct;
     float nb[4][8];
+    if (nc == kBS) {
+      // every load first (w, R and the value rows, 16 bytes at a time), then
+      // the choice between R and V[idx]: no load waits on another
+      float wa[4];
+      float4 rv[4][2], vv[4][2];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < 4; ++i) {
+        const int a = I * kBS + 4 * rg + i;
+        const bool in = I < NB && a < t;
+        const size_t e = static_cast<size_t>(a) * dv + c0 + 8 * cg;
+        wa[i] = in ? w[a] : 0.f;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int a = I * kBS + 4 * rg + i, q = ct * kBS + 8 * cg + j;
-        nb[i][j] = (I < NB && q < nc) ? -rhs(a, c0 + q) : 0.f;
+        for (int hf = 0; hf < 2; ++hf) {
+          rv[i][hf] = in ? *reinterpret_cast<const float4*>(B + e + 4 * hf) : make_float4(0.f, 0.f, 0.f, 0.f);
+          vv[i][hf] = in ? *reinterpret_cast<const float4*>(Vc + e + 4 * hf) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
       }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          const float4 v4 = wa[i] > 0.f ? rv[i][hf] : vv[i][hf];
+          nb[i][4 * hf] = -v4.x;
+          nb[i][4 * hf + 1] = -v4.y;
+          nb[i][4 * hf + 2] = -v4.z;
+          nb[i][4 * hf + 3] = -v4.w;
+        }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int a = I * kBS + 4 * rg + i, q = ct * kBS + 8 * cg + j;
+          nb[i][j] = (I < NB && q < nc) ? -rhs(a, c0 + q) : 0.f;
+        }
+    }
     __syncthreads();
     reg_tri_solve<true>(S, sm.dinv, NB, nct, nb, sm.T2);
     reg_tri_solve<false>(S, sm.dinv, NB, nct, nb, sm.T2);
