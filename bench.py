@@ -454,8 +454,22 @@ def main():
         ms_e2e = max_over_ranks(e0.elapsed_time(e1) / a.e2e_steps, dist, dev)
         h2d = sum(x.numel() * x.element_size() for x in pinned[0])
         d2h = sum(x.numel() * x.element_size() for x in hout)
+        # this machine's pinned host -> device copy rate for the same tensors,
+        # copies alone: the floor under the upload that e2e overlaps with step 1
+        dst = [torch.empty_like(x, device=dev) for x in pinned[0]]
+        c0 = torch.cuda.Event(enable_timing=True)
+        c1 = torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for i in range(4):
+            for d_, s_ in zip(dst, pinned[i % N_LAYERS]):
+                d_.copy_(s_, non_blocking=True)
+        c1.record(stream)
+        torch.cuda.synchronize()
+        ms_copy = c0.elapsed_time(c1) / 4
+        del dst
         e2e = {"value": job_value(ms_e2e, world), "unit": "ms", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h}
+               "d2h_bytes_per_step": d2h, "h2d_copy_ms": ms_copy,
+               "h2d_copy_gbs": h2d / (ms_copy * 1e-3) / 1e9}
 
     # the fast path (two-pass selection, redistributed beta, direct values)
     # on the same layers, 256-query subsets drawn per layer
