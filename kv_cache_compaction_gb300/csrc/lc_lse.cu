@@ -171,9 +171,14 @@ __global__ void __launch_bounds__(192, 1)
 
 // Compact log mass, bf16 inputs with at most 256 selected keys: the scores of
 // a 128-query tile against all keys come from one chain of MMAs with N = t_pad
-// (C_k resident in shared memory for the whole CTA), and two epilogue
-// warpgroups take alternate tiles (S double-buffered in TMEM, 2 x 256
-// columns), each thread reducing its query's row with an online log-sum-exp.
+// (C_k resident in shared memory for the whole CTA); S is double-buffered in
+// TMEM (2 x 256 columns), alternate tiles going to two pairs of epilogue
+// warpgroups.  Within a pair each warpgroup reduces half of every query row
+// with an online log-sum-exp (a thread per row): the reduction is a chain of
+// TMEM load, row max and exponentials per 32 columns, bound by latency, so
+// four warpgroups in flight instead of two keep the exponential unit busier.
+// The second half's (max, sum) reaches the first through shared memory
+// (mbarriers, two buffers per pair), which combines and writes the row.
 // CTAs are persistent over a contiguous range of query tiles of one head.
 template <int D>
 struct CL2Layout {
@@ -182,12 +187,14 @@ struct CL2Layout {
   static constexpr int Q_BYTES = kBM * D * 2;
   static constexpr int OFF_Q = KC_BYTES;
   static constexpr int OFF_CB = OFF_Q + 2 * Q_BYTES;
-  static constexpr int OFF_BAR = OFF_CB + 256 * 4;
+  static constexpr int OFF_X = OFF_CB + 256 * 4;            // [pair][buffer][row] float2
+  static constexpr int OFF_BAR = OFF_X + 2 * 2 * kBM * 8;
   static constexpr int SMEM = 1024 + OFF_BAR + 256;
+  static constexpr int THREADS = 64 + 4 * 128;
 };
 
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(CL2Layout<D>::THREADS, 1)
     compact_lse2_kernel(const __grid_constant__ CUtensorMap mQ,
                         const __grid_constant__ CUtensorMap mKc, const CompactLseParams p,
                         int tiles_per_split) {
@@ -204,7 +211,10 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* s_full = bars + 5;   // [2]
   uint64_t* s_free = bars + 7;   // [2]
   uint64_t* mma_drain = bars + 9;  // MMA completion before exit
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(mma_drain + 1);
+  uint64_t* x_full = bars + 10;  // [pair][buffer]: second half's row results written
+  uint64_t* x_free = bars + 14;  // [pair][buffer]: read by the first half
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 18);
+  float2* xch = reinterpret_cast<float2*>(base + L::OFF_X);
   __shared__ volatile int abort_flag;
   const int warp = warp_id(), lane = lane_id();
   const int h = blockIdx.y;
@@ -222,7 +232,11 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&q_full[i], 1);
       mbar_init(&q_empty[i], 1);
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 128);
+      mbar_init(&s_free[i], 256);  // both halves have read S
+    }
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&x_full[i], 128);
+      mbar_init(&x_free[i], 128);
     }
     mbar_init(mma_drain, 1);
     fence_mbar_init();
@@ -279,21 +293,23 @@ __global__ void __launch_bounds__(320, 1)
       }
     }
   } else {
-    const int g = (warp - 2) >> 2;
+    const int wg = (warp - 2) >> 2;
+    const int g = wg & 1, hh = wg >> 1;  // tile parity, column half
     const int wq = warp & 3;
     const int row = wq * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const float s2 = p.scale_log2;
+    const int half = p.t_pad / 2;
     bool ok = nt > g && wait_bar(k_full, 0, &abort_flag, p.err);
     for (int i = g; ok && i < nt; i += 2) {
-      const int n = i >> 1;
+      const int n = i >> 1, xb = g * 2 + (n & 1);
       if (!wait_bar(&s_full[g], n & 1, &abort_flag, p.err)) { ok = false; break; }
       tc_fence_after();
       float mref = -kInf, l = 0.f;
-      for (int c = 0; c < p.t_pad / 32; ++c) {
+      for (int c = 0; c < half / 32; ++c) {
         float v[32];
-        tmem_ld32(tbase + g * 256 + c * 32 + lane_off, v);
-        const float4* cb4 = reinterpret_cast<const float4*>(sCB + c * 32);
+        tmem_ld32(tbase + g * 256 + hh * half + c * 32 + lane_off, v);
+        const float4* cb4 = reinterpret_cast<const float4*>(sCB + hh * half + c * 32);
         float mx = -kInf;
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
@@ -318,6 +334,26 @@ __global__ void __launch_bounds__(320, 1)
       }
       tc_fence_before();
       mbar_arrive(&s_free[g]);
+      if (hh == 1) {
+        // hand this half's (max, sum) to the first half
+        if (n >= 2 && !wait_bar(&x_free[xb], ((n >> 1) - 1) & 1, &abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
+        xch[xb * kBM + row] = make_float2(mref, l);
+        mbar_arrive(&x_full[xb]);
+        continue;
+      }
+      if (!wait_bar(&x_full[xb], (n >> 1) & 1, &abort_flag, p.err)) { ok = false; break; }
+      const float2 o = xch[xb * kBM + row];
+      mbar_arrive(&x_free[xb]);
+      {
+        const float m2 = fmaxf(mref, o.x);
+        if (m2 > -kInf) {
+          l = (mref > -kInf ? l * ex2(mref - m2) : 0.f) + (o.x > -kInf ? o.y * ex2(o.x - m2) : 0.f);
+          mref = m2;
+        }
+      }
       const int qr = (t0 + i) * kBM + row;
       if (qr < p.n_q_pad) {
         if (p.part)
@@ -362,7 +398,7 @@ cudaError_t launch_compact_lse_resident(OperandMode mode, const CUtensorMap& mQ,
   auto go = [&](auto kern, int smem) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    kern<<<dim3(grid_x, H, kstride / p.t_pad), 320, smem, st>>>(mQ, mKc, p, tps);
+    kern<<<dim3(grid_x, H, kstride / p.t_pad), 64 + 4 * 128, smem, st>>>(mQ, mKc, p, tps);
     return cudaGetLastError();
   };
   switch (mode) {
