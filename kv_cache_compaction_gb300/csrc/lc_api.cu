@@ -498,10 +498,10 @@ lc_status run_fit(const Ctx& ca, const void* qop, const void* kop, const void* V
 
   // ---- step 4: mass system and NNLS
   {
-    LC_PROF(c, "mass_rows", 2);
+    LC_PROF(c, "mass_rows", 1);
     LC_CUDA(launch_mass_rows(c.at<float>(p.m_pad), c.at<float>(p.lse_pad), c.at<float>(p.rowsh2),
-                             c.at<float>(p.rowb), p.H, p.n_q, p.n_q_pad, c.st));
-    LC_CUDA(launch_fill_colb2(c.at<float>(p.colb2), p.H, p.t, p.t_pad, c.st));
+                             c.at<float>(p.rowb), p.H, p.n_q, p.n_q_pad, c.st,
+                             c.at<float>(p.colb2), p.t, p.t_pad));
   }
   const int slabs = p.n_q_pad / 64;
   const int npairs = p.nblk * (p.nblk + 1) / 2;
@@ -541,10 +541,9 @@ lc_status run_fit(const Ctx& ca, const void* qop, const void* kop, const void* V
       LC_CUDA(launch_gram(p.mode, false, mKc, mQ64, mOhi, mOlo, g, p.H, g5_split, c.st));
   }
   {
-    LC_PROF(c, "reduce_mass", 2);
-    LC_CUDA(launch_reduce_gram(c.at<float>(p.gpart), c.at<float>(p.G), g5_split, p.H, p.t_pad, c.st));
-    LC_CUDA(launch_reduce_partials(c.at<float>(p.cpart), c.at<float>(p.c), g5_split, H * p.t_pad,
-                                   c.st));
+    LC_PROF(c, "reduce_mass", 1);
+    LC_CUDA(launch_reduce_gram(c.at<float>(p.gpart), c.at<float>(p.G), g5_split, p.H, p.t_pad, c.st,
+                               c.at<float>(p.cpart), c.at<float>(p.c)));
   }
   if (cs && cs->st != ca.st) {
     LC_CUDA(cudaEventRecord(handoff, ca.st));

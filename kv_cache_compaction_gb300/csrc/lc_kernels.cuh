@@ -197,11 +197,16 @@ cudaError_t launch_reduce_partials(const float* part, float* out, int nsplit, si
                                    cudaStream_t st);
 cudaError_t launch_symmetrize(float* G, int H, int t_pad, cudaStream_t st);
 // Split-partial sum of a symmetric system built as its upper block triangle,
-// written symmetric (fused sum and transpose).
+// written symmetric (fused sum and transpose); with cpart, the same launch
+// also sums the right-hand side's partials ([nsplit][H][t_pad]) into cout.
 cudaError_t launch_reduce_gram(const float* part, float* out, int nsplit, int H, int t_pad,
-                               cudaStream_t st);
+                               cudaStream_t st, const float* cpart = nullptr,
+                               float* cout = nullptr);
+// Per-query shift and mass rows of the mass system; with colb2, the same
+// launch also fills the per-key biases as launch_fill_colb2 does.
 cudaError_t launch_mass_rows(const float* rowmax_pad, const float* lse_pad, float* rowsh2,
-                             float* row_b, int H, int n_q, int n_q_pad, cudaStream_t st);
+                             float* row_b, int H, int n_q, int n_q_pad, cudaStream_t st,
+                             float* colb2 = nullptr, int t = 0, int t_pad = 0);
 cudaError_t launch_fill_colb2(float* colb2, int H, int t, int t_pad, cudaStream_t st);
 // lc2_pad[h][r] = log2 sum_z part_z.sum 2^(part_z.max) for r < n, +inf for
 // the padding rows n <= r < n_pad.

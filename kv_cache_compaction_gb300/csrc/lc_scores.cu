@@ -575,11 +575,22 @@ __global__ void reduce_partials_kernel(const float4* part, float4* out, int nspl
 // of one head sums the tile and writes it and, through shared memory, its
 // transpose.
 __global__ void __launch_bounds__(256) reduce_gram_kernel(const float* part, float* out,
-                                                         int nsplit, int t_pad) {
+                                                         int nsplit, int t_pad,
+                                                         const float* cpart, float* cout) {
   __shared__ float tile[32][33];
   const int h = blockIdx.y;
   int ti = 0, rem = blockIdx.x;
   const int nt = t_pad / 32;
+  if (rem == nt * (nt + 1) / 2) {
+    // the CTA after the tiles sums the head's right-hand-side partials
+    const size_t n4 = static_cast<size_t>(gridDim.y) * t_pad / 4;
+    for (int i = threadIdx.x; i < t_pad / 4; i += blockDim.x) {
+      const size_t e = static_cast<size_t>(h) * t_pad / 4 + i;
+      reinterpret_cast<float4*>(cout)[e] =
+          sum_splits(reinterpret_cast<const float4*>(cpart) + e, n4, nsplit);
+    }
+    return;
+  }
   while (rem >= nt - ti) {
     rem -= nt - ti;
     ++ti;
@@ -623,11 +634,15 @@ __global__ void symmetrize_kernel(float* G, int H, int t_pad) {
 
 // Per-query shift and right-hand side of the mass fit, base 2:
 // rowsh2 = m * log2(e) (+inf in padded rows), row_b = exp(lse - m) (0 there).
+// Per-query shift and mass of the mass system and, when colb2 is given, its
+// per-key base-2 biases (0 for the t kept keys, -inf for the padding): one
+// launch for both.
 __global__ void mass_rows_kernel(const float* m_pad, const float* lse_pad, float* rowsh2,
-                                 float* row_b, int H, int n_q, int n_q_pad) {
+                                 float* row_b, int H, int n_q, int n_q_pad, float* colb2, int t,
+                                 int t_pad) {
   const size_t n = static_cast<size_t>(H) * n_q_pad;
-  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
-       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n; i += stride) {
     const int r = static_cast<int>(i % n_q_pad);
     if (r < n_q) {
       rowsh2[i] = m_pad[i] * kLog2e;
@@ -636,6 +651,11 @@ __global__ void mass_rows_kernel(const float* m_pad, const float* lse_pad, float
       rowsh2[i] = kInf;
       row_b[i] = 0.f;
     }
+  }
+  if (colb2) {
+    const size_t nc = static_cast<size_t>(H) * t_pad;
+    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < nc; i += stride)
+      colb2[i] = static_cast<int>(i % t_pad) < t ? 0.f : -kInf;
   }
 }
 
@@ -915,10 +935,12 @@ cudaError_t launch_reduce_partials(const float* part, float* out, int nsplit, si
 }
 
 cudaError_t launch_reduce_gram(const float* part, float* out, int nsplit, int H, int t_pad,
-                               cudaStream_t st) {
+                               cudaStream_t st, const float* cpart, float* cout) {
   if (t_pad % 32) return cudaErrorInvalidValue;
   const int nt = t_pad / 32;
-  reduce_gram_kernel<<<dim3(nt * (nt + 1) / 2, H), 256, 0, st>>>(part, out, nsplit, t_pad);
+  const int ntile = nt * (nt + 1) / 2;
+  reduce_gram_kernel<<<dim3(ntile + (cpart ? 1 : 0), H), 256, 0, st>>>(part, out, nsplit, t_pad,
+                                                                       cpart, cout);
   return cudaGetLastError();
 }
 
@@ -928,9 +950,10 @@ cudaError_t launch_symmetrize(float* G, int H, int t_pad, cudaStream_t st) {
 }
 
 cudaError_t launch_mass_rows(const float* rowmax_pad, const float* lse_pad, float* rowsh2,
-                             float* row_b, int H, int n_q, int n_q_pad, cudaStream_t st) {
+                             float* row_b, int H, int n_q, int n_q_pad, cudaStream_t st,
+                             float* colb2, int t, int t_pad) {
   mass_rows_kernel<<<grid_for(static_cast<size_t>(H) * n_q_pad), 256, 0, st>>>(
-      rowmax_pad, lse_pad, rowsh2, row_b, H, n_q, n_q_pad);
+      rowmax_pad, lse_pad, rowsh2, row_b, H, n_q, n_q_pad, colb2, t, t_pad);
   return cudaGetLastError();
 }
 
