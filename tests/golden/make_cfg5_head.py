@@ -1,4 +1,4 @@
-"""Write ``cfg5_head0.npz``: the float64 oracle's compaction of head 0 of the
+"""Write ``cfg5_head<h>.npz``: the float64 oracle's compaction of head h of the
 long-context workload (131072 cached keys, 524288 reference queries, d = 128,
 t = 1024, bf16 inputs with 64 planted needles).
 
@@ -16,7 +16,8 @@ stored rather than recomputed by the GPU test that reads it.  Stored:
 * ``inputs_sha256``: a digest of head 0's bf16 inputs, so that the test can
   tell whether the generator on its machine drew the same layer.
 
-Usage: ``python tests/golden/make_cfg5_head0.py`` from the repository root.
+Usage: ``python tests/golden/make_cfg5_head.py [h]`` from the repository root
+(h = 0 by default).
 """
 from __future__ import annotations
 
@@ -34,9 +35,6 @@ sys.path.insert(0, ROOT)
 import oracle  # noqa: E402
 import synth  # noqa: E402
 
-OUT = os.path.join(HERE, "cfg5_head0.npz")
-
-
 def inputs_digest(d) -> str:
     h = hashlib.sha256()
     for k in ("Q", "K", "V"):
@@ -44,9 +42,10 @@ def inputs_digest(d) -> str:
     return h.hexdigest()
 
 
-def main():
-    w = synth.workload("cfg5", H=1)
-    d = synth.make(w)
+def main(head: int):
+    out = os.path.join(HERE, f"cfg5_head{head}.npz")
+    w = synth.workload("cfg5")
+    d = synth.make(w, heads=[head])
     Q, K, V = d["Q"][0], d["K"][0], d["V"][0]
     t0 = time.time()
     r = oracle.compact_head(Q, K, V, w.t, w.softmax_scale)
@@ -54,13 +53,13 @@ def main():
     rows = np.unique(np.concatenate([np.asarray(d["needle_rows"][0]),
                                      rng.choice(w.n_q, 448, replace=False)]))
     np.savez_compressed(
-        OUT, u=r["u"].astype(np.float32), idx=r["idx"].astype(np.int32), w=r["w"],
+        out, u=r["u"].astype(np.float32), idx=r["idx"].astype(np.int32), w=r["w"],
         beta=r["beta"], Cv=r["Cv"].astype(np.float32), rows=rows.astype(np.int64),
         m=r["m"][rows], lse=r["lse"][rows], nnls_status=np.int32(r["nnls"]["status"]),
         ols_status=np.int32(r["ols_status"]), inputs_sha256=np.array(inputs_digest(d)))
-    print(f"wrote {OUT} in {time.time() - t0:.0f} s; NNLS {r['nnls']}, "
+    print(f"wrote {out} in {time.time() - t0:.0f} s; NNLS {r['nnls']}, "
           f"{int(np.sum(r['w'] > 0))} positive weights")
 
 
 if __name__ == "__main__":
-    main()
+    main(int(sys.argv[1]) if len(sys.argv) > 1 else 0)
