@@ -2,9 +2,10 @@
 configuration the benchmark uses (one compact_layer call over all heads of a
 layer).  The oracle recomputes whole heads where it finishes in seconds (cfg2
 and cfg3 every head, cfg4 sampled layers); for the long-context layer (cfg5,
-131072 keys) head 0's oracle compaction is stored (tests/golden/, written by
-a script that calls only the oracle), and the rest is checked on single query
-rows and on properties of the GPU's own outputs.  Every expected value comes
+131072 keys) the oracle's compactions of heads 0 and 1 are stored
+(tests/golden/, written by a script that calls only the oracle), and the
+rest is checked on single query rows and on properties of the GPU's own
+outputs.  Every expected value comes
 from the generator or the oracle."""
 import hashlib
 import os
@@ -158,7 +159,7 @@ def test_cfg5_fit_t1024(comp):
     assert relf(cg, r["Cv"]) <= FIT_REL, f"Cv relF {relf(cg, r['Cv']):.2e}"
 
 
-GOLDEN_CFG5 = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "cfg5_head0.npz")
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
 
 def _inputs_digest(d, h):
@@ -168,36 +169,38 @@ def _inputs_digest(d, h):
     return dig.hexdigest()
 
 
-def test_cfg5_head0_against_stored_oracle(comp, cfg5):
-    """Head 0 of the long-context layer (131072 keys, 524288 queries, t = 1024)
-    against the float64 oracle's compaction of the same head, stored by
-    tests/golden/make_cfg5_head0.py (a little over an hour of host time, so
-    it is not recomputed here): key scores within the score tolerance, row
-    statistics of the stored sample rows, the selection exact up to
-    near-ties, and w, beta and C_v within the fit tolerance.  Where a near-tie
-    made the selections differ, the GPU's fit is compared on the oracle's
-    selection instead (lc_fit_only, from the GPU's own step-1 statistics as
-    in lc_compact_layer)."""
-    g = np.load(GOLDEN_CFG5)
+@pytest.mark.parametrize("h", [0, 1])
+def test_cfg5_head_against_stored_oracle(comp, cfg5, h):
+    """Heads 0 and 1 of the long-context layer (131072 keys, 524288 queries,
+    t = 1024) against the float64 oracle's compaction of the same head,
+    stored by tests/golden/make_cfg5_head.py (a little over an hour of host
+    time per head, so it is not recomputed here): key scores within the score
+    tolerance, row statistics of the stored sample rows, the selection exact
+    up to near-ties, and w, beta and C_v within the fit tolerance.  Where a
+    near-tie made the selections differ, the GPU's fit is compared on the
+    oracle's selection instead (lc_fit_only, from the GPU's own step-1
+    statistics as in lc_compact_layer)."""
+    g = np.load(os.path.join(GOLDEN, f"cfg5_head{h}.npz"))
     w, d = cfg5["w"], cfg5["d"]
-    assert _inputs_digest(d, 0) == str(g["inputs_sha256"]), "the generator drew another layer"
+    assert _inputs_digest(d, h) == str(g["inputs_sha256"]), "the generator drew another layer"
     assert int(g["nnls_status"]) == 0 and int(g["ols_status"]) == 0
-    err = float(np.max(np.abs(cfg5["u"][0] - g["u"])))
+    err = float(np.max(np.abs(cfg5["u"][h] - g["u"])))
     assert err <= SCORE_ABS, f"max |u_gpu - u| = {err:.2e}"
     rows = g["rows"]
-    assert np.max(np.abs(cfg5["lse"][0][rows] - g["lse"])) <= LSE_ABS
-    assert np.max(np.abs(cfg5["m"][0][rows] - g["m"])) <= LSE_ABS
-    idx, wg, bg, cg = (x[0] for x in cfg5["out"])
+    assert np.max(np.abs(cfg5["lse"][h][rows] - g["lse"])) <= LSE_ABS
+    assert np.max(np.abs(cfg5["m"][h][rows] - g["m"])) <= LSE_ABS
+    idx, wg, bg, cg = (x[h] for x in cfg5["out"])
     ref = {"w": g["w"], "beta": g["beta"], "Cv": g["Cv"]}
-    overlap = near_tie_swap(idx, g["idx"], g["u"], w.t, "cfg5 head 0")
-    print(f"cfg5 head 0: selection overlap {overlap:.4f}")
+    overlap = near_tie_swap(idx, g["idx"], g["u"], w.t, f"cfg5 head {h}")
+    print(f"cfg5 head {h}: selection overlap {overlap:.4f}")
     if overlap == 1.0:
-        gate_fit(wg, bg, cg, ref, "cfg5 head 0")
+        gate_fit(wg, bg, cg, ref, f"cfg5 head {h}")
         return
-    wf, bf, cf = comp.fit_only(dev(d["Q"][:1], w.dtype), dev(d["K"][:1], w.dtype),
-                               dev(d["V"][:1], w.dtype), dev_i32(g["idx"][None]),
-                               dev_f32(cfg5["m"][:1]), dev_f32(cfg5["lse"][:1]),
-                               dev_f32(cfg5["O"][:1]))
+    wf, bf, cf = comp.fit_only(dev(d["Q"][h:h + 1], w.dtype), dev(d["K"][h:h + 1], w.dtype),
+                               dev(d["V"][h:h + 1], w.dtype), dev_i32(g["idx"][None]),
+                               dev_f32(cfg5["m"][h:h + 1]), dev_f32(cfg5["lse"][h:h + 1]),
+                               dev_f32(cfg5["O"][h:h + 1]))
     rep = comp.report(1)
     assert rep.device_error_bits == 0 and rep.head_status[0] == 0, rep
-    gate_fit(host(wf)[0], host(bf)[0], host(cf)[0], ref, "cfg5 head 0 (on the oracle's selection)")
+    gate_fit(host(wf)[0], host(bf)[0], host(cf)[0], ref,
+             f"cfg5 head {h} (on the oracle's selection)")
