@@ -55,6 +55,13 @@ def test_bf16_block_kernel_chains(comp, P):
     _fit_case(comp, w)
 
 
+@pytest.mark.parametrize("P", [129, 130])
+def test_bf16_block_kernel_chains_d64(comp, P):
+    # d = 64: the output system's R blocks fold 64-column accumulators
+    w = synth.workload("cfg2", H=1, T=256, d=64, t=128, n_q_override=64 * 64 * P, seed=750 + P)
+    _fit_case(comp, w)
+
+
 @pytest.mark.parametrize("P", [64, 65, 129, 130])
 def test_fp32_block_kernel_chains(comp, P):
     # cfg1's own shape and compression (T = 512, t = 32): with iid scores and
