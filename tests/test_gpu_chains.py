@@ -13,7 +13,8 @@ and statistics:
 * P = 65: a second chunk of one slab, added at the end;
 * P = 129: chunk 1 closed by the last slab but one (bf16 kernel: folded by
   its group after its loop; fp32 kernel: in the loop);
-* P = 130, 193: folds in the loop, and for 193 also after the loop.
+* P = 130, 193: folds in the loop, and for 193 also after the loop;
+* a ragged query count whose last CTA has a shorter chain than the others.
 
 The all-pairs kernel (t = 256, bf16) is run where the minimum split decides
 the launch (8320 slabs for one head).  Every expected value comes from the
@@ -68,6 +69,16 @@ def test_fp32_block_kernel_chains(comp, P):
     # half of the keys kept the output system is too ill-conditioned for an
     # fp32 fit to meet the tolerance whatever the chain length
     w = synth.workload("cfg1", n_q_override=64 * 64 * P, seed=800 + P)
+    _fit_case(comp, w)
+
+
+@pytest.mark.parametrize("name", ["cfg2", "cfg1"])
+def test_ragged_chains(comp, name):
+    # n_q = 64 * 64 * 129 + 77: 8258 slabs of 64 rows (the last one partial)
+    # split 130 per CTA, so the last CTA sums 68 slabs (one chunk and four
+    # slabs) while the others fold two chunks
+    kw = {"H": 1, "T": 256, "t": 128} if name == "cfg2" else {}
+    w = synth.workload(name, n_q_override=64 * 64 * 129 + 77, seed=950, **kw)
     _fit_case(comp, w)
 
 
