@@ -1,0 +1,45 @@
+"""Many KV heads in one call, up to the largest count the library accepts
+(4096): one lc_compact_layer call against the oracle's compaction of each
+checked head, and properties of every head's outputs.  Every expected value
+comes from the generator or the oracle."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from gpu_util import check_layer_fits, compactor, host, inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def comp():
+    return compactor()
+
+
+def _run(comp, w, checked):
+    d, Q, K, V = inputs(w)
+    idx, wg, bg, cg = (host(x) for x in comp.compact_layer(Q, K, V, w.t))
+    rep = comp.report(w.H)
+    assert rep.device_error_bits == 0
+    assert all(s == 0 for s in rep.head_status), "a head did not finish cleanly"
+    # every head: an ascending selection of t distinct keys, w >= 0, beta = log w
+    assert np.all(np.diff(idx, axis=1) > 0) and idx.min() >= 0 and idx.max() < w.T
+    assert np.all(wg >= 0) and np.all(np.isfinite(wg)) and np.all(np.isfinite(cg))
+    pos = wg > 0
+    assert np.allclose(bg[pos], np.log(wg[pos]), rtol=0, atol=1e-5)
+    assert np.all(np.isneginf(bg[~pos]))
+    refs = {h: oracle.compact_head(d["Q"][h], d["K"][h], d["V"][h], w.t, w.softmax_scale)
+            for h in checked}
+    check_layer_fits(comp, w, Q, K, V, refs, idx, wg, bg, cg)
+
+
+def test_64_heads_every_head(comp):
+    w = synth.workload("cfg2", H=64, G=1, T=160, t=24, seed=61)
+    _run(comp, w, range(w.H))
+
+
+def test_4096_heads(comp):
+    # the largest head count, on a tiny head shape; four heads against the oracle
+    w = synth.workload("cfg2", H=4096, G=1, T=24, d=64, t=6, seed=62)
+    _run(comp, w, (0, 1, 2047, 4095))
