@@ -117,7 +117,7 @@ def check_layer_fits(comp, w, Q, K, V, refs, idx, wg, bg, cg):
                                    dev_i32(np.stack([r["idx"] for r in sel])),
                                    dev_f32(np.stack([r["m"] for r in sel])),
                                    dev_f32(np.stack([r["lse"] for r in sel])),
-                                   dev_f32(np.stack([r["O"] for r in sel])))
+                                   dev_f32(np.stack([r["O"] for r in sel])), scale=w.scale)
         rep = comp.report(len(refit))
         assert rep.device_error_bits == 0
         wf, bf, cf = host(wf), host(bf), host(cf)

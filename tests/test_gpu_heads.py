@@ -43,3 +43,22 @@ def test_4096_heads(comp):
     # the largest head count, on a tiny head shape; four heads against the oracle
     w = synth.workload("cfg2", H=4096, G=1, T=24, d=64, t=6, seed=62)
     _run(comp, w, (0, 1, 2047, 4095))
+
+
+@pytest.mark.parametrize("name,kw", [
+    ("cfg1", {}),                                       # fp32 inputs, d = 64
+    ("cfg2", {"H": 2, "T": 384, "G": 2, "t": 48}),      # bf16, d = 128
+])
+def test_unit_scale(comp, name, kw):
+    """s = 1 (configuration 1's second reading): logits 8-11x larger than
+    with 1/sqrt(d), so nearly one-hot attention and wide exponent ranges in
+    every max-shift; the scale is passed through the ABI."""
+    w = synth.workload(name, scale=1.0, seed=63, **kw)
+    d, Q, K, V = inputs(w)
+    idx, wg, bg, cg = (host(x) for x in comp.compact_layer(Q, K, V, w.t, scale=1.0))
+    rep = comp.report(w.H)
+    assert rep.device_error_bits == 0
+    refs = {h: oracle.compact_head(d["Q"][h], d["K"][h], d["V"][h], w.t, 1.0) for h in range(w.H)}
+    for h in range(w.H):
+        assert rep.head_status[h] in (0, 6), rep.head_status  # 6: singular system, ridge added
+    check_layer_fits(comp, w, Q, K, V, refs, idx, wg, bg, cg)
