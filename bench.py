@@ -377,7 +377,8 @@ def main():
             ms = kern[k][0] / max(kern[k][1], 1)
             tf = f / (ms * 1e-3) / 1e12
             qkt[k] = {"tflops": tf, "frac_of_burst": tf / pk["bf16_tflops"],
-                      "frac_of_sustained": tf / pk["bf16_tflops_sustained"], "ms": ms}
+                      "frac_of_sustained": tf / pk["bf16_tflops_sustained"], "ms": ms,
+                      "traffic": traffic_for(k)}
     # the two small memory-side kernels against HBM: the top-t select reads
     # the scores u and writes idx; the key gather reads and writes t rows of K
     hbm_bytes = {"select_topt": H * w.T * 4 + H * t * 4, "gather_keys": 2 * H * t * dd * 2}
