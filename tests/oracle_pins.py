@@ -572,9 +572,10 @@ def check_heldout_errors(o):
 # ------------------------------------------------ farthest-first traversal -
 def check_farthest_first(o):
     """Farthest-first traversal against a from-scratch recomputation of every
-    step; the chosen distances never increase; and on tiny sets the result
-    is within the traversal's factor-2 bound of the exhaustive optimum of
-    the k-center problem it approximates (Gonzalez 1985)."""
+    step; the chosen distances never increase; on tiny sets the result is
+    within the traversal's factor-2 bound of the exhaustive optimum of the
+    k-center problem it approximates (Gonzalez 1985); exact distance ties go
+    to the lowest index."""
     rng = _rng(53)
     K = rng.normal(size=(40, 3))
     seeds = [5, 17]
@@ -604,6 +605,12 @@ def check_farthest_first(o):
     assert rad <= 2 * opt + 1e-12, f"radius {rad} > 2 x optimum {opt}"
     # all keys taken: the traversal stops
     assert len(o.farthest_first(K[:4], [0], 10)) == 3
+    # exact ties (integer points, so every squared distance is exact): the
+    # lowest index wins.  From the seed at the origin, (2,0), (-2,0), (0,2)
+    # tie at 4 and are taken in index order; then the four unit points tie
+    # at 1 and the lowest two follow.
+    P = np.array([[0, 0], [1, 0], [-1, 0], [0, 1], [0, -1], [2, 0], [-2, 0], [0, 2]], float)
+    assert list(o.farthest_first(P, [0], 6)) == [5, 6, 7, 1, 2]
 
 
 # ------------------------------------------------- baseline AM variant -----

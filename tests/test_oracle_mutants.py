@@ -220,11 +220,118 @@ def _no_ridge(o):
     o.ols = f
 
 
+def _farthest_ties_high(o):
+    # distance ties in farthest-first broken towards the higher index
+    def f(K, seeds, M):
+        K = np.asarray(K, float)
+        S = [int(s) for s in seeds]
+        N = K.shape[0]
+        taken = np.zeros(N, bool)
+        taken[S] = True
+        mind = np.full(N, np.inf)
+        for j in S:
+            mind = np.minimum(mind, ((K - K[j]) ** 2).sum(axis=1))
+        added = []
+        while len(S) < M and not taken.all():
+            cand = np.where(taken, -np.inf, mind)
+            i = int(N - 1 - np.argmax(cand[::-1]))  # last maximum
+            added.append(i)
+            S.append(i)
+            taken[i] = True
+            mind = np.minimum(mind, ((K - K[i]) ** 2).sum(axis=1))
+        return np.asarray(added, np.int64)
+    o.farthest_first = f
+
+
+def _lse_is_max(o):
+    # the log-normaliser replaced by the row maximum
+    orig = o.full_stats
+
+    def f(Q, K, V, scale):
+        m, lse, O = orig(Q, K, V, scale)
+        return m, m.copy(), O
+    o.full_stats = f
+
+
+def _select_by_score(o):
+    # the kept keys returned in score order instead of ascending index order
+    orig = o.select
+
+    def f(u, t):
+        idx = orig(u, t)
+        return idx[np.argsort(-np.asarray(u)[idx], kind="stable")]
+    o.select = f
+
+
+def _nnls_clipped(o):
+    # the unconstrained least-squares solution clipped at zero in place of NNLS
+    def f(G, c, max_outer=0, max_inner=0, tol=None):
+        w = np.linalg.lstsq(np.asarray(G, float), np.asarray(c, float), rcond=None)[0]
+        return np.maximum(w, 0.0), {"outer": 1, "inner": 1, "status": o.OK}
+    o.nnls_lh = f
+
+
+def _weights_over_queries(o):
+    # the compact softmax normalised over the queries instead of the keys
+    def f(Q, Kc, beta, scale):
+        L = scale * (np.asarray(Q, float) @ np.asarray(Kc, float).T) + np.asarray(beta, float)[None, :]
+        E = np.exp(L - L.max(axis=0, keepdims=True))
+        return E / E.sum(axis=0, keepdims=True)
+    o.compact_weights = f
+
+
+def _ridge_too_large(o):
+    # the singular-system ridge a thousand times too large
+    orig = o.ridge
+    o.ridge = lambda M: 1000.0 * orig(M)
+
+
+def _redistribute_over_T(o):
+    # the dropped mass shared over all T keys instead of the t kept ones
+    orig = o.redistribute_beta
+
+    def f(Q, K, short, idx, scale):
+        b = orig(Q, K, short, idx, scale)
+        return np.log1p(np.expm1(b) * len(idx) / np.asarray(K).shape[0])
+    o.redistribute_beta = f
+
+
+def _combine_drops_appended(o):
+    # tokens appended after compaction left out of the attention
+    def f(Q, Ck, beta, Cv, Knew, Vnew, n_vis, scale):
+        beta = np.asarray(beta, float)
+        return o.branch_attention(Q, Ck, Cv, np.where(np.isfinite(beta), beta, 0.0),
+                                  np.isfinite(beta)[None, :], scale)
+    o.combine_attention = f
+
+
+def _bounded_opposite_bound(o):
+    # a weight that leaves [lo, hi] pinned at the opposite bound
+    def f(G, c, lo, hi, iters):
+        G, c = np.asarray(G, float), np.asarray(c, float)
+        w = np.zeros(c.size)
+        free = np.ones(c.size, bool)
+        it = 0
+        while it < iters and free.any():
+            it += 1
+            F, B = np.flatnonzero(free), np.flatnonzero(~free)
+            w[F] = np.linalg.solve(G[np.ix_(F, F)], c[F] - G[np.ix_(F, B)] @ w[B])
+            low, high = free & (w < lo), free & (w > hi)
+            w[low], w[high] = hi, lo
+            if not (low.any() or high.any()):
+                break
+            free &= ~(low | high)
+        return w, it
+    o.bounded_ls = f
+
+
 MUTANTS = [_no_scale, _unnormalised_output, _score_plus_lse, _score_min, _ties_high,
            _no_stepback, _mass_unshifted, _weights_no_bias, _ols_diag, _second_pass_full_lse,
            _delta_not_shared, _delta_by_difference, _combine_unbiased, _mass_error_signed,
            _farthest_by_sum, _rms_as_mean, _bounded_pins_at_zero, _off_support_zeroed,
-           _support_ignored, _duplicate_keeps_later, _no_ridge]
+           _support_ignored, _duplicate_keeps_later, _no_ridge, _farthest_ties_high, _lse_is_max,
+           _select_by_score, _nnls_clipped, _weights_over_queries, _ridge_too_large,
+           _redistribute_over_T, _combine_drops_appended, _bounded_opposite_bound]
 
 
 @pytest.mark.parametrize("mutate", MUTANTS, ids=lambda f: f.__name__)
