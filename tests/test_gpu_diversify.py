@@ -70,6 +70,30 @@ def test_small_heads(comp, d):
         check_sequence(K[h], seeds[h], out[h], 40)
 
 
+@pytest.mark.parametrize("T,d", [(8, 64), (4096, 64), (4096, 128), (131072, 64)])
+def test_exact_ties(comp, T, d):
+    """Keys with small integer coordinates: every squared distance is an
+    integer, exact in bf16 inputs and fp32 sums, so distance ties are exact
+    and frequent (within a CTA's slice and between the CTAs of a cluster)
+    and the whole sequence must equal the oracle's, every tie going to the
+    lowest index.  T = 8 is the hand-checked point set of the oracle's pin
+    (the origin as seed; (2,0), (-2,0), (0,2), then two unit points)."""
+    if T == 8:
+        K = np.zeros((1, T, d))
+        K[0, :, :2] = [[0, 0], [1, 0], [-1, 0], [0, 1], [0, -1], [2, 0], [-2, 0], [0, 2]]
+        seeds = np.array([[0]], np.int32)
+        M = 6
+    else:
+        rng = np.random.default_rng(T + d)
+        K = rng.integers(-2, 3, size=(2, T, d)).astype(np.float64)
+        seeds = np.stack([rng.choice(T, 2, replace=False) for _ in range(2)]).astype(np.int32)
+        M = 34
+    out = _run(comp, K, seeds, M)
+    for h in range(K.shape[0]):
+        ref = oracle.farthest_first(K[h], seeds[h], M)
+        assert out[h].tolist() == ref.tolist(), f"head {h}: {out[h].tolist()} vs {ref.tolist()}"
+
+
 def test_runs_out_of_keys(comp):
     """M = T: the traversal takes every key once."""
     w = synth.workload("cfg2", H=1, G=1, T=5, t=3, seed=9)
