@@ -697,6 +697,56 @@ def check_variant_t_equals_T(o):
     _close(r["Cv"], V, 1e-6, "variant t=T: C_v = V")
 
 
+def check_chunk_boundaries(o):
+    """The oracle forms its sums over query rows in chunks of o.CHUNK rows.
+    With n = 2 CHUNK + 37 rows, every chunked function must agree with the
+    same function evaluated on groups of rows that straddle the chunk
+    boundaries, each group shorter than a chunk: row-wise results row by
+    row, sums over rows as the sum over the groups, maxima as the maximum
+    over the groups, the mean-square score through its group means.  A
+    dropped, repeated or misplaced chunk breaks one of these."""
+    rng = _rng(97)
+    n, T, d, s = 2 * o.CHUNK + 37, 24, 8, 0.35
+    Q = rng.normal(size=(n, d))
+    K = rng.normal(size=(T, d))
+    V = rng.normal(size=(T, 5))
+    cuts = [0, 700, o.CHUNK - 3, o.CHUNK + 5, 2 * o.CHUNK - 1, 2 * o.CHUNK + 20, n]
+    groups = list(zip(cuts[:-1], cuts[1:]))
+    assert all(0 < b - a < o.CHUNK for a, b in groups)
+
+    def close(x, y):
+        assert np.allclose(x, y, rtol=1e-12, atol=1e-14), float(np.max(np.abs(np.asarray(x) - y)))
+
+    m, lse, O = o.full_stats(Q, K, V, s)
+    parts = [o.full_stats(Q[a:b], K, V, s) for a, b in groups]
+    for k, full in enumerate((m, lse, O)):
+        close(full, np.concatenate([p[k] for p in parts]))
+    close(o.lse_over(Q, K, s), np.concatenate([o.lse_over(Q[a:b], K, s) for a, b in groups]))
+    bias = rng.normal(size=T)
+    valid = rng.random((n, T)) < 0.7
+    out, lz = o.branch_attention(Q, K, V, bias, valid, s)
+    bp = [o.branch_attention(Q[a:b], K, V, bias, valid[a:b], s) for a, b in groups]
+    close(out, np.concatenate([p[0] for p in bp]))
+    close(lz, np.concatenate([p[1] for p in bp]))
+    close(o.key_scores(Q, K, lse, s),
+          np.max([o.key_scores(Q[a:b], K, lse[a:b], s) for a, b in groups], axis=0))
+    u = o.rms_key_scores(Q, K, lse, s)
+    ms = sum((b - a) * np.exp(2.0 * o.rms_key_scores(Q[a:b], K, lse[a:b], s)) for a, b in groups)
+    close(u, 0.5 * np.log(ms / n))
+    Kc = K[:6]
+    G, c, bb = o.mass_system(Q, Kc, m, lse, s)
+    gp = [o.mass_system(Q[a:b], Kc, m[a:b], lse[a:b], s) for a, b in groups]
+    close(G, sum(p[0] for p in gp))
+    close(c, sum(p[1] for p in gp))
+    close(bb, sum(p[2] for p in gp))
+    w = np.array([0.5, 0.0, 1.5, 2.0, 0.0, 0.25])
+    sup, H, R = o.output_system(Q, Kc, w, O, s)
+    op = [o.output_system(Q[a:b], Kc, w, O[a:b], s) for a, b in groups]
+    assert all(np.array_equal(sup, p[0]) for p in op)
+    close(H, sum(p[1] for p in op))
+    close(R, sum(p[2] for p in op))
+
+
 ALL_CHECKS = [
     check_full_stats_brute, check_full_stats_closed_forms, check_key_scores_brute,
     check_select, check_mass_system_brute, check_nnls_bruteforce, check_nnls_scipy, check_nnls_planted_and_kkt,
@@ -705,4 +755,5 @@ ALL_CHECKS = [
     check_fit_reduces_error, check_two_pass_brute, check_two_pass_full_shortlist,
     check_redistribute, check_combine_single_softmax, check_heldout_errors,
     check_farthest_first, check_rms_scores, check_bounded_ls, check_variant_t_equals_T,
+    check_chunk_boundaries,
 ]

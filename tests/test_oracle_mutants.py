@@ -325,13 +325,28 @@ def _bounded_opposite_bound(o):
     o.bounded_ls = f
 
 
+def _chunk_tail_dropped(o):
+    # the last, partial chunk of query rows never visited
+    def ch(n, size=o.CHUNK):
+        return [(a, a + size) for a in range(0, n - size + 1, size)] or [(0, n)]
+    o._chunks = ch
+
+
+def _chunks_overlap(o):
+    # each chunk after the first starting one row early (that row counted twice)
+    def ch(n, size=o.CHUNK):
+        return [(max(0, a - 1), min(n, a + size)) for a in range(0, n, size)]
+    o._chunks = ch
+
+
 MUTANTS = [_no_scale, _unnormalised_output, _score_plus_lse, _score_min, _ties_high,
            _no_stepback, _mass_unshifted, _weights_no_bias, _ols_diag, _second_pass_full_lse,
            _delta_not_shared, _delta_by_difference, _combine_unbiased, _mass_error_signed,
            _farthest_by_sum, _rms_as_mean, _bounded_pins_at_zero, _off_support_zeroed,
            _support_ignored, _duplicate_keeps_later, _no_ridge, _farthest_ties_high, _lse_is_max,
            _select_by_score, _nnls_clipped, _weights_over_queries, _ridge_too_large,
-           _redistribute_over_T, _combine_drops_appended, _bounded_opposite_bound]
+           _redistribute_over_T, _combine_drops_appended, _bounded_opposite_bound,
+           _chunk_tail_dropped, _chunks_overlap]
 
 
 @pytest.mark.parametrize("mutate", MUTANTS, ids=lambda f: f.__name__)
