@@ -154,9 +154,10 @@ def _random_problem(rng, n, t):
 
 
 def check_mass_system_brute(o):
-    """G = A^T A, c = A^T b in per-query max-shifted form, against loops:
-    A_ij = exp(s q_i.c_j - m_i), b_i = exp(lse_i - m_i) with m_i the full-row
-    max and lse_i the full log mass."""
+    """G = A^T A, c = A^T b and b.b in per-query max-shifted form, against
+    loops: A_ij = exp(s q_i.c_j - m_i), b_i = exp(lse_i - m_i) with m_i the
+    full-row max and lse_i the full log mass; and the residual ||A w - b||^2
+    = w^T G w - 2 c^T w + b.b at an arbitrary w."""
     rng = _rng(45)
     n_q, T, d, t = 5, 8, 3, 3
     Q = rng.standard_normal((n_q, d)) * 3
@@ -179,6 +180,17 @@ def check_mass_system_brute(o):
             mx = max(logit)
             ref += math.exp(logit[idx[j]] - mx) * sum(math.exp(x - mx) for x in logit)
         _close(c[j], ref, 1e-11, "mass right-hand side")
+    ref = 0.0
+    for i in range(n_q):
+        logit = [s * float(Q[i] @ K[l]) for l in range(T)]
+        mx = max(logit)
+        ref += sum(math.exp(x - mx) for x in logit) ** 2
+    _close(bb, ref, 1e-11, "mass b.b")
+    # the residual identity the three terms exist for, at an arbitrary w
+    w = np.array([0.3, 1.7, 0.05])
+    A = np.array([[math.exp(s * float(Q[i] @ K[l]) - m[i]) for l in idx] for i in range(n_q)])
+    b = np.array([math.exp(lse[i] - m[i]) for i in range(n_q)])
+    _close(w @ G @ w - 2 * c @ w + bb, float(np.sum((A @ w - b) ** 2)), 1e-10, "mass residual")
 
 
 def check_nnls_bruteforce(o):

@@ -339,6 +339,16 @@ def _chunks_overlap(o):
     o._chunks = ch
 
 
+def _bb_dropped(o):
+    # the constant term b.b of the mass residual left at zero
+    orig = o.mass_system
+
+    def f(Q, Kc, m, lse, scale):
+        G, c, _ = orig(Q, Kc, m, lse, scale)
+        return G, c, 0.0
+    o.mass_system = f
+
+
 MUTANTS = [_no_scale, _unnormalised_output, _score_plus_lse, _score_min, _ties_high,
            _no_stepback, _mass_unshifted, _weights_no_bias, _ols_diag, _second_pass_full_lse,
            _delta_not_shared, _delta_by_difference, _combine_unbiased, _mass_error_signed,
@@ -346,7 +356,7 @@ MUTANTS = [_no_scale, _unnormalised_output, _score_plus_lse, _score_min, _ties_h
            _support_ignored, _duplicate_keeps_later, _no_ridge, _farthest_ties_high, _lse_is_max,
            _select_by_score, _nnls_clipped, _weights_over_queries, _ridge_too_large,
            _redistribute_over_T, _combine_drops_appended, _bounded_opposite_bound,
-           _chunk_tail_dropped, _chunks_overlap]
+           _chunk_tail_dropped, _chunks_overlap, _bb_dropped]
 
 
 @pytest.mark.parametrize("mutate", MUTANTS, ids=lambda f: f.__name__)
